@@ -1,0 +1,408 @@
+"""Benchmark of one paged GQA decode step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--impl ours|reference] [--partition-tokens T] [--compute mma|simt]
+
+One "step" = the whole hot path over one batch: split kernel (phase 1) +
+merge kernel (phase 2), through the C ABI.  Prints ONE JSON line (rank 0).
+
+metric  : K/V-read HBM GB/s = unique K/V bytes a step must read / step time
+          (unit GB/s, higher is better); us per step and tokens/s ride along.
+value   : device-timed with CUDA events on the launching stream, inputs
+          resident in HBM; K steps between barrier + synchronize, max over ranks.
+e2e     : the same metric through pa_decode with the step's inputs (q, block
+          table, lengths) copied from pinned host memory and the output read
+          back every step.
+roofline: the split kernel alone (CUDA events around phase 1 in the same timed
+          loop) against the measured HBM copy bandwidth.
+cpu_baseline / --impl reference: the float64 oracle on the host cores, on a
+          bounded sample of the same workload.
+N > 1   : independent replicas (the path has no exchange step), one per GPU,
+          scaling "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "serving_mix_b256_g4_d128"
+METRIC = "paged GQA decode: K/V-read HBM GB/s (% of GB300 peak); µs per decode step"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    """Hash of the kernel sources: ncu traffic figures are tied to it."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_gqa_decode_pa_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, opts_key: str):
+    """dram bytes per split-kernel launch from a committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{workload}|{opts_key}")
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        inside = [r for (t, r) in self.rows if self.t0 - 0.2 <= t <= self.t1 + 0.2]
+        if not inside and self.rows:
+            inside = [min(self.rows, key=lambda x: abs(x[0] - self.t1))[1]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            parts = [x.strip() for x in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_workload(name):
+    from paged_gqa_decode_pa_gb300 import workloads as wl
+
+    return wl.make(name)
+
+
+def oracle_sample(w, budget_s: float, seed: int = 0):
+    """Time the oracle on a bounded sample of (b, h) pairs of the workload.
+
+    Returns (GB/s over the sample's K/V bytes, seconds, pairs, threads)."""
+    import oracle
+
+    oracle.build()
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(w.B * w.H)
+    pairs_all = np.stack([order // w.H, order % w.H], axis=1).astype(np.int32)
+    # calibrate on a few pairs, then size the sample for the budget
+    n = min(len(pairs_all), max(threads, 8))
+    while True:
+        pairs = pairs_all[:n]
+        t = time.perf_counter()
+        oracle.decode(w.q, w.k_cache, w.v_cache, w.block_table, w.cache_seqlens, w.scale,
+                      w.dtype, pairs=pairs)
+        dt = time.perf_counter() - t
+        if dt >= 0.25 * budget_s or n >= len(pairs_all):
+            break
+        grow = max(2.0, min(16.0, 0.5 * budget_s / max(dt, 1e-3)))
+        n = min(len(pairs_all), int(n * grow))
+    # K/V bytes of the sample: each pair reads its sequence's K and V rows of
+    # one kv head (the oracle does not share them across the group)
+    toks = w.cache_seqlens[pairs[:, 0]].astype(np.int64).sum()
+    nbytes = int(toks) * w.d * 2 * 2
+    return nbytes / dt / 1e9, dt, pairs, threads
+
+
+def run_reference(args, rank, world):
+    """The oracle timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    w = make_workload(args.config)
+    per_step = max(0.05, min(1.0, 90.0 / max(1, args.steps + args.warmup)))
+    gbs, dt, pairs, threads = oracle_sample(w, per_step)
+    import oracle
+
+    for _ in range(args.warmup):
+        oracle.decode(w.q, w.k_cache, w.v_cache, w.block_table, w.cache_seqlens, w.scale,
+                      w.dtype, pairs=pairs)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(w.q, w.k_cache, w.v_cache, w.block_table, w.cache_seqlens, w.scale,
+                      w.dtype, pairs=pairs)
+    el = time.perf_counter() - t
+    toks = int(w.cache_seqlens[pairs[:, 0]].astype(np.int64).sum())
+    nbytes = toks * w.d * 4
+    value = nbytes * args.steps / el / 1e9
+    sample = (f"{len(pairs)} of {w.B * w.H} (sequence, query head) outputs per step, "
+              f"{toks} cached tokens")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, args), "gpu_launches": 0,
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, args):
+    return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "d": w.d,
+            "block_size": w.block_size, "max_blocks_per_seq": w.max_blocks_per_seq,
+            "num_blocks": w.num_blocks, "dtype": w.dtype,
+            "mean_seqlen": round(float(np.mean(w.cache_seqlens)), 1),
+            "max_seqlen": int(np.max(w.cache_seqlens)),
+            "partition_tokens": args.partition_tokens, "compute": args.compute,
+            "kv_bytes_per_step": w.kv_bytes(),
+            "l2": ("inputs larger than L2" if w.kv_bytes() > 2 * L2_BYTES
+                   else "L2 flushed between timed steps"),
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import paged_gqa_decode_pa_gb300 as pg
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = make_workload(args.config)
+    q, k, v, t, sl = w.torch_tensors(dev)
+    out = torch.empty((w.B, w.H, w.d), dtype=torch.float32, device=dev)
+    opts = pg.options(partition_tokens=args.partition_tokens, compute=args.compute)
+    shape = pg.shape_of(q, k, t)
+    ws = pg.alloc_workspace(shape, opts, dev)
+    stream = torch.cuda.current_stream(dev)
+    kv_bytes = w.kv_bytes()
+    flush = kv_bytes <= 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+
+    def step():
+        pg.pa_decode_split(q, k, v, t, sl, w.scale, out, ws, opts)
+        pg.pa_decode_merge(q, k, v, t, sl, w.scale, out, ws, opts)
+
+    for _ in range(args.warmup):
+        if flush:
+            scratch.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if pg.pa_read_status(ws) != 0:
+        raise RuntimeError("device status bits set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local_rank))
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_begin()
+    for i in range(K):
+        if flush:
+            scratch.fill_(1.0)
+        ev[i][0].record(stream)
+        pg.pa_decode_split(q, k, v, t, sl, w.scale, out, ws, opts)
+        ev[i][1].record(stream)
+        pg.pa_decode_merge(q, k, v, t, sl, w.scale, out, ws, opts)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_end()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    split_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    if flush:
+        total_ms = float(sum(step_ms))
+    else:
+        total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    if pg.pa_read_status(ws) != 0:
+        raise RuntimeError("device status bits set during the timed steps")
+
+    # ---- e2e: host buffers, copies inside the timed region
+    Ke = max(3, min(K, 200))
+    q_h = q.cpu().pin_memory()
+    t_h = t.cpu().pin_memory()
+    sl_h = sl.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = q_h.numel() * q_h.element_size() + t_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * 4
+    for _ in range(2):
+        q.copy_(q_h, non_blocking=True)
+        pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(Ke):
+        q.copy_(q_h, non_blocking=True)
+        t.copy_(t_h, non_blocking=True)
+        sl.copy_(sl_h, non_blocking=True)
+        pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+
+    # ---- max over ranks
+    vals = torch.tensor([total_ms, e2e_ms, float(np.mean(split_ms))], dtype=torch.float64,
+                        device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
+    total_ms, e2e_ms, split_avg_ms = [float(x) for x in vals.tolist()]
+    if rank != 0:
+        return
+    ms_per_step = total_ms / K
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    e2e_value = world * kv_bytes / (e2e_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    achieved = kv_bytes / (split_avg_ms * 1e-3) / 1e9
+    opts_key = f"part={args.partition_tokens},compute={args.compute}"
+    traffic = recorded_traffic(w.name, opts_key)
+    cpu = None
+    if args.cpu_baseline_s > 0 and world == 1:
+        gbs, dt, pairs, threads = oracle_sample(w, args.cpu_baseline_s)
+        toks = int(w.cache_seqlens[pairs[:, 0]].astype(np.int64).sum())
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{len(pairs)} of {w.B * w.H} (sequence, query head) outputs, "
+                         f"{toks} cached tokens, {dt:.1f} s"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "tokens_per_s": round(world * w.B / (ms_per_step * 1e-3), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic", "config": workload_config(w, args),
+        "gpu_launches": 2 * K,
+        "roofline": {"bound": "hbm", "kernel": "pa_split_kernel",
+                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": kv_bytes,
+                     "avg_launch_us": round(split_avg_ms * 1e3, 3)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_ms * 1e3, 2)},
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--compute", default="mma", choices=["mma", "simt", "auto"])
+    ap.add_argument("--cpu-baseline-s", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline sample (0 = skip)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import __graft_entry__
+
+    __graft_entry__.build()
+    if world > 1:
+        import torch
+
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * pagedgqa.h -- C ABI of the paged grouped-query decode attention library
+ * (libpagedgqa.so, CUDA, sm_103a).
+ *
+ * The operation (one decode step, one query token per sequence):
+ *
+ *   for every sequence b < B and query head h < H, with G = H / Hkv and
+ *   kv head j = floor(h / G):
+ *     out[b,h,:] = softmax_t( scale * q[b,h,:] . K_b[t,:] ) V_b[t,:],
+ *                  t = 0 .. cache_seqlens[b]-1
+ *   where K_b[t] / V_b[t] is row t % bs of physical block
+ *   block_table[b][t / bs], kv head j, of the shared K/V pool.
+ *
+ * Sources, by page and section:
+ *   - "Paged Attention Kernel Architecture for BI-V100": section 1 (problem
+ *     definition), section 2 (split-KV partitions holding a (max_score,
+ *     exp_sum, weighted_v) state merged by a combine op; a separate merge
+ *     kernel), section 4 (one CTA per kv head serves all G query heads),
+ *     section 6 (phase 1 partitioned attention, phase 2 cross-partition
+ *     reduction).
+ *   - "Paged attention" (Hugging Face Transformers docs), decoding path:
+ *     block_table of shape (batch, max_blocks_per_seq) of physical block
+ *     ids with -1 for unallocated blocks; cache_seqlens is the key length;
+ *     the cache is indexed and then updated in place.
+ *   - "v10_triton_paged_gqa", Core Principle: block-table translation,
+ *     valid-token mask, running max / exp-sum / accumulator recurrence;
+ *     the captured launch is replayed while inputs change in place.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers to dense, row-major memory the
+ *     caller owns; the library allocates nothing and keeps no per-call state.
+ *   - Every pointer must be 16-byte aligned.
+ *   - Layouts (dt = fp16 or bf16, the same for q, k and v):
+ *       q              [B, H, d]            dt
+ *       k_cache        [P, bs, Hkv, d]      dt   (P = num_blocks)
+ *       v_cache        [P, bs, Hkv, d]      dt
+ *       block_table    [B, max_blocks_per_seq] int32, -1 = unallocated
+ *       cache_seqlens  [B]                  int32
+ *       out            [B, H, d]            float32
+ *       k_new, v_new   [B, Hkv, d]          dt
+ *   - Supported: d in {64, 128, 256}; bs in {16, 32, 64}; H % Hkv == 0 and
+ *     G = H / Hkv <= 8; 0 <= B <= PA_MAX_BATCH (B == 0 is a no-op).
+ *   - Work is enqueued on `stream` (NULL = legacy default stream).  No entry
+ *     point synchronises, allocates, or picks a launch shape from device
+ *     data, so pa_decode and pa_cache_append can be captured in a CUDA graph
+ *     and replayed after the inputs are changed in place.  The first call on
+ *     a device performs one-time host-side setup (kernel attributes,
+ *     occupancy query); make it before beginning a stream capture.
+ *   - Host-side errors are reported by the return code before anything is
+ *     enqueued.  Data errors found on the device never trap and never wait:
+ *     they set a bit in the status word kept at the start of the workspace
+ *     and make the affected outputs NaN (see pa_read_status).
+ */
+#ifndef PAGEDGQA_H
+#define PAGEDGQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st* pa_stream_t;
+
+#define PA_MAX_BATCH 8192
+
+/* Return codes (host side). */
+#define PA_OK 0
+#define PA_ERR_NULL (-1)        /* a required pointer is NULL */
+#define PA_ERR_SHAPE (-2)       /* unsupported or inconsistent shape / dtype */
+#define PA_ERR_ALIGN (-3)       /* a pointer is not 16-byte aligned */
+#define PA_ERR_WORKSPACE (-4)   /* workspace smaller than pa_workspace_size */
+#define PA_ERR_CUDA (-5)        /* a CUDA runtime/driver call failed */
+#define PA_ERR_OPTION (-6)      /* invalid pa_options value */
+
+/* Device status bits (sticky in the workspace status word). */
+#define PA_STATUS_BAD_BLOCK 0x1u   /* a table entry inside a sequence's length is
+                                      -1 or >= num_blocks; that (b, kv head)'s
+                                      output heads are NaN */
+#define PA_STATUS_BAD_SEQLEN 0x2u  /* cache_seqlens[b] < 0 or > max_blocks_per_seq*bs;
+                                      all of sequence b's outputs are NaN */
+#define PA_STATUS_TIMEOUT 0x4u     /* a pipeline wait gave up (never expected);
+                                      outputs of that step are unreliable */
+#define PA_STATUS_NO_SLOT 0x8u     /* pa_cache_append: position cache_seqlens[b]
+                                      has no table column or an unmapped entry;
+                                      nothing was written for that sequence */
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+typedef enum {
+  PA_COMPUTE_AUTO = 0, /* library choice (tensor-core mma) */
+  PA_COMPUTE_SIMT = 1, /* fp32 FMA on CUDA cores */
+  PA_COMPUTE_MMA = 2   /* mma.sync m16n8k16 tensor-core products, fp32 accumulate */
+} pa_compute;
+
+typedef struct pa_shape {
+  int32_t batch;              /* B: sequences, one query token each */
+  int32_t num_heads;          /* H: query heads */
+  int32_t num_kv_heads;       /* Hkv: kv heads, H % Hkv == 0 */
+  int32_t head_dim;           /* d */
+  int32_t block_size;         /* bs: tokens per physical block */
+  int32_t max_blocks_per_seq; /* columns of block_table */
+  int32_t num_blocks;         /* P: physical blocks in the pool */
+  int32_t dtype;              /* pa_dtype of q, k_cache, v_cache, k_new, v_new */
+} pa_shape;
+
+typedef struct pa_options {
+  /* Split-KV partition size in tokens.  0: balanced split chosen on the
+   * device each step from the actual lengths (every CTA of the persistent
+   * grid gets an equal share of the (sequence, kv head, block) work).
+   * > 0: fixed partitions of this many tokens (a multiple of block_size),
+   * e.g. 512 as in the BI-V100 design's PARTITION_SIZE. */
+  int32_t partition_tokens;
+  int32_t compute;   /* pa_compute */
+  int32_t num_ctas;  /* persistent grid size; 0 = one full wave of resident
+                        CTAs on the current device.  Setting it makes
+                        pa_workspace_size independent of the device. */
+  int32_t stages;    /* K/V pipeline stages per CTA; 0 = library choice */
+} pa_options;
+
+/* Bytes of workspace pa_decode / pa_decode_split / pa_decode_merge /
+ * pa_cache_append need for this shape and these options (NULL = defaults).
+ * The workspace holds the status word, the per-step length prefix sums and
+ * the split-KV partial states (m, l, weighted_v[d]) in float32.  The caller
+ * allocates it once, zero-fills it once (the status word must start at 0),
+ * and may reuse it for every later call with the same shape and options.
+ * Two calls in flight at the same time must not share a workspace.
+ * Returns PA_OK and writes *bytes, or a negative code.  With
+ * options->num_ctas == 0 the size depends on the current device's SM count. */
+int pa_workspace_size(const pa_shape* shape, const pa_options* options, size_t* bytes);
+
+/* One decode step: out = paged GQA decode attention (formula at the top).
+ * Launches the split kernel (phase 1: each persistent CTA streams its share
+ * of (sequence, kv head, block) work through a multi-stage TMA pipeline and
+ * computes all G query heads of the kv head at once) and, when some
+ * sequence was split across CTAs, the merge kernel (phase 2: combine op over
+ * that sequence's pieces).  Sequences with cache_seqlens[b] == 0 get out = 0.
+ * scale multiplies q . k (typically 1/sqrt(d)).  Table entries at or beyond
+ * ceil(cache_seqlens[b] / bs) are never read.
+ * Errors: PA_ERR_* before any launch; device-side data errors as status
+ * bits (PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_SEQLEN). */
+int pa_decode(const pa_shape* shape, const pa_options* options, const void* q,
+              const void* k_cache, const void* v_cache, const int32_t* block_table,
+              const int32_t* cache_seqlens, float scale, float* out, void* workspace,
+              size_t workspace_bytes, pa_stream_t stream);
+
+/* Phase 1 of pa_decode alone (same arguments).  Writes the outputs of every
+ * sequence handled whole by one CTA and the partial states of the others. */
+int pa_decode_split(const pa_shape* shape, const pa_options* options, const void* q,
+                    const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    const int32_t* cache_seqlens, float scale, float* out, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream);
+
+/* Phase 2 of pa_decode alone (same arguments; q, k_cache and v_cache are not
+ * read).  Must follow pa_decode_split of the same step on the same stream. */
+int pa_decode_merge(const pa_shape* shape, const pa_options* options, const void* q,
+                    const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    const int32_t* cache_seqlens, float scale, float* out, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream);
+
+/* Append one new token per sequence to the paged cache, in place: for every
+ * b and kv head j, k_new[b,j,:] and v_new[b,j,:] are copied bit for bit to
+ * row (cache_seqlens[b] % bs) of physical block
+ * block_table[b][cache_seqlens[b] / bs] (the Hugging Face decoding-path
+ * example: the next token of a sequence goes into the block that holds
+ * position cache_seqlens[b]).  cache_seqlens is NOT incremented: the caller
+ * does that (in place, so a captured graph stays valid).  A sequence whose
+ * position has no table column or an unmapped entry gets no write and sets
+ * PA_STATUS_NO_SLOT.  The workspace only needs room for the status word
+ * (any workspace sized for pa_decode works). */
+int pa_cache_append(const pa_shape* shape, const void* k_new, const void* v_new,
+                    void* k_cache, void* v_cache, const int32_t* block_table,
+                    const int32_t* cache_seqlens, void* workspace, size_t workspace_bytes,
+                    pa_stream_t stream);
+
+/* Copy the status word of `workspace` to *flags (host), then clear it.
+ * Synchronises `stream`.  Returns PA_OK or PA_ERR_*. */
+int pa_read_status(void* workspace, uint32_t* flags, pa_stream_t stream);
+
+/* Text for a return code (negative) or a status bit set (positive). */
+const char* pa_status_string(int code);
+
+/* Host replica of the device work split, for inspection and tests.  Given
+ * host lengths, lists the pieces CTA `cta` of a grid of `num_ctas` processes:
+ * pieces[5*i .. 5*i+4] = (b, kv_head, first_block, end_block, slot) where
+ * slot is the workspace slot of its partial state, or -1 when the piece is a
+ * whole sequence/kv-head whose output the CTA writes directly.  Returns the
+ * number of pieces (at most max_pieces are written), or a negative code. */
+int pa_plan_pieces(const pa_shape* shape, const pa_options* options,
+                   const int32_t* cache_seqlens_host, int32_t num_ctas, int32_t cta,
+                   int32_t* pieces, int32_t max_pieces);
+
+/* Host replica of the merge kernel's piece discovery.  Merge index `seg`
+ * (balanced split: 0 <= seg < num_ctas, the segment that begins in split CTA
+ * seg and continues past it; fixed split: 0 <= seg < B * Hkv, segment
+ * (seg / Hkv, seg % Hkv)) combines the pieces in slots[0..n-1], in this
+ * order, into out[b_j[0], heads of kv head b_j[1], :].  Returns n (0 when that
+ * index merges nothing; b_j is then (-1, -1)) or a negative code. */
+int pa_plan_merge(const pa_shape* shape, const pa_options* options,
+                  const int32_t* cache_seqlens_host, int32_t num_ctas, int32_t seg,
+                  int32_t* b_j, int32_t* slots, int32_t max_slots);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDGQA_H */

@@ -1,0 +1,297 @@
+"""ctypes binding of libpagedgqa.so, one Python function per C entry point.
+
+Argument marshalling only: shapes are read off the torch tensors, pointers
+and the current CUDA stream are passed through, return codes become
+exceptions.  Every step of the computation runs in the library's kernels;
+there is no other code path.  If the library is not built, every call raises
+``LibraryNotBuilt``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedgqa.so")
+
+PA_OK = 0
+PA_ERR_NULL = -1
+PA_ERR_SHAPE = -2
+PA_ERR_ALIGN = -3
+PA_ERR_WORKSPACE = -4
+PA_ERR_CUDA = -5
+PA_ERR_OPTION = -6
+
+PA_STATUS_BAD_BLOCK = 0x1
+PA_STATUS_BAD_SEQLEN = 0x2
+PA_STATUS_TIMEOUT = 0x4
+PA_STATUS_NO_SLOT = 0x8
+
+PA_F16 = 0
+PA_BF16 = 1
+
+PA_COMPUTE_AUTO = 0
+PA_COMPUTE_SIMT = 1
+PA_COMPUTE_MMA = 2
+_COMPUTE = {"auto": PA_COMPUTE_AUTO, "simt": PA_COMPUTE_SIMT, "mma": PA_COMPUTE_MMA}
+
+# Every symbol include/pagedgqa.h declares.
+EXPORTS = ("pa_workspace_size", "pa_decode", "pa_decode_split", "pa_decode_merge",
+           "pa_cache_append", "pa_read_status", "pa_status_string", "pa_plan_pieces",
+           "pa_plan_merge", "pa_version")
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class PagedGQAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (code {code})")
+
+
+class pa_shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class pa_options(ctypes.Structure):
+    _fields_ = [("partition_tokens", ctypes.c_int32), ("compute", ctypes.c_int32),
+                ("num_ctas", ctypes.c_int32), ("stages", ctypes.c_int32)]
+
+
+def options(partition_tokens: int = 0, compute: str = "auto", num_ctas: int = 0,
+            stages: int = 0) -> pa_options:
+    return pa_options(int(partition_tokens), _COMPUTE[compute] if isinstance(compute, str)
+                      else int(compute), int(num_ctas), int(stages))
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded library (raises LibraryNotBuilt if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise LibraryNotBuilt(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m paged_gqa_decode_pa_gb300.build` (or __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.c_void_p
+        SP = ctypes.POINTER(pa_shape)
+        OP = ctypes.POINTER(pa_options)
+        i32 = ctypes.c_int32
+        L.pa_workspace_size.argtypes = [SP, OP, ctypes.POINTER(ctypes.c_size_t)]
+        L.pa_workspace_size.restype = ctypes.c_int
+        for name in ("pa_decode", "pa_decode_split", "pa_decode_merge"):
+            fn = getattr(L, name)
+            fn.argtypes = [SP, OP, P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_size_t, P]
+            fn.restype = ctypes.c_int
+        L.pa_cache_append.argtypes = [SP, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.pa_cache_append.restype = ctypes.c_int
+        L.pa_read_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+        L.pa_read_status.restype = ctypes.c_int
+        L.pa_status_string.argtypes = [ctypes.c_int]
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_plan_pieces.argtypes = [SP, OP, P, i32, i32, P, i32]
+        L.pa_plan_pieces.restype = ctypes.c_int
+        L.pa_plan_merge.argtypes = [SP, OP, P, i32, i32, P, P, i32]
+        L.pa_plan_merge.restype = ctypes.c_int
+        L.pa_version.argtypes = []
+        L.pa_version.restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def status_string(code: int) -> str:
+    try:
+        return lib().pa_status_string(int(code)).decode()
+    except LibraryNotBuilt:
+        return f"code {code}"
+
+
+def _check(rc: int, where: str):
+    if rc != PA_OK:
+        raise PagedGQAError(rc, where)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"q/k/v must be float16 or bfloat16, got {t.dtype}")
+
+
+def shape_of(q, k_cache, block_table) -> pa_shape:
+    """pa_shape from q [B,H,d], k_cache [P,bs,Hkv,d], block_table [B,maxblk]."""
+    B, H, d = q.shape
+    P, bs, Hkv, d2 = k_cache.shape
+    if d2 != d or block_table.shape[0] != B:
+        raise ValueError("inconsistent q / k_cache / block_table shapes")
+    return pa_shape(B, H, Hkv, d, bs, block_table.shape[1], P, _dtype_code(q))
+
+
+def _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out):
+    import torch
+
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_table", block_table), ("cache_seqlens", cache_seqlens),
+                    ("out", out)):
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if k_cache is not None and (k_cache.dtype != q.dtype or v_cache.dtype != q.dtype
+                                or v_cache.shape != k_cache.shape):
+        raise ValueError("q, k_cache and v_cache must share dtype; k/v shapes must match")
+    if block_table.dtype != torch.int32 or cache_seqlens.dtype != torch.int32:
+        raise TypeError("block_table and cache_seqlens must be int32")
+    if out is not None and (out.dtype != torch.float32 or tuple(out.shape) != tuple(q.shape)):
+        raise TypeError("out must be float32 with q's shape [B, H, d]")
+
+
+def pa_workspace_size(shape: pa_shape, opts: Optional[pa_options] = None) -> int:
+    n = ctypes.c_size_t(0)
+    rc = lib().pa_workspace_size(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                                 ctypes.byref(n))
+    _check(rc, "pa_workspace_size")
+    return int(n.value)
+
+
+def alloc_workspace(shape: pa_shape, opts: Optional[pa_options] = None, device=None):
+    """Zero-filled device workspace of pa_workspace_size bytes (torch uint8)."""
+    import torch
+
+    return torch.zeros(pa_workspace_size(shape, opts), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def _decode_call(name, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                 workspace, opts, stream):
+    _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out)
+    shape = shape_of(q, k_cache, block_table)
+    fn = getattr(lib(), name)
+    rc = fn(ctypes.byref(shape), ctypes.byref(opts) if opts else None, _ptr(q), _ptr(k_cache),
+            _ptr(v_cache), _ptr(block_table), _ptr(cache_seqlens), float(scale), _ptr(out),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, name)
+
+
+def pa_decode(q, k_cache, v_cache, block_table, cache_seqlens, scale, out, workspace,
+              opts: Optional[pa_options] = None, stream=None) -> None:
+    """out[B,H,d] (fp32) = paged GQA decode attention; see include/pagedgqa.h."""
+    _decode_call("pa_decode", q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                 workspace, opts, stream)
+
+
+def pa_decode_split(q, k_cache, v_cache, block_table, cache_seqlens, scale, out, workspace,
+                    opts: Optional[pa_options] = None, stream=None) -> None:
+    _decode_call("pa_decode_split", q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                 workspace, opts, stream)
+
+
+def pa_decode_merge(q, k_cache, v_cache, block_table, cache_seqlens, scale, out, workspace,
+                    opts: Optional[pa_options] = None, stream=None) -> None:
+    _decode_call("pa_decode_merge", q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                 workspace, opts, stream)
+
+
+def pa_cache_append(k_new, v_new, k_cache, v_cache, block_table, cache_seqlens, workspace,
+                    stream=None) -> None:
+    """Write k_new/v_new [B,Hkv,d] at position cache_seqlens[b] (in place)."""
+    import torch
+
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache),
+                    ("v_cache", v_cache), ("block_table", block_table),
+                    ("cache_seqlens", cache_seqlens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k_new.dtype != k_cache.dtype or v_new.dtype != k_cache.dtype:
+        raise TypeError("k_new/v_new must have the cache dtype")
+    if block_table.dtype != torch.int32 or cache_seqlens.dtype != torch.int32:
+        raise TypeError("block_table and cache_seqlens must be int32")
+    P, bs, Hkv, d = k_cache.shape
+    B = block_table.shape[0]
+    if tuple(k_new.shape) != (B, Hkv, d) or tuple(v_new.shape) != (B, Hkv, d):
+        raise ValueError("k_new/v_new must be [B, Hkv, d]")
+    shape = pa_shape(B, Hkv, Hkv, d, bs, block_table.shape[1], P, _dtype_code(k_cache))
+    rc = lib().pa_cache_append(ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                               _ptr(v_cache), _ptr(block_table), _ptr(cache_seqlens),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream))
+    _check(rc, "pa_cache_append")
+
+
+def pa_read_status(workspace, stream=None) -> int:
+    """Read and clear the sticky device status bits (synchronises the stream)."""
+    v = ctypes.c_uint32(0)
+    rc = lib().pa_read_status(_ptr(workspace), ctypes.byref(v), _stream(stream))
+    _check(rc, "pa_read_status")
+    return int(v.value)
+
+
+def pa_plan_pieces(shape: pa_shape, opts: Optional[pa_options], lens_host, num_ctas: int,
+                   cta: int):
+    """Host replica of the work split: list of (b, j, blk0, blk1, slot)."""
+    import numpy as np
+
+    lens = np.ascontiguousarray(lens_host, dtype=np.int32)
+    n = lib().pa_plan_pieces(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                             lens.ctypes.data, int(num_ctas), int(cta), None, 0)
+    if n < 0:
+        _check(n, "pa_plan_pieces")
+    buf = np.zeros((max(n, 1), 5), dtype=np.int32)
+    m = lib().pa_plan_pieces(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                             lens.ctypes.data, int(num_ctas), int(cta), buf.ctypes.data, n)
+    assert m == n
+    return [tuple(int(x) for x in row) for row in buf[:n]]
+
+
+def pa_plan_merge(shape: pa_shape, opts: Optional[pa_options], lens_host, num_ctas: int,
+                  seg: int, max_slots: int = 1 << 16):
+    """Host replica of merge index `seg`: ((b, j), [slots]) or None."""
+    import numpy as np
+
+    lens = np.ascontiguousarray(lens_host, dtype=np.int32)
+    bj = np.zeros(2, dtype=np.int32)
+    slots = np.zeros(max_slots, dtype=np.int32)
+    n = lib().pa_plan_merge(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                            lens.ctypes.data, int(num_ctas), int(seg), bj.ctypes.data,
+                            slots.ctypes.data, max_slots)
+    if n < 0:
+        _check(n, "pa_plan_merge")
+    if n == 0:
+        return None
+    return (int(bj[0]), int(bj[1])), [int(s) for s in slots[:n]]
+
+
+def pa_version() -> int:
+    return int(lib().pa_version())

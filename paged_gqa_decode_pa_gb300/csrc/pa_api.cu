@@ -1,0 +1,631 @@
+// pa_api.cu -- the C ABI of libpagedgqa.so (see include/pagedgqa.h): argument
+// checks, per-device setup, TMA tensor maps, and the phase-2 merge and cache
+// append kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "pa_kernels.cuh"
+#include "pa_ptx.cuh"
+#include "pagedgqa.h"
+
+using namespace pa;
+
+namespace {
+
+// ------------------------------------------------------------------ merge
+
+// Phase 2: combine the partial states of every segment that the split kernel
+// cut across CTAs (or partitions).  Block (g * D/64 + dc, q) handles head g,
+// dims [64 dc, 64 dc + 64) of the split segments q*16 .. q*16+15 (balanced:
+// the segment beginning in split CTA seg; fixed: segment (b, j) = seg).
+// 256 threads = 4 piece groups x 64 dims; pieces are visited in a fixed
+// order, so the result is deterministic.  Combine op: "Paged Attention Kernel
+// Architecture for BI-V100", section 2, Level 1 binary op / Level 3.
+__global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs a) {
+  const int nchunk = a.D / 64;
+  const int g = blockIdx.x / nchunk, dc = blockIdx.x % nchunk;
+  const int tid = threadIdx.x;
+  const int pg = tid >> 6, dl = tid & 63;
+  const int dim = dc * 64 + dl;
+  __shared__ float red[4][64];
+  __shared__ float wred[kMergeThreads / 32];
+  __shared__ float sM, sL;
+  const int nseg = a.part_blocks == 0 ? a.num_ctas : a.B * a.Hkv;
+  const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas};
+  for (int si = 0; si < kMergeSegs; ++si) {
+    const int seg = blockIdx.y * kMergeSegs + si;
+    if (seg >= nseg) break;
+    int4 desc = make_int4(-1, 0, 0, 0);
+    if (a.part_blocks == 0) desc = a.ws_desc[seg];
+    const MergeSeg ms = merge_segment(sched, seg, desc.x, desc.y, desc.z, desc.w, a.ws_pre);
+    const int np = ms.np;
+    if (np == 0) continue;
+    const int b = ms.b, j = ms.j;
+    auto slot_of = [&](int p) -> int64_t { return ms.slot(p); };
+    // M = max_p m_p
+    float m = -INFINITY;
+    for (int p = tid; p < np; p += kMergeThreads) m = fmaxf(m, a.ws_ml[(slot_of(p) * a.G + g) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((tid & 31) == 0) wred[tid >> 5] = m;
+    __syncthreads();
+    if (tid == 0) {
+      float x = wred[0];
+      for (int w = 1; w < kMergeThreads / 32; ++w) x = fmaxf(x, wred[w]);
+      sM = x;
+    }
+    __syncthreads();
+    const float M = sM;
+    // L = sum_p l_p 2^(m_p - M)
+    float l = 0.f;
+    for (int p = tid; p < np; p += kMergeThreads) {
+      const int64_t s = slot_of(p);
+      l += a.ws_ml[(s * a.G + g) * 2 + 1] * ex2(a.ws_ml[(s * a.G + g) * 2] - M);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    __syncthreads();  // wred reuse
+    if ((tid & 31) == 0) wred[tid >> 5] = l;
+    __syncthreads();
+    if (tid == 0) {
+      float x = 0.f;
+      for (int w = 0; w < kMergeThreads / 32; ++w) x += wred[w];
+      sL = x;
+    }
+    // out = sum_p 2^(m_p - M) acc_p / L
+    float acc = 0.f;
+    for (int p = pg; p < np; p += 4) {
+      const int64_t s = slot_of(p);
+      acc = fmaf(ex2(a.ws_ml[(s * a.G + g) * 2] - M), a.ws_acc[(s * a.G + g) * a.D + dim], acc);
+    }
+    red[pg][dl] = acc;
+    __syncthreads();
+    if (pg == 0) {
+      const float o = (red[0][dl] + red[1][dl]) + (red[2][dl] + red[3][dl]);
+      a.out[((int64_t)b * a.H + (int64_t)j * a.G + g) * a.D + dim] = o / sL;
+    }
+    __syncthreads();
+  }
+}
+
+// --------------------------------------------------------------- append
+
+// Copy k_new / v_new rows of sequence b = blockIdx.x into the slot of
+// position cache_seqlens[b] ("Paged attention", decoding path example).
+__global__ void pa_append_kernel(const AppendArgs a) {
+  const int b = blockIdx.x;
+  const int32_t pos = __ldg(a.seqlens + b);
+  bool ok = pos >= 0 && (int64_t)pos < (int64_t)a.maxblk * a.bs;
+  int32_t phys = -1;
+  if (ok) phys = __ldg(a.table + (int64_t)b * a.maxblk + pos / a.bs);
+  ok = ok && phys >= 0 && phys < a.P;
+  if (!ok) {
+    if (threadIdx.x == 0) atomicOr(a.status, PA_STATUS_NO_SLOT);
+    return;
+  }
+  const int row = pos % a.bs;
+  const int units = a.D / 8;  // 16-byte units per row
+  for (int u = threadIdx.x; u < a.Hkv * units; u += blockDim.x) {
+    const int j = u / units, e = u % units;
+    const int64_t dst = (((int64_t)phys * a.bs + row) * a.Hkv + j) * a.D + (int64_t)e * 8;
+    const int64_t src = ((int64_t)b * a.Hkv + j) * a.D + (int64_t)e * 8;
+    *reinterpret_cast<uint4*>(a.k_cache + dst) = __ldg(reinterpret_cast<const uint4*>(a.k_new + src));
+    *reinterpret_cast<uint4*>(a.v_cache + dst) = __ldg(reinterpret_cast<const uint4*>(a.v_new + src));
+  }
+}
+
+// ----------------------------------------------------------- host helpers
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kHeaderBytes = 256;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+struct FuncCache {
+  const void* fn;
+  int dev;
+  size_t smem;
+  int occ;
+};
+constexpr int kFuncCacheSize = 256;
+FuncCache g_funcs[kFuncCacheSize];
+int g_nfuncs = 0;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const pa_shape* s) {
+  if (!s) return PA_ERR_NULL;
+  if (s->batch < 0 || s->batch > PA_MAX_BATCH) return PA_ERR_SHAPE;
+  if (s->num_heads < 1 || s->num_kv_heads < 1) return PA_ERR_SHAPE;
+  if (s->num_heads % s->num_kv_heads != 0) return PA_ERR_SHAPE;
+  const int G = s->num_heads / s->num_kv_heads;
+  if (G > kGMax) return PA_ERR_SHAPE;
+  if (s->head_dim != 64 && s->head_dim != 128 && s->head_dim != 256) return PA_ERR_SHAPE;
+  if (s->block_size != 16 && s->block_size != 32 && s->block_size != 64) return PA_ERR_SHAPE;
+  if (s->max_blocks_per_seq < 1 || s->num_blocks < 1) return PA_ERR_SHAPE;
+  if ((int64_t)s->max_blocks_per_seq * s->block_size > INT32_MAX) return PA_ERR_SHAPE;
+  if ((int64_t)s->batch * s->max_blocks_per_seq > INT32_MAX) return PA_ERR_SHAPE;
+  if (s->dtype != PA_F16 && s->dtype != PA_BF16) return PA_ERR_SHAPE;
+  return PA_OK;
+}
+
+int check_options(const pa_shape* s, const pa_options* o) {
+  if (!o) return PA_OK;
+  if (o->partition_tokens < 0) return PA_ERR_OPTION;
+  if (o->partition_tokens > 0 && o->partition_tokens % s->block_size != 0) return PA_ERR_OPTION;
+  if (o->compute < PA_COMPUTE_AUTO || o->compute > PA_COMPUTE_MMA) return PA_ERR_OPTION;
+  if (o->num_ctas < 0 || o->num_ctas > (1 << 20)) return PA_ERR_OPTION;
+  if (o->stages < 0 || o->stages == 1 || o->stages > kMaxStages) return PA_ERR_OPTION;
+  return PA_OK;
+}
+
+struct Plan {
+  int D, G, bs, mode, stages;
+  int part_blocks;
+  int grid;  // split kernel CTAs
+  size_t smem;
+  int64_t slots;
+  size_t off_pre, off_desc, off_ml, off_acc, total;
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+int choose_mode(const pa_options* o) {
+  const int c = o ? o->compute : PA_COMPUTE_AUTO;
+  return c == PA_COMPUTE_SIMT ? kSimt : kMma;
+}
+
+// Stage count: fill about half of an SM's shared memory (two CTAs per SM).
+int choose_stages(const pa_shape* s, const pa_options* o, int mode) {
+  if (o && o->stages > 0) return o->stages;
+  const int G = s->num_heads / s->num_kv_heads;
+  const SmemLayout L0 = split_smem_layout(s->head_dim, s->block_size, G, s->batch, 0, mode);
+  const int budget = 112 * 1024;
+  int S = (budget - (int)L0.total) / (int)L0.stage_bytes;
+  if (S > kMaxStages) S = kMaxStages;
+  if (S < 2) S = 2;
+  return S;
+}
+
+const void* kernel_for(int dtype, int D, int mode) {
+#define PA_PICK(T, DD)                                                                 \
+  if (D == DD) return mode == kSimt ? split_kernel_ptr<T, DD, kSimt>()                \
+                                    : split_kernel_ptr<T, DD, kMma>();
+  if (dtype == PA_BF16) {
+    PA_PICK(__nv_bfloat16, 64)
+    PA_PICK(__nv_bfloat16, 128)
+    PA_PICK(__nv_bfloat16, 256)
+  } else {
+    PA_PICK(__half, 64)
+    PA_PICK(__half, 128)
+    PA_PICK(__half, 256)
+  }
+#undef PA_PICK
+  return nullptr;
+}
+
+// Occupancy of the split kernel for this smem size on device `dev`; also
+// raises the kernel's dynamic shared-memory limit (once).
+int occupancy(const void* fn, int dev, size_t smem, int* occ_out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < g_nfuncs; ++i) {
+    if (g_funcs[i].fn == fn && g_funcs[i].dev == dev && g_funcs[i].smem == smem) {
+      *occ_out = g_funcs[i].occ;
+      return PA_OK;
+    }
+  }
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return PA_ERR_CUDA;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kSplitThreads, smem) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (occ < 1) return PA_ERR_SHAPE;
+  if (g_nfuncs < kFuncCacheSize) g_funcs[g_nfuncs++] = FuncCache{fn, dev, smem, occ};
+  *occ_out = occ;
+  return PA_OK;
+}
+
+int device_sms(int* dev_out, int* sms_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_dev[dev].ready) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PA_ERR_CUDA;
+    g_dev[dev].sms = sms;
+    g_dev[dev].ready = true;
+  }
+  *dev_out = dev;
+  *sms_out = g_dev[dev].sms;
+  return PA_OK;
+}
+
+// Sizes and offsets of everything one call needs.  `need_device` = false
+// only when options->num_ctas fixes the grid (pure host computation).
+int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  rc = check_options(s, o);
+  if (rc) return rc;
+  p->D = s->head_dim;
+  p->G = s->num_heads / s->num_kv_heads;
+  p->bs = s->block_size;
+  p->mode = choose_mode(o);
+  p->stages = choose_stages(s, o, p->mode);
+  p->part_blocks = (o && o->partition_tokens > 0) ? o->partition_tokens / s->block_size : 0;
+  const SmemLayout L = split_smem_layout(p->D, p->bs, p->G, s->batch, p->stages, p->mode);
+  p->smem = L.total;
+  if (p->smem > 227 * 1024) return PA_ERR_SHAPE;
+  const bool fixed_grid = o && o->num_ctas > 0;
+  if (fixed_grid) p->grid = o->num_ctas;
+  if (setup_kernel || !fixed_grid) {
+    int dev, sms, occ;
+    rc = device_sms(&dev, &sms);
+    if (rc) return rc;
+    const void* fn = kernel_for(s->dtype, p->D, p->mode);
+    if (!fn) return PA_ERR_SHAPE;
+    rc = occupancy(fn, dev, p->smem, &occ);
+    if (rc) return rc;
+    if (!fixed_grid) p->grid = sms * occ;
+  }
+  if (p->part_blocks == 0) {
+    p->slots = 2 * (int64_t)p->grid;
+  } else {
+    const int64_t nparts = (s->max_blocks_per_seq + p->part_blocks - 1) / p->part_blocks;
+    p->slots = (int64_t)s->batch * s->num_kv_heads * nparts;
+  }
+  size_t off = kHeaderBytes;
+  p->off_pre = off;
+  off = round256(off + sizeof(int32_t) * (size_t)(s->batch + 1));
+  p->off_desc = off;
+  off = round256(off + sizeof(int4) * (size_t)p->grid);
+  p->off_ml = off;
+  off = round256(off + sizeof(float) * 2 * (size_t)p->slots * p->G);
+  p->off_acc = off;
+  off = round256(off + sizeof(float) * (size_t)p->slots * p->G * p->D);
+  p->total = off;
+  return PA_OK;
+}
+
+int get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return PA_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return PA_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return PA_OK;
+}
+
+// 4-D map over a [P, bs, Hkv, D] pool: dims (D, Hkv, bs, P), box (64, 1, bs, 1),
+// 128-byte swizzle.  One box = 64 dims of the bs rows of one kv head of one
+// physical block.
+int make_pool_map(CUtensorMap* map, const void* pool, const pa_shape* s) {
+  const uint64_t D = (uint64_t)s->head_dim, Hkv = (uint64_t)s->num_kv_heads;
+  const uint64_t bs = (uint64_t)s->block_size, P = (uint64_t)s->num_blocks;
+  cuuint64_t dims[4] = {D, Hkv, bs, P};
+  cuuint64_t strides[3] = {D * 2, Hkv * D * 2, bs * Hkv * D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)bs, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt =
+      s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = g_encode(map, dt, 4, const_cast<void*>(pool), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+struct Call {
+  Plan plan;
+  SplitArgs sa;
+  MergeArgs ma;
+};
+
+int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k_cache,
+            const void* v_cache, const int32_t* block_table, const int32_t* cache_seqlens,
+            float scale, float* out, void* workspace, size_t workspace_bytes, bool need_kv,
+            Call* c) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (!block_table || !cache_seqlens || !out || !workspace) return PA_ERR_NULL;
+  if (need_kv && (!q || !k_cache || !v_cache)) return PA_ERR_NULL;
+  if (!aligned16(block_table) || !aligned16(cache_seqlens) || !aligned16(out) ||
+      !aligned16(workspace))
+    return PA_ERR_ALIGN;
+  if (need_kv && (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)))
+    return PA_ERR_ALIGN;
+  if (!(scale == scale)) return PA_ERR_SHAPE;  // NaN scale
+  rc = make_plan(s, o, false, &c->plan);
+  if (rc) return rc;
+  if (workspace_bytes < c->plan.total) return PA_ERR_WORKSPACE;
+  if (need_kv) {
+    // kernel attributes (dynamic shared memory limit) before the first launch
+    rc = make_plan(s, o, true, &c->plan);
+    if (rc) return rc;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const Plan& p = c->plan;
+  SplitArgs& a = c->sa;
+  a.q = static_cast<const uint16_t*>(q);
+  a.table = block_table;
+  a.seqlens = cache_seqlens;
+  a.out = out;
+  a.ws_ml = reinterpret_cast<float*>(ws + p.off_ml);
+  a.ws_acc = reinterpret_cast<float*>(ws + p.off_acc);
+  a.ws_pre = reinterpret_cast<int32_t*>(ws + p.off_pre);
+  a.ws_desc = reinterpret_cast<int4*>(ws + p.off_desc);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.B = s->batch;
+  a.H = s->num_heads;
+  a.Hkv = s->num_kv_heads;
+  a.G = p.G;
+  a.bs = s->block_size;
+  a.maxblk = s->max_blocks_per_seq;
+  a.P = s->num_blocks;
+  a.part_blocks = p.part_blocks;
+  a.stages = p.stages;
+  a.qscale = scale * 1.4426950408889634f;  // log2(e)
+  MergeArgs& m = c->ma;
+  m.seqlens = cache_seqlens;
+  m.out = out;
+  m.ws_ml = a.ws_ml;
+  m.ws_acc = a.ws_acc;
+  m.ws_pre = a.ws_pre;
+  m.ws_desc = a.ws_desc;
+  m.B = a.B;
+  m.H = a.H;
+  m.Hkv = a.Hkv;
+  m.G = a.G;
+  m.D = p.D;
+  m.bs = a.bs;
+  m.maxblk = a.maxblk;
+  m.part_blocks = a.part_blocks;
+  m.num_ctas = p.grid;
+  return PA_OK;
+}
+
+int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cache, Call* c,
+                       cudaStream_t stream) {
+  int rc = get_encoder();
+  if (rc) return rc;
+  alignas(64) CUtensorMap tmk;
+  alignas(64) CUtensorMap tmv;
+  rc = make_pool_map(&tmk, k_cache, s);
+  if (rc) return rc;
+  rc = make_pool_map(&tmv, v_cache, s);
+  if (rc) return rc;
+  const Plan& p = c->plan;
+  cudaError_t e = cudaErrorInvalidValue;
+#define PA_LAUNCH(T, DD)                                                                      \
+  if (p.D == DD)                                                                              \
+    e = p.mode == kSimt ? launch_split<T, DD, kSimt>(tmk, tmv, c->sa, p.grid, p.smem, stream) \
+                        : launch_split<T, DD, kMma>(tmk, tmv, c->sa, p.grid, p.smem, stream);
+  if (s->dtype == PA_BF16) {
+    PA_LAUNCH(__nv_bfloat16, 64)
+    PA_LAUNCH(__nv_bfloat16, 128)
+    PA_LAUNCH(__nv_bfloat16, 256)
+  } else {
+    PA_LAUNCH(__half, 64)
+    PA_LAUNCH(__half, 128)
+    PA_LAUNCH(__half, 256)
+  }
+#undef PA_LAUNCH
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int launch_merge_phase(Call* c, cudaStream_t stream) {
+  const Plan& p = c->plan;
+  const int nseg = p.part_blocks == 0 ? p.grid : c->sa.B * c->sa.Hkv;
+  dim3 grid(p.G * (p.D / 64), (nseg + kMergeSegs - 1) / kMergeSegs);
+  pa_merge_kernel<<<grid, kMergeThreads, 0, stream>>>(c->ma);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+int pa_workspace_size(const pa_shape* shape, const pa_options* options, size_t* bytes) {
+  if (!shape || !bytes) return PA_ERR_NULL;
+  Plan p;
+  int rc = make_plan(shape, options, false, &p);
+  if (rc) return rc;
+  *bytes = p.total;
+  return PA_OK;
+}
+
+int pa_decode_split(const pa_shape* shape, const pa_options* options, const void* q,
+                    const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    const int32_t* cache_seqlens, float scale, float* out, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream) {
+  if (shape && shape->batch == 0 && check_shape(shape) == PA_OK) return PA_OK;
+  Call c;
+  int rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                   workspace, workspace_bytes, true, &c);
+  if (rc) return rc;
+  return launch_split_phase(shape, k_cache, v_cache, &c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_decode_merge(const pa_shape* shape, const pa_options* options, const void* q,
+                    const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    const int32_t* cache_seqlens, float scale, float* out, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream) {
+  if (shape && shape->batch == 0 && check_shape(shape) == PA_OK) return PA_OK;
+  Call c;
+  int rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                   workspace, workspace_bytes, false, &c);
+  if (rc) return rc;
+  return launch_merge_phase(&c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_decode(const pa_shape* shape, const pa_options* options, const void* q,
+              const void* k_cache, const void* v_cache, const int32_t* block_table,
+              const int32_t* cache_seqlens, float scale, float* out, void* workspace,
+              size_t workspace_bytes, pa_stream_t stream) {
+  if (shape && shape->batch == 0 && check_shape(shape) == PA_OK) return PA_OK;
+  Call c;
+  int rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                   workspace, workspace_bytes, true, &c);
+  if (rc) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = launch_split_phase(shape, k_cache, v_cache, &c, st);
+  if (rc) return rc;
+  return launch_merge_phase(&c, st);
+}
+
+int pa_cache_append(const pa_shape* shape, const void* k_new, const void* v_new, void* k_cache,
+                    void* v_cache, const int32_t* block_table, const int32_t* cache_seqlens,
+                    void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !cache_seqlens || !workspace)
+    return PA_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(block_table) || !aligned16(cache_seqlens) || !aligned16(workspace))
+    return PA_ERR_ALIGN;
+  if (workspace_bytes < kHeaderBytes) return PA_ERR_WORKSPACE;
+  if (shape->batch == 0) return PA_OK;
+  AppendArgs a;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.k_cache = static_cast<uint16_t*>(k_cache);
+  a.v_cache = static_cast<uint16_t*>(v_cache);
+  a.table = block_table;
+  a.seqlens = cache_seqlens;
+  a.status = static_cast<uint32_t*>(workspace);
+  a.B = shape->batch;
+  a.Hkv = shape->num_kv_heads;
+  a.D = shape->head_dim;
+  a.bs = shape->block_size;
+  a.maxblk = shape->max_blocks_per_seq;
+  a.P = shape->num_blocks;
+  pa_append_kernel<<<shape->batch, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_read_status(void* workspace, uint32_t* flags, pa_stream_t stream) {
+  if (!workspace || !flags) return PA_ERR_NULL;
+  if (!aligned16(workspace)) return PA_ERR_ALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof v, st) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+  *flags = v;
+  return PA_OK;
+}
+
+const char* pa_status_string(int code) {
+  switch (code) {
+    case PA_OK: return "ok";
+    case PA_ERR_NULL: return "a required pointer is NULL";
+    case PA_ERR_SHAPE: return "unsupported or inconsistent shape or dtype";
+    case PA_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case PA_ERR_WORKSPACE: return "workspace smaller than pa_workspace_size";
+    case PA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case PA_ERR_OPTION: return "invalid pa_options value";
+    default: break;
+  }
+  if (code > 0) {
+    if (code & PA_STATUS_TIMEOUT) return "device: a pipeline wait gave up";
+    if (code & PA_STATUS_BAD_SEQLEN) return "device: cache_seqlens entry out of range";
+    if (code & PA_STATUS_BAD_BLOCK) return "device: block_table entry unmapped or out of range";
+    if (code & PA_STATUS_NO_SLOT) return "device: appended token has no cache slot";
+  }
+  return "unknown code";
+}
+
+int pa_plan_pieces(const pa_shape* shape, const pa_options* options,
+                   const int32_t* cache_seqlens_host, int32_t num_ctas, int32_t cta,
+                   int32_t* pieces, int32_t max_pieces) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  rc = check_options(shape, options);
+  if (rc) return rc;
+  if (!cache_seqlens_host || (!pieces && max_pieces > 0)) return PA_ERR_NULL;
+  if (num_ctas < 1 || cta < 0 || cta >= num_ctas) return PA_ERR_OPTION;
+  const int B = shape->batch;
+  const int part_blocks =
+      (options && options->partition_tokens > 0) ? options->partition_tokens / shape->block_size : 0;
+  int32_t* pre = new int32_t[B + 1];
+  pre[0] = 0;
+  for (int b = 0; b < B; ++b)
+    pre[b + 1] = pre[b] + seq_count(seq_blocks(cache_seqlens_host[b], shape->block_size,
+                                               shape->max_blocks_per_seq),
+                                    part_blocks);
+  const SchedShape sched{B, shape->num_kv_heads, shape->block_size, shape->max_blocks_per_seq,
+                         part_blocks, num_ctas};
+  PieceIter it;
+  it.init(pre, cache_seqlens_host, sched, cta);
+  Piece pc;
+  int n = 0;
+  while (it.next(pc)) {
+    if (n < max_pieces) {
+      pieces[5 * n + 0] = pc.b;
+      pieces[5 * n + 1] = pc.j;
+      pieces[5 * n + 2] = pc.blk0;
+      pieces[5 * n + 3] = pc.blk1;
+      pieces[5 * n + 4] = pc.slot;
+    }
+    ++n;
+  }
+  delete[] pre;
+  return n;
+}
+
+int pa_plan_merge(const pa_shape* shape, const pa_options* options,
+                  const int32_t* cache_seqlens_host, int32_t num_ctas, int32_t seg,
+                  int32_t* b_j, int32_t* slots, int32_t max_slots) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  rc = check_options(shape, options);
+  if (rc) return rc;
+  if (!cache_seqlens_host || !b_j || (!slots && max_slots > 0)) return PA_ERR_NULL;
+  if (num_ctas < 1 || seg < 0) return PA_ERR_OPTION;
+  const int B = shape->batch;
+  const int part_blocks =
+      (options && options->partition_tokens > 0) ? options->partition_tokens / shape->block_size : 0;
+  const int nseg = part_blocks == 0 ? num_ctas : B * shape->num_kv_heads;
+  if (seg >= nseg) return PA_ERR_OPTION;
+  int32_t* pre = new int32_t[B + 1];
+  pre[0] = 0;
+  for (int b = 0; b < B; ++b)
+    pre[b + 1] = pre[b] + seq_count(seq_blocks(cache_seqlens_host[b], shape->block_size,
+                                               shape->max_blocks_per_seq),
+                                    part_blocks);
+  const SchedShape sched{B, shape->num_kv_heads, shape->block_size, shape->max_blocks_per_seq,
+                         part_blocks, num_ctas};
+  int32_t db = -1, dj = 0, dlast = 0, dslot = 0;
+  if (part_blocks == 0 && !balanced_split_segment(pre, sched, seg, db, dj, dlast, dslot)) db = -1;
+  const MergeSeg ms = merge_segment(sched, seg, db, dj, dlast, dslot, pre);
+  b_j[0] = ms.np > 0 ? ms.b : -1;
+  b_j[1] = ms.np > 0 ? ms.j : -1;
+  for (int p = 0; p < ms.np && p < max_slots; ++p) slots[p] = (int32_t)ms.slot(p);
+  delete[] pre;
+  return ms.np;
+}
+
+}  // extern "C"

@@ -1,0 +1,117 @@
+// pa_kernels.cuh -- internal interface between the host API (pa_api.cu) and
+// the kernels: argument blocks, the shared-memory carve-up of the split
+// kernel (computed identically on host and device), and launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa_sched.cuh"
+
+namespace pa {
+
+constexpr int kConsumerWarps = 4;                       // warps that compute
+constexpr int kSplitThreads = 32 * (1 + kConsumerWarps);  // + one producer warp
+constexpr int kMaxStages = 32;
+constexpr int kGMax = 8;       // query heads per kv head handled by one CTA
+constexpr int kMergeSegs = 16;  // segments examined by one merge CTA
+constexpr int kMergeThreads = 256;
+
+enum Mode { kSimt = 1, kMma = 2 };
+
+struct SplitArgs {
+  const uint16_t* q;        // [B, H, D] raw 16-bit patterns
+  const int32_t* table;     // [B, maxblk]
+  const int32_t* seqlens;   // [B]
+  float* out;               // [B, H, D]
+  float* ws_ml;             // [slots][G][2] (max in log2 units, exp-sum)
+  float* ws_acc;            // [slots][G][D] unnormalised weighted V
+  int32_t* ws_pre;          // [B + 1] prefix sums of the per-sequence count
+  int4* ws_desc;            // [grid] balanced split: segment beginning in CTA c
+  uint32_t* status;         // sticky PA_STATUS_* bits
+  int32_t B, H, Hkv, G, bs, maxblk, P;
+  int32_t part_blocks;      // 0 = balanced split
+  int32_t stages;
+  float qscale;             // scale * log2(e): scores are kept in log2 units
+};
+
+struct MergeArgs {
+  const int32_t* seqlens;
+  float* out;
+  const float* ws_ml;
+  const float* ws_acc;
+  const int32_t* ws_pre;
+  const int4* ws_desc;
+  int32_t B, H, Hkv, G, D, bs, maxblk;
+  int32_t part_blocks;
+  int32_t num_ctas;  // grid of the split kernel
+};
+
+struct AppendArgs {
+  const uint16_t* k_new;  // [B, Hkv, D]
+  const uint16_t* v_new;
+  uint16_t* k_cache;      // [P, bs, Hkv, D]
+  uint16_t* v_cache;
+  const int32_t* table;
+  const int32_t* seqlens;
+  uint32_t* status;
+  int32_t B, Hkv, D, bs, maxblk, P;
+};
+
+// Byte offsets inside the split kernel's dynamic shared memory, relative to
+// a 1024-byte aligned base.
+struct SmemLayout {
+  uint32_t full, empty, info, abort_flag;  // pipeline barriers and stage info
+  uint32_t stage;                          // stages: [S][K chunks | V chunks]
+  uint32_t stage_bytes;
+  uint32_t mo, mm, ml, mbad;               // per-warp partial states for the merge
+  uint32_t qs, ps;                         // CUDA-core path: q (fp32), p per warp
+  uint32_t pre;                            // [B + 1] prefix sums
+  uint32_t total;                          // bytes to request (incl. alignment slack)
+};
+
+PA_HD uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+PA_HD SmemLayout split_smem_layout(int D, int bs, int G, int B, int S, int mode) {
+  SmemLayout L;
+  L.full = 0;
+  L.empty = 8 * kMaxStages;
+  L.info = 16 * kMaxStages;
+  L.abort_flag = 20 * kMaxStages;
+  L.stage = 1024;
+  L.stage_bytes = 4u * (uint32_t)D * (uint32_t)bs;  // K + V, 2 bytes each
+  uint32_t off = L.stage + (uint32_t)S * L.stage_bytes;
+  L.mo = off;
+  off += (uint32_t)(kConsumerWarps * G * (D + 4)) * 4u;
+  L.mm = off;
+  off += kConsumerWarps * kGMax * 4u;
+  L.ml = off;
+  off += kConsumerWarps * kGMax * 4u;
+  L.mbad = off;
+  off += 16;
+  off = align_up(off, 16);
+  if (mode == kSimt) {
+    L.qs = off;
+    off += (uint32_t)(G * D) * 4u;
+    L.ps = off;
+    off += (uint32_t)(kConsumerWarps * bs * kGMax) * 4u;
+  } else {
+    L.qs = L.ps = 0;
+  }
+  L.pre = off;
+  off += (uint32_t)(B + 1) * 4u;
+  off = align_up(off, 16);
+  L.total = off + 1024;  // slack to align the base to 1024 bytes
+  return L;
+}
+
+// Launchers (explicitly instantiated in pa_split_*.cu).
+template <typename T, int D, int MODE>
+cudaError_t launch_split(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a,
+                         int grid, size_t smem, cudaStream_t stream);
+
+template <typename T, int D, int MODE>
+const void* split_kernel_ptr();
+
+}  // namespace pa

@@ -1,0 +1,245 @@
+// pa_sched.cuh -- how the persistent split kernel divides one decode step's
+// work among its CTAs, and how the merge kernel finds the pieces again.
+// Compiled for host and device so that pa_plan_pieces (host) and the kernels
+// run the very same code.
+//
+// Work unit: one physical block of one (sequence b, kv head j) "segment".
+// Segment (b, j) holds nblk_b = ceil(len_b / bs) units.
+//
+// Balanced split (partition_tokens == 0): units are ordered (b, j, block);
+// CTA c of C_eff owns units [floor(U c / C_eff), floor(U (c+1) / C_eff)),
+// U = Hkv * sum_b nblk_b.  A CTA's range cuts at most two segments (its first
+// and its last piece), so each CTA writes at most two partial states:
+// slot 2c (the piece that starts at the CTA's first unit) and slot 2c+1 (the
+// CTA's last piece, when it is partial and not also the first).  A segment
+// that lies inside one CTA is finished there and written straight to `out`.
+//
+// Fixed split (partition_tokens > 0, part_blocks = partition_tokens / bs):
+// segment (b, j) has np_b = ceil(nblk_b / part_blocks) partitions; items are
+// ordered (b, partition, j) so the Hkv sibling heads of one partition are
+// adjacent and CTAs c, c+1, ... read the same physical blocks together.
+// CTA c takes items c, c + C, c + 2C, ...; item i writes partial slot i
+// (or `out` directly when np_b == 1).
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define PA_HD __host__ __device__ __forceinline__
+#else
+#define PA_HD inline
+#endif
+
+namespace pa {
+
+// Fewest units (blocks) a CTA of the balanced split is given: avoids
+// spreading tiny steps over many CTAs whose fixed costs would dominate.
+constexpr int kMinUnitsPerCta = 4;
+
+struct SchedShape {
+  int32_t B, Hkv, bs, maxblk;
+  int32_t part_blocks;  // 0 = balanced
+  int32_t num_ctas;     // launched persistent grid
+};
+
+// Blocks of a sequence; lengths outside [0, maxblk*bs] count as empty (the
+// kernels flag them separately).
+PA_HD int32_t seq_blocks(int32_t len, int32_t bs, int32_t maxblk) {
+  if (len <= 0 || (int64_t)len > (int64_t)maxblk * bs) return 0;
+  return (len + bs - 1) / bs;
+}
+
+PA_HD bool seq_len_valid(int32_t len, int32_t bs, int32_t maxblk) {
+  return len >= 0 && (int64_t)len <= (int64_t)maxblk * bs;
+}
+
+// Per-sequence count that the prefix sums run over.
+PA_HD int32_t seq_count(int32_t nblk, int32_t part_blocks) {
+  return part_blocks > 0 ? (nblk + part_blocks - 1) / part_blocks : nblk;
+}
+
+// Largest b in [0, B) with mult * pre[b] <= x, for x < mult * pre[B]
+// (pre is non-decreasing with pre[0] == 0).
+PA_HD int32_t find_seq(const int32_t* pre, int32_t B, int64_t mult, int64_t x) {
+  int32_t lo = 0, hi = B;
+  while (hi - lo > 1) {
+    int32_t mid = (lo + hi) >> 1;
+    if (mult * (int64_t)pre[mid] <= x)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------- balanced
+
+PA_HD int32_t balanced_ctas(int64_t U, int32_t C) {
+  int64_t want = (U + kMinUnitsPerCta - 1) / kMinUnitsPerCta;
+  if (want < 1) want = 1;
+  return (int32_t)(want < C ? want : C);
+}
+
+PA_HD int64_t balanced_begin(int64_t U, int32_t Ce, int32_t c) {
+  return (U * (int64_t)c) / Ce;
+}
+
+// The CTA whose range holds unit u (0 <= u < U).
+PA_HD int32_t balanced_cta_of(int64_t U, int32_t Ce, int64_t u) {
+  return (int32_t)(((u + 1) * (int64_t)Ce - 1) / U);
+}
+
+struct Piece {
+  int32_t b, j, blk0, blk1;  // blocks [blk0, blk1) of segment (b, j)
+  int32_t slot;              // partial-state slot, or -1 = whole segment
+};
+
+// Iterates the pieces one CTA processes, in processing order.
+struct PieceIter {
+  const int32_t* pre;     // [B+1] prefix sums of seq_count
+  const int32_t* lens;    // [B] (fixed split needs nblk per sequence)
+  SchedShape s;
+  int32_t cta;
+  // balanced state
+  int64_t U, u, u_end, u_begin;
+  int32_t Ce;
+  // fixed state
+  int64_t item, items;
+
+  PA_HD void init(const int32_t* pre_, const int32_t* lens_, const SchedShape& s_,
+                  int32_t cta_) {
+    pre = pre_;
+    lens = lens_;
+    s = s_;
+    cta = cta_;
+    if (s.part_blocks == 0) {
+      U = (int64_t)s.Hkv * pre[s.B];
+      Ce = balanced_ctas(U, s.num_ctas);
+      if (cta < Ce && U > 0) {
+        u_begin = balanced_begin(U, Ce, cta);
+        u_end = balanced_begin(U, Ce, cta + 1);
+      } else {
+        u_begin = u_end = 0;
+      }
+      u = u_begin;
+      items = item = 0;
+    } else {
+      items = (int64_t)s.Hkv * pre[s.B];
+      item = cta;
+      U = u = u_end = u_begin = 0;
+      Ce = s.num_ctas;
+    }
+  }
+
+  // Next piece; false when the CTA has no more work.
+  PA_HD bool next(Piece& p) {
+    if (s.part_blocks == 0) {
+      if (u >= u_end) return false;
+      int32_t b = find_seq(pre, s.B, s.Hkv, u);
+      int32_t n = pre[b + 1] - pre[b];
+      int64_t r = u - (int64_t)s.Hkv * pre[b];
+      int32_t j = (int32_t)(r / n);
+      int32_t blk0 = (int32_t)(r % n);
+      int64_t avail = u_end - u;
+      int32_t cnt = (int64_t)(n - blk0) < avail ? (n - blk0) : (int32_t)avail;
+      p.b = b;
+      p.j = j;
+      p.blk0 = blk0;
+      p.blk1 = blk0 + cnt;
+      if (blk0 == 0 && cnt == n)
+        p.slot = -1;
+      else
+        p.slot = 2 * cta + (u == u_begin ? 0 : 1);
+      u += cnt;
+      return true;
+    }
+    if (item >= items) return false;
+    int32_t b = find_seq(pre, s.B, s.Hkv, item);
+    int64_t r = item - (int64_t)s.Hkv * pre[b];
+    int32_t part = (int32_t)(r / s.Hkv);
+    int32_t j = (int32_t)(r % s.Hkv);
+    int32_t nb = seq_blocks(lens[b], s.bs, s.maxblk);
+    int32_t np = pre[b + 1] - pre[b];
+    p.b = b;
+    p.j = j;
+    p.blk0 = part * s.part_blocks;
+    p.blk1 = (part + 1) * s.part_blocks < nb ? (part + 1) * s.part_blocks : nb;
+    p.slot = (np == 1) ? -1 : (int32_t)item;
+    item += s.num_ctas;
+    return true;
+  }
+};
+
+// Balanced split: the segment that begins inside CTA c and continues past
+// its range, if any.  Returns false when CTA c has none.  On success gives
+// the segment, the last CTA holding one of its pieces, and the slot of the
+// piece in CTA c.  Every such segment has exactly one such CTA, so merging
+// it there (and only there) merges every split segment once.
+PA_HD bool balanced_split_segment(const int32_t* pre, const SchedShape& s, int32_t c,
+                                  int32_t& b, int32_t& j, int32_t& c_last, int32_t& slot) {
+  int64_t U = (int64_t)s.Hkv * pre[s.B];
+  if (U <= 0) return false;
+  int32_t Ce = balanced_ctas(U, s.num_ctas);
+  if (c >= Ce) return false;
+  int64_t u0 = balanced_begin(U, Ce, c);
+  int64_t u1 = balanced_begin(U, Ce, c + 1);
+  if (u1 <= u0) return false;
+  int64_t last = u1 - 1;
+  b = find_seq(pre, s.B, s.Hkv, last);
+  int32_t n = pre[b + 1] - pre[b];
+  int64_t r = last - (int64_t)s.Hkv * pre[b];
+  j = (int32_t)(r / n);
+  int64_t seg_begin = (int64_t)s.Hkv * pre[b] + (int64_t)j * n;
+  int64_t seg_end = seg_begin + n;
+  if (seg_end <= u1) return false;     // finishes inside c
+  if (seg_begin < u0) return false;    // began in an earlier CTA
+  c_last = balanced_cta_of(U, Ce, seg_end - 1);
+  slot = 2 * c + (seg_begin == u0 ? 0 : 1);
+  return true;
+}
+
+// The pieces merge index `seg` combines: balanced split -- the segment that
+// begins in split CTA seg and continues past it (desc as written by the split
+// kernel from balanced_split_segment); fixed split -- segment (b, j) =
+// (seg / Hkv, seg % Hkv) when it has more than one partition.
+struct MergeSeg {
+  int32_t b, j, np;   // np = number of pieces (0: nothing to merge)
+  int32_t seg, Hkv;
+  int32_t balanced;
+  int64_t slot0;      // balanced: slot of piece 0
+  int64_t fbase;      // fixed: slot of partition 0
+
+  PA_HD int64_t slot(int32_t p) const {
+    if (balanced) return p == 0 ? slot0 : 2 * (int64_t)(seg + p);
+    return fbase + (int64_t)p * Hkv;
+  }
+};
+
+// desc = (b, j, c_last, slot) or b < 0.  pre only read for the fixed split.
+PA_HD MergeSeg merge_segment(const SchedShape& s, int32_t seg, int32_t db, int32_t dj,
+                             int32_t dlast, int32_t dslot, const int32_t* pre) {
+  MergeSeg m;
+  m.seg = seg;
+  m.Hkv = s.Hkv;
+  m.balanced = s.part_blocks == 0;
+  m.np = 0;
+  m.b = m.j = 0;
+  m.slot0 = m.fbase = 0;
+  if (m.balanced) {
+    if (db < 0) return m;
+    m.b = db;
+    m.j = dj;
+    m.np = dlast - seg + 1;
+    m.slot0 = dslot;
+  } else {
+    m.b = seg / s.Hkv;
+    m.j = seg % s.Hkv;
+    const int32_t n = pre[m.b + 1] - pre[m.b];
+    if (n <= 1) return m;
+    m.np = n;
+    m.fbase = (int64_t)s.Hkv * pre[m.b] + m.j;
+  }
+  return m;
+}
+
+}  // namespace pa

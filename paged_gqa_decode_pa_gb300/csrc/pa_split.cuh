@@ -1,0 +1,660 @@
+// pa_split.cuh -- phase 1 of paged GQA decode: the persistent split kernel.
+//
+// One CTA = 1 producer warp + 4 consumer warps.  Each CTA walks the pieces
+// the schedule (pa_sched.cuh) gives it.  A piece is a run of physical blocks
+// of one (sequence b, kv head j) segment.
+//
+//   producer: prefetches the piece's block-table entries (32 per warp load),
+//     validates each id, and streams the K and V rows of kv head j of every
+//     block into a ring of `stages` shared-memory stages with 4-D TMA tensor
+//     loads (box = 64 dims x bs rows, 128-byte swizzle), completing on the
+//     stage's mbarrier.  Block table indirection happens here, once per block
+//     ("Paged Attention Kernel Architecture for BI-V100", section 3).
+//   consumers: block k of the CTA's stream goes to warp k % 4.  A warp runs
+//     the online-softmax recurrence over its blocks for all G query heads of
+//     kv head j at once ("v10_triton_paged_gqa", Core Principle; GQA
+//     amortisation of the BI-V100 design, section 4: each K/V byte is read
+//     from HBM once for the whole group).  At the end of a piece the four
+//     warp states are combined with the (max, exp-sum, weighted-V) combine op
+//     (BI-V100 design, section 2, Levels 1-2) and written either as the final
+//     output or as a partial state for the merge kernel (section 2, Level 3).
+//
+// Scores are kept in log2 units (q is pre-multiplied by scale*log2(e)) so
+// every exponential is one ex2 instruction; the merge kernel uses the same
+// units.
+//
+// Tensor-core variant (kMma): per 16-token tile, S^T[16 tokens x 8 heads] =
+// K[16 x d] . Q'^T[d x 8] and O^T[d x 8] += V^T[d x 16] . P^T[16 x 8] with
+// mma.sync m16n8k16 (fp32 accumulate).  Q' and P are split into a high and a
+// low 16-bit part (x = hi + lo) so that both products keep ~16 significant
+// bits; heads beyond G are zero columns.
+// CUDA-core variant (kSimt): lane <-> token for q.k (fp32 FMA), lane <->
+// dimension pair for p.V.
+#pragma once
+
+#include <math.h>
+
+#include "pa_kernels.cuh"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a stuck pipeline, never expected
+constexpr uint32_t kStatusBadBlock = 0x1u;
+constexpr uint32_t kStatusBadSeqlen = 0x2u;
+constexpr uint32_t kStatusTimeout = 0x4u;
+constexpr uint32_t kInfoBad = 0x10000u;
+
+// Byte offset of the 16-byte unit `unit` (0..7) of row `row` inside one
+// 128B-swizzled [rows][64] chunk tile written by TMA (tile base 1024-aligned).
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t unit) {
+  return row * 128u + ((unit ^ (row & 7u)) << 4);
+}
+
+// ------------------------------------------------------------------ prologue
+
+// Prefix sums of the per-sequence counts into pre[0..B] (shared memory).
+__device__ __forceinline__ void build_prefix(const SplitArgs& a, int32_t* pre, int32_t* scratch) {
+  const int tid = threadIdx.x;
+  const int T = blockDim.x;
+  const int per = (a.B + T - 1) / T;
+  const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b)
+    local += seq_count(seq_blocks(__ldg(a.seqlens + b), a.bs, a.maxblk), a.part_blocks);
+  // inclusive scan of `local` over the block
+  const int lane = tid & 31, warp = tid >> 5;
+  int x = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int w = 0; w < T / 32; ++w) {
+      int t = scratch[w];
+      scratch[w] = run;
+      run += t;
+    }
+    pre[a.B] = run;
+  }
+  __syncthreads();
+  int run = scratch[warp] + x - local;
+  for (int b = b0; b < b1; ++b) {
+    pre[b] = run;
+    run += seq_count(seq_blocks(__ldg(a.seqlens + b), a.bs, a.maxblk), a.part_blocks);
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------- consumer state
+
+template <typename T, int D>
+struct MmaState {
+  uint32_t qh[D / 16][2], ql[D / 16][2];  // B fragments of Q' (hi / lo)
+  float o[D / 16][4];                     // O^T accumulators
+  float m0, m1, l0, l1;                   // heads 2t and 2t+1 of this lane
+  bool bad;
+
+  __device__ __forceinline__ void load_q(const SplitArgs& a, int b, int j) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const bool live = g < a.G;
+    const uint16_t* qrow = a.q + ((int64_t)b * a.H + (int64_t)j * a.G + (live ? g : 0)) * D;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t hi = 0, lo = 0;
+        if (live) {
+          uint32_t raw = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + half * 8 + 2 * t));
+          float x0 = Cvt<T>::widen(static_cast<uint16_t>(raw & 0xffffu)) * a.qscale;
+          float x1 = Cvt<T>::widen(static_cast<uint16_t>(raw >> 16)) * a.qscale;
+          hi = Cvt<T>::pack(x0, x1);
+          lo = Cvt<T>::pack(x0 - Cvt<T>::low(hi), x1 - Cvt<T>::high(hi));
+        }
+        qh[ks][half] = hi;
+        ql[ks][half] = lo;
+      }
+    }
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[i][c] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+    bad = false;
+  }
+
+  // One block of `bs` tokens, `valid` of them real, K chunks at kb, V at vb.
+  __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, int bs, int valid) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t chunk = (uint32_t)bs * 128u;
+    for (int r0 = 0; r0 < valid; r0 += 16) {
+      // ---- S^T = K . Q'^T  (rows: tokens r0..r0+15, cols: heads)
+      float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const uint32_t tok = (uint32_t)r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const uint32_t uh = (uint32_t)(lane >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          const uint32_t addr = kb + (uint32_t)(ks >> 2) * chunk + swz(tok, 2u * (ks & 3) + uh);
+          ldmatrix_x4(addr, a0, a1, a2, a3);
+          mma_16816<T>(sh, a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
+          mma_16816<T>(sl, a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
+        }
+      }
+      const int tr = r0 + (lane >> 2);
+      float s0 = sh[0] + sl[0], s1 = sh[1] + sl[1], s2 = sh[2] + sl[2], s3 = sh[3] + sl[3];
+      if (tr >= valid) s0 = s1 = -INFINITY;
+      if (tr + 8 >= valid) s2 = s3 = -INFINITY;
+      // ---- online softmax update for heads 2t, 2t+1
+      float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+      }
+      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+      const float u0 = (n0 == -INFINITY) ? 0.f : n0;
+      const float u1 = (n1 == -INFINITY) ? 0.f : n1;
+      const float al0 = ex2(m0 - u0), al1 = ex2(m1 - u1);
+      const float p0 = ex2(s0 - u0), p1 = ex2(s1 - u1), p2 = ex2(s2 - u0), p3 = ex2(s3 - u1);
+      l0 = l0 * al0 + (p0 + p2);
+      l1 = l1 * al1 + (p1 + p3);
+      m0 = n0;
+      m1 = n1;
+#pragma unroll
+      for (int dt = 0; dt < D / 16; ++dt) {
+        o[dt][0] *= al0;
+        o[dt][1] *= al1;
+        o[dt][2] *= al0;
+        o[dt][3] *= al1;
+      }
+      // ---- P^T fragments (k = tokens, n = heads), hi + lo parts
+      const uint32_t h01 = Cvt<T>::pack(p0, p1), h23 = Cvt<T>::pack(p2, p3);
+      const uint32_t e01 = Cvt<T>::pack(p0 - Cvt<T>::low(h01), p1 - Cvt<T>::high(h01));
+      const uint32_t e23 = Cvt<T>::pack(p2 - Cvt<T>::low(h23), p3 - Cvt<T>::high(h23));
+      const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+      const uint32_t bl0 = movmatrix_trans(e01), bl1 = movmatrix_trans(e23);
+      // ---- O^T += V^T . P^T
+      {
+        const uint32_t tok = (uint32_t)r0 + (lane & 7) + (lane >> 4) * 8;
+        const uint32_t uh = (uint32_t)((lane >> 3) & 1);
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt) {
+          uint32_t a0, a1, a2, a3;
+          const uint32_t addr = vb + (uint32_t)(dt >> 2) * chunk + swz(tok, 2u * (dt & 3) + uh);
+          ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+          mma_16816<T>(o[dt], a0, a1, a2, a3, bh0, bh1);
+          mma_16816<T>(o[dt], a0, a1, a2, a3, bl0, bl1);
+        }
+      }
+    }
+  }
+
+  // Publish this warp's state for the CTA-level combine.
+  __device__ __forceinline__ void publish(uint8_t* smem, const SmemLayout& L, int w, int G) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    float* mm = reinterpret_cast<float*>(smem + L.mm) + w * kGMax;
+    float* ml = reinterpret_cast<float*>(smem + L.ml) + w * kGMax;
+    if (g == 0) {
+      mm[2 * t] = m0;
+      mm[2 * t + 1] = m1;
+      ml[2 * t] = l0;
+      ml[2 * t + 1] = l1;
+    }
+    float* mo = reinterpret_cast<float*>(smem + L.mo) + (size_t)w * G * (D + 4);
+    const int h0 = 2 * t, h1 = 2 * t + 1;
+#pragma unroll
+    for (int dt = 0; dt < D / 16; ++dt) {
+      const int dim = dt * 16 + g;
+      if (h0 < G) {
+        mo[h0 * (D + 4) + dim] = o[dt][0];
+        mo[h0 * (D + 4) + dim + 8] = o[dt][2];
+      }
+      if (h1 < G) {
+        mo[h1 * (D + 4) + dim] = o[dt][1];
+        mo[h1 * (D + 4) + dim + 8] = o[dt][3];
+      }
+    }
+    if (lane == 0) reinterpret_cast<int*>(smem + L.mbad)[w] = bad ? 1 : 0;
+  }
+};
+
+template <typename T, int D>
+struct SimtState {
+  float acc[kGMax][D / 32];  // dims c*64 + 2*lane + e, e in {0,1}, chunk c
+  float m[kGMax], l[kGMax];  // m: warp-uniform; l: this lane's tokens only
+  bool bad;
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int g = 0; g < kGMax; ++g) {
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) acc[g][i] = 0.f;
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+    }
+    bad = false;
+  }
+
+  // qs: shared [G][D] fp32 q*scale*log2e.  ps: this warp's [bs][8] fp32.
+  __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, int bs, int valid,
+                                        const float* qs, float* ps, int G) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t chunk = (uint32_t)bs * 128u;
+    // ---------------- q . k : lane <-> token (bs == 16: heads split by half-warp)
+    const int tpass = bs < 32 ? bs : 32;
+    const int GH = (G + 1) >> 1;
+    const int h0 = (bs == 16) ? (lane >> 4) * GH : 0;
+    const int h1 = (bs == 16) ? min(G, h0 + GH) : G;
+    float mx[kGMax];
+#pragma unroll
+    for (int g = 0; g < kGMax; ++g) mx[g] = -INFINITY;
+    for (int tb = 0; tb < bs; tb += tpass) {
+      const int tt = tb + (lane % tpass);
+      float s[kGMax];
+#pragma unroll
+      for (int g = 0; g < kGMax; ++g) s[g] = 0.f;
+#pragma unroll 4
+      for (int c8 = 0; c8 < D / 8; ++c8) {
+        const uint4 kr = lds128(kb + (uint32_t)(c8 >> 3) * chunk + swz(tt, c8 & 7));
+        float kf[8];
+        kf[0] = Cvt<T>::low(kr.x);
+        kf[1] = Cvt<T>::high(kr.x);
+        kf[2] = Cvt<T>::low(kr.y);
+        kf[3] = Cvt<T>::high(kr.y);
+        kf[4] = Cvt<T>::low(kr.z);
+        kf[5] = Cvt<T>::high(kr.z);
+        kf[6] = Cvt<T>::low(kr.w);
+        kf[7] = Cvt<T>::high(kr.w);
+#pragma unroll
+        for (int g = 0; g < kGMax; ++g) {
+          if (g >= h0 && g < h1) {
+            const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + c8 * 8);
+            const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + c8 * 8 + 4);
+            float v = s[g];
+            v = fmaf(qa.x, kf[0], v);
+            v = fmaf(qa.y, kf[1], v);
+            v = fmaf(qa.z, kf[2], v);
+            v = fmaf(qa.w, kf[3], v);
+            v = fmaf(qb.x, kf[4], v);
+            v = fmaf(qb.y, kf[5], v);
+            v = fmaf(qb.z, kf[6], v);
+            v = fmaf(qb.w, kf[7], v);
+            s[g] = v;
+          }
+        }
+      }
+      const bool live = tt < valid;
+#pragma unroll
+      for (int g = 0; g < kGMax; ++g) {
+        if (!(g >= h0 && g < h1) || !live) s[g] = -INFINITY;
+        // stash raw scores in the p buffer; exponentiated below
+        if (g >= h0 && g < h1) ps[tt * kGMax + g] = s[g];
+        mx[g] = fmaxf(mx[g], s[g]);
+      }
+    }
+    // block max per head, made warp-uniform
+#pragma unroll
+    for (int g = 0; g < kGMax; ++g) {
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
+    }
+    float alpha[kGMax], mu[kGMax];
+#pragma unroll
+    for (int g = 0; g < kGMax; ++g) {
+      const float n = fmaxf(m[g], mx[g]);
+      mu[g] = (n == -INFINITY) ? 0.f : n;
+      alpha[g] = ex2(m[g] - mu[g]);
+      m[g] = n;
+      l[g] *= alpha[g];
+    }
+    __syncwarp();
+    // p = 2^(s - m) for this lane's (token, heads), back into the buffer
+    for (int tb = 0; tb < bs; tb += tpass) {
+      const int tt = tb + (lane % tpass);
+#pragma unroll
+      for (int g = 0; g < kGMax; ++g) {
+        if (g >= h0 && g < h1) {
+          const float p = (tt < valid) ? ex2(ps[tt * kGMax + g] - mu[g]) : 0.f;
+          ps[tt * kGMax + g] = p;
+          l[g] += p;
+        }
+      }
+    }
+    __syncwarp();
+    // ---------------- p . V : lane <-> dimension pair
+#pragma unroll
+    for (int g = 0; g < kGMax; ++g)
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) acc[g][i] *= alpha[g];
+    const uint32_t col = (uint32_t)((lane & 3) * 4);
+    const uint32_t unit = (uint32_t)(lane >> 2);
+    for (int t = 0; t < valid; ++t) {
+      const float4 pa = *reinterpret_cast<const float4*>(ps + t * kGMax);
+      const float4 pb = *reinterpret_cast<const float4*>(ps + t * kGMax + 4);
+      const float p[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const uint32_t v = lds32(vb + (uint32_t)c * chunk + swz(t, unit) + col);
+        const float v0 = Cvt<T>::low(v), v1 = Cvt<T>::high(v);
+#pragma unroll
+        for (int g = 0; g < kGMax; ++g) {
+          if (g < G) {
+            acc[g][2 * c] = fmaf(p[g], v0, acc[g][2 * c]);
+            acc[g][2 * c + 1] = fmaf(p[g], v1, acc[g][2 * c + 1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  __device__ __forceinline__ void publish(uint8_t* smem, const SmemLayout& L, int w, int G) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int g = 0; g < kGMax; ++g) {
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], off);
+    }
+    float* mm = reinterpret_cast<float*>(smem + L.mm) + w * kGMax;
+    float* ml = reinterpret_cast<float*>(smem + L.ml) + w * kGMax;
+    if (lane == 0) {
+#pragma unroll
+      for (int g = 0; g < kGMax; ++g) {
+        mm[g] = m[g];
+        ml[g] = l[g];
+      }
+    }
+    float* mo = reinterpret_cast<float*>(smem + L.mo) + (size_t)w * G * (D + 4);
+#pragma unroll
+    for (int g = 0; g < kGMax; ++g) {
+      if (g < G) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          float2 v = make_float2(acc[g][2 * c], acc[g][2 * c + 1]);
+          *reinterpret_cast<float2*>(mo + g * (D + 4) + c * 64 + 2 * lane) = v;
+        }
+      }
+    }
+    if (lane == 0) reinterpret_cast<int*>(smem + L.mbad)[w] = bad ? 1 : 0;
+  }
+};
+
+// CTA-level combine of the four warp states of one piece (consumer threads).
+template <int D>
+__device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem, const SmemLayout& L,
+                                              const Piece& pc) {
+  const int ct = threadIdx.x - 32;
+  const int G = a.G;
+  const float* mm = reinterpret_cast<const float*>(smem + L.mm);
+  const float* ml = reinterpret_cast<const float*>(smem + L.ml);
+  const float* mo = reinterpret_cast<const float*>(smem + L.mo);
+  const int* mbad = reinterpret_cast<const int*>(smem + L.mbad);
+  bool bad = false;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) bad |= (mbad[w] != 0);
+  const float qnan = __int_as_float(0x7fc00000);
+  for (int idx = ct; idx < G * D; idx += 32 * kConsumerWarps) {
+    const int g = idx / D, dim = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * kGMax + g]);
+    float Lsum = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = mm[w * kGMax + g];
+      const float e = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+      Lsum = fmaf(e, ml[w * kGMax + g], Lsum);
+      o = fmaf(e, mo[(w * G + g) * (D + 4) + dim], o);
+    }
+    if (pc.slot < 0) {
+      float* dst = a.out + ((int64_t)pc.b * a.H + (int64_t)pc.j * G + g) * D + dim;
+      *dst = bad ? qnan : o / Lsum;
+    } else {
+      a.ws_acc[((int64_t)pc.slot * G + g) * D + dim] = bad ? qnan : o;
+      if (dim == 0) {
+        a.ws_ml[((int64_t)pc.slot * G + g) * 2 + 0] = M;
+        a.ws_ml[((int64_t)pc.slot * G + g) * 2 + 1] = bad ? qnan : Lsum;
+      }
+    }
+  }
+}
+
+template <typename T, int D, int MODE>
+__global__ void __launch_bounds__(kSplitThreads, 1)
+    pa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                    const SplitArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_addr);
+  const SmemLayout L = split_smem_layout(D, a.bs, a.G, a.B, a.stages, MODE);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int S = a.stages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  int32_t* pre = reinterpret_cast<int32_t*>(smem + L.pre);
+  __shared__ int32_t scan_scratch[kSplitThreads / 32];
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(base + L.full + 8 * s, 1);
+      mbar_init(base + L.empty + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  build_prefix(a, pre, scan_scratch);  // contains __syncthreads
+
+  const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, (int32_t)gridDim.x};
+  const int cta = blockIdx.x;
+
+  // Sequences with no cached token: out = 0; invalid length: NaN + status.
+  for (int b = cta; b < a.B; b += gridDim.x) {
+    const int32_t len = __ldg(a.seqlens + b);
+    if (seq_blocks(len, a.bs, a.maxblk) != 0) continue;
+    const bool ok = seq_len_valid(len, a.bs, a.maxblk);
+    const float v = ok ? 0.f : __int_as_float(0x7fc00000);
+    float* row = a.out + (int64_t)b * a.H * D;
+    for (int i = tid; i < a.H * D; i += blockDim.x) row[i] = v;
+    if (!ok && tid == 0) atomicOr(a.status, kStatusBadSeqlen);
+  }
+  if (tid == 0) {
+    if (cta == 0) {
+      // prefix sums for the merge kernel
+      for (int b = 0; b <= a.B; ++b) a.ws_pre[b] = pre[b];
+    }
+    if (a.part_blocks == 0) {
+      int32_t b, j, c_last, slot;
+      int4 desc = make_int4(-1, 0, 0, 0);
+      if (balanced_split_segment(pre, sched, cta, b, j, c_last, slot)) desc = make_int4(b, j, c_last, slot);
+      a.ws_desc[cta] = desc;
+    }
+  }
+
+  PieceIter it;
+  it.init(pre, a.seqlens, sched, cta);
+  Piece pc;
+  const uint32_t stage_bytes = L.stage_bytes;
+  const uint32_t chunk = (uint32_t)a.bs * 128u;
+  constexpr int NC = D / 64;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t policy = l2_policy_evict_first();
+    uint32_t k = 0;
+    bool stop = false;
+    while (!stop && it.next(pc)) {
+      const int32_t len = __ldg(a.seqlens + pc.b);
+      const int32_t* trow = a.table + (int64_t)pc.b * a.maxblk;
+      for (int c0 = pc.blk0; c0 < pc.blk1 && !stop; c0 += 32) {
+        const int idx = c0 + lane;
+        const int32_t e = (idx < pc.blk1) ? __ldg(trow + idx) : 0;
+        const int n = min(32, pc.blk1 - c0);
+        for (int t = 0; t < n; ++t) {
+          const int32_t phys = __shfl_sync(0xffffffffu, e, t);
+          if (lane == 0 && !stop) {
+            const uint32_t s = k % (uint32_t)S;
+            const uint32_t full = base + L.full + 8 * s, empty = base + L.empty + 8 * s;
+            bool ok = true;
+            if (k >= (uint32_t)S) ok = mbar_wait_bounded(empty, ((k / S) + 1) & 1, abort_flag, kWaitLimitNs);
+            if (!ok) {
+              atomicOr(a.status, kStatusTimeout);
+              stop = true;
+            } else {
+              const int blk = c0 + t;
+              const int valid = min(a.bs, len - blk * a.bs);
+              const bool bad = phys < 0 || phys >= a.P;
+              reinterpret_cast<volatile uint32_t*>(smem + L.info)[s] =
+                  (uint32_t)valid | (bad ? kInfoBad : 0u);
+              if (bad) {
+                atomicOr(a.status, kStatusBadBlock);
+                mbar_arrive(full);
+              } else {
+                mbar_arrive_expect_tx(full, stage_bytes);
+                const uint32_t kdst = base + L.stage + s * stage_bytes;
+                const uint32_t vdst = kdst + NC * chunk;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                  tma_load_4d(kdst + c * chunk, &tmk, full, c * 64, pc.j, 0, phys, policy);
+                  tma_load_4d(vdst + c * chunk, &tmv, full, c * 64, pc.j, 0, phys, policy);
+                }
+              }
+            }
+          }
+          stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+          if (stop) break;
+          ++k;
+        }
+      }
+    }
+    if (stop && lane == 0) {
+      // Drain: wait (bounded, ignoring the abort flag) for the copies this
+      // warp issued into the last min(k, S) stages before the CTA may exit.
+      volatile int never = 0;
+      const uint32_t first = k > (uint32_t)S ? k - (uint32_t)S : 0u;
+      for (uint32_t kk = first; kk < k; ++kk) {
+        const uint32_t s = kk % (uint32_t)S;
+        mbar_wait_bounded(base + L.full + 8 * s, (kk / S) & 1, &never, kWaitLimitNs / 4);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int w = warp - 1;
+  uint32_t k = 0;
+  if constexpr (MODE == kMma) {
+    MmaState<T, D> st;
+    while (it.next(pc)) {
+      st.load_q(a, pc.b, pc.j);
+      st.reset();
+      for (int blk = pc.blk0; blk < pc.blk1; ++blk, ++k) {
+        if ((int)(k % kConsumerWarps) != w) continue;
+        const uint32_t s = k % (uint32_t)S;
+        const bool ok = mbar_wait_bounded(base + L.full + 8 * s, (k / S) & 1, abort_flag, kWaitLimitNs);
+        const uint32_t info = reinterpret_cast<volatile uint32_t*>(smem + L.info)[s];
+        const int valid = (int)(info & 0xffffu);
+        if (!ok || (info & kInfoBad)) {
+          st.bad = true;
+          if (!ok && lane == 0) atomicOr(a.status, kStatusTimeout);
+        } else {
+          const uint32_t kb = base + L.stage + s * stage_bytes;
+          const uint32_t vb = kb + NC * chunk;
+          if (valid < a.bs) {
+            // zero the V rows past the sequence end so that p = 0 rows add 0
+            const int rows = a.bs - valid;
+            for (int u = lane; u < rows * 8 * NC; u += 32) {
+              const int c = u / (rows * 8), rem = u % (rows * 8);
+              sts128(vb + c * chunk + (uint32_t)(valid + rem / 8) * 128u + (rem % 8) * 16u,
+                     make_uint4(0u, 0u, 0u, 0u));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          st.block(kb, vb, a.bs, valid);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(base + L.empty + 8 * s);
+      }
+      st.publish(smem, L, w, a.G);
+      named_bar_sync(1, 32 * kConsumerWarps);
+      combine_piece<D>(a, smem, L, pc);
+      named_bar_sync(1, 32 * kConsumerWarps);
+    }
+  } else {
+    SimtState<T, D> st;
+    float* qs = reinterpret_cast<float*>(smem + L.qs);
+    float* ps = reinterpret_cast<float*>(smem + L.ps) + w * a.bs * kGMax;
+    const int ct = tid - 32;
+    while (it.next(pc)) {
+      // q * scale * log2e for the G heads of kv head j (shared by the warps)
+      const uint16_t* qrow = a.q + ((int64_t)pc.b * a.H + (int64_t)pc.j * a.G) * D;
+      for (int i = ct; i < a.G * D; i += 32 * kConsumerWarps)
+        qs[i] = Cvt<T>::widen(__ldg(qrow + i)) * a.qscale;
+      named_bar_sync(1, 32 * kConsumerWarps);
+      st.reset();
+      for (int blk = pc.blk0; blk < pc.blk1; ++blk, ++k) {
+        if ((int)(k % kConsumerWarps) != w) continue;
+        const uint32_t s = k % (uint32_t)S;
+        const bool ok = mbar_wait_bounded(base + L.full + 8 * s, (k / S) & 1, abort_flag, kWaitLimitNs);
+        const uint32_t info = reinterpret_cast<volatile uint32_t*>(smem + L.info)[s];
+        const int valid = (int)(info & 0xffffu);
+        if (!ok || (info & kInfoBad)) {
+          st.bad = true;
+          if (!ok && lane == 0) atomicOr(a.status, kStatusTimeout);
+        } else {
+          const uint32_t kb = base + L.stage + s * stage_bytes;
+          st.block(kb, kb + NC * chunk, a.bs, valid, qs, ps, a.G);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(base + L.empty + 8 * s);
+      }
+      st.publish(smem, L, w, a.G);
+      named_bar_sync(1, 32 * kConsumerWarps);
+      combine_piece<D>(a, smem, L, pc);
+      named_bar_sync(1, 32 * kConsumerWarps);
+    }
+  }
+}
+
+template <typename T, int D, int MODE>
+cudaError_t launch_split(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a,
+                         int grid, size_t smem, cudaStream_t stream) {
+  pa_split_kernel<T, D, MODE><<<grid, kSplitThreads, smem, stream>>>(tmk, tmv, a);
+  return cudaGetLastError();
+}
+
+template <typename T, int D, int MODE>
+const void* split_kernel_ptr() {
+  return reinterpret_cast<const void*>(&pa_split_kernel<T, D, MODE>);
+}
+
+}  // namespace pa
+
+#define PA_INSTANTIATE_SPLIT(T, D, MODE)                                                     \
+  template cudaError_t pa::launch_split<T, D, MODE>(const CUtensorMap&, const CUtensorMap&,  \
+                                                    const pa::SplitArgs&, int, size_t,       \
+                                                    cudaStream_t);                           \
+  template const void* pa::split_kernel_ptr<T, D, MODE>();

@@ -1,0 +1,5 @@
+// Instantiations of the split kernel for bf16 storage, head_dim 128.
+#include "pa_split.cuh"
+
+PA_INSTANTIATE_SPLIT(__nv_bfloat16, 128, pa::kMma)
+PA_INSTANTIATE_SPLIT(__nv_bfloat16, 128, pa::kSimt)

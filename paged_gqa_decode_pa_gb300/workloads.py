@@ -8,8 +8,9 @@ the oracle, and is the one piece of code both sides share.
 Recipe (every workload): ``numpy.random.default_rng(seed)`` drawn in the
 fixed order lengths -> block permutation -> q -> K -> V (-> outlier rows);
 values are float32 N(0,1) rounded to nearest-even into fp16 or bf16 and kept
-as raw 16-bit patterns (``uint16``).  Large pools are drawn in chunks of whole
-physical blocks from the same generator.
+as raw 16-bit patterns (``uint16``).  Pools above 2^24 elements are drawn in
+chunks of whole physical blocks, chunk i from child generator i of
+``rng.spawn``.
 
 The shapes follow the settings the pages describe:
   * ``p5_example``          -- the Hugging Face "Paged attention" decoding-path
@@ -34,6 +35,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
 from typing import Optional
 
 import numpy as np
@@ -41,7 +43,7 @@ import numpy as np
 F16 = "f16"
 BF16 = "bf16"
 
-_CHUNK_ELEMS = 1 << 25  # elements drawn per chunk for large pools
+_CHUNK_ELEMS = 1 << 24  # elements per chunk for large pools
 
 
 @dataclasses.dataclass
@@ -133,16 +135,33 @@ def nan_bits(dtype: str) -> int:
 
 
 def _normal_bits(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
-    """N(0,1) float32 draws rounded into the storage type, chunked by rows."""
+    """N(0,1) float32 draws rounded into the storage type.
+
+    Arrays up to _CHUNK_ELEMS elements are drawn from `rng` directly.  Larger
+    ones are cut into chunks of whole leading-axis rows, each drawn from its
+    own child generator (rng.spawn, deterministic), filled by a thread pool.
+    """
     shape = tuple(int(s) for s in shape)
     out = np.empty(shape, dtype=np.uint16)
     rows = shape[0]
     per_row = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+    if rows * per_row <= _CHUNK_ELEMS:
+        out[...] = to_bits(rng.standard_normal(shape, dtype=np.float32), dtype)
+        return out
     step = max(1, _CHUNK_ELEMS // max(per_row, 1))
-    for r0 in range(0, rows, step):
+    starts = list(range(0, rows, step))
+    children = rng.spawn(len(starts))
+
+    def fill(i):
+        r0 = starts[i]
         r1 = min(rows, r0 + step)
-        x = rng.standard_normal((r1 - r0,) + shape[1:], dtype=np.float32)
+        x = children[i].standard_normal((r1 - r0,) + shape[1:], dtype=np.float32)
         out[r0:r1] = to_bits(x, dtype)
+
+    import concurrent.futures as cf
+
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, range(len(starts))))
     return out
 
 
