@@ -225,6 +225,7 @@ def workload_config(w, args):
             "mean_seqlen": round(float(np.mean(w.cache_seqlens)), 1),
             "max_seqlen": int(np.max(w.cache_seqlens)),
             "partition_tokens": args.partition_tokens, "compute": args.compute,
+            "stages": args.stages,
             "kv_bytes_per_step": w.kv_bytes(),
             "l2": ("inputs larger than L2" if w.kv_bytes() > 2 * L2_BYTES
                    else "L2 flushed between timed steps"),
@@ -241,7 +242,8 @@ def run_ours(args, rank, world, local_rank):
     w = make_workload(args.config)
     q, k, v, t, sl = w.torch_tensors(dev)
     out = torch.empty((w.B, w.H, w.d), dtype=torch.float32, device=dev)
-    opts = pg.options(partition_tokens=args.partition_tokens, compute=args.compute)
+    opts = pg.options(partition_tokens=args.partition_tokens, compute=args.compute,
+                      stages=args.stages)
     shape = pg.shape_of(q, k, t)
     ws = pg.alloc_workspace(shape, opts, dev)
     stream = torch.cuda.current_stream(dev)
@@ -337,7 +339,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_value = world * kv_bytes / (e2e_ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
     achieved = kv_bytes / (split_avg_ms * 1e-3) / 1e9
-    opts_key = f"part={args.partition_tokens},compute={args.compute}"
+    opts_key = f"part={args.partition_tokens},compute={args.compute},stages={args.stages}"
     traffic = recorded_traffic(w.name, opts_key)
     cpu = None
     if args.cpu_baseline_s > 0 and world == 1:
@@ -377,6 +379,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--compute", default="mma", choices=["mma", "simt", "auto"])
+    ap.add_argument("--stages", type=int, default=0, help="pipeline stages (0 = library choice)")
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample (0 = skip)")
     args = ap.parse_args()

@@ -117,7 +117,8 @@ typedef struct pa_options {
   int32_t num_ctas;  /* persistent grid size; 0 = one full wave of resident
                         CTAs on the current device.  Setting it makes
                         pa_workspace_size independent of the device. */
-  int32_t stages;    /* K/V pipeline stages per CTA; 0 = library choice */
+  int32_t stages;    /* TMA ring slots per warp (16-token K/V stages,
+                        1..8); 0 = library choice */
 } pa_options;
 
 /* Bytes of workspace pa_decode / pa_decode_split / pa_decode_merge /

@@ -20,78 +20,71 @@ namespace {
 
 // ------------------------------------------------------------------ merge
 
-// Phase 2: combine the partial states of every segment that the split kernel
-// cut across CTAs (or partitions).  Block (g * D/64 + dc, q) handles head g,
-// dims [64 dc, 64 dc + 64) of the split segments q*16 .. q*16+15 (balanced:
-// the segment beginning in split CTA seg; fixed: segment (b, j) = seg).
-// 256 threads = 4 piece groups x 64 dims; pieces are visited in a fixed
-// order, so the result is deterministic.  Combine op: "Paged Attention Kernel
+// Phase 2: combine the partial states of every segment the split kernel cut
+// across CTAs (balanced split) or partitions (fixed split).  Block
+// (seg, g) merges head g of merge index seg (pa_sched.cuh, merge_segment):
+// warp w folds pieces w, w+4, ... with the combine op, lanes over the head
+// dimension; the four warp states are folded the same way in a fixed order,
+// so the result is deterministic.  Combine op: "Paged Attention Kernel
 // Architecture for BI-V100", section 2, Level 1 binary op / Level 3.
-__global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs a) {
-  const int nchunk = a.D / 64;
-  const int g = blockIdx.x / nchunk, dc = blockIdx.x % nchunk;
-  const int tid = threadIdx.x;
-  const int pg = tid >> 6, dl = tid & 63;
-  const int dim = dc * 64 + dl;
-  __shared__ float red[4][64];
-  __shared__ float wred[kMergeThreads / 32];
-  __shared__ float sM, sL;
-  const int nseg = a.part_blocks == 0 ? a.num_ctas : a.B * a.Hkv;
-  const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas};
-  for (int si = 0; si < kMergeSegs; ++si) {
-    const int seg = blockIdx.y * kMergeSegs + si;
-    if (seg >= nseg) break;
-    int4 desc = make_int4(-1, 0, 0, 0);
-    if (a.part_blocks == 0) desc = a.ws_desc[seg];
-    const MergeSeg ms = merge_segment(sched, seg, desc.x, desc.y, desc.z, desc.w, a.ws_pre);
-    const int np = ms.np;
-    if (np == 0) continue;
-    const int b = ms.b, j = ms.j;
-    auto slot_of = [&](int p) -> int64_t { return ms.slot(p); };
-    // M = max_p m_p
-    float m = -INFINITY;
-    for (int p = tid; p < np; p += kMergeThreads) m = fmaxf(m, a.ws_ml[(slot_of(p) * a.G + g) * 2]);
+template <int D>
+__device__ __forceinline__ void merge_segment_head(const MergeArgs& a, const MergeSeg& ms, int g) {
+  constexpr int NV = D / 32;  // dims per lane: lane + 32 i
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  __shared__ float wm[kMergeThreads / 32], wl[kMergeThreads / 32];
+  __shared__ float wacc[kMergeThreads / 32][D];
+  float m = -INFINITY, l = 0.f, acc[NV];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if ((tid & 31) == 0) wred[tid >> 5] = m;
-    __syncthreads();
-    if (tid == 0) {
-      float x = wred[0];
-      for (int w = 1; w < kMergeThreads / 32; ++w) x = fmaxf(x, wred[w]);
-      sM = x;
-    }
-    __syncthreads();
-    const float M = sM;
-    // L = sum_p l_p 2^(m_p - M)
-    float l = 0.f;
-    for (int p = tid; p < np; p += kMergeThreads) {
-      const int64_t s = slot_of(p);
-      l += a.ws_ml[(s * a.G + g) * 2 + 1] * ex2(a.ws_ml[(s * a.G + g) * 2] - M);
-    }
+  for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+  for (int p = w; p < ms.np; p += kMergeThreads / 32) {
+    const int64_t s = ms.slot(p);
+    const float mp = a.ws_ml[(s * a.G + g) * 2];
+    const float lp = a.ws_ml[(s * a.G + g) * 2 + 1];
+    const float* ap = a.ws_acc + (s * a.G + g) * D;
+    const float mn = fmaxf(m, mp);
+    const float sa = (m == -INFINITY) ? 0.f : ex2(m - mn);
+    const float sb = ex2(mp - mn);
+    l = l * sa + lp * sb;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    __syncthreads();  // wred reuse
-    if ((tid & 31) == 0) wred[tid >> 5] = l;
-    __syncthreads();
-    if (tid == 0) {
-      float x = 0.f;
-      for (int w = 0; w < kMergeThreads / 32; ++w) x += wred[w];
-      sL = x;
-    }
-    // out = sum_p 2^(m_p - M) acc_p / L
-    float acc = 0.f;
-    for (int p = pg; p < np; p += 4) {
-      const int64_t s = slot_of(p);
-      acc = fmaf(ex2(a.ws_ml[(s * a.G + g) * 2] - M), a.ws_acc[(s * a.G + g) * a.D + dim], acc);
-    }
-    red[pg][dl] = acc;
-    __syncthreads();
-    if (pg == 0) {
-      const float o = (red[0][dl] + red[1][dl]) + (red[2][dl] + red[3][dl]);
-      a.out[((int64_t)b * a.H + (int64_t)j * a.G + g) * a.D + dim] = o / sL;
-    }
-    __syncthreads();
+    for (int i = 0; i < NV; ++i) acc[i] = acc[i] * sa + ap[lane + 32 * i] * sb;
+    m = mn;
   }
+  if (lane == 0) {
+    wm[w] = m;
+    wl[w] = l;
+  }
+#pragma unroll
+  for (int i = 0; i < NV; ++i) wacc[w][lane + 32 * i] = acc[i];
+  __syncthreads();
+  if (w == 0) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < kMergeThreads / 32; ++v) M = fmaxf(M, wm[v]);
+    float Lsum = 0.f, o[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) o[i] = 0.f;
+#pragma unroll
+    for (int v = 0; v < kMergeThreads / 32; ++v) {
+      const float e = (wm[v] == -INFINITY) ? 0.f : ex2(wm[v] - M);
+      Lsum = fmaf(e, wl[v], Lsum);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) o[i] = fmaf(e, wacc[v][lane + 32 * i], o[i]);
+    }
+    float* dst = a.out + ((int64_t)ms.b * a.H + (int64_t)ms.j * a.G + g) * D;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) dst[lane + 32 * i] = o[i] / Lsum;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs a) {
+  const int seg = blockIdx.x, g = blockIdx.y;
+  const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas};
+  int4 desc = make_int4(-1, 0, 0, 0);
+  if (a.part_blocks == 0) desc = a.ws_desc[seg];
+  const MergeSeg ms = merge_segment(sched, seg, desc.x, desc.y, desc.z, desc.w, a.ws_pre);
+  if (ms.np == 0) return;
+  merge_segment_head<D>(a, ms, g);
 }
 
 // --------------------------------------------------------------- append
@@ -124,6 +117,7 @@ __global__ void pa_append_kernel(const AppendArgs a) {
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kHeaderBytes = 256;
+constexpr int kMaxDynamicSmem = 227 * 1024 - 64;  // minus the kernel's static shared memory
 
 struct DeviceInfo {
   bool ready = false;
@@ -169,12 +163,12 @@ int check_options(const pa_shape* s, const pa_options* o) {
   if (o->partition_tokens > 0 && o->partition_tokens % s->block_size != 0) return PA_ERR_OPTION;
   if (o->compute < PA_COMPUTE_AUTO || o->compute > PA_COMPUTE_MMA) return PA_ERR_OPTION;
   if (o->num_ctas < 0 || o->num_ctas > (1 << 20)) return PA_ERR_OPTION;
-  if (o->stages < 0 || o->stages == 1 || o->stages > kMaxStages) return PA_ERR_OPTION;
+  if (o->stages < 0 || o->stages > kMaxSlots / kMaxWarps) return PA_ERR_OPTION;
   return PA_OK;
 }
 
 struct Plan {
-  int D, G, bs, mode, stages;
+  int D, G, bs, mode, warps, ring;
   int part_blocks;
   int grid;  // split kernel CTAs
   size_t smem;
@@ -189,16 +183,17 @@ int choose_mode(const pa_options* o) {
   return c == PA_COMPUTE_SIMT ? kSimt : kMma;
 }
 
-// Stage count: fill about half of an SM's shared memory (two CTAs per SM).
-int choose_stages(const pa_shape* s, const pa_options* o, int mode) {
-  if (o && o->stages > 0) return o->stages;
+// Ring slots per warp: two 16-token stages per warp by default (the loads of
+// the next tile are in flight while one is computed), fewer when shared
+// memory does not hold them, at most what fits in about 220 KB.
+int choose_ring(const pa_shape* s, const pa_options* o, int mode, int W) {
   const int G = s->num_heads / s->num_kv_heads;
-  const SmemLayout L0 = split_smem_layout(s->head_dim, s->block_size, G, s->batch, 0, mode);
-  const int budget = 112 * 1024;
-  int S = (budget - (int)L0.total) / (int)L0.stage_bytes;
-  if (S > kMaxStages) S = kMaxStages;
-  if (S < 2) S = 2;
-  return S;
+  const SmemLayout L0 = split_smem_layout(s->head_dim, G, s->batch, W, 0, mode);
+  int fit = (220 * 1024 - (int)L0.total) / (W * (int)L0.stage_bytes);
+  if (fit > kMaxSlots / W) fit = kMaxSlots / W;
+  if (o && o->stages > 0) return o->stages <= fit ? o->stages : -1;
+  int R = fit < 2 ? fit : 2;
+  return R;
 }
 
 const void* kernel_for(int dtype, int D, int mode) {
@@ -228,11 +223,14 @@ int occupancy(const void* fn, int dev, size_t smem, int* occ_out) {
       return PA_OK;
     }
   }
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
+  bool attr_set = false;
+  for (int i = 0; i < g_nfuncs; ++i)
+    if (g_funcs[i].fn == fn && g_funcs[i].dev == dev) attr_set = true;
+  if (!attr_set && cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kMaxDynamicSmem) != cudaSuccess)
     return PA_ERR_CUDA;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kSplitThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, 32 * kMaxWarps, smem) != cudaSuccess)
     return PA_ERR_CUDA;
   if (occ < 1) return PA_ERR_SHAPE;
   if (g_nfuncs < kFuncCacheSize) g_funcs[g_nfuncs++] = FuncCache{fn, dev, smem, occ};
@@ -268,11 +266,13 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
   p->G = s->num_heads / s->num_kv_heads;
   p->bs = s->block_size;
   p->mode = choose_mode(o);
-  p->stages = choose_stages(s, o, p->mode);
+  p->warps = kMaxWarps;
+  p->ring = choose_ring(s, o, p->mode, p->warps);
+  if (p->ring < 1) return (o && o->stages > 0) ? PA_ERR_OPTION : PA_ERR_SHAPE;
   p->part_blocks = (o && o->partition_tokens > 0) ? o->partition_tokens / s->block_size : 0;
-  const SmemLayout L = split_smem_layout(p->D, p->bs, p->G, s->batch, p->stages, p->mode);
+  const SmemLayout L = split_smem_layout(p->D, p->G, s->batch, p->warps, p->ring, p->mode);
   p->smem = L.total;
-  if (p->smem > 227 * 1024) return PA_ERR_SHAPE;
+  if (p->smem > (size_t)kMaxDynamicSmem) return PA_ERR_SHAPE;
   const bool fixed_grid = o && o->num_ctas > 0;
   if (fixed_grid) p->grid = o->num_ctas;
   if (setup_kernel || !fixed_grid) {
@@ -317,15 +317,15 @@ int get_encoder() {
   return PA_OK;
 }
 
-// 4-D map over a [P, bs, Hkv, D] pool: dims (D, Hkv, bs, P), box (64, 1, bs, 1),
-// 128-byte swizzle.  One box = 64 dims of the bs rows of one kv head of one
+// 4-D map over a [P, bs, Hkv, D] pool: dims (D, Hkv, bs, P), box (64, 1, 16, 1),
+// 128-byte swizzle.  One box = 64 dims of 16 rows of one kv head of one
 // physical block.
 int make_pool_map(CUtensorMap* map, const void* pool, const pa_shape* s) {
   const uint64_t D = (uint64_t)s->head_dim, Hkv = (uint64_t)s->num_kv_heads;
   const uint64_t bs = (uint64_t)s->block_size, P = (uint64_t)s->num_blocks;
   cuuint64_t dims[4] = {D, Hkv, bs, P};
   cuuint64_t strides[3] = {D * 2, Hkv * D * 2, bs * Hkv * D * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)bs, 1};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt =
       s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -383,7 +383,8 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.maxblk = s->max_blocks_per_seq;
   a.P = s->num_blocks;
   a.part_blocks = p.part_blocks;
-  a.stages = p.stages;
+  a.warps = p.warps;
+  a.ring = p.ring;
   a.qscale = scale * 1.4426950408889634f;  // log2(e)
   MergeArgs& m = c->ma;
   m.seqlens = cache_seqlens;
@@ -418,8 +419,9 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
   cudaError_t e = cudaErrorInvalidValue;
 #define PA_LAUNCH(T, DD)                                                                      \
   if (p.D == DD)                                                                              \
-    e = p.mode == kSimt ? launch_split<T, DD, kSimt>(tmk, tmv, c->sa, p.grid, p.smem, stream) \
-                        : launch_split<T, DD, kMma>(tmk, tmv, c->sa, p.grid, p.smem, stream);
+    e = p.mode == kSimt                                                                       \
+            ? launch_split<T, DD, kSimt>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream)   \
+            : launch_split<T, DD, kMma>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream);
   if (s->dtype == PA_BF16) {
     PA_LAUNCH(__nv_bfloat16, 64)
     PA_LAUNCH(__nv_bfloat16, 128)
@@ -436,8 +438,10 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
 int launch_merge_phase(Call* c, cudaStream_t stream) {
   const Plan& p = c->plan;
   const int nseg = p.part_blocks == 0 ? p.grid : c->sa.B * c->sa.Hkv;
-  dim3 grid(p.G * (p.D / 64), (nseg + kMergeSegs - 1) / kMergeSegs);
-  pa_merge_kernel<<<grid, kMergeThreads, 0, stream>>>(c->ma);
+  dim3 grid(nseg, p.G);
+  if (p.D == 64) pa_merge_kernel<64><<<grid, kMergeThreads, 0, stream>>>(c->ma);
+  if (p.D == 128) pa_merge_kernel<128><<<grid, kMergeThreads, 0, stream>>>(c->ma);
+  if (p.D == 256) pa_merge_kernel<256><<<grid, kMergeThreads, 0, stream>>>(c->ma);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -11,12 +11,11 @@
 
 namespace pa {
 
-constexpr int kConsumerWarps = 4;                       // warps that compute
-constexpr int kSplitThreads = 32 * (1 + kConsumerWarps);  // + one producer warp
-constexpr int kMaxStages = 32;
+constexpr int kMaxWarps = 8;   // warps per split CTA (each runs its own TMA ring)
+constexpr int kMaxSlots = 64;  // warps x ring slots
 constexpr int kGMax = 8;       // query heads per kv head handled by one CTA
-constexpr int kMergeSegs = 16;  // segments examined by one merge CTA
-constexpr int kMergeThreads = 256;
+constexpr int kTile = 16;      // tokens per pipeline stage (one mma row tile)
+constexpr int kMergeThreads = 128;
 
 enum Mode { kSimt = 1, kMma = 2 };
 
@@ -32,7 +31,8 @@ struct SplitArgs {
   uint32_t* status;         // sticky PA_STATUS_* bits
   int32_t B, H, Hkv, G, bs, maxblk, P;
   int32_t part_blocks;      // 0 = balanced split
-  int32_t stages;
+  int32_t warps;            // warps per CTA (= blockDim.x / 32)
+  int32_t ring;             // TMA ring slots per warp
   float qscale;             // scale * log2(e): scores are kept in log2 units
 };
 
@@ -62,40 +62,39 @@ struct AppendArgs {
 // Byte offsets inside the split kernel's dynamic shared memory, relative to
 // a 1024-byte aligned base.
 struct SmemLayout {
-  uint32_t full, empty, info, abort_flag;  // pipeline barriers and stage info
-  uint32_t stage;                          // stages: [S][K chunks | V chunks]
+  uint32_t full, info, abort_flag;  // per slot: mbarrier, (valid rows | bad)
+  uint32_t stage;                   // [W][R] stages: K chunks | V chunks, 16 rows each
   uint32_t stage_bytes;
-  uint32_t mo, mm, ml, mbad;               // per-warp partial states for the merge
-  uint32_t qs, ps;                         // CUDA-core path: q (fp32), p per warp
-  uint32_t pre;                            // [B + 1] prefix sums
-  uint32_t total;                          // bytes to request (incl. alignment slack)
+  uint32_t mo, mm, ml, mbad;        // per-warp partial states for the CTA combine
+  uint32_t qs, ps;                  // CUDA-core path: q (fp32), p per warp
+  uint32_t pre;                     // [B + 1] prefix sums
+  uint32_t total;                   // bytes to request (incl. alignment slack)
 };
 
 PA_HD uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-PA_HD SmemLayout split_smem_layout(int D, int bs, int G, int B, int S, int mode) {
+PA_HD SmemLayout split_smem_layout(int D, int G, int B, int W, int R, int mode) {
   SmemLayout L;
   L.full = 0;
-  L.empty = 8 * kMaxStages;
-  L.info = 16 * kMaxStages;
-  L.abort_flag = 20 * kMaxStages;
+  L.info = 8 * kMaxSlots;
+  L.abort_flag = 12 * kMaxSlots;
   L.stage = 1024;
-  L.stage_bytes = 4u * (uint32_t)D * (uint32_t)bs;  // K + V, 2 bytes each
-  uint32_t off = L.stage + (uint32_t)S * L.stage_bytes;
+  L.stage_bytes = 4u * (uint32_t)D * (uint32_t)kTile;  // K + V tiles, 2 bytes each
+  uint32_t off = L.stage + (uint32_t)(W * R) * L.stage_bytes;
   L.mo = off;
-  off += (uint32_t)(kConsumerWarps * G * (D + 4)) * 4u;
+  off += (uint32_t)(W * G * (D + 4)) * 4u;
   L.mm = off;
-  off += kConsumerWarps * kGMax * 4u;
+  off += (uint32_t)W * kGMax * 4u;
   L.ml = off;
-  off += kConsumerWarps * kGMax * 4u;
+  off += (uint32_t)W * kGMax * 4u;
   L.mbad = off;
-  off += 16;
+  off += (uint32_t)W * 4u;
   off = align_up(off, 16);
   if (mode == kSimt) {
     L.qs = off;
     off += (uint32_t)(G * D) * 4u;
     L.ps = off;
-    off += (uint32_t)(kConsumerWarps * bs * kGMax) * 4u;
+    off += (uint32_t)(W * kTile * kGMax) * 4u;
   } else {
     L.qs = L.ps = 0;
   }
@@ -109,7 +108,7 @@ PA_HD SmemLayout split_smem_layout(int D, int bs, int G, int B, int S, int mode)
 // Launchers (explicitly instantiated in pa_split_*.cu).
 template <typename T, int D, int MODE>
 cudaError_t launch_split(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a,
-                         int grid, size_t smem, cudaStream_t stream);
+                         int grid, int threads, size_t smem, cudaStream_t stream);
 
 template <typename T, int D, int MODE>
 const void* split_kernel_ptr();

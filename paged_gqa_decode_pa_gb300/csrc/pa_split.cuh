@@ -1,23 +1,26 @@
 // pa_split.cuh -- phase 1 of paged GQA decode: the persistent split kernel.
 //
-// One CTA = 1 producer warp + 4 consumer warps.  Each CTA walks the pieces
-// the schedule (pa_sched.cuh) gives it.  A piece is a run of physical blocks
-// of one (sequence b, kv head j) segment.
+// One CTA per SM, W warps (8).  Each CTA walks the pieces the schedule
+// (pa_sched.cuh) gives it; a piece is a run of physical blocks of one
+// (sequence b, kv head j) segment, cut into 16-token tiles.  Tile t of a
+// piece belongs to warp t % W.
 //
-//   producer: prefetches the piece's block-table entries (32 per warp load),
-//     validates each id, and streams the K and V rows of kv head j of every
-//     block into a ring of `stages` shared-memory stages with 4-D TMA tensor
-//     loads (box = 64 dims x bs rows, 128-byte swizzle), completing on the
-//     stage's mbarrier.  Block table indirection happens here, once per block
-//     ("Paged Attention Kernel Architecture for BI-V100", section 3).
-//   consumers: block k of the CTA's stream goes to warp k % 4.  A warp runs
-//     the online-softmax recurrence over its blocks for all G query heads of
-//     kv head j at once ("v10_triton_paged_gqa", Core Principle; GQA
-//     amortisation of the BI-V100 design, section 4: each K/V byte is read
-//     from HBM once for the whole group).  At the end of a piece the four
-//     warp states are combined with the (max, exp-sum, weighted-V) combine op
-//     (BI-V100 design, section 2, Levels 1-2) and written either as the final
-//     output or as a partial state for the merge kernel (section 2, Level 3).
+// Every warp runs its own pipeline: a ring of R shared-memory stages, each
+// holding the K and V rows (kv head j) of one 16-token tile.  The warp loads
+// the tile's physical block id from the block table (32 ids per warp-wide
+// load, "Paged Attention Kernel Architecture for BI-V100", section 3: the
+// table indirection), checks it, and lane 0 issues 4-D TMA tensor loads (box
+// = 64 dims x 16 rows, 128-byte swizzle) that complete on the stage's
+// mbarrier.  After computing tile n the warp refills the same stage with
+// tile n + R, so loads of R tiles are always in flight per warp.
+//
+// A warp keeps the online-softmax state (running max, exp-sum, weighted-V
+// accumulator; "v10_triton_paged_gqa", Core Principle) of ALL G query heads
+// of kv head j: each K/V byte is read from HBM once for the whole group (the
+// BI-V100 design, section 4).  At the end of a piece the W warp states are
+// folded with the (max, exp-sum, weighted-V) combine op (section 2, Levels
+// 1-2) and written as the final output or as a partial state for the merge
+// kernel (section 2, Level 3).
 //
 // Scores are kept in log2 units (q is pre-multiplied by scale*log2(e)) so
 // every exponential is one ex2 instruction; the merge kernel uses the same
@@ -132,45 +135,51 @@ struct MmaState {
     bad = false;
   }
 
-  // One block of `bs` tokens, `valid` of them real, K chunks at kb, V at vb.
-  __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, int bs, int valid) {
+  // One 16-token tile, `valid` (1..16) of its rows real; K chunks at kb, V
+  // chunks at vb, each chunk a 128B-swizzled [16][64] tile of 2 KB.
+  __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int valid) {
     const int lane = threadIdx.x & 31;
-    const uint32_t chunk = (uint32_t)bs * 128u;
-    for (int r0 = 0; r0 < valid; r0 += 16) {
-      // ---- S^T = K . Q'^T  (rows: tokens r0..r0+15, cols: heads)
-      float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const uint32_t tok = (uint32_t)r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const uint32_t uh = (uint32_t)(lane >> 4);
+    constexpr uint32_t chunk = kTile * 128u;
+    // ---- S^T = K . Q'^T  (rows: the 16 tokens, cols: heads); four
+    // independent accumulator chains (hi/lo x even/odd k-step)
+    float acc4[4][4] = {};
+    {
+      const uint32_t tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const uint32_t uh = (uint32_t)(lane >> 4);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          const uint32_t addr = kb + (uint32_t)(ks >> 2) * chunk + swz(tok, 2u * (ks & 3) + uh);
-          ldmatrix_x4(addr, a0, a1, a2, a3);
-          mma_16816<T>(sh, a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
-          mma_16816<T>(sl, a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
-        }
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        const uint32_t addr = kb + (uint32_t)(ks >> 2) * chunk + swz(tok, 2u * (ks & 3) + uh);
+        ldmatrix_x4(addr, a0, a1, a2, a3);
+        mma_16816<T>(acc4[ks & 1], a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
+        mma_16816<T>(acc4[2 + (ks & 1)], a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
       }
-      const int tr = r0 + (lane >> 2);
-      float s0 = sh[0] + sl[0], s1 = sh[1] + sl[1], s2 = sh[2] + sl[2], s3 = sh[3] + sl[3];
-      if (tr >= valid) s0 = s1 = -INFINITY;
-      if (tr + 8 >= valid) s2 = s3 = -INFINITY;
-      // ---- online softmax update for heads 2t, 2t+1
-      float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+    }
+    const int tr = lane >> 2;
+    float s0 = (acc4[0][0] + acc4[1][0]) + (acc4[2][0] + acc4[3][0]);
+    float s1 = (acc4[0][1] + acc4[1][1]) + (acc4[2][1] + acc4[3][1]);
+    float s2 = (acc4[0][2] + acc4[1][2]) + (acc4[2][2] + acc4[3][2]);
+    float s3 = (acc4[0][3] + acc4[1][3]) + (acc4[2][3] + acc4[3][3]);
+    if (tr >= valid) s0 = s1 = -INFINITY;
+    if (tr + 8 >= valid) s2 = s3 = -INFINITY;
+    // ---- online softmax update for heads 2t, 2t+1
+    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
-      }
-      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-      const float u0 = (n0 == -INFINITY) ? 0.f : n0;
-      const float u1 = (n1 == -INFINITY) ? 0.f : n1;
-      const float al0 = ex2(m0 - u0), al1 = ex2(m1 - u1);
-      const float p0 = ex2(s0 - u0), p1 = ex2(s1 - u1), p2 = ex2(s2 - u0), p3 = ex2(s3 - u1);
-      l0 = l0 * al0 + (p0 + p2);
-      l1 = l1 * al1 + (p1 + p3);
-      m0 = n0;
-      m1 = n1;
+    for (int off = 4; off < 32; off <<= 1) {
+      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+    }
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    const float u0 = (n0 == -INFINITY) ? 0.f : n0;
+    const float u1 = (n1 == -INFINITY) ? 0.f : n1;
+    const float al0 = ex2(m0 - u0), al1 = ex2(m1 - u1);
+    const float p0 = ex2(s0 - u0), p1 = ex2(s1 - u1), p2 = ex2(s2 - u0), p3 = ex2(s3 - u1);
+    l0 = l0 * al0 + (p0 + p2);
+    l1 = l1 * al1 + (p1 + p3);
+    m0 = n0;
+    m1 = n1;
+    // rescale the accumulator only when some running max moved
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
       for (int dt = 0; dt < D / 16; ++dt) {
         o[dt][0] *= al0;
@@ -178,24 +187,24 @@ struct MmaState {
         o[dt][2] *= al0;
         o[dt][3] *= al1;
       }
-      // ---- P^T fragments (k = tokens, n = heads), hi + lo parts
-      const uint32_t h01 = Cvt<T>::pack(p0, p1), h23 = Cvt<T>::pack(p2, p3);
-      const uint32_t e01 = Cvt<T>::pack(p0 - Cvt<T>::low(h01), p1 - Cvt<T>::high(h01));
-      const uint32_t e23 = Cvt<T>::pack(p2 - Cvt<T>::low(h23), p3 - Cvt<T>::high(h23));
-      const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-      const uint32_t bl0 = movmatrix_trans(e01), bl1 = movmatrix_trans(e23);
-      // ---- O^T += V^T . P^T
-      {
-        const uint32_t tok = (uint32_t)r0 + (lane & 7) + (lane >> 4) * 8;
-        const uint32_t uh = (uint32_t)((lane >> 3) & 1);
+    }
+    // ---- P^T fragments (k = tokens, n = heads), hi + lo parts
+    const uint32_t h01 = Cvt<T>::pack(p0, p1), h23 = Cvt<T>::pack(p2, p3);
+    const uint32_t e01 = Cvt<T>::pack(p0 - Cvt<T>::low(h01), p1 - Cvt<T>::high(h01));
+    const uint32_t e23 = Cvt<T>::pack(p2 - Cvt<T>::low(h23), p3 - Cvt<T>::high(h23));
+    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+    const uint32_t bl0 = movmatrix_trans(e01), bl1 = movmatrix_trans(e23);
+    // ---- O^T += V^T . P^T
+    {
+      const uint32_t tok = (lane & 7) + (lane >> 4) * 8;
+      const uint32_t uh = (uint32_t)((lane >> 3) & 1);
 #pragma unroll
-        for (int dt = 0; dt < D / 16; ++dt) {
-          uint32_t a0, a1, a2, a3;
-          const uint32_t addr = vb + (uint32_t)(dt >> 2) * chunk + swz(tok, 2u * (dt & 3) + uh);
-          ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-          mma_16816<T>(o[dt], a0, a1, a2, a3, bh0, bh1);
-          mma_16816<T>(o[dt], a0, a1, a2, a3, bl0, bl1);
-        }
+      for (int dt = 0; dt < D / 16; ++dt) {
+        uint32_t a0, a1, a2, a3;
+        const uint32_t addr = vb + (uint32_t)(dt >> 2) * chunk + swz(tok, 2u * (dt & 3) + uh);
+        ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+        mma_16816<T>(o[dt], a0, a1, a2, a3, bh0, bh1);
+        mma_16816<T>(o[dt], a0, a1, a2, a3, bl0, bl1);
       }
     }
   }
@@ -252,90 +261,76 @@ struct SimtState {
     bad = false;
   }
 
-  // qs: shared [G][D] fp32 q*scale*log2e.  ps: this warp's [bs][8] fp32.
-  __device__ __forceinline__ void block(uint32_t kb, uint32_t vb, int bs, int valid,
-                                        const float* qs, float* ps, int G) {
+  // One 16-token tile, `valid` (1..16) rows real.  qs: shared [G][D] fp32
+  // q*scale*log2e.  ps: this warp's [16][8] fp32 buffer.  Lanes 0-15 and
+  // 16-31 take the same 16 tokens for the two halves of the G heads.
+  __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int valid, const float* qs,
+                                       float* ps, int G) {
     const int lane = threadIdx.x & 31;
-    const uint32_t chunk = (uint32_t)bs * 128u;
-    // ---------------- q . k : lane <-> token (bs == 16: heads split by half-warp)
-    const int tpass = bs < 32 ? bs : 32;
+    constexpr uint32_t chunk = kTile * 128u;
+    // ---------------- q . k : lane <-> token
     const int GH = (G + 1) >> 1;
-    const int h0 = (bs == 16) ? (lane >> 4) * GH : 0;
-    const int h1 = (bs == 16) ? min(G, h0 + GH) : G;
-    float mx[kGMax];
+    const int h0 = (lane >> 4) * GH;
+    const int h1 = min(G, h0 + GH);
+    const int tt = lane & 15;
+    float s[kGMax];
 #pragma unroll
-    for (int g = 0; g < kGMax; ++g) mx[g] = -INFINITY;
-    for (int tb = 0; tb < bs; tb += tpass) {
-      const int tt = tb + (lane % tpass);
-      float s[kGMax];
-#pragma unroll
-      for (int g = 0; g < kGMax; ++g) s[g] = 0.f;
+    for (int g = 0; g < kGMax; ++g) s[g] = 0.f;
 #pragma unroll 4
-      for (int c8 = 0; c8 < D / 8; ++c8) {
-        const uint4 kr = lds128(kb + (uint32_t)(c8 >> 3) * chunk + swz(tt, c8 & 7));
-        float kf[8];
-        kf[0] = Cvt<T>::low(kr.x);
-        kf[1] = Cvt<T>::high(kr.x);
-        kf[2] = Cvt<T>::low(kr.y);
-        kf[3] = Cvt<T>::high(kr.y);
-        kf[4] = Cvt<T>::low(kr.z);
-        kf[5] = Cvt<T>::high(kr.z);
-        kf[6] = Cvt<T>::low(kr.w);
-        kf[7] = Cvt<T>::high(kr.w);
-#pragma unroll
-        for (int g = 0; g < kGMax; ++g) {
-          if (g >= h0 && g < h1) {
-            const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + c8 * 8);
-            const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + c8 * 8 + 4);
-            float v = s[g];
-            v = fmaf(qa.x, kf[0], v);
-            v = fmaf(qa.y, kf[1], v);
-            v = fmaf(qa.z, kf[2], v);
-            v = fmaf(qa.w, kf[3], v);
-            v = fmaf(qb.x, kf[4], v);
-            v = fmaf(qb.y, kf[5], v);
-            v = fmaf(qb.z, kf[6], v);
-            v = fmaf(qb.w, kf[7], v);
-            s[g] = v;
-          }
-        }
-      }
-      const bool live = tt < valid;
+    for (int c8 = 0; c8 < D / 8; ++c8) {
+      const uint4 kr = lds128(kb + (uint32_t)(c8 >> 3) * chunk + swz(tt, c8 & 7));
+      float kf[8];
+      kf[0] = Cvt<T>::low(kr.x);
+      kf[1] = Cvt<T>::high(kr.x);
+      kf[2] = Cvt<T>::low(kr.y);
+      kf[3] = Cvt<T>::high(kr.y);
+      kf[4] = Cvt<T>::low(kr.z);
+      kf[5] = Cvt<T>::high(kr.z);
+      kf[6] = Cvt<T>::low(kr.w);
+      kf[7] = Cvt<T>::high(kr.w);
 #pragma unroll
       for (int g = 0; g < kGMax; ++g) {
-        if (!(g >= h0 && g < h1) || !live) s[g] = -INFINITY;
-        // stash raw scores in the p buffer; exponentiated below
-        if (g >= h0 && g < h1) ps[tt * kGMax + g] = s[g];
-        mx[g] = fmaxf(mx[g], s[g]);
+        if (g >= h0 && g < h1) {
+          const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + c8 * 8);
+          const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + c8 * 8 + 4);
+          float v = s[g];
+          v = fmaf(qa.x, kf[0], v);
+          v = fmaf(qa.y, kf[1], v);
+          v = fmaf(qa.z, kf[2], v);
+          v = fmaf(qa.w, kf[3], v);
+          v = fmaf(qb.x, kf[4], v);
+          v = fmaf(qb.y, kf[5], v);
+          v = fmaf(qb.z, kf[6], v);
+          v = fmaf(qb.w, kf[7], v);
+          s[g] = v;
+        }
       }
     }
-    // block max per head, made warp-uniform
+    const bool live = tt < valid;
+    float mx[kGMax];
+#pragma unroll
+    for (int g = 0; g < kGMax; ++g) {
+      const bool mine = g >= h0 && g < h1;
+      if (!mine || !live) s[g] = -INFINITY;
+      mx[g] = s[g];
+    }
+    // tile max per head, made warp-uniform (other half's heads are -inf here)
 #pragma unroll
     for (int g = 0; g < kGMax; ++g) {
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xffffffffu, mx[g], off));
     }
-    float alpha[kGMax], mu[kGMax];
+    float alpha[kGMax];
 #pragma unroll
     for (int g = 0; g < kGMax; ++g) {
       const float n = fmaxf(m[g], mx[g]);
-      mu[g] = (n == -INFINITY) ? 0.f : n;
-      alpha[g] = ex2(m[g] - mu[g]);
+      const float mu = (n == -INFINITY) ? 0.f : n;
+      alpha[g] = ex2(m[g] - mu);
       m[g] = n;
-      l[g] *= alpha[g];
-    }
-    __syncwarp();
-    // p = 2^(s - m) for this lane's (token, heads), back into the buffer
-    for (int tb = 0; tb < bs; tb += tpass) {
-      const int tt = tb + (lane % tpass);
-#pragma unroll
-      for (int g = 0; g < kGMax; ++g) {
-        if (g >= h0 && g < h1) {
-          const float p = (tt < valid) ? ex2(ps[tt * kGMax + g] - mu[g]) : 0.f;
-          ps[tt * kGMax + g] = p;
-          l[g] += p;
-        }
-      }
+      const bool mine = g >= h0 && g < h1;
+      const float p = (mine && live) ? ex2(s[g] - mu) : 0.f;
+      l[g] = l[g] * alpha[g] + p;
+      if (mine) ps[tt * kGMax + g] = p;
     }
     __syncwarp();
     // ---------------- p . V : lane <-> dimension pair
@@ -396,28 +391,24 @@ struct SimtState {
   }
 };
 
-// CTA-level combine of the four warp states of one piece (consumer threads).
+// CTA-level combine of the W warp states of one piece (all threads).
 template <int D>
 __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem, const SmemLayout& L,
-                                              const Piece& pc) {
-  const int ct = threadIdx.x - 32;
+                                              const Piece& pc, int W) {
   const int G = a.G;
   const float* mm = reinterpret_cast<const float*>(smem + L.mm);
   const float* ml = reinterpret_cast<const float*>(smem + L.ml);
   const float* mo = reinterpret_cast<const float*>(smem + L.mo);
   const int* mbad = reinterpret_cast<const int*>(smem + L.mbad);
   bool bad = false;
-#pragma unroll
-  for (int w = 0; w < kConsumerWarps; ++w) bad |= (mbad[w] != 0);
+  for (int w = 0; w < W; ++w) bad |= (mbad[w] != 0);
   const float qnan = __int_as_float(0x7fc00000);
-  for (int idx = ct; idx < G * D; idx += 32 * kConsumerWarps) {
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int g = idx / D, dim = idx % D;
     float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * kGMax + g]);
+    for (int w = 0; w < W; ++w) M = fmaxf(M, mm[w * kGMax + g]);
     float Lsum = 0.f, o = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
+    for (int w = 0; w < W; ++w) {
       const float mw = mm[w * kGMax + g];
       const float e = (mw == -INFINITY) ? 0.f : ex2(mw - M);
       Lsum = fmaf(e, ml[w * kGMax + g], Lsum);
@@ -436,32 +427,104 @@ __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem,
   }
 }
 
+// Number of the piece's tiles that belong to warp w (tiles t = w, w+W, ...).
+__device__ __forceinline__ int warp_tiles(const Piece& pc, int subs, int w, int W) {
+  const int nt = (pc.blk1 - pc.blk0) * subs;
+  return nt > w ? (nt - w + W - 1) / W : 0;
+}
+
+// The issuing side of one warp's pipeline: walks the warp's tile stream
+// (all pieces of the CTA, tiles w, w+W, ... of each) ahead of the computing
+// side and loads tile n into ring slot n % R.
+struct Issuer {
+  PieceIter it;
+  Piece pc;
+  int i, cnt;        // next tile index (of this warp) in pc, and their count
+  int cache_base;    // tile index whose table entry lane 0 holds, -1 = none
+  int32_t entry;     // this lane's table entry (tile cache_base + lane)
+  int32_t len;       // cache_seqlens[pc.b]
+  uint32_t n;        // next stream position
+  bool done;
+};
+
+template <int D>
+__device__ __forceinline__ void issue_next(Issuer& is, const SplitArgs& a, const CUtensorMap* tmk,
+                                           const CUtensorMap* tmv, uint8_t* smem, uint32_t base,
+                                           const SmemLayout& L, int w, int W, int R, int subs) {
+  const int lane = threadIdx.x & 31;
+  while (!is.done && is.i >= is.cnt) {
+    if (!is.it.next(is.pc)) {
+      is.done = true;
+      break;
+    }
+    is.i = 0;
+    is.cnt = warp_tiles(is.pc, subs, w, W);
+    is.cache_base = -1;
+    is.len = __ldg(a.seqlens + is.pc.b);
+  }
+  if (is.done) return;
+  if (is.cache_base < 0 || is.i >= is.cache_base + 32) {
+    is.cache_base = is.i;
+    const int ii = is.i + lane;
+    int32_t e = 0;
+    if (ii < is.cnt) {
+      const int t = w + W * ii;
+      e = __ldg(a.table + (int64_t)is.pc.b * a.maxblk + is.pc.blk0 + t / subs);
+    }
+    is.entry = e;
+  }
+  const int32_t phys = __shfl_sync(0xffffffffu, is.entry, is.i - is.cache_base);
+  if (lane == 0) {
+    const int t = w + W * is.i;
+    const int blk = is.pc.blk0 + t / subs, h = t % subs;
+    const int valid = max(0, min(kTile, is.len - blk * a.bs - h * kTile));
+    const bool bad = phys < 0 || phys >= a.P;
+    const uint32_t slot = (uint32_t)w * R + is.n % (uint32_t)R;
+    const uint32_t full = base + L.full + 8 * slot;
+    reinterpret_cast<volatile uint32_t*>(smem + L.info)[slot] = (uint32_t)valid | (bad ? kInfoBad : 0u);
+    if (bad || valid == 0) {
+      if (bad && h == 0) atomicOr(a.status, kStatusBadBlock);
+      mbar_arrive(full);
+    } else {
+      constexpr int NC = D / 64;
+      constexpr uint32_t chunk = kTile * 128u;
+      mbar_arrive_expect_tx(full, L.stage_bytes);
+      const uint32_t kdst = base + L.stage + slot * L.stage_bytes;
+      const uint32_t vdst = kdst + NC * chunk;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        tma_load_4d(kdst + c * chunk, tmk, full, c * 64, is.pc.j, h * kTile, phys);
+        tma_load_4d(vdst + c * chunk, tmv, full, c * 64, is.pc.j, h * kTile, phys);
+      }
+    }
+  }
+  ++is.i;
+  ++is.n;
+}
+
 template <typename T, int D, int MODE>
-__global__ void __launch_bounds__(kSplitThreads, 1)
+__global__ void __launch_bounds__(32 * kMaxWarps, 1)
     pa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                     const SplitArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
-  const SmemLayout L = split_smem_layout(D, a.bs, a.G, a.B, a.stages, MODE);
+  const int W = a.warps, R = a.ring;
+  const SmemLayout L = split_smem_layout(D, a.G, a.B, W, R, MODE);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int S = a.stages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   int32_t* pre = reinterpret_cast<int32_t*>(smem + L.pre);
-  __shared__ int32_t scan_scratch[kSplitThreads / 32];
+  __shared__ int32_t scan_scratch[kMaxWarps];
 
   if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(base + L.full + 8 * s, 1);
-      mbar_init(base + L.empty + 8 * s, 1);
-    }
+    for (int s = 0; s < W * R; ++s) mbar_init(base + L.full + 8 * s, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (lane == 0) {
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
   }
@@ -493,156 +556,102 @@ __global__ void __launch_bounds__(kSplitThreads, 1)
     }
   }
 
+  const int w = warp;
+  const int subs = a.bs / kTile;  // 16-token tiles per physical block
+  constexpr int NC = D / 64;
+  constexpr uint32_t chunk = kTile * 128u;
+
+  // ---- the warp's issuing side: prime the ring with the first R tiles
+  Issuer is;
+  is.it.init(pre, a.seqlens, sched, cta);
+  is.i = is.cnt = 0;
+  is.cache_base = -1;
+  is.entry = 0;
+  is.len = 0;
+  is.n = 0;
+  is.done = false;
+  for (int r = 0; r < R; ++r) issue_next<D>(is, a, &tmk, &tmv, smem, base, L, w, W, R, subs);
+
+  // ---- the warp's computing side
   PieceIter it;
   it.init(pre, a.seqlens, sched, cta);
   Piece pc;
-  const uint32_t stage_bytes = L.stage_bytes;
-  const uint32_t chunk = (uint32_t)a.bs * 128u;
-  constexpr int NC = D / 64;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    const uint64_t policy = l2_policy_evict_first();
-    uint32_t k = 0;
-    bool stop = false;
-    while (!stop && it.next(pc)) {
-      const int32_t len = __ldg(a.seqlens + pc.b);
-      const int32_t* trow = a.table + (int64_t)pc.b * a.maxblk;
-      for (int c0 = pc.blk0; c0 < pc.blk1 && !stop; c0 += 32) {
-        const int idx = c0 + lane;
-        const int32_t e = (idx < pc.blk1) ? __ldg(trow + idx) : 0;
-        const int n = min(32, pc.blk1 - c0);
-        for (int t = 0; t < n; ++t) {
-          const int32_t phys = __shfl_sync(0xffffffffu, e, t);
-          if (lane == 0 && !stop) {
-            const uint32_t s = k % (uint32_t)S;
-            const uint32_t full = base + L.full + 8 * s, empty = base + L.empty + 8 * s;
-            bool ok = true;
-            if (k >= (uint32_t)S) ok = mbar_wait_bounded(empty, ((k / S) + 1) & 1, abort_flag, kWaitLimitNs);
-            if (!ok) {
-              atomicOr(a.status, kStatusTimeout);
-              stop = true;
-            } else {
-              const int blk = c0 + t;
-              const int valid = min(a.bs, len - blk * a.bs);
-              const bool bad = phys < 0 || phys >= a.P;
-              reinterpret_cast<volatile uint32_t*>(smem + L.info)[s] =
-                  (uint32_t)valid | (bad ? kInfoBad : 0u);
-              if (bad) {
-                atomicOr(a.status, kStatusBadBlock);
-                mbar_arrive(full);
-              } else {
-                mbar_arrive_expect_tx(full, stage_bytes);
-                const uint32_t kdst = base + L.stage + s * stage_bytes;
-                const uint32_t vdst = kdst + NC * chunk;
-#pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                  tma_load_4d(kdst + c * chunk, &tmk, full, c * 64, pc.j, 0, phys, policy);
-                  tma_load_4d(vdst + c * chunk, &tmv, full, c * 64, pc.j, 0, phys, policy);
-                }
-              }
-            }
-          }
-          stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
-          if (stop) break;
-          ++k;
-        }
-      }
+  uint32_t n = 0;  // stream position being consumed
+  MmaState<T, D> mst;
+  SimtState<T, D> sst;
+  float* qs = reinterpret_cast<float*>(smem + L.qs);
+  float* ps = reinterpret_cast<float*>(smem + L.ps) + w * kTile * kGMax;
+  while (it.next(pc)) {
+    if constexpr (MODE == kMma) {
+      mst.load_q(a, pc.b, pc.j);
+      mst.reset();
+    } else {
+      // q * scale * log2e for the G heads of kv head j (shared by the warps)
+      const uint16_t* qrow = a.q + ((int64_t)pc.b * a.H + (int64_t)pc.j * a.G) * D;
+      for (int i = tid; i < a.G * D; i += blockDim.x) qs[i] = Cvt<T>::widen(__ldg(qrow + i)) * a.qscale;
+      named_bar_sync(1, blockDim.x);
+      sst.reset();
     }
-    if (stop && lane == 0) {
-      // Drain: wait (bounded, ignoring the abort flag) for the copies this
-      // warp issued into the last min(k, S) stages before the CTA may exit.
-      volatile int never = 0;
-      const uint32_t first = k > (uint32_t)S ? k - (uint32_t)S : 0u;
-      for (uint32_t kk = first; kk < k; ++kk) {
-        const uint32_t s = kk % (uint32_t)S;
-        mbar_wait_bounded(base + L.full + 8 * s, (kk / S) & 1, &never, kWaitLimitNs / 4);
-      }
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int w = warp - 1;
-  uint32_t k = 0;
-  if constexpr (MODE == kMma) {
-    MmaState<T, D> st;
-    while (it.next(pc)) {
-      st.load_q(a, pc.b, pc.j);
-      st.reset();
-      for (int blk = pc.blk0; blk < pc.blk1; ++blk, ++k) {
-        if ((int)(k % kConsumerWarps) != w) continue;
-        const uint32_t s = k % (uint32_t)S;
-        const bool ok = mbar_wait_bounded(base + L.full + 8 * s, (k / S) & 1, abort_flag, kWaitLimitNs);
-        const uint32_t info = reinterpret_cast<volatile uint32_t*>(smem + L.info)[s];
-        const int valid = (int)(info & 0xffffu);
-        if (!ok || (info & kInfoBad)) {
-          st.bad = true;
-          if (!ok && lane == 0) atomicOr(a.status, kStatusTimeout);
-        } else {
-          const uint32_t kb = base + L.stage + s * stage_bytes;
-          const uint32_t vb = kb + NC * chunk;
-          if (valid < a.bs) {
+    bool bad = false;
+    const int cnt = warp_tiles(pc, subs, w, W);
+    for (int i = 0; i < cnt; ++i, ++n) {
+      const uint32_t slot = (uint32_t)w * R + n % (uint32_t)R;
+      const bool ok = mbar_wait_bounded(base + L.full + 8 * slot, (n / R) & 1, abort_flag, kWaitLimitNs);
+      const uint32_t info = reinterpret_cast<volatile uint32_t*>(smem + L.info)[slot];
+      const int valid = (int)(info & 0xffffu);
+      if (!ok || (info & kInfoBad)) {
+        bad = true;
+        if (!ok && lane == 0) atomicOr(a.status, kStatusTimeout);
+      } else if (valid > 0) {
+        const uint32_t kb = base + L.stage + slot * L.stage_bytes;
+        const uint32_t vb = kb + NC * chunk;
+        if constexpr (MODE == kMma) {
+          if (valid < kTile) {
             // zero the V rows past the sequence end so that p = 0 rows add 0
-            const int rows = a.bs - valid;
+            const int rows = kTile - valid;
             for (int u = lane; u < rows * 8 * NC; u += 32) {
               const int c = u / (rows * 8), rem = u % (rows * 8);
               sts128(vb + c * chunk + (uint32_t)(valid + rem / 8) * 128u + (rem % 8) * 16u,
                      make_uint4(0u, 0u, 0u, 0u));
             }
             fence_proxy_async_smem();
-            __syncwarp();
           }
-          st.block(kb, vb, a.bs, valid);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(base + L.empty + 8 * s);
-      }
-      st.publish(smem, L, w, a.G);
-      named_bar_sync(1, 32 * kConsumerWarps);
-      combine_piece<D>(a, smem, L, pc);
-      named_bar_sync(1, 32 * kConsumerWarps);
-    }
-  } else {
-    SimtState<T, D> st;
-    float* qs = reinterpret_cast<float*>(smem + L.qs);
-    float* ps = reinterpret_cast<float*>(smem + L.ps) + w * a.bs * kGMax;
-    const int ct = tid - 32;
-    while (it.next(pc)) {
-      // q * scale * log2e for the G heads of kv head j (shared by the warps)
-      const uint16_t* qrow = a.q + ((int64_t)pc.b * a.H + (int64_t)pc.j * a.G) * D;
-      for (int i = ct; i < a.G * D; i += 32 * kConsumerWarps)
-        qs[i] = Cvt<T>::widen(__ldg(qrow + i)) * a.qscale;
-      named_bar_sync(1, 32 * kConsumerWarps);
-      st.reset();
-      for (int blk = pc.blk0; blk < pc.blk1; ++blk, ++k) {
-        if ((int)(k % kConsumerWarps) != w) continue;
-        const uint32_t s = k % (uint32_t)S;
-        const bool ok = mbar_wait_bounded(base + L.full + 8 * s, (k / S) & 1, abort_flag, kWaitLimitNs);
-        const uint32_t info = reinterpret_cast<volatile uint32_t*>(smem + L.info)[s];
-        const int valid = (int)(info & 0xffffu);
-        if (!ok || (info & kInfoBad)) {
-          st.bad = true;
-          if (!ok && lane == 0) atomicOr(a.status, kStatusTimeout);
+          __syncwarp();
+          mst.tile(kb, vb, valid);
         } else {
-          const uint32_t kb = base + L.stage + s * stage_bytes;
-          st.block(kb, kb + NC * chunk, a.bs, valid, qs, ps, a.G);
+          sst.tile(kb, vb, valid, qs, ps, a.G);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(base + L.empty + 8 * s);
       }
-      st.publish(smem, L, w, a.G);
-      named_bar_sync(1, 32 * kConsumerWarps);
-      combine_piece<D>(a, smem, L, pc);
-      named_bar_sync(1, 32 * kConsumerWarps);
+      __syncwarp();
+      if (*abort_flag) is.done = true;  // stop issuing after a timeout
+      issue_next<D>(is, a, &tmk, &tmv, smem, base, L, w, W, R, subs);
+    }
+    if constexpr (MODE == kMma) {
+      mst.bad |= bad;
+      mst.publish(smem, L, w, a.G);
+    } else {
+      sst.bad |= bad;
+      sst.publish(smem, L, w, a.G);
+    }
+    named_bar_sync(1, blockDim.x);
+    combine_piece<D>(a, smem, L, pc, W);
+    named_bar_sync(1, blockDim.x);
+  }
+  if (*abort_flag && lane == 0) {
+    // Drain: wait (bounded, ignoring the abort flag) for this warp's copies
+    // still in flight before the CTA may exit.
+    volatile int never = 0;
+    for (uint32_t kk = n; kk < is.n; ++kk) {
+      const uint32_t slot = (uint32_t)w * R + kk % (uint32_t)R;
+      mbar_wait_bounded(base + L.full + 8 * slot, (kk / R) & 1, &never, kWaitLimitNs / 4);
     }
   }
 }
 
 template <typename T, int D, int MODE>
 cudaError_t launch_split(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a,
-                         int grid, size_t smem, cudaStream_t stream) {
-  pa_split_kernel<T, D, MODE><<<grid, kSplitThreads, smem, stream>>>(tmk, tmv, a);
+                         int grid, int threads, size_t smem, cudaStream_t stream) {
+  pa_split_kernel<T, D, MODE><<<grid, threads, smem, stream>>>(tmk, tmv, a);
   return cudaGetLastError();
 }
 
@@ -655,6 +664,6 @@ const void* split_kernel_ptr() {
 
 #define PA_INSTANTIATE_SPLIT(T, D, MODE)                                                     \
   template cudaError_t pa::launch_split<T, D, MODE>(const CUtensorMap&, const CUtensorMap&,  \
-                                                    const pa::SplitArgs&, int, size_t,       \
+                                                    const pa::SplitArgs&, int, int, size_t,  \
                                                     cudaStream_t);                           \
   template const void* pa::split_kernel_ptr<T, D, MODE>();

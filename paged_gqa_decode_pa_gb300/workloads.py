@@ -274,11 +274,17 @@ def serving_mix_lengths(seed: int = 5, B: int = 256) -> np.ndarray:
     return np.clip(np.round(x), 1, 32768).astype(np.int32)
 
 
-def serving_mix_b256_g4_d128(seed: int = 5, poison: bool = False) -> Workload:
-    lens = serving_mix_lengths(seed)
+def serving_mix_b256_g4_d128(seed: int = 5, poison: bool = False, B: int = 256) -> Workload:
+    lens = serving_mix_lengths(seed, B)
     return random_workload(lens, 32, 8, 128, 32, dtype=BF16, seed=seed + 1000, maxblk=1024,
                            outlier_frac=0.01, outlier_scale=8.0, poison=poison,
-                           name="serving_mix_b256_g4_d128")
+                           name=f"serving_mix_b{B}_g4_d128")
+
+
+def serving_mix_b32_g4_d128(seed: int = 5, poison: bool = False) -> Workload:
+    """The serving mix at 32 sequences (~0.4 GB of K/V, still above L2): the
+    size used for detailed profiler captures."""
+    return serving_mix_b256_g4_d128(seed, poison, B=32)
 
 
 WORKLOADS = {
@@ -287,6 +293,7 @@ WORKLOADS = {
     "long_ctx_100k_g6_d256": long_ctx_100k_g6_d256,
     "prefix_share_b64_g8_d128": prefix_share_b64_g8_d128,
     "serving_mix_b256_g4_d128": serving_mix_b256_g4_d128,
+    "serving_mix_b32_g4_d128": serving_mix_b32_g4_d128,
 }
 
 

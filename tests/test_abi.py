@@ -66,7 +66,7 @@ def test_rejects_bad_arguments_before_any_cuda_call():
         assert call_decode(bad, o) == pg.PA_ERR_SHAPE
     assert call_decode(s, pg.options(partition_tokens=48, num_ctas=8)) == pg.PA_ERR_OPTION
     assert call_decode(s, pg.options(compute=9, num_ctas=8)) == pg.PA_ERR_OPTION
-    assert call_decode(s, pg.options(stages=1, num_ctas=8)) == pg.PA_ERR_OPTION
+    assert call_decode(s, pg.options(stages=-1, num_ctas=8)) == pg.PA_ERR_OPTION
     assert call_decode(s, pg.options(stages=99, num_ctas=8)) == pg.PA_ERR_OPTION
     # an empty batch is a no-op and needs no pointers
     assert call_decode(shape(B=0), o, q=None, k=None, v=None, t=None, sl=None, out=None,
