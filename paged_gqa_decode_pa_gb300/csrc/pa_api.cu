@@ -30,54 +30,56 @@ namespace {
 template <int D>
 __device__ __forceinline__ void merge_segment_head(const MergeArgs& a, const MergeSeg& ms, int g) {
   constexpr int NV = D / 32;  // dims per lane: lane + 32 i
+  constexpr int NW = kMergeThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  __shared__ float wm[kMergeThreads / 32], wl[kMergeThreads / 32];
-  __shared__ float wacc[kMergeThreads / 32][D];
-  float m = -INFINITY, l = 0.f, acc[NV];
+  __shared__ float red[NW];
+  __shared__ float wl[NW];
+  __shared__ float wacc[NW][D];
+  // pass 1: M = max_p m_p (pieces spread over all threads)
+  float m = -INFINITY;
+  for (int p = tid; p < ms.np; p += kMergeThreads) m = fmaxf(m, a.ws_ml[(ms.slot(p) * a.G + g) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red[w] = m;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int v = 1; v < NW; ++v) M = fmaxf(M, red[v]);
+  // pass 2: warp w sums pieces w, w+NW, ... with weights 2^(m_p - M); the
+  // iterations are independent, so their loads overlap
+  float l = 0.f, acc[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) acc[i] = 0.f;
-  for (int p = w; p < ms.np; p += kMergeThreads / 32) {
+#pragma unroll 4
+  for (int p = w; p < ms.np; p += NW) {
     const int64_t s = ms.slot(p);
-    const float mp = a.ws_ml[(s * a.G + g) * 2];
-    const float lp = a.ws_ml[(s * a.G + g) * 2 + 1];
+    const float e = ex2(a.ws_ml[(s * a.G + g) * 2] - M);
+    l = fmaf(e, a.ws_ml[(s * a.G + g) * 2 + 1], l);
     const float* ap = a.ws_acc + (s * a.G + g) * D;
-    const float mn = fmaxf(m, mp);
-    const float sa = (m == -INFINITY) ? 0.f : ex2(m - mn);
-    const float sb = ex2(mp - mn);
-    l = l * sa + lp * sb;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) acc[i] = acc[i] * sa + ap[lane + 32 * i] * sb;
-    m = mn;
+    for (int i = 0; i < NV; ++i) acc[i] = fmaf(e, ap[lane + 32 * i], acc[i]);
   }
-  if (lane == 0) {
-    wm[w] = m;
-    wl[w] = l;
-  }
+  if (lane == 0) wl[w] = l;
 #pragma unroll
   for (int i = 0; i < NV; ++i) wacc[w][lane + 32 * i] = acc[i];
   __syncthreads();
-  if (w == 0) {
-    float M = -INFINITY;
+  float L = 0.f;
 #pragma unroll
-    for (int v = 0; v < kMergeThreads / 32; ++v) M = fmaxf(M, wm[v]);
-    float Lsum = 0.f, o[NV];
+  for (int v = 0; v < NW; ++v) L += wl[v];
+  float* dst = a.out + ((int64_t)ms.b * a.H + (int64_t)ms.j * a.G + g) * D;
+  for (int d = tid; d < D; d += kMergeThreads) {
+    float o = 0.f;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) o[i] = 0.f;
-#pragma unroll
-    for (int v = 0; v < kMergeThreads / 32; ++v) {
-      const float e = (wm[v] == -INFINITY) ? 0.f : ex2(wm[v] - M);
-      Lsum = fmaf(e, wl[v], Lsum);
-#pragma unroll
-      for (int i = 0; i < NV; ++i) o[i] = fmaf(e, wacc[v][lane + 32 * i], o[i]);
-    }
-    float* dst = a.out + ((int64_t)ms.b * a.H + (int64_t)ms.j * a.G + g) * D;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) dst[lane + 32 * i] = o[i] / Lsum;
+    for (int v = 0; v < NW; ++v) o += wacc[v][d];
+    dst[d] = o / L;
   }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs a) {
+  // With programmatic dependent launch this grid may start while the split
+  // kernel is finishing: wait until its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int seg = blockIdx.x, g = blockIdx.y;
   const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas};
   int4 desc = make_int4(-1, 0, 0, 0);
@@ -435,14 +437,27 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-int launch_merge_phase(Call* c, cudaStream_t stream) {
+// `overlap`: launch as a programmatic dependent of the split kernel that was
+// just enqueued on the same stream (its CTAs may be scheduled while the
+// split kernel drains; griddepcontrol.wait orders the reads).
+int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   const Plan& p = c->plan;
   const int nseg = p.part_blocks == 0 ? p.grid : c->sa.B * c->sa.Hkv;
-  dim3 grid(nseg, p.G);
-  if (p.D == 64) pa_merge_kernel<64><<<grid, kMergeThreads, 0, stream>>>(c->ma);
-  if (p.D == 128) pa_merge_kernel<128><<<grid, kMergeThreads, 0, stream>>>(c->ma);
-  if (p.D == 256) pa_merge_kernel<256><<<grid, kMergeThreads, 0, stream>>>(c->ma);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nseg, p.G);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (p.D == 64) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<64>, c->ma);
+  if (p.D == 128) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<128>, c->ma);
+  if (p.D == 256) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<256>, c->ma);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace
@@ -481,7 +496,7 @@ int pa_decode_merge(const pa_shape* shape, const pa_options* options, const void
   int rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                    workspace, workspace_bytes, false, &c);
   if (rc) return rc;
-  return launch_merge_phase(&c, reinterpret_cast<cudaStream_t>(stream));
+  return launch_merge_phase(&c, reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 int pa_decode(const pa_shape* shape, const pa_options* options, const void* q,
@@ -496,7 +511,7 @@ int pa_decode(const pa_shape* shape, const pa_options* options, const void* q,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = launch_split_phase(shape, k_cache, v_cache, &c, st);
   if (rc) return rc;
-  return launch_merge_phase(&c, st);
+  return launch_merge_phase(&c, st, true);
 }
 
 int pa_cache_append(const pa_shape* shape, const void* k_new, const void* v_new, void* k_cache,

@@ -529,6 +529,8 @@ __global__ void __launch_bounds__(32 * kMaxWarps, 1)
     tma_prefetch_desc(&tmv);
   }
   build_prefix(a, pre, scan_scratch);  // contains __syncthreads
+  // The merge kernel may be scheduled now; it waits for this grid to finish.
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, (int32_t)gridDim.x};
   const int cta = blockIdx.x;
