@@ -54,11 +54,16 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+SPLIT_SOURCES = ("pa_split.cuh", "pa_ptx.cuh", "pa_kernels.cuh", "pa_sched.cuh")
+
+
 def source_hash() -> str:
-    """Hash of the kernel sources: ncu traffic figures are tied to it."""
+    """Hash of the split kernel's sources: recorded ncu traffic is tied to it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_gqa_decode_pa_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    names = sorted(f for f in os.listdir(csrc)
+                   if f in SPLIT_SOURCES or (f.startswith("pa_split_") and f.endswith(".cu")))
+    for f in names:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
@@ -144,6 +149,22 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def max_over_ranks(values, device="cpu"):
+    """Element-wise max of per-rank timings over all ranks (a no-op when
+    torch.distributed is not initialised)."""
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbs(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """All ranks' bytes of one step divided by the slowest rank's step time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
 
 
 def make_workload(name):
@@ -339,16 +360,13 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / Ke
 
     # ---- max over ranks
-    vals = torch.tensor([total_ms, e2e_ms, float(np.mean(split_ms)), float(np.mean(merge_ms))],
-                        dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
-    total_ms, e2e_ms, split_avg_ms, merge_avg_ms = [float(x) for x in vals.tolist()]
+    total_ms, e2e_ms, split_avg_ms, merge_avg_ms = max_over_ranks(
+        [total_ms, e2e_ms, float(np.mean(split_ms)), float(np.mean(merge_ms))], dev)
     if rank != 0:
         return
     ms_per_step = total_ms / K
-    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
-    e2e_value = world * kv_bytes / (e2e_ms * 1e-3) / 1e9
+    value = whole_job_gbs(kv_bytes, world, ms_per_step)
+    e2e_value = whole_job_gbs(kv_bytes, world, e2e_ms)
     peak, peak_kind = peaks()
     achieved = kv_bytes / (split_avg_ms * 1e-3) / 1e9
     opts_key = f"part={args.partition_tokens},compute={args.compute},stages={args.stages}"
