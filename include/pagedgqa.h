@@ -74,6 +74,8 @@ typedef struct CUstream_st* pa_stream_t;
 #define PA_ERR_WORKSPACE (-4)   /* workspace smaller than pa_workspace_size */
 #define PA_ERR_CUDA (-5)        /* a CUDA runtime/driver call failed */
 #define PA_ERR_OPTION (-6)      /* invalid pa_options value */
+#define PA_ERR_SCRATCH_LIMIT (-7) /* pa_decode_noalloc: needs more scratch than
+                                     PA_STATIC_SCRATCH_BYTES */
 
 /* Device status bits (sticky in the workspace status word). */
 #define PA_STATUS_BAD_BLOCK 0x1u   /* a table entry inside a sequence's length is
@@ -182,6 +184,33 @@ int pa_read_status(void* workspace, uint32_t* flags, pa_stream_t stream);
 
 /* Text for a return code (negative) or a status bit set (positive). */
 const char* pa_status_string(int code);
+
+/* pa_decode without a workspace: nothing is allocated, by the caller or
+ * by the library.  (No page describes this; it serves callers that cannot
+ * allocate device memory where they run decode -- e.g. a plugin whose host
+ * framework owns all device allocations, or a serving loop that fixes its
+ * memory at start-up and may not call cudaMalloc on its hot path.)
+ *
+ * Same arguments and result as pa_decode, minus the workspace.  The scratch
+ * the kernels need lives in one static device array of PA_STATIC_SCRATCH_BYTES
+ * that every GPU loading this library holds until the process exits.  A
+ * problem whose pa_workspace_size exceeds that size is rejected with
+ * PA_ERR_SCRATCH_LIMIT before anything is enqueued (the default balanced
+ * split needs well under 4 MiB for B <= PA_MAX_BATCH, G <= 8, d <= 256 on a
+ * 152-SM GPU; large fixed partitions may not fit).
+ *   status: device pointer to a uint32 that receives the PA_STATUS_* bits
+ *           (OR-ed in; the caller zeroes it), or NULL to drop them.
+ * The first call on each device looks up the array's device address and
+ * zeroes its status word (with that device current); make that first call
+ * before any stream capture.  All calls share the one array and it keeps
+ * the previous call's contents (each call rewrites everything it reads), so
+ * two calls that may overlap on the GPU -- on different streams, or from
+ * different threads -- race and give wrong results: serialise them. */
+#define PA_STATIC_SCRATCH_BYTES (8u << 20)
+int pa_decode_noalloc(const pa_shape* shape, const pa_options* options, const void* q,
+                      const void* k_cache, const void* v_cache, const int32_t* block_table,
+                      const int32_t* cache_seqlens, float scale, float* out, uint32_t* status,
+                      pa_stream_t stream);
 
 /* Host replica of the device work split, for inspection and tests.  Given
  * host lengths, lists the pieces CTA `cta` of a grid of `num_ctas` processes:

@@ -23,6 +23,7 @@ PA_ERR_ALIGN = -3
 PA_ERR_WORKSPACE = -4
 PA_ERR_CUDA = -5
 PA_ERR_OPTION = -6
+PA_ERR_SCRATCH_LIMIT = -7
 
 PA_STATUS_BAD_BLOCK = 0x1
 PA_STATUS_BAD_SEQLEN = 0x2
@@ -40,7 +41,7 @@ _COMPUTE = {"auto": PA_COMPUTE_AUTO, "simt": PA_COMPUTE_SIMT, "mma": PA_COMPUTE_
 # Every symbol include/pagedgqa.h declares.
 EXPORTS = ("pa_workspace_size", "pa_decode", "pa_decode_split", "pa_decode_merge",
            "pa_cache_append", "pa_read_status", "pa_status_string", "pa_plan_pieces",
-           "pa_plan_merge", "pa_version")
+           "pa_plan_merge", "pa_version", "pa_decode_noalloc")
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -98,6 +99,8 @@ def lib():
             fn = getattr(L, name)
             fn.argtypes = [SP, OP, P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_size_t, P]
             fn.restype = ctypes.c_int
+        L.pa_decode_noalloc.argtypes = [SP, OP, P, P, P, P, P, ctypes.c_float, P, P, P]
+        L.pa_decode_noalloc.restype = ctypes.c_int
         L.pa_cache_append.argtypes = [SP, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.pa_cache_append.restype = ctypes.c_int
         L.pa_read_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
@@ -222,6 +225,21 @@ def pa_decode_merge(q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                     opts: Optional[pa_options] = None, stream=None) -> None:
     _decode_call("pa_decode_merge", q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                  workspace, opts, stream)
+
+
+def pa_decode_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, scale, out, status=None,
+                      opts: Optional[pa_options] = None, stream=None) -> None:
+    """pa_decode for callers that cannot allocate device memory: the kernels'
+    scratch lives in a fixed static device array inside the library (see
+    include/pagedgqa.h).  `status` is an optional int32/uint32 CUDA tensor of
+    one element that receives the device status bits."""
+    _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out)
+    shape = shape_of(q, k_cache, block_table)
+    rc = lib().pa_decode_noalloc(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                                 _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                 _ptr(cache_seqlens), float(scale), _ptr(out), _ptr(status),
+                                 _stream(stream))
+    _check(rc, "pa_decode_noalloc")
 
 
 def pa_cache_append(k_new, v_new, k_cache, v_cache, block_table, cache_seqlens, workspace,

@@ -566,6 +566,9 @@ const char* pa_status_string(int code) {
     case PA_ERR_WORKSPACE: return "workspace smaller than pa_workspace_size";
     case PA_ERR_CUDA: return "a CUDA runtime or driver call failed";
     case PA_ERR_OPTION: return "invalid pa_options value";
+    case PA_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than the built-in static buffer "
+             "(PA_STATIC_SCRATCH_BYTES) of pa_decode_noalloc holds";
     default: break;
   }
   if (code > 0) {
@@ -648,3 +651,69 @@ int pa_plan_merge(const pa_shape* shape, const pa_options* options,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without any caller-provided or library-allocated workspace.
+//
+// Some callers cannot allocate device memory where they run a decode step:
+// a plugin whose host framework owns every device allocation, or a serving
+// loop that fixes its memory at start-up and may not call cudaMalloc (which
+// can also synchronise the device) on its hot path.  For them the scratch the
+// split and merge kernels need (status word, prefix sums, merge descriptors,
+// partial states) lives in one file-scope device array of a fixed size,
+// reserved on every GPU that loads this library for as long as the process
+// runs.  Nothing here calls cudaMalloc, cudaFree or an allocating library
+// routine.
+
+static __device__ __align__(256) uint8_t g_pa_static_scratch[PA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+void* g_static_ptr[kMaxDevices];
+
+// Once per device, with that device current: the array's device address.
+// (In host code the array's name is only a host-side stand-in.)
+int static_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pa_static_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
+    // the status word must start at zero
+    if (cudaMemset(p, 0, kHeaderBytes) != cudaSuccess) return PA_ERR_CUDA;
+    g_static_ptr[dev] = p;
+  }
+  *ptr = g_static_ptr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_decode_noalloc(const pa_shape* shape, const pa_options* options, const void* q,
+                                 const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, const int32_t* cache_seqlens,
+                                 float scale, float* out, uint32_t* status, pa_stream_t stream) {
+  if (shape && shape->batch == 0 && check_shape(shape) == PA_OK) return PA_OK;
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  rc = check_options(shape, options);
+  if (rc) return rc;
+  if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return PA_ERR_ALIGN;
+  Plan plan;
+  rc = make_plan(shape, options, false, &plan);
+  if (rc) return rc;
+  if (plan.total > (size_t)PA_STATIC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  rc = static_scratch(&scratch);
+  if (rc) return rc;
+  Call c;
+  rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+               scratch, (size_t)PA_STATIC_SCRATCH_BYTES, true, &c);
+  if (rc) return rc;
+  if (status) c.sa.status = status;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = launch_split_phase(shape, k_cache, v_cache, &c, st);
+  if (rc) return rc;
+  return launch_merge_phase(&c, st, true);
+}
