@@ -185,17 +185,17 @@ int choose_mode(const pa_options* o) {
   return c == PA_COMPUTE_SIMT ? kSimt : kMma;
 }
 
-// Ring slots per warp: two 16-token stages per warp by default (the loads of
-// the next tile are in flight while one is computed), fewer when shared
-// memory does not hold them, at most what fits in about 220 KB.
+// Ring slots per warp: 2 by default (measured best for every head dimension:
+// one tile computing, one in flight), fewer when shared memory does not hold
+// them; at most what fits in the per-block limit.
 int choose_ring(const pa_shape* s, const pa_options* o, int mode, int W) {
   const int G = s->num_heads / s->num_kv_heads;
   const SmemLayout L0 = split_smem_layout(s->head_dim, G, s->batch, W, 0, mode);
-  int fit = (220 * 1024 - (int)L0.total) / (W * (int)L0.stage_bytes);
+  int fit = (kMaxDynamicSmem - (int)L0.total) / (W * (int)L0.stage_bytes);
   if (fit > kMaxSlots / W) fit = kMaxSlots / W;
   if (o && o->stages > 0) return o->stages <= fit ? o->stages : -1;
-  int R = fit < 2 ? fit : 2;
-  return R;
+  const int want = 2;
+  return fit < want ? fit : want;
 }
 
 const void* kernel_for(int dtype, int D, int mode) {
@@ -217,7 +217,7 @@ const void* kernel_for(int dtype, int D, int mode) {
 
 // Occupancy of the split kernel for this smem size on device `dev`; also
 // raises the kernel's dynamic shared-memory limit (once).
-int occupancy(const void* fn, int dev, size_t smem, int* occ_out) {
+int occupancy(const void* fn, int dev, size_t smem, int threads, int* occ_out) {
   std::lock_guard<std::mutex> lk(g_mu);
   for (int i = 0; i < g_nfuncs; ++i) {
     if (g_funcs[i].fn == fn && g_funcs[i].dev == dev && g_funcs[i].smem == smem) {
@@ -232,7 +232,7 @@ int occupancy(const void* fn, int dev, size_t smem, int* occ_out) {
                                         kMaxDynamicSmem) != cudaSuccess)
     return PA_ERR_CUDA;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, 32 * kMaxWarps, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, smem) != cudaSuccess)
     return PA_ERR_CUDA;
   if (occ < 1) return PA_ERR_SHAPE;
   if (g_nfuncs < kFuncCacheSize) g_funcs[g_nfuncs++] = FuncCache{fn, dev, smem, occ};
@@ -268,7 +268,7 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
   p->G = s->num_heads / s->num_kv_heads;
   p->bs = s->block_size;
   p->mode = choose_mode(o);
-  p->warps = kMaxWarps;
+  p->warps = split_warps(p->D);
   p->ring = choose_ring(s, o, p->mode, p->warps);
   if (p->ring < 1) return (o && o->stages > 0) ? PA_ERR_OPTION : PA_ERR_SHAPE;
   p->part_blocks = (o && o->partition_tokens > 0) ? o->partition_tokens / s->block_size : 0;
@@ -283,7 +283,7 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
     if (rc) return rc;
     const void* fn = kernel_for(s->dtype, p->D, p->mode);
     if (!fn) return PA_ERR_SHAPE;
-    rc = occupancy(fn, dev, p->smem, &occ);
+    rc = occupancy(fn, dev, p->smem, 32 * p->warps, &occ);
     if (rc) return rc;
     if (!fixed_grid) p->grid = sms * occ;
   }
@@ -319,19 +319,20 @@ int get_encoder() {
   return PA_OK;
 }
 
-// 4-D map over a [P, bs, Hkv, D] pool: dims (D, Hkv, bs, P), box (64, 1, 16, 1),
-// 128-byte swizzle.  One box = 64 dims of 16 rows of one kv head of one
-// physical block.
+// 5-D map over a [P, bs, Hkv, D] pool: dims (64, bs, D/64, Hkv, P) with
+// element, row, 64-dim chunk, kv head and block strides; box (64, 16, D/64,
+// 1, 1), 128-byte swizzle.  One box = 16 rows of one kv head of one physical
+// block, landing in shared memory as D/64 chunk tiles of [16][64].
 int make_pool_map(CUtensorMap* map, const void* pool, const pa_shape* s) {
   const uint64_t D = (uint64_t)s->head_dim, Hkv = (uint64_t)s->num_kv_heads;
   const uint64_t bs = (uint64_t)s->block_size, P = (uint64_t)s->num_blocks;
-  cuuint64_t dims[4] = {D, Hkv, bs, P};
-  cuuint64_t strides[3] = {D * 2, Hkv * D * 2, bs * Hkv * D * 2};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTile, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
+  cuuint64_t dims[5] = {64, bs, D / 64, Hkv, P};
+  cuuint64_t strides[4] = {Hkv * D * 2, 128, D * 2, bs * Hkv * D * 2};
+  cuuint32_t box[5] = {64, (cuuint32_t)kTile, (cuuint32_t)(D / 64), 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUtensorMapDataType dt =
       s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUresult r = g_encode(map, dt, 4, const_cast<void*>(pool), dims, strides, box, estr,
+  CUresult r = g_encode(map, dt, 5, const_cast<void*>(pool), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;

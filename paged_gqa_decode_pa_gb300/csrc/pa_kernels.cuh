@@ -12,6 +12,10 @@
 namespace pa {
 
 constexpr int kMaxWarps = 8;   // warps per split CTA (each runs its own TMA ring)
+
+// Warps per split CTA for a head dimension: 8, or 4 for d = 256 so that each
+// warp can keep three 16 KB stages in flight within the shared memory.
+PA_HD constexpr int split_warps(int D) { return D == 256 ? 4 : kMaxWarps; }
 constexpr int kMaxSlots = 64;  // warps x ring slots
 constexpr int kGMax = 8;       // query heads per kv head handled by one CTA
 constexpr int kTile = 16;      // tokens per pipeline stage (one mma row tile)
@@ -66,7 +70,8 @@ struct SmemLayout {
   uint32_t stage;                   // [W][R] stages: K chunks | V chunks, 16 rows each
   uint32_t stage_bytes;
   uint32_t mo, mm, ml, mbad;        // per-warp partial states for the CTA combine
-  uint32_t qs, ps;                  // CUDA-core path: q (fp32), p per warp
+  uint32_t qs;                      // [G][D+4] fp32 q * scale * log2(e) of the current piece
+  uint32_t ps;                      // CUDA-core path: p per warp
   uint32_t pre;                     // [B + 1] prefix sums
   uint32_t total;                   // bytes to request (incl. alignment slack)
 };
@@ -90,13 +95,13 @@ PA_HD SmemLayout split_smem_layout(int D, int G, int B, int W, int R, int mode) 
   L.mbad = off;
   off += (uint32_t)W * 4u;
   off = align_up(off, 16);
+  L.qs = off;
+  off += (uint32_t)(G * (D + 4)) * 4u;
   if (mode == kSimt) {
-    L.qs = off;
-    off += (uint32_t)(G * D) * 4u;
     L.ps = off;
     off += (uint32_t)(W * kTile * kGMax) * 4u;
   } else {
-    L.qs = L.ps = 0;
+    L.ps = 0;
   }
   L.pre = off;
   off += (uint32_t)(B + 1) * 4u;

@@ -102,22 +102,22 @@ struct MmaState {
   float m0, m1, l0, l1;                   // heads 2t and 2t+1 of this lane
   bool bad;
 
-  __device__ __forceinline__ void load_q(const SplitArgs& a, int b, int j) {
+  // B fragments of q' = q * scale * log2(e) for the 8 head columns, from
+  // the CTA's shared fp32 copy qs [G][D+4] (heads >= G are zero columns).
+  __device__ __forceinline__ void load_q(const float* qs, int G) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const bool live = g < a.G;
-    const uint16_t* qrow = a.q + ((int64_t)b * a.H + (int64_t)j * a.G + (live ? g : 0)) * D;
+    const bool live = g < G;
+    const float* qrow = qs + (live ? g : 0) * (D + 4);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t hi = 0, lo = 0;
         if (live) {
-          uint32_t raw = __ldg(reinterpret_cast<const uint32_t*>(qrow + ks * 16 + half * 8 + 2 * t));
-          float x0 = Cvt<T>::widen(static_cast<uint16_t>(raw & 0xffffu)) * a.qscale;
-          float x1 = Cvt<T>::widen(static_cast<uint16_t>(raw >> 16)) * a.qscale;
-          hi = Cvt<T>::pack(x0, x1);
-          lo = Cvt<T>::pack(x0 - Cvt<T>::low(hi), x1 - Cvt<T>::high(hi));
+          const float2 x = *reinterpret_cast<const float2*>(qrow + ks * 16 + half * 8 + 2 * t);
+          hi = Cvt<T>::pack(x.x, x.y);
+          lo = Cvt<T>::pack(x.x - Cvt<T>::low(hi), x.y - Cvt<T>::high(hi));
         }
         qh[ks][half] = hi;
         ql[ks][half] = lo;
@@ -291,8 +291,8 @@ struct SimtState {
 #pragma unroll
       for (int g = 0; g < kGMax; ++g) {
         if (g >= h0 && g < h1) {
-          const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + c8 * 8);
-          const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + c8 * 8 + 4);
+          const float4 qa = *reinterpret_cast<const float4*>(qs + g * (D + 4) + c8 * 8);
+          const float4 qb = *reinterpret_cast<const float4*>(qs + g * (D + 4) + c8 * 8 + 4);
           float v = s[g];
           v = fmaf(qa.x, kf[0], v);
           v = fmaf(qa.y, kf[1], v);
@@ -428,29 +428,41 @@ __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem,
 }
 
 // Number of the piece's tiles that belong to warp w (tiles t = w, w+W, ...).
-__device__ __forceinline__ int warp_tiles(const Piece& pc, int subs, int w, int W) {
-  const int nt = (pc.blk1 - pc.blk0) * subs;
+template <int W>
+__device__ __forceinline__ int warp_tiles(const Piece& pc, int sl, int w) {
+  const int nt = (pc.blk1 - pc.blk0) << sl;
   return nt > w ? (nt - w + W - 1) / W : 0;
 }
 
-// The issuing side of one warp's pipeline: walks the warp's tile stream
-// (all pieces of the CTA, tiles w, w+W, ... of each) ahead of the computing
-// side and loads tile n into ring slot n % R.
+// The issuing side of one warp's pipeline: walks the warp's tile stream (all
+// pieces of the CTA, tiles w, w+W, ... of each) R tiles ahead of the
+// computing side and loads each tile into the ring slot the computing side
+// has just freed.  Block-table entries are read 32 tiles at a time, one
+// window ahead.
 struct Issuer {
   PieceIter it;
   Piece pc;
   int i, cnt;        // next tile index (of this warp) in pc, and their count
-  int cache_base;    // tile index whose table entry lane 0 holds, -1 = none
-  int32_t entry;     // this lane's table entry (tile cache_base + lane)
+  int win;           // first tile index of the current table window
+  int32_t entry;     // this lane's entry of the current window (tile win + lane)
+  int32_t entry_next;  // ... of the next window (tile win + 32 + lane)
   int32_t len;       // cache_seqlens[pc.b]
-  uint32_t n;        // next stream position
+  uint32_t issued;   // tiles issued so far
   bool done;
 };
 
-template <int D>
+template <int W>
+__device__ __forceinline__ int32_t table_entry(const SplitArgs& a, const Piece& pc, int cnt, int ii,
+                                               int sl, int w) {
+  if (ii >= cnt) return 0;
+  const int t = w + W * ii;
+  return __ldg(a.table + (int64_t)pc.b * a.maxblk + pc.blk0 + (t >> sl));
+}
+
+template <int D, int W>
 __device__ __forceinline__ void issue_next(Issuer& is, const SplitArgs& a, const CUtensorMap* tmk,
-                                           const CUtensorMap* tmv, uint8_t* smem, uint32_t base,
-                                           const SmemLayout& L, int w, int W, int R, int subs) {
+                                           const CUtensorMap* tmv, uint32_t base,
+                                           const SmemLayout& L, int w, uint32_t slot, int sl) {
   const int lane = threadIdx.x & 31;
   while (!is.done && is.i >= is.cnt) {
     if (!is.it.next(is.pc)) {
@@ -458,65 +470,92 @@ __device__ __forceinline__ void issue_next(Issuer& is, const SplitArgs& a, const
       break;
     }
     is.i = 0;
-    is.cnt = warp_tiles(is.pc, subs, w, W);
-    is.cache_base = -1;
+    is.cnt = warp_tiles<W>(is.pc, sl, w);
+    is.win = 0;
     is.len = __ldg(a.seqlens + is.pc.b);
+    is.entry = table_entry<W>(a, is.pc, is.cnt, lane, sl, w);
+    is.entry_next = table_entry<W>(a, is.pc, is.cnt, 32 + lane, sl, w);
   }
   if (is.done) return;
-  if (is.cache_base < 0 || is.i >= is.cache_base + 32) {
-    is.cache_base = is.i;
-    const int ii = is.i + lane;
-    int32_t e = 0;
-    if (ii < is.cnt) {
-      const int t = w + W * ii;
-      e = __ldg(a.table + (int64_t)is.pc.b * a.maxblk + is.pc.blk0 + t / subs);
-    }
-    is.entry = e;
+  if (is.i >= is.win + 32) {
+    is.win += 32;
+    is.entry = is.entry_next;
+    is.entry_next = table_entry<W>(a, is.pc, is.cnt, is.win + 32 + lane, sl, w);
   }
-  const int32_t phys = __shfl_sync(0xffffffffu, is.entry, is.i - is.cache_base);
+  const int32_t phys = __shfl_sync(0xffffffffu, is.entry, is.i - is.win);
   if (lane == 0) {
     const int t = w + W * is.i;
-    const int blk = is.pc.blk0 + t / subs, h = t % subs;
+    const int blk = is.pc.blk0 + (t >> sl), h = t & ((1 << sl) - 1);
     const int valid = max(0, min(kTile, is.len - blk * a.bs - h * kTile));
     const bool bad = phys < 0 || phys >= a.P;
-    const uint32_t slot = (uint32_t)w * R + is.n % (uint32_t)R;
-    const uint32_t full = base + L.full + 8 * slot;
-    reinterpret_cast<volatile uint32_t*>(smem + L.info)[slot] = (uint32_t)valid | (bad ? kInfoBad : 0u);
+    const uint32_t gslot = (uint32_t)w * a.ring + slot;
+    const uint32_t full = base + L.full + 8 * gslot;
+    sts32(base + L.info + 4 * gslot, (uint32_t)valid | (bad ? kInfoBad : 0u));
     if (bad || valid == 0) {
       if (bad && h == 0) atomicOr(a.status, kStatusBadBlock);
       mbar_arrive(full);
     } else {
-      constexpr int NC = D / 64;
       constexpr uint32_t chunk = kTile * 128u;
       mbar_arrive_expect_tx(full, L.stage_bytes);
-      const uint32_t kdst = base + L.stage + slot * L.stage_bytes;
-      const uint32_t vdst = kdst + NC * chunk;
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        tma_load_4d(kdst + c * chunk, tmk, full, c * 64, is.pc.j, h * kTile, phys);
-        tma_load_4d(vdst + c * chunk, tmv, full, c * 64, is.pc.j, h * kTile, phys);
-      }
+      const uint32_t kdst = base + L.stage + gslot * L.stage_bytes;
+      tma_load_5d(kdst, tmk, full, 0, h * kTile, 0, is.pc.j, phys);
+      tma_load_5d(kdst + (D / 64) * chunk, tmv, full, 0, h * kTile, 0, is.pc.j, phys);
     }
   }
   ++is.i;
-  ++is.n;
+  ++is.issued;
 }
 
+// q' = q * scale * log2(e) of piece pc's G heads into the shared fp32 buffer
+// (all threads).  The loads are issued first; `finish` stores them.
+template <int D>
+struct QPrefetch {
+  static constexpr int kPer = (kGMax * D / 2 + 32 * 4 - 1) / (32 * 4);  // words per thread, >= 4 warps
+  uint32_t v[kPer];
+  __device__ __forceinline__ void start(const SplitArgs& a, const Piece& pc) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(
+        a.q + ((int64_t)pc.b * a.H + (int64_t)pc.j * a.G) * D);
+    const int nw = a.G * D / 2;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
+      v[k] = (i < nw) ? __ldg(src + i) : 0u;
+    }
+  }
+  template <typename T>
+  __device__ __forceinline__ void finish(const SplitArgs& a, float* qs) {
+    const int nw = a.G * D / 2;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
+      if (i < nw) {
+        const int g = (2 * i) / D, d = (2 * i) % D;
+        float2 x;
+        x.x = Cvt<T>::low(v[k]) * a.qscale;
+        x.y = Cvt<T>::high(v[k]) * a.qscale;
+        *reinterpret_cast<float2*>(qs + g * (D + 4) + d) = x;
+      }
+    }
+  }
+};
+
 template <typename T, int D, int MODE>
-__global__ void __launch_bounds__(32 * kMaxWarps, 1)
+__global__ void __launch_bounds__(32 * split_warps(D), 1)
     pa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                     const SplitArgs a) {
+  constexpr int W = split_warps(D);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
-  const int W = a.warps, R = a.ring;
+  const int R = a.ring;
   const SmemLayout L = split_smem_layout(D, a.G, a.B, W, R, MODE);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   int32_t* pre = reinterpret_cast<int32_t*>(smem + L.pre);
+  float* qs = reinterpret_cast<float*>(smem + L.qs);
   __shared__ int32_t scan_scratch[kMaxWarps];
 
   if (tid == 0) {
@@ -559,7 +598,7 @@ __global__ void __launch_bounds__(32 * kMaxWarps, 1)
   }
 
   const int w = warp;
-  const int subs = a.bs / kTile;  // 16-token tiles per physical block
+  const int sl = a.bs == 16 ? 0 : (a.bs == 32 ? 1 : 2);  // log2(16-token tiles per block)
   constexpr int NC = D / 64;
   constexpr uint32_t chunk = kTile * 128u;
 
@@ -567,45 +606,52 @@ __global__ void __launch_bounds__(32 * kMaxWarps, 1)
   Issuer is;
   is.it.init(pre, a.seqlens, sched, cta);
   is.i = is.cnt = 0;
-  is.cache_base = -1;
-  is.entry = 0;
+  is.win = 0;
+  is.entry = is.entry_next = 0;
   is.len = 0;
-  is.n = 0;
+  is.issued = 0;
   is.done = false;
-  for (int r = 0; r < R; ++r) issue_next<D>(is, a, &tmk, &tmv, smem, base, L, w, W, R, subs);
+  for (int r = 0; r < R; ++r) issue_next<D, W>(is, a, &tmk, &tmv, base, L, w, (uint32_t)r, sl);
 
-  // ---- the warp's computing side
+  // ---- the computing side
   PieceIter it;
   it.init(pre, a.seqlens, sched, cta);
   Piece pc;
-  uint32_t n = 0;  // stream position being consumed
+  bool have = it.next(pc);
+  if (have) {
+    QPrefetch<D> qp;
+    qp.start(a, pc);
+    qp.template finish<T>(a, qs);
+  }
+  __syncthreads();
+  uint32_t slot = 0, phase = 0;  // ring slot to consume next; per-slot parity bits
+  uint32_t consumed = 0;
   MmaState<T, D> mst;
   SimtState<T, D> sst;
-  float* qs = reinterpret_cast<float*>(smem + L.qs);
   float* ps = reinterpret_cast<float*>(smem + L.ps) + w * kTile * kGMax;
-  while (it.next(pc)) {
+  while (have) {
     if constexpr (MODE == kMma) {
-      mst.load_q(a, pc.b, pc.j);
+      mst.load_q(qs, a.G);
       mst.reset();
     } else {
-      // q * scale * log2e for the G heads of kv head j (shared by the warps)
-      const uint16_t* qrow = a.q + ((int64_t)pc.b * a.H + (int64_t)pc.j * a.G) * D;
-      for (int i = tid; i < a.G * D; i += blockDim.x) qs[i] = Cvt<T>::widen(__ldg(qrow + i)) * a.qscale;
-      named_bar_sync(1, blockDim.x);
       sst.reset();
     }
     bool bad = false;
-    const int cnt = warp_tiles(pc, subs, w, W);
-    for (int i = 0; i < cnt; ++i, ++n) {
-      const uint32_t slot = (uint32_t)w * R + n % (uint32_t)R;
-      const bool ok = mbar_wait_bounded(base + L.full + 8 * slot, (n / R) & 1, abort_flag, kWaitLimitNs);
-      const uint32_t info = reinterpret_cast<volatile uint32_t*>(smem + L.info)[slot];
+    const int cnt = warp_tiles<W>(pc, sl, w);
+    for (int i = 0; i < cnt; ++i) {
+      const uint32_t gslot = (uint32_t)w * R + slot;
+      const bool ok = mbar_wait_bounded(base + L.full + 8 * gslot, (phase >> slot) & 1u, abort_flag,
+                                        kWaitLimitNs);
+      const uint32_t info = lds32(base + L.info + 4 * gslot);
       const int valid = (int)(info & 0xffffu);
       if (!ok || (info & kInfoBad)) {
         bad = true;
-        if (!ok && lane == 0) atomicOr(a.status, kStatusTimeout);
+        if (!ok) {
+          if (lane == 0) atomicOr(a.status, kStatusTimeout);
+          is.done = true;  // stop issuing after a timeout
+        }
       } else if (valid > 0) {
-        const uint32_t kb = base + L.stage + slot * L.stage_bytes;
+        const uint32_t kb = base + L.stage + gslot * L.stage_bytes;
         const uint32_t vb = kb + NC * chunk;
         if constexpr (MODE == kMma) {
           if (valid < kTile) {
@@ -625,8 +671,10 @@ __global__ void __launch_bounds__(32 * kMaxWarps, 1)
         }
       }
       __syncwarp();
-      if (*abort_flag) is.done = true;  // stop issuing after a timeout
-      issue_next<D>(is, a, &tmk, &tmv, smem, base, L, w, W, R, subs);
+      phase ^= 1u << slot;
+      ++consumed;
+      issue_next<D, W>(is, a, &tmk, &tmv, base, L, w, slot, sl);
+      slot = (slot + 1 == (uint32_t)R) ? 0u : slot + 1;
     }
     if constexpr (MODE == kMma) {
       mst.bad |= bad;
@@ -636,16 +684,26 @@ __global__ void __launch_bounds__(32 * kMaxWarps, 1)
       sst.publish(smem, L, w, a.G);
     }
     named_bar_sync(1, blockDim.x);
+    // start loading the next piece's q while this piece is being combined
+    Piece next;
+    PieceIter peek = it;
+    const bool more = peek.next(next);
+    QPrefetch<D> qp;
+    if (more) qp.start(a, next);
     combine_piece<D>(a, smem, L, pc, W);
+    if (more) qp.template finish<T>(a, qs);
     named_bar_sync(1, blockDim.x);
+    have = it.next(pc);
   }
   if (*abort_flag && lane == 0) {
     // Drain: wait (bounded, ignoring the abort flag) for this warp's copies
     // still in flight before the CTA may exit.
     volatile int never = 0;
-    for (uint32_t kk = n; kk < is.n; ++kk) {
-      const uint32_t slot = (uint32_t)w * R + kk % (uint32_t)R;
-      mbar_wait_bounded(base + L.full + 8 * slot, (kk / R) & 1, &never, kWaitLimitNs / 4);
+    for (uint32_t kk = consumed; kk < is.issued; ++kk) {
+      mbar_wait_bounded(base + L.full + 8 * ((uint32_t)w * R + slot), (phase >> slot) & 1u, &never,
+                        kWaitLimitNs / 4);
+      phase ^= 1u << slot;
+      slot = (slot + 1 == (uint32_t)R) ? 0u : slot + 1;
     }
   }
 }
