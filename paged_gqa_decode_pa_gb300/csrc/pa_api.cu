@@ -27,15 +27,19 @@ namespace {
 // dimension; the four warp states are folded the same way in a fixed order,
 // so the result is deterministic.  Combine op: "Paged Attention Kernel
 // Architecture for BI-V100", section 2, Level 1 binary op / Level 3.
-template <int D>
-__device__ __forceinline__ void merge_segment_head(const MergeArgs& a, const MergeSeg& ms, int g) {
-  constexpr int NV = D / 32;  // dims per lane: lane + 32 i
+// Block (seg, g, c) folds head g, dims [64c, 64c+64) of merge index seg.
+// Pieces are taken 32 at a time: lane k of every warp loads (m, l) of piece
+// k of the batch, so the batch's weights 2^(m_p - M) need one round trip;
+// then warp w accumulates pieces w, w+4, ... of the batch, lanes over the 64
+// dims as float2, with 8 pieces' loads issued before they are used.
+__device__ __forceinline__ void merge_segment_chunk(const MergeArgs& a, const MergeSeg& ms, int g,
+                                                    int c) {
   constexpr int NW = kMergeThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   __shared__ float red[NW];
   __shared__ float wl[NW];
-  __shared__ float wacc[NW][D];
-  // pass 1: M = max_p m_p (pieces spread over all threads)
+  __shared__ float2 wacc[NW][32];
+  // pass 1: M = max_p m_p
   float m = -INFINITY;
   for (int p = tid; p < ms.np; p += kMergeThreads) m = fmaxf(m, a.ws_ml[(ms.slot(p) * a.G + g) * 2]);
 #pragma unroll
@@ -45,48 +49,76 @@ __device__ __forceinline__ void merge_segment_head(const MergeArgs& a, const Mer
   float M = red[0];
 #pragma unroll
   for (int v = 1; v < NW; ++v) M = fmaxf(M, red[v]);
-  // pass 2: warp w sums pieces w, w+NW, ... with weights 2^(m_p - M); the
-  // iterations are independent, so their loads overlap
-  float l = 0.f, acc[NV];
+  // pass 2
+  float l = 0.f;
+  float2 acc = make_float2(0.f, 0.f);
+  for (int p0 = 0; p0 < ms.np; p0 += 32) {
+    const int nb = min(32, ms.np - p0);
+    float e_lane = 0.f;
+    int64_t s_lane = 0;
+    if (lane < nb) {
+      s_lane = ms.slot(p0 + lane);
+      const float mp = a.ws_ml[(s_lane * a.G + g) * 2];
+      const float lp = a.ws_ml[(s_lane * a.G + g) * 2 + 1];
+      e_lane = ex2(mp - M);
+      if (w == 0) l = fmaf(e_lane, lp, l);  // each piece's l counted once
+    }
+    for (int k0 = w; k0 < nb; k0 += 8 * NW) {
+      float2 x[8];
+      float e[8];
 #pragma unroll
-  for (int i = 0; i < NV; ++i) acc[i] = 0.f;
-#pragma unroll 4
-  for (int p = w; p < ms.np; p += NW) {
-    const int64_t s = ms.slot(p);
-    const float e = ex2(a.ws_ml[(s * a.G + g) * 2] - M);
-    l = fmaf(e, a.ws_ml[(s * a.G + g) * 2 + 1], l);
-    const float* ap = a.ws_acc + (s * a.G + g) * D;
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u * NW;
+        const int kk = k < nb ? k : 0;
+        const int64_t s = __shfl_sync(0xffffffffu, s_lane, kk);
+        e[u] = __shfl_sync(0xffffffffu, e_lane, kk);
+        x[u] = k < nb ? *reinterpret_cast<const float2*>(a.ws_acc + (s * a.G + g) * a.D + c * 64 + 2 * lane)
+                      : make_float2(0.f, 0.f);
+        if (k >= nb) e[u] = 0.f;
+      }
 #pragma unroll
-    for (int i = 0; i < NV; ++i) acc[i] = fmaf(e, ap[lane + 32 * i], acc[i]);
+      for (int u = 0; u < 8; ++u) {
+        acc.x = fmaf(e[u], x[u].x, acc.x);
+        acc.y = fmaf(e[u], x[u].y, acc.y);
+      }
+    }
+  }
+  // the l partial sums live in warp 0's lanes
+  if (w == 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   }
   if (lane == 0) wl[w] = l;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) wacc[w][lane + 32 * i] = acc[i];
+  wacc[w][lane] = acc;
   __syncthreads();
-  float L = 0.f;
+  if (w == 0) {
+    const float L = wl[0];
+    float2 o = wacc[0][lane];
 #pragma unroll
-  for (int v = 0; v < NW; ++v) L += wl[v];
-  float* dst = a.out + ((int64_t)ms.b * a.H + (int64_t)ms.j * a.G + g) * D;
-  for (int d = tid; d < D; d += kMergeThreads) {
-    float o = 0.f;
-#pragma unroll
-    for (int v = 0; v < NW; ++v) o += wacc[v][d];
-    dst[d] = o / L;
+    for (int v = 1; v < NW; ++v) {
+      o.x += wacc[v][lane].x;
+      o.y += wacc[v][lane].y;
+    }
+    float* dst = a.out + ((int64_t)ms.b * a.H + (int64_t)ms.j * a.G + g) * a.D + c * 64 + 2 * lane;
+    *reinterpret_cast<float2*>(dst) = make_float2(o.x / L, o.y / L);
   }
 }
 
-template <int D>
 __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs a) {
   // With programmatic dependent launch this grid may start while the split
   // kernel is finishing: wait until its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int seg = blockIdx.x, g = blockIdx.y;
+  const int seg = blockIdx.x, g = blockIdx.y, c = blockIdx.z;
   const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas};
   int4 desc = make_int4(-1, 0, 0, 0);
   if (a.part_blocks == 0) desc = a.ws_desc[seg];
   const MergeSeg ms = merge_segment(sched, seg, desc.x, desc.y, desc.z, desc.w, a.ws_pre);
   if (ms.np == 0) return;
-  merge_segment_head<D>(a, ms, g);
+  // gridDim.z == D/64: one chunk per block; gridDim.z == 1: all chunks here
+  for (int cc = c; cc < a.D / 64; cc += gridDim.z) {
+    merge_segment_chunk(a, ms, g, cc);
+    __syncthreads();  // shared scratch reuse
+  }
 }
 
 // --------------------------------------------------------------- append
@@ -445,7 +477,8 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   const Plan& p = c->plan;
   const int nseg = p.part_blocks == 0 ? p.grid : c->sa.B * c->sa.Hkv;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nseg, p.G);
+  // long heads get one block per 64-dim chunk (few segments, many pieces)
+  cfg.gridDim = dim3(nseg, p.G, p.D == 256 ? p.D / 64 : 1);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -454,10 +487,7 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
-  cudaError_t e = cudaErrorInvalidValue;
-  if (p.D == 64) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<64>, c->ma);
-  if (p.D == 128) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<128>, c->ma);
-  if (p.D == 256) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<256>, c->ma);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, pa_merge_kernel, c->ma);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
