@@ -246,7 +246,7 @@ def workload_config(w, args):
             "mean_seqlen": round(float(np.mean(w.cache_seqlens)), 1),
             "max_seqlen": int(np.max(w.cache_seqlens)),
             "partition_tokens": args.partition_tokens, "compute": args.compute,
-            "stages": args.stages,
+            "stages": args.stages, "graph": bool(args.graph),
             "kv_bytes_per_step": w.kv_bytes(),
             "l2": ("inputs larger than L2" if w.kv_bytes() > 2 * L2_BYTES
                    else "L2 flushed between timed steps"),
@@ -287,6 +287,21 @@ def run_ours(args, rank, world, local_rank):
     uuid = getattr(props, "uuid", None)
     sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local_rank))
 
+    graph = None
+    if args.graph:
+        # one decode step captured once and replayed (host launch cost removed)
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+        cap.synchronize()
+        with torch.cuda.graph(graph, stream=cap):
+            pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+
     # ---- timed region 1 (the value): K decode steps through pa_decode
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler.start()
@@ -299,7 +314,10 @@ def run_ours(args, rank, world, local_rank):
         if flush:
             scratch.fill_(1.0)
         ev[i][0].record(stream)
-        pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+        if graph is not None:
+            graph.replay()
+        else:
+            pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     sampler.mark_end()
@@ -423,6 +441,8 @@ def main():
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--compute", default="mma", choices=["mma", "simt", "auto"])
     ap.add_argument("--stages", type=int, default=0, help="pipeline stages (0 = library choice)")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay one captured CUDA graph of pa_decode per step")
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample (0 = skip)")
     args = ap.parse_args()

@@ -163,6 +163,24 @@ int pa_decode_merge(const pa_shape* shape, const pa_options* options, const void
                     const int32_t* cache_seqlens, float scale, float* out, void* workspace,
                     size_t workspace_bytes, pa_stream_t stream);
 
+/* Fused append-and-attend (the decoding path of the Hugging Face "Paged
+ * attention" page: the kernel indexes the cache through block_table and
+ * updates it in place).  For every sequence b: k_new[b,:,:] and v_new[b,:,:]
+ * are written to position cache_seqlens[b] exactly as pa_cache_append writes
+ * them, and out[b] attends over the cache_seqlens[b] + 1 tokens including
+ * the new one -- in one pass: the one tile that holds the new position takes
+ * the new row from k_new/v_new while also storing it.  cache_seqlens is not
+ * incremented (the caller does that).  Arguments as pa_decode, plus
+ * k_new/v_new [B, Hkv, d] and the pools writable.  A new position past the
+ * table (cache_seqlens[b] + 1 > max_blocks_per_seq * bs) sets
+ * PA_STATUS_BAD_SEQLEN | PA_STATUS_NO_SLOT; an unmapped entry for it sets
+ * PA_STATUS_BAD_BLOCK; in both cases sequence b's outputs are NaN and its row
+ * is not written.  Same workspace as pa_decode. */
+int pa_decode_append(const pa_shape* shape, const pa_options* options, const void* q,
+                     const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                     const int32_t* block_table, const int32_t* cache_seqlens, float scale,
+                     float* out, void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
 /* Append one new token per sequence to the paged cache, in place: for every
  * b and kv head j, k_new[b,j,:] and v_new[b,j,:] are copied bit for bit to
  * row (cache_seqlens[b] % bs) of physical block

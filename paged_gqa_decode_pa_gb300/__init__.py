@@ -7,7 +7,8 @@ missing -- there is no other implementation to fall back to.
 """
 from ._binding import (  # noqa: F401
     EXPORTS, LIB_PATH, LibraryNotBuilt, PagedGQAError, alloc_workspace, lib, options,
-    pa_cache_append, pa_decode, pa_decode_merge, pa_decode_noalloc, pa_decode_split, pa_options,
+    pa_cache_append, pa_decode, pa_decode_append, pa_decode_merge, pa_decode_noalloc,
+    pa_decode_split, pa_options,
     pa_plan_merge, pa_plan_pieces, pa_read_status, pa_shape, pa_version, pa_workspace_size,
     shape_of, status_string,
     PA_OK, PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_ALIGN, PA_ERR_WORKSPACE, PA_ERR_CUDA,

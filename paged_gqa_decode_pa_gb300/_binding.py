@@ -41,7 +41,7 @@ _COMPUTE = {"auto": PA_COMPUTE_AUTO, "simt": PA_COMPUTE_SIMT, "mma": PA_COMPUTE_
 # Every symbol include/pagedgqa.h declares.
 EXPORTS = ("pa_workspace_size", "pa_decode", "pa_decode_split", "pa_decode_merge",
            "pa_cache_append", "pa_read_status", "pa_status_string", "pa_plan_pieces",
-           "pa_plan_merge", "pa_version", "pa_decode_noalloc")
+           "pa_plan_merge", "pa_version", "pa_decode_noalloc", "pa_decode_append")
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -99,6 +99,9 @@ def lib():
             fn = getattr(L, name)
             fn.argtypes = [SP, OP, P, P, P, P, P, ctypes.c_float, P, P, ctypes.c_size_t, P]
             fn.restype = ctypes.c_int
+        L.pa_decode_append.argtypes = [SP, OP, P, P, P, P, P, P, P, ctypes.c_float, P, P,
+                                       ctypes.c_size_t, P]
+        L.pa_decode_append.restype = ctypes.c_int
         L.pa_decode_noalloc.argtypes = [SP, OP, P, P, P, P, P, ctypes.c_float, P, P, P]
         L.pa_decode_noalloc.restype = ctypes.c_int
         L.pa_cache_append.argtypes = [SP, P, P, P, P, P, P, P, ctypes.c_size_t, P]
@@ -225,6 +228,26 @@ def pa_decode_merge(q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                     opts: Optional[pa_options] = None, stream=None) -> None:
     _decode_call("pa_decode_merge", q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                  workspace, opts, stream)
+
+
+def pa_decode_append(q, k_new, v_new, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                     workspace, opts: Optional[pa_options] = None, stream=None) -> None:
+    """Write k_new/v_new [B,Hkv,d] at position cache_seqlens[b] and attend over
+    cache_seqlens[b] + 1 tokens, in one pass (see include/pagedgqa.h)."""
+    _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out)
+    P_, bs, Hkv, d = k_cache.shape
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != k_cache.dtype:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of the cache dtype")
+        if tuple(t.shape) != (q.shape[0], Hkv, d):
+            raise ValueError(f"{name} must be [B, Hkv, d]")
+    shape = shape_of(q, k_cache, block_table)
+    rc = lib().pa_decode_append(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                                _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(block_table), _ptr(cache_seqlens), float(scale), _ptr(out),
+                                _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream))
+    _check(rc, "pa_decode_append")
 
 
 def pa_decode_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, scale, out, status=None,

@@ -421,6 +421,9 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.warps = p.warps;
   a.ring = p.ring;
   a.qscale = scale * 1.4426950408889634f;  // log2(e)
+  a.len_add = 0;
+  a.k_new = a.v_new = nullptr;
+  a.k_pool = a.v_pool = nullptr;
   MergeArgs& m = c->ma;
   m.seqlens = cache_seqlens;
   m.out = out;
@@ -440,15 +443,51 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   return PA_OK;
 }
 
+// Encoded pool maps are cached by (pool address, shape): encoding is host
+// work of a few microseconds per map, and a decode loop reuses its pools.
+struct MapEntry {
+  const void* pool;
+  int32_t D, Hkv, bs, P, dtype;
+  alignas(64) CUtensorMap map;
+};
+constexpr int kMapCache = 32;
+MapEntry g_maps[kMapCache];
+int g_nmaps = 0, g_next_map = 0;
+
+int pool_map(CUtensorMap* out, const void* pool, const pa_shape* s) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < g_nmaps; ++i) {
+    const MapEntry& e = g_maps[i];
+    if (e.pool == pool && e.D == s->head_dim && e.Hkv == s->num_kv_heads &&
+        e.bs == s->block_size && e.P == s->num_blocks && e.dtype == s->dtype) {
+      *out = e.map;
+      return PA_OK;
+    }
+  }
+  MapEntry e;
+  e.pool = pool;
+  e.D = s->head_dim;
+  e.Hkv = s->num_kv_heads;
+  e.bs = s->block_size;
+  e.P = s->num_blocks;
+  e.dtype = s->dtype;
+  const int rc = make_pool_map(&e.map, pool, s);
+  if (rc) return rc;
+  const int slot = g_nmaps < kMapCache ? g_nmaps++ : (g_next_map++ % kMapCache);
+  g_maps[slot] = e;
+  *out = e.map;
+  return PA_OK;
+}
+
 int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cache, Call* c,
                        cudaStream_t stream) {
   int rc = get_encoder();
   if (rc) return rc;
   alignas(64) CUtensorMap tmk;
   alignas(64) CUtensorMap tmv;
-  rc = make_pool_map(&tmk, k_cache, s);
+  rc = pool_map(&tmk, k_cache, s);
   if (rc) return rc;
-  rc = make_pool_map(&tmv, v_cache, s);
+  rc = pool_map(&tmv, v_cache, s);
   if (rc) return rc;
   const Plan& p = c->plan;
   cudaError_t e = cudaErrorInvalidValue;
@@ -539,6 +578,28 @@ int pa_decode(const pa_shape* shape, const pa_options* options, const void* q,
   int rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                    workspace, workspace_bytes, true, &c);
   if (rc) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = launch_split_phase(shape, k_cache, v_cache, &c, st);
+  if (rc) return rc;
+  return launch_merge_phase(&c, st, true);
+}
+
+int pa_decode_append(const pa_shape* shape, const pa_options* options, const void* q,
+                     const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                     const int32_t* block_table, const int32_t* cache_seqlens, float scale,
+                     float* out, void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (shape && shape->batch == 0 && check_shape(shape) == PA_OK) return PA_OK;
+  if (!k_new || !v_new) return PA_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PA_ERR_ALIGN;
+  Call c;
+  int rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                   workspace, workspace_bytes, true, &c);
+  if (rc) return rc;
+  c.sa.len_add = 1;
+  c.sa.k_new = static_cast<const uint16_t*>(k_new);
+  c.sa.v_new = static_cast<const uint16_t*>(v_new);
+  c.sa.k_pool = static_cast<uint16_t*>(k_cache);
+  c.sa.v_pool = static_cast<uint16_t*>(v_cache);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = launch_split_phase(shape, k_cache, v_cache, &c, st);
   if (rc) return rc;

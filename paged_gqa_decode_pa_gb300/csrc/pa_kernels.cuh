@@ -38,6 +38,13 @@ struct SplitArgs {
   int32_t warps;            // warps per CTA (= blockDim.x / 32)
   int32_t ring;             // TMA ring slots per warp
   float qscale;             // scale * log2(e): scores are kept in log2 units
+  // fused append: each sequence's new K/V row (k_new/v_new [B, Hkv, D]) is
+  // written to position cache_seqlens[b] of the pool and attended to
+  int32_t len_add;          // 0, or 1 with the fused append
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint16_t* k_pool;         // the pools, writable (fused append only)
+  uint16_t* v_pool;
 };
 
 struct MergeArgs {
@@ -66,7 +73,7 @@ struct AppendArgs {
 // Byte offsets inside the split kernel's dynamic shared memory, relative to
 // a 1024-byte aligned base.
 struct SmemLayout {
-  uint32_t full, info, abort_flag;  // per slot: mbarrier, (valid rows | bad)
+  uint32_t full, info, abort_flag;  // per slot: mbarrier, (phys << 32 | bad | valid rows)
   uint32_t stage;                   // [W][R] stages: K chunks | V chunks, 16 rows each
   uint32_t stage_bytes;
   uint32_t mo, mm, ml, mbad;        // per-warp partial states for the CTA combine
@@ -82,7 +89,6 @@ PA_HD SmemLayout split_smem_layout(int D, int G, int B, int W, int R, int mode) 
   SmemLayout L;
   L.full = 0;
   L.info = 8 * kMaxSlots;
-  L.abort_flag = 12 * kMaxSlots;
   L.stage = 1024;
   L.stage_bytes = 4u * (uint32_t)D * (uint32_t)kTile;  // K + V tiles, 2 bytes each
   uint32_t off = L.stage + (uint32_t)(W * R) * L.stage_bytes;
@@ -94,6 +100,8 @@ PA_HD SmemLayout split_smem_layout(int D, int G, int B, int W, int R, int mode) 
   off += (uint32_t)W * kGMax * 4u;
   L.mbad = off;
   off += (uint32_t)W * 4u;
+  L.abort_flag = off;
+  off += 4u;
   off = align_up(off, 16);
   L.qs = off;
   off += (uint32_t)(G * (D + 4)) * 4u;

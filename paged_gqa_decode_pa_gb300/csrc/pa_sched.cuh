@@ -40,6 +40,7 @@ struct SchedShape {
   int32_t B, Hkv, bs, maxblk;
   int32_t part_blocks;  // 0 = balanced
   int32_t num_ctas;     // launched persistent grid
+  int32_t len_add;      // 1 when the step also appends each sequence's new token
 };
 
 // Blocks of a sequence; lengths outside [0, maxblk*bs] count as empty (the
@@ -51,6 +52,14 @@ PA_HD int32_t seq_blocks(int32_t len, int32_t bs, int32_t maxblk) {
 
 PA_HD bool seq_len_valid(int32_t len, int32_t bs, int32_t maxblk) {
   return len >= 0 && (int64_t)len <= (int64_t)maxblk * bs;
+}
+
+// The length a step attends to: the stored length plus `add` (1 when the
+// step also appends the new token), or -1 when that is not a valid length.
+PA_HD int32_t eff_len(int32_t stored, int32_t add, int32_t bs, int32_t maxblk) {
+  if (stored < 0) return -1;
+  const int64_t e = (int64_t)stored + add;
+  return e > (int64_t)maxblk * bs ? -1 : (int32_t)e;
 }
 
 // Per-sequence count that the prefix sums run over.
@@ -158,7 +167,7 @@ struct PieceIter {
     int64_t r = item - (int64_t)s.Hkv * pre[b];
     int32_t part = (int32_t)(r / s.Hkv);
     int32_t j = (int32_t)(r % s.Hkv);
-    int32_t nb = seq_blocks(lens[b], s.bs, s.maxblk);
+    int32_t nb = seq_blocks(eff_len(lens[b], s.len_add, s.bs, s.maxblk), s.bs, s.maxblk);
     int32_t np = pre[b + 1] - pre[b];
     p.b = b;
     p.j = j;

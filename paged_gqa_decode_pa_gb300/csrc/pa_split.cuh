@@ -46,6 +46,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: a stuck pipeline, neve
 constexpr uint32_t kStatusBadBlock = 0x1u;
 constexpr uint32_t kStatusBadSeqlen = 0x2u;
 constexpr uint32_t kStatusTimeout = 0x4u;
+constexpr uint32_t kStatusNoSlot = 0x8u;
 constexpr uint32_t kInfoBad = 0x10000u;
 
 // Byte offset of the 16-byte unit `unit` (0..7) of row `row` inside one
@@ -64,7 +65,8 @@ __device__ __forceinline__ void build_prefix(const SplitArgs& a, int32_t* pre, i
   const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
   int local = 0;
   for (int b = b0; b < b1; ++b)
-    local += seq_count(seq_blocks(__ldg(a.seqlens + b), a.bs, a.maxblk), a.part_blocks);
+    local += seq_count(seq_blocks(eff_len(__ldg(a.seqlens + b), a.len_add, a.bs, a.maxblk), a.bs, a.maxblk),
+                       a.part_blocks);
   // inclusive scan of `local` over the block
   const int lane = tid & 31, warp = tid >> 5;
   int x = local;
@@ -88,7 +90,8 @@ __device__ __forceinline__ void build_prefix(const SplitArgs& a, int32_t* pre, i
   int run = scratch[warp] + x - local;
   for (int b = b0; b < b1; ++b) {
     pre[b] = run;
-    run += seq_count(seq_blocks(__ldg(a.seqlens + b), a.bs, a.maxblk), a.part_blocks);
+    run += seq_count(seq_blocks(eff_len(__ldg(a.seqlens + b), a.len_add, a.bs, a.maxblk), a.bs, a.maxblk),
+                     a.part_blocks);
   }
   __syncthreads();
 }
@@ -472,7 +475,7 @@ __device__ __forceinline__ void issue_next(Issuer& is, const SplitArgs& a, const
     is.i = 0;
     is.cnt = warp_tiles<W>(is.pc, sl, w);
     is.win = 0;
-    is.len = __ldg(a.seqlens + is.pc.b);
+    is.len = eff_len(__ldg(a.seqlens + is.pc.b), a.len_add, a.bs, a.maxblk);
     is.entry = table_entry<W>(a, is.pc, is.cnt, lane, sl, w);
     is.entry_next = table_entry<W>(a, is.pc, is.cnt, 32 + lane, sl, w);
   }
@@ -490,7 +493,8 @@ __device__ __forceinline__ void issue_next(Issuer& is, const SplitArgs& a, const
     const bool bad = phys < 0 || phys >= a.P;
     const uint32_t gslot = (uint32_t)w * a.ring + slot;
     const uint32_t full = base + L.full + 8 * gslot;
-    sts32(base + L.info + 4 * gslot, (uint32_t)valid | (bad ? kInfoBad : 0u));
+    sts64(base + L.info + 8 * gslot,
+          ((uint64_t)(uint32_t)phys << 32) | (uint32_t)valid | (bad ? kInfoBad : 0u));
     if (bad || valid == 0) {
       if (bad && h == 0) atomicOr(a.status, kStatusBadBlock);
       mbar_arrive(full);
@@ -571,18 +575,19 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   // The merge kernel may be scheduled now; it waits for this grid to finish.
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, (int32_t)gridDim.x};
+  const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, (int32_t)gridDim.x, a.len_add};
   const int cta = blockIdx.x;
 
-  // Sequences with no cached token: out = 0; invalid length: NaN + status.
+  // Sequences with no cached token: out = 0; invalid length: NaN + status
+  // (with the fused append also "no slot": nothing is written for them).
   for (int b = cta; b < a.B; b += gridDim.x) {
-    const int32_t len = __ldg(a.seqlens + b);
+    const int32_t len = eff_len(__ldg(a.seqlens + b), a.len_add, a.bs, a.maxblk);
     if (seq_blocks(len, a.bs, a.maxblk) != 0) continue;
     const bool ok = seq_len_valid(len, a.bs, a.maxblk);
     const float v = ok ? 0.f : __int_as_float(0x7fc00000);
     float* row = a.out + (int64_t)b * a.H * D;
     for (int i = tid; i < a.H * D; i += blockDim.x) row[i] = v;
-    if (!ok && tid == 0) atomicOr(a.status, kStatusBadSeqlen);
+    if (!ok && tid == 0) atomicOr(a.status, kStatusBadSeqlen | (a.len_add ? kStatusNoSlot : 0u));
   }
   if (tid == 0) {
     if (cta == 0) {
@@ -638,11 +643,14 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     }
     bool bad = false;
     const int cnt = warp_tiles<W>(pc, sl, w);
+    // fused append: the position of this sequence's new token
+    const int32_t new_pos = a.len_add ? __ldg(a.seqlens + pc.b) : -1;
     for (int i = 0; i < cnt; ++i) {
       const uint32_t gslot = (uint32_t)w * R + slot;
       const bool ok = mbar_wait_bounded(base + L.full + 8 * gslot, (phase >> slot) & 1u, abort_flag,
                                         kWaitLimitNs);
-      const uint32_t info = lds32(base + L.info + 4 * gslot);
+      const uint64_t info64 = lds64(base + L.info + 8 * gslot);
+      const uint32_t info = (uint32_t)info64;
       const int valid = (int)(info & 0xffffu);
       if (!ok || (info & kInfoBad)) {
         bad = true;
@@ -653,6 +661,28 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       } else if (valid > 0) {
         const uint32_t kb = base + L.stage + gslot * L.stage_bytes;
         const uint32_t vb = kb + NC * chunk;
+        if (new_pos >= 0) {
+          // The tile holding the new token: put k_new/v_new into its row
+          // here and into the pool slot (no other CTA reads this row).
+          const int t = w + W * i;
+          const int tok0 = (pc.blk0 + (t >> sl)) * a.bs + (t & ((1 << sl) - 1)) * kTile;
+          const int r = new_pos - tok0;
+          if (r >= 0 && r < kTile) {
+            const int32_t phys = (int32_t)(info64 >> 32);
+            const int64_t src = ((int64_t)pc.b * a.Hkv + pc.j) * D;
+            const int64_t dst = (((int64_t)phys * a.bs + (new_pos % a.bs)) * a.Hkv + pc.j) * D;
+            for (int u = lane; u < D / 8; u += 32) {
+              const uint4 kv = __ldg(reinterpret_cast<const uint4*>(a.k_new + src) + u);
+              const uint4 vv = __ldg(reinterpret_cast<const uint4*>(a.v_new + src) + u);
+              sts128(kb + (uint32_t)(u >> 3) * chunk + swz(r, u & 7), kv);
+              sts128(vb + (uint32_t)(u >> 3) * chunk + swz(r, u & 7), vv);
+              reinterpret_cast<uint4*>(a.k_pool + dst)[u] = kv;
+              reinterpret_cast<uint4*>(a.v_pool + dst)[u] = vv;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
         if constexpr (MODE == kMma) {
           if (valid < kTile) {
             // zero the V rows past the sequence end so that p = 0 rows add 0

@@ -124,3 +124,111 @@ def test_captured_graph_replays_with_inputs_changed_in_place():
         w.v_cache = bits_of(v)
         assert_close(out.cpu().numpy().astype(np.float64), run_oracle(w), f"replay {step}")
     assert pg.pa_read_status(ws) == 0
+
+
+# ------------------------------------------------- fused append-and-attend
+
+
+def with_room(w, rng):
+    """Give every sequence a mapped block for position len (the new token)."""
+    table = w.block_table.copy()
+    extra = 0
+    for b in range(w.B):
+        pos = int(w.cache_seqlens[b])
+        if pos // w.block_size < table.shape[1] and table[b, pos // w.block_size] < 0:
+            table[b, pos // w.block_size] = w.num_blocks + extra
+            extra += 1
+    if extra:
+        pad = wl.to_bits(rng.standard_normal((extra,) + w.k_cache.shape[1:], dtype=np.float32),
+                         w.dtype)
+        w.k_cache = np.concatenate([w.k_cache, pad])
+        w.v_cache = np.concatenate([w.v_cache, pad])
+    w.block_table = table
+    w.num_blocks += extra
+    return w
+
+
+def fused_vs_oracle(w, opts=None, seed=0):
+    rng = np.random.default_rng(seed)
+    k_new = wl.to_bits(rng.standard_normal((w.B, w.Hkv, w.d), dtype=np.float32), w.dtype)
+    v_new = wl.to_bits(rng.standard_normal((w.B, w.Hkv, w.d), dtype=np.float32), w.dtype)
+    q, k, v, t, sl = w.torch_tensors("cuda")
+    tdt = k.dtype
+    kn = torch.from_numpy(k_new.view(np.int16)).view(tdt).cuda()
+    vn = torch.from_numpy(v_new.view(np.int16)).view(tdt).cuda()
+    out = torch.full((w.B, w.H, w.d), float("nan"), dtype=torch.float32, device="cuda")
+    ws = pg.alloc_workspace(pg.shape_of(q, k, t), opts)
+    pg.pa_decode_append(q, kn, vn, k, v, t, sl, w.scale, out, ws, opts)
+    status = pg.pa_read_status(ws)
+    kc, vc, _, rc = oracle.append(k_new, v_new, w.k_cache, w.v_cache, w.block_table,
+                                  w.cache_seqlens)
+    return out.cpu().numpy().astype(np.float64), status, bits_of(k), bits_of(v), kc, vc, rc
+
+
+@pytest.mark.parametrize("mode", ["mma", "simt"])
+def test_fused_append_on_the_page_example(mode):
+    g = json.load(open(GOLDEN))
+    w = wl.p5_example(seed=301)
+    got, st, kb, vb, kc, vc, rc = fused_vs_oracle(w, pg.options(compute=mode), seed=1)
+    assert st == 0 and rc == 0
+    assert np.array_equal(kb, kc) and np.array_equal(vb, vc)
+    changed = np.argwhere((kb != w.k_cache).any(axis=(2, 3)))
+    assert sorted(map(tuple, changed.tolist())) == sorted(map(tuple, g["expected_append_slot"]))
+    ref = oracle.decode(w.q, kc, vc, w.block_table, w.cache_seqlens + 1, w.scale, w.dtype)
+    assert_close(got, ref, "fused append, page example")
+
+
+FUSED = [
+    # lengths chosen so new tokens land at row 0 of a new block, at a 16-row
+    # tile boundary, mid-tile, at the last row of a block, and as the very
+    # first token of a sequence
+    ("bs16_d128_g8", dict(lens=[0, 15, 16, 31, 32, 100, 999], H=16, Hkv=2, d=128, bs=16,
+                          dtype="bf16")),
+    ("bs32_d64_g7_f16", dict(lens=[1, 31, 32, 47, 48, 64, 2000], H=14, Hkv=2, d=64, bs=32,
+                             dtype="f16")),
+    ("bs64_d256_g6", dict(lens=[63, 64, 65, 80, 3000], H=12, Hkv=2, d=256, bs=64, dtype="bf16")),
+    ("bs32_d128_g4", dict(lens=list(wl.serving_mix_lengths(7, 12) // 8), H=32, Hkv=8, d=128,
+                          bs=32, dtype="bf16", outlier_frac=0.01)),
+]
+
+
+@pytest.mark.parametrize("mode", ["mma", "simt"])
+@pytest.mark.parametrize("name,kw", FUSED, ids=[f[0] for f in FUSED])
+def test_fused_append_matches_append_then_decode(name, kw, mode):
+    kw = dict(kw)
+    lens = kw.pop("lens")
+    rng = np.random.default_rng(len(name))
+    maxblk = max((n + 1 + kw["bs"] - 1) // kw["bs"] for n in lens) + 1
+    for opts in (pg.options(compute=mode), pg.options(compute=mode, num_ctas=5),
+                 pg.options(compute=mode, partition_tokens=kw["bs"] * 2)):
+        w = with_room(wl.random_workload(lens, seed=len(name) + 3, maxblk=maxblk, **kw), rng)
+        got, st, kb, vb, kc, vc, rc = fused_vs_oracle(w, opts, seed=5)
+        assert st == 0 and rc == 0, (st, rc)
+        assert np.array_equal(kb, kc) and np.array_equal(vb, vc)
+        ref = oracle.decode(w.q, kc, vc, w.block_table, w.cache_seqlens + 1, w.scale, w.dtype)
+        assert_close(got, ref, f"fused {name} {mode}")
+        # the first token of an empty sequence: its output is v_new exactly
+        for b, n in enumerate(lens):
+            if n == 0:
+                for h in range(w.H):
+                    vrow = wl.from_bits(vc[w.block_table[b, 0], 0, h // w.G], w.dtype)
+                    np.testing.assert_allclose(got[b, h], vrow, rtol=0, atol=1e-6)
+
+
+def test_fused_append_without_a_slot():
+    w = wl.random_workload([10, 48, 5], H=8, Hkv=2, d=64, bs=16, dtype="bf16", seed=9, maxblk=3)
+    # sequence 1 is full (48 = 3 blocks x 16): no position for a new token;
+    # sequence 2's block for position 5 is unmapped
+    w.block_table[2, 0] = -1
+    got, st, kb, vb, kc, vc, rc = fused_vs_oracle(w, seed=2)
+    assert st & pg.PA_STATUS_BAD_SEQLEN and st & pg.PA_STATUS_NO_SLOT
+    assert st & pg.PA_STATUS_BAD_BLOCK
+    assert np.isnan(got[1]).all() and np.isnan(got[2]).all()
+    # sequence 0 is appended and attended normally
+    assert np.array_equal(kb[w.block_table[0, 0], 10], kc[w.block_table[0, 0], 10])
+    ref = oracle.decode(w.q[[0]], kc, vc, w.block_table[[0]], np.array([11], np.int32), w.scale,
+                        w.dtype)[0]
+    assert_close(got[0], ref, "sequence with a slot")
+    # nothing else in the pools changed
+    diff = np.argwhere((kb != w.k_cache).any(axis=(2, 3)))
+    assert diff.tolist() == [[int(w.block_table[0, 0]), 10]]
