@@ -167,6 +167,29 @@ def whole_job_gbs(bytes_per_rank_step: int, world: int, ms_per_step: float) -> f
     return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
 
 
+def make_room_for_next_token(w):
+    """Map a fresh physical block (appended to the pool) wherever a
+    sequence's next position has none, as a serving engine would before a
+    fused append step."""
+    bs = w.block_size
+    if int(w.cache_seqlens.max()) // bs >= w.block_table.shape[1]:
+        # a full row: widen every row by one unmapped column
+        w.block_table = np.pad(w.block_table, ((0, 0), (0, 1)), constant_values=-1)
+        w.max_blocks_per_seq += 1
+    table = w.block_table
+    extra = 0
+    for b in range(w.B):
+        col = int(w.cache_seqlens[b]) // bs
+        if table[b, col] < 0:
+            table[b, col] = w.num_blocks + extra
+            extra += 1
+    if extra:
+        pad = np.zeros((extra,) + w.k_cache.shape[1:], dtype=np.uint16)
+        w.k_cache = np.concatenate([w.k_cache, pad])
+        w.v_cache = np.concatenate([w.v_cache, pad])
+        w.num_blocks += extra
+
+
 def make_workload(name):
     from paged_gqa_decode_pa_gb300 import workloads as wl
 
@@ -247,6 +270,7 @@ def workload_config(w, args):
             "max_seqlen": int(np.max(w.cache_seqlens)),
             "partition_tokens": args.partition_tokens, "compute": args.compute,
             "stages": args.stages, "graph": bool(args.graph),
+            "fused_append": bool(args.fused_append),
             "kv_bytes_per_step": w.kv_bytes(),
             "l2": ("inputs larger than L2" if w.kv_bytes() > 2 * L2_BYTES
                    else "L2 flushed between timed steps"),
@@ -261,6 +285,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = make_workload(args.config)
+    if args.fused_append:
+        make_room_for_next_token(w)
     q, k, v, t, sl = w.torch_tensors(dev)
     out = torch.empty((w.B, w.H, w.d), dtype=torch.float32, device=dev)
     opts = pg.options(partition_tokens=args.partition_tokens, compute=args.compute,
@@ -287,6 +313,21 @@ def run_ours(args, rank, world, local_rank):
     uuid = getattr(props, "uuid", None)
     sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local_rank))
 
+    if args.fused_append:
+        # each step writes a new K/V row at position len and attends over
+        # len + 1 tokens (the lengths are not advanced, so every step
+        # rewrites the same slots)
+        gen = torch.Generator(device=dev).manual_seed(1)
+        kn = torch.randn((w.B, w.Hkv, w.d), generator=gen, device=dev).to(k.dtype)
+        vn = torch.randn((w.B, w.Hkv, w.d), generator=gen, device=dev).to(k.dtype)
+        kv_bytes += w.B * w.Hkv * w.d * 2 * 2  # the appended rows
+
+        def decode_step():
+            pg.pa_decode_append(q, kn, vn, k, v, t, sl, w.scale, out, ws, opts)
+    else:
+        def decode_step():
+            pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+
     graph = None
     if args.graph:
         # one decode step captured once and replayed (host launch cost removed)
@@ -294,10 +335,10 @@ def run_ours(args, rank, world, local_rank):
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(stream)
         with torch.cuda.stream(cap):
-            pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+            decode_step()
         cap.synchronize()
         with torch.cuda.graph(graph, stream=cap):
-            pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+            decode_step()
         for _ in range(args.warmup):
             graph.replay()
         torch.cuda.synchronize()
@@ -317,7 +358,7 @@ def run_ours(args, rank, world, local_rank):
         if graph is not None:
             graph.replay()
         else:
-            pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+            decode_step()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     sampler.mark_end()
@@ -441,6 +482,8 @@ def main():
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--compute", default="mma", choices=["mma", "simt", "auto"])
     ap.add_argument("--stages", type=int, default=0, help="pipeline stages (0 = library choice)")
+    ap.add_argument("--fused-append", action="store_true",
+                    help="time pa_decode_append (write the new token, attend over len+1)")
     ap.add_argument("--graph", action="store_true",
                     help="replay one captured CUDA graph of pa_decode per step")
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0,

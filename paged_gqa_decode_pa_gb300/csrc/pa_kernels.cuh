@@ -78,6 +78,8 @@ struct SmemLayout {
   uint32_t stage_bytes;
   uint32_t mo, mm, ml, mbad;        // per-warp partial states for the CTA combine
   uint32_t qs;                      // [G][D+4] fp32 q * scale * log2(e) of the current piece
+  uint32_t zrow;                    // one all-zero K/V row (D x 2 bytes)
+  uint32_t nrow;                    // per warp: the appended token's K and V rows
   uint32_t ps;                      // CUDA-core path: p per warp
   uint32_t pre;                     // [B + 1] prefix sums
   uint32_t total;                   // bytes to request (incl. alignment slack)
@@ -100,11 +102,15 @@ PA_HD SmemLayout split_smem_layout(int D, int G, int B, int W, int R, int mode) 
   off += (uint32_t)W * kGMax * 4u;
   L.mbad = off;
   off += (uint32_t)W * 4u;
-  L.abort_flag = off;
-  off += 4u;
+  L.abort_flag = off;  // followed by the current piece's stored length
+  off += 8u;
   off = align_up(off, 16);
   L.qs = off;
   off += (uint32_t)(G * (D + 4)) * 4u;
+  L.zrow = off;
+  off += (uint32_t)D * 2u;
+  L.nrow = off;
+  off += (uint32_t)(W * 2 * D) * 2u;
   if (mode == kSimt) {
     L.ps = off;
     off += (uint32_t)(W * kTile * kGMax) * 4u;

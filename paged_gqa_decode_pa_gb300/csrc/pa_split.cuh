@@ -140,7 +140,14 @@ struct MmaState {
 
   // One 16-token tile, `valid` (1..16) of its rows real; K chunks at kb, V
   // chunks at vb, each chunk a 128B-swizzled [16][64] tile of 2 KB.
-  __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int valid) {
+  //
+  // ldmatrix takes one row address per lane, so two kinds of rows are read
+  // from outside the TMA stage (which no thread ever writes): V rows past the
+  // sequence end read the CTA's zero row, and row `new_r` (the token being
+  // appended, or -1) reads the warp's copy of the new K/V rows at nk / nv.
+  // Those buffers are unswizzled: 64-dim chunk c, unit u at c*128 + u*16.
+  __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int valid, int new_r, uint32_t nk,
+                                       uint32_t nv, uint32_t zrow) {
     const int lane = threadIdx.x & 31;
     constexpr uint32_t chunk = kTile * 128u;
     // ---- S^T = K . Q'^T  (rows: the 16 tokens, cols: heads); four
@@ -149,10 +156,13 @@ struct MmaState {
     {
       const uint32_t tok = (lane & 7) + ((lane >> 3) & 1) * 8;
       const uint32_t uh = (uint32_t)(lane >> 4);
+      const bool knew = (int)tok == new_r;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t a0, a1, a2, a3;
-        const uint32_t addr = kb + (uint32_t)(ks >> 2) * chunk + swz(tok, 2u * (ks & 3) + uh);
+        const uint32_t unit = 2u * (ks & 3) + uh;
+        const uint32_t addr = knew ? nk + (uint32_t)(ks >> 2) * 128u + unit * 16u
+                                   : kb + (uint32_t)(ks >> 2) * chunk + swz(tok, unit);
         ldmatrix_x4(addr, a0, a1, a2, a3);
         mma_16816<T>(acc4[ks & 1], a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
         mma_16816<T>(acc4[2 + (ks & 1)], a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
@@ -197,14 +207,19 @@ struct MmaState {
     const uint32_t e23 = Cvt<T>::pack(p2 - Cvt<T>::low(h23), p3 - Cvt<T>::high(h23));
     const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
     const uint32_t bl0 = movmatrix_trans(e01), bl1 = movmatrix_trans(e23);
-    // ---- O^T += V^T . P^T
+    // ---- O^T += V^T . P^T  (rows past the end read zeros, so p = 0 adds 0
+    // even where the pool holds NaN)
     {
       const uint32_t tok = (lane & 7) + (lane >> 4) * 8;
       const uint32_t uh = (uint32_t)((lane >> 3) & 1);
+      const bool vplain = (int)tok == new_r || (int)tok >= valid;
+      const uint32_t vrow = (int)tok == new_r ? nv : zrow;
 #pragma unroll
       for (int dt = 0; dt < D / 16; ++dt) {
         uint32_t a0, a1, a2, a3;
-        const uint32_t addr = vb + (uint32_t)(dt >> 2) * chunk + swz(tok, 2u * (dt & 3) + uh);
+        const uint32_t unit = 2u * (dt & 3) + uh;
+        const uint32_t addr = vplain ? vrow + (uint32_t)(dt >> 2) * 128u + unit * 16u
+                                     : vb + (uint32_t)(dt >> 2) * chunk + swz(tok, unit);
         ldmatrix_x4_trans(addr, a0, a1, a2, a3);
         mma_16816<T>(o[dt], a0, a1, a2, a3, bh0, bh1);
         mma_16816<T>(o[dt], a0, a1, a2, a3, bl0, bl1);
@@ -267,8 +282,9 @@ struct SimtState {
   // One 16-token tile, `valid` (1..16) rows real.  qs: shared [G][D] fp32
   // q*scale*log2e.  ps: this warp's [16][8] fp32 buffer.  Lanes 0-15 and
   // 16-31 take the same 16 tokens for the two halves of the G heads.
+  // Rows as in MmaState::tile: row new_r (or -1) is read from nk / nv.
   __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int valid, const float* qs,
-                                       float* ps, int G) {
+                                       float* ps, int G, int new_r, uint32_t nk, uint32_t nv) {
     const int lane = threadIdx.x & 31;
     constexpr uint32_t chunk = kTile * 128u;
     // ---------------- q . k : lane <-> token
@@ -281,7 +297,8 @@ struct SimtState {
     for (int g = 0; g < kGMax; ++g) s[g] = 0.f;
 #pragma unroll 4
     for (int c8 = 0; c8 < D / 8; ++c8) {
-      const uint4 kr = lds128(kb + (uint32_t)(c8 >> 3) * chunk + swz(tt, c8 & 7));
+      const uint4 kr = lds128(tt == new_r ? nk + (uint32_t)(c8 >> 3) * 128u + (uint32_t)(c8 & 7) * 16u
+                                          : kb + (uint32_t)(c8 >> 3) * chunk + swz(tt, c8 & 7));
       float kf[8];
       kf[0] = Cvt<T>::low(kr.x);
       kf[1] = Cvt<T>::high(kr.x);
@@ -349,7 +366,8 @@ struct SimtState {
       const float p[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        const uint32_t v = lds32(vb + (uint32_t)c * chunk + swz(t, unit) + col);
+        const uint32_t v = lds32(t == new_r ? nv + (uint32_t)c * 128u + unit * 16u + col
+                                            : vb + (uint32_t)c * chunk + swz(t, unit) + col);
         const float v0 = Cvt<T>::low(v), v1 = Cvt<T>::high(v);
 #pragma unroll
         for (int g = 0; g < kGMax; ++g) {
@@ -516,7 +534,9 @@ template <int D>
 struct QPrefetch {
   static constexpr int kPer = (kGMax * D / 2 + 32 * 4 - 1) / (32 * 4);  // words per thread, >= 4 warps
   uint32_t v[kPer];
+  int32_t len;  // stored cache_seqlens of the piece's sequence (thread 0)
   __device__ __forceinline__ void start(const SplitArgs& a, const Piece& pc) {
+    if (threadIdx.x == 0) len = __ldg(a.seqlens + pc.b);
     const uint32_t* src = reinterpret_cast<const uint32_t*>(
         a.q + ((int64_t)pc.b * a.H + (int64_t)pc.j * a.G) * D);
     const int nw = a.G * D / 2;
@@ -527,7 +547,8 @@ struct QPrefetch {
     }
   }
   template <typename T>
-  __device__ __forceinline__ void finish(const SplitArgs& a, float* qs) {
+  __device__ __forceinline__ void finish(const SplitArgs& a, float* qs, int32_t* len_out) {
+    if (threadIdx.x == 0) *len_out = len;
     const int nw = a.G * D / 2;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
@@ -560,6 +581,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   int32_t* pre = reinterpret_cast<int32_t*>(smem + L.pre);
   float* qs = reinterpret_cast<float*>(smem + L.qs);
+  int32_t* piece_len = reinterpret_cast<int32_t*>(smem + L.abort_flag + 4);
   __shared__ int32_t scan_scratch[kMaxWarps];
 
   if (tid == 0) {
@@ -567,6 +589,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  for (int i = tid; i < D / 8; i += blockDim.x) sts128(base + L.zrow + 16u * i, make_uint4(0u, 0u, 0u, 0u));
   if (lane == 0) {
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
@@ -626,7 +649,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   if (have) {
     QPrefetch<D> qp;
     qp.start(a, pc);
-    qp.template finish<T>(a, qs);
+    qp.template finish<T>(a, qs, piece_len);
   }
   __syncthreads();
   uint32_t slot = 0, phase = 0;  // ring slot to consume next; per-slot parity bits
@@ -643,8 +666,22 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     }
     bool bad = false;
     const int cnt = warp_tiles<W>(pc, sl, w);
-    // fused append: the position of this sequence's new token
-    const int32_t new_pos = a.len_add ? __ldg(a.seqlens + pc.b) : -1;
+    // fused append: the position of this sequence's new token; the warp
+    // whose tile holds it loads the new K/V row now, ahead of that tile
+    int32_t new_pos = -1;
+    uint4 nk = make_uint4(0u, 0u, 0u, 0u), nv = nk;
+    if (a.len_add) {
+      const int32_t p0 = *reinterpret_cast<volatile int32_t*>(piece_len);
+      const int rel = p0 - pc.blk0 * a.bs;
+      if (rel >= 0 && rel < (pc.blk1 - pc.blk0) * a.bs && ((rel >> 4) % W) == w) {
+        new_pos = p0;
+        const int64_t src = ((int64_t)pc.b * a.Hkv + pc.j) * D;
+        if (lane < D / 8) {
+          nk = __ldg(reinterpret_cast<const uint4*>(a.k_new + src) + lane);
+          nv = __ldg(reinterpret_cast<const uint4*>(a.v_new + src) + lane);
+        }
+      }
+    }
     for (int i = 0; i < cnt; ++i) {
       const uint32_t gslot = (uint32_t)w * R + slot;
       const bool ok = mbar_wait_bounded(base + L.full + 8 * gslot, (phase >> slot) & 1u, abort_flag,
@@ -661,43 +698,32 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       } else if (valid > 0) {
         const uint32_t kb = base + L.stage + gslot * L.stage_bytes;
         const uint32_t vb = kb + NC * chunk;
+        int new_r = -1;
+        const uint32_t nkr = base + L.nrow + (uint32_t)w * 4u * D, nvr = nkr + 2u * D;
         if (new_pos >= 0) {
-          // The tile holding the new token: put k_new/v_new into its row
-          // here and into the pool slot (no other CTA reads this row).
+          // The tile holding the new token: its row comes from the warp's
+          // copy of k_new/v_new, which also goes to the pool slot (no other
+          // CTA reads this row).
           const int t = w + W * i;
           const int tok0 = (pc.blk0 + (t >> sl)) * a.bs + (t & ((1 << sl) - 1)) * kTile;
           const int r = new_pos - tok0;
           if (r >= 0 && r < kTile) {
             const int32_t phys = (int32_t)(info64 >> 32);
-            const int64_t src = ((int64_t)pc.b * a.Hkv + pc.j) * D;
             const int64_t dst = (((int64_t)phys * a.bs + (new_pos % a.bs)) * a.Hkv + pc.j) * D;
-            for (int u = lane; u < D / 8; u += 32) {
-              const uint4 kv = __ldg(reinterpret_cast<const uint4*>(a.k_new + src) + u);
-              const uint4 vv = __ldg(reinterpret_cast<const uint4*>(a.v_new + src) + u);
-              sts128(kb + (uint32_t)(u >> 3) * chunk + swz(r, u & 7), kv);
-              sts128(vb + (uint32_t)(u >> 3) * chunk + swz(r, u & 7), vv);
-              reinterpret_cast<uint4*>(a.k_pool + dst)[u] = kv;
-              reinterpret_cast<uint4*>(a.v_pool + dst)[u] = vv;
+            if (lane < D / 8) {
+              sts128(nkr + lane * 16u, nk);
+              sts128(nvr + lane * 16u, nv);
+              reinterpret_cast<uint4*>(a.k_pool + dst)[lane] = nk;
+              reinterpret_cast<uint4*>(a.v_pool + dst)[lane] = nv;
             }
-            fence_proxy_async_smem();
             __syncwarp();
+            new_r = r;
           }
         }
         if constexpr (MODE == kMma) {
-          if (valid < kTile) {
-            // zero the V rows past the sequence end so that p = 0 rows add 0
-            const int rows = kTile - valid;
-            for (int u = lane; u < rows * 8 * NC; u += 32) {
-              const int c = u / (rows * 8), rem = u % (rows * 8);
-              sts128(vb + c * chunk + (uint32_t)(valid + rem / 8) * 128u + (rem % 8) * 16u,
-                     make_uint4(0u, 0u, 0u, 0u));
-            }
-            fence_proxy_async_smem();
-          }
-          __syncwarp();
-          mst.tile(kb, vb, valid);
+          mst.tile(kb, vb, valid, new_r, nkr, nvr, base + L.zrow);
         } else {
-          sst.tile(kb, vb, valid, qs, ps, a.G);
+          sst.tile(kb, vb, valid, qs, ps, a.G, new_r, nkr, nvr);
         }
       }
       __syncwarp();
@@ -721,7 +747,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     QPrefetch<D> qp;
     if (more) qp.start(a, next);
     combine_piece<D>(a, smem, L, pc, W);
-    if (more) qp.template finish<T>(a, qs);
+    if (more) qp.template finish<T>(a, qs, piece_len);
     named_bar_sync(1, blockDim.x);
     have = it.next(pc);
   }
