@@ -76,6 +76,10 @@ typedef struct CUstream_st* pa_stream_t;
 #define PA_ERR_OPTION (-6)      /* invalid pa_options value */
 #define PA_ERR_SCRATCH_LIMIT (-7) /* pa_decode_noalloc: needs more scratch than
                                      PA_STATIC_SCRATCH_BYTES */
+#define PA_ERR_STATE (-8)       /* block manager: invalid handle, sequence id,
+                                   index or request; nothing was changed */
+#define PA_ERR_NO_BLOCKS (-9)   /* block manager: the free list is too short;
+                                   nothing was changed */
 
 /* Device status bits (sticky in the workspace status word). */
 #define PA_STATUS_BAD_BLOCK 0x1u   /* a table entry inside a sequence's length is
@@ -249,6 +253,90 @@ int pa_plan_pieces(const pa_shape* shape, const pa_options* options,
 int pa_plan_merge(const pa_shape* shape, const pa_options* options,
                   const int32_t* cache_seqlens_host, int32_t num_ctas, int32_t seg,
                   int32_t* b_j, int32_t* slots, int32_t max_slots);
+
+/* ------------------------------------------------------------------------
+ * Block manager (host side) and block copy (device side).
+ *
+ * The host allocator of the pool of physical blocks, as the block manager of
+ * the "paged-attention-runtime" design page (sections "System component
+ * flow" and "BlockManager") describes it: a free list of physical block ids,
+ * a reference count per block, and for every sequence the ordered list of
+ * the blocks that hold its tokens (its row of block_table).  Its operations
+ * are that page's allocate_blocks / free_sequence / share_prefix / cow_block:
+ *   - sharing a prefix puts the source's first n blocks into the target's
+ *     list and raises each one's count by one;
+ *   - copy-on-write of a block whose count is above one takes a fresh block
+ *     from the free list for the writer (count 1), lowers the old block's
+ *     count, and leaves the data move to the caller (pa_copy_blocks);
+ *   - a block whose count falls to zero goes back to the free list.
+ * The manager owns host memory only; it never touches the device.  Every
+ * call is serialised by a mutex inside the handle, so one handle may be used
+ * from several host threads.  All calls return PA_OK (or a count) on
+ * success, PA_ERR_STATE for a NULL handle / out-of-range id / impossible
+ * request and PA_ERR_NO_BLOCKS when the free list is too short; on an error
+ * the manager is left exactly as it was.  The free list is a stack: a new
+ * manager hands out ids 0, 1, 2, ... and a block freed later is the next one
+ * handed out.
+ * ------------------------------------------------------------------------ */
+typedef struct pa_block_manager pa_block_manager;
+
+/* A manager for physical blocks 0..num_blocks-1 of block_size tokens, for
+ * sequence ids 0..max_seqs-1 of at most max_blocks_per_seq blocks each.
+ * Returns NULL when an argument is < 1 or memory runs out. */
+pa_block_manager* pa_bm_create(int32_t num_blocks, int32_t block_size, int32_t max_seqs,
+                               int32_t max_blocks_per_seq);
+void pa_bm_destroy(pa_block_manager* bm);
+
+/* allocate_blocks(seq, n): append n fresh blocks (count 1) to seq's list. */
+int pa_bm_allocate(pa_block_manager* bm, int32_t seq, int32_t n);
+
+/* free_sequence(seq): lower the count of every block of seq, return those
+ * that reach zero to the free list, and empty seq's list. */
+int pa_bm_free_sequence(pa_block_manager* bm, int32_t seq);
+
+/* share_prefix(src, dst, n): dst (which must own no blocks) gets src's first
+ * n blocks, each block's count raised by one. */
+int pa_bm_share_prefix(pa_block_manager* bm, int32_t src, int32_t dst, int32_t n);
+
+/* cow_block(seq, index): make block `index` of seq private before a write.
+ * *old_block = the block seq held there; *new_block = the block it holds
+ * now.  They differ only when the old block was shared: then the caller must
+ * copy old -> new on the device (pa_copy_blocks) before writing into it. */
+int pa_bm_copy_on_write(pa_block_manager* bm, int32_t seq, int32_t index, int32_t* old_block,
+                        int32_t* new_block);
+
+/* Make position `pos` of seq writable, as a decode step needs before
+ * appending token pos: pos / block_size == the number of blocks seq owns
+ * appends one fresh block (*old_block == *new_block); an earlier index is
+ * cow_block(seq, pos / block_size).  A larger index is PA_ERR_STATE. */
+int pa_bm_reserve_slot(pa_block_manager* bm, int32_t seq, int32_t pos, int32_t* old_block,
+                       int32_t* new_block);
+
+/* Write the block_table rows of the sequences seq_ids[0..rows-1] into the
+ * host array table[rows][cols] (int32, -1 past each sequence's blocks).
+ * PA_ERR_STATE if a sequence owns more than cols blocks. */
+int pa_bm_block_table(pa_block_manager* bm, const int32_t* seq_ids, int32_t rows, int32_t cols,
+                      int32_t* table);
+
+/* Counters: PA_BM_FREE_BLOCKS (arg unused), PA_BM_REF_COUNT (arg = block),
+ * PA_BM_SEQ_BLOCKS (arg = sequence).  Returns the count or PA_ERR_STATE. */
+#define PA_BM_FREE_BLOCKS 0
+#define PA_BM_REF_COUNT 1
+#define PA_BM_SEQ_BLOCKS 2
+int pa_bm_query(pa_block_manager* bm, int32_t what, int32_t arg);
+
+/* Device half of copy-on-write: for i < n_pairs, physical block
+ * pairs[2i+1] of k_cache and of v_cache becomes a bit-for-bit copy of block
+ * pairs[2i] (all bs rows, all kv heads).  `pairs` is a DEVICE int32 array
+ * [n_pairs, 2] so a captured graph can replay with new pairs.  Only
+ * num_kv_heads, head_dim, block_size and num_blocks of `shape` are used
+ * (head_dim a multiple of 8).  A pair with an id outside [0, num_blocks)
+ * copies nothing and ORs PA_STATUS_BAD_BLOCK into *status (device uint32,
+ * may be NULL).  Destinations must be distinct and no destination may be
+ * another pair's source (the copies run concurrently).  k_cache and v_cache
+ * must be 16-byte aligned; 0 <= n_pairs <= 65535. */
+int pa_copy_blocks(const pa_shape* shape, void* k_cache, void* v_cache, const int32_t* pairs,
+                   int32_t n_pairs, uint32_t* status, pa_stream_t stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int pa_version(void);

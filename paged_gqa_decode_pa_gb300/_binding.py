@@ -24,6 +24,12 @@ PA_ERR_WORKSPACE = -4
 PA_ERR_CUDA = -5
 PA_ERR_OPTION = -6
 PA_ERR_SCRATCH_LIMIT = -7
+PA_ERR_STATE = -8
+PA_ERR_NO_BLOCKS = -9
+
+PA_BM_FREE_BLOCKS = 0
+PA_BM_REF_COUNT = 1
+PA_BM_SEQ_BLOCKS = 2
 
 PA_STATUS_BAD_BLOCK = 0x1
 PA_STATUS_BAD_SEQLEN = 0x2
@@ -41,7 +47,10 @@ _COMPUTE = {"auto": PA_COMPUTE_AUTO, "simt": PA_COMPUTE_SIMT, "mma": PA_COMPUTE_
 # Every symbol include/pagedgqa.h declares.
 EXPORTS = ("pa_workspace_size", "pa_decode", "pa_decode_split", "pa_decode_merge",
            "pa_cache_append", "pa_read_status", "pa_status_string", "pa_plan_pieces",
-           "pa_plan_merge", "pa_version", "pa_decode_noalloc", "pa_decode_append")
+           "pa_plan_merge", "pa_version", "pa_decode_noalloc", "pa_decode_append",
+           "pa_bm_create", "pa_bm_destroy", "pa_bm_allocate", "pa_bm_free_sequence",
+           "pa_bm_share_prefix", "pa_bm_copy_on_write", "pa_bm_reserve_slot",
+           "pa_bm_block_table", "pa_bm_query", "pa_copy_blocks")
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -114,6 +123,23 @@ def lib():
         L.pa_plan_pieces.restype = ctypes.c_int
         L.pa_plan_merge.argtypes = [SP, OP, P, i32, i32, P, P, i32]
         L.pa_plan_merge.restype = ctypes.c_int
+        L.pa_bm_create.argtypes = [i32, i32, i32, i32]
+        L.pa_bm_create.restype = P
+        L.pa_bm_destroy.argtypes = [P]
+        L.pa_bm_destroy.restype = None
+        L.pa_bm_allocate.argtypes = [P, i32, i32]
+        L.pa_bm_free_sequence.argtypes = [P, i32]
+        L.pa_bm_share_prefix.argtypes = [P, i32, i32, i32]
+        for name in ("pa_bm_copy_on_write", "pa_bm_reserve_slot"):
+            getattr(L, name).argtypes = [P, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        L.pa_bm_block_table.argtypes = [P, P, i32, i32, P]
+        L.pa_bm_query.argtypes = [P, i32, i32]
+        for name in ("pa_bm_allocate", "pa_bm_free_sequence", "pa_bm_share_prefix",
+                     "pa_bm_copy_on_write", "pa_bm_reserve_slot", "pa_bm_block_table",
+                     "pa_bm_query"):
+            getattr(L, name).restype = ctypes.c_int
+        L.pa_copy_blocks.argtypes = [SP, P, P, P, i32, P, P]
+        L.pa_copy_blocks.restype = ctypes.c_int
         L.pa_version.argtypes = []
         L.pa_version.restype = ctypes.c_int
         _lib = L
@@ -332,6 +358,137 @@ def pa_plan_merge(shape: pa_shape, opts: Optional[pa_options], lens_host, num_ct
     if n == 0:
         return None
     return (int(bj[0]), int(bj[1])), [int(s) for s in slots[:n]]
+
+
+class BlockManager:
+    """Owner of a pa_block_manager handle (the C calls below take it as `bm`).
+
+    Host allocator of the physical-block pool: free list, per-block reference
+    count, per-sequence block lists; allocate / free_sequence / share_prefix /
+    copy-on-write as the "paged-attention-runtime" design page's BlockManager
+    section describes them."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_seqs: int,
+                 max_blocks_per_seq: int):
+        self.handle = pa_bm_create(num_blocks, block_size, max_seqs, max_blocks_per_seq)
+        self.block_size = int(block_size)
+
+    def close(self):
+        if self.handle:
+            pa_bm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def allocate(self, seq: int, n: int):
+        pa_bm_allocate(self.handle, seq, n)
+
+    def free_sequence(self, seq: int):
+        pa_bm_free_sequence(self.handle, seq)
+
+    def share_prefix(self, src: int, dst: int, n: int):
+        pa_bm_share_prefix(self.handle, src, dst, n)
+
+    def copy_on_write(self, seq: int, index: int):
+        return pa_bm_copy_on_write(self.handle, seq, index)
+
+    def reserve_slot(self, seq: int, pos: int):
+        return pa_bm_reserve_slot(self.handle, seq, pos)
+
+    def block_table(self, seq_ids, cols: int):
+        return pa_bm_block_table(self.handle, seq_ids, cols)
+
+    def free_blocks(self) -> int:
+        return pa_bm_query(self.handle, PA_BM_FREE_BLOCKS, 0)
+
+    def ref_count(self, block: int) -> int:
+        return pa_bm_query(self.handle, PA_BM_REF_COUNT, block)
+
+    def num_seq_blocks(self, seq: int) -> int:
+        return pa_bm_query(self.handle, PA_BM_SEQ_BLOCKS, seq)
+
+
+def pa_bm_create(num_blocks: int, block_size: int, max_seqs: int, max_blocks_per_seq: int):
+    h = lib().pa_bm_create(int(num_blocks), int(block_size), int(max_seqs),
+                           int(max_blocks_per_seq))
+    if not h:
+        raise PagedGQAError(PA_ERR_STATE, "pa_bm_create")
+    return h
+
+
+def pa_bm_destroy(bm) -> None:
+    lib().pa_bm_destroy(bm)
+
+
+def pa_bm_allocate(bm, seq: int, n: int) -> None:
+    _check(lib().pa_bm_allocate(bm, int(seq), int(n)), "pa_bm_allocate")
+
+
+def pa_bm_free_sequence(bm, seq: int) -> None:
+    _check(lib().pa_bm_free_sequence(bm, int(seq)), "pa_bm_free_sequence")
+
+
+def pa_bm_share_prefix(bm, src: int, dst: int, n: int) -> None:
+    _check(lib().pa_bm_share_prefix(bm, int(src), int(dst), int(n)), "pa_bm_share_prefix")
+
+
+def _bm_pair_call(name, bm, a: int, b: int):
+    old, new = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    _check(getattr(lib(), name)(bm, int(a), int(b), ctypes.byref(old), ctypes.byref(new)), name)
+    return int(old.value), int(new.value)
+
+
+def pa_bm_copy_on_write(bm, seq: int, index: int):
+    """(old_block, new_block); they differ when the caller must copy old -> new."""
+    return _bm_pair_call("pa_bm_copy_on_write", bm, seq, index)
+
+
+def pa_bm_reserve_slot(bm, seq: int, pos: int):
+    """(old_block, new_block) for the block that will hold token `pos` of seq."""
+    return _bm_pair_call("pa_bm_reserve_slot", bm, seq, pos)
+
+
+def pa_bm_block_table(bm, seq_ids, cols: int):
+    """int32 numpy array [len(seq_ids), cols], -1 past each sequence's blocks."""
+    import numpy as np
+
+    ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+    table = np.empty((ids.size, int(cols)), dtype=np.int32)
+    _check(lib().pa_bm_block_table(bm, ids.ctypes.data, int(ids.size), int(cols),
+                                   table.ctypes.data), "pa_bm_block_table")
+    return table
+
+
+def pa_bm_query(bm, what: int, arg: int = 0) -> int:
+    r = lib().pa_bm_query(bm, int(what), int(arg))
+    if r < 0:
+        _check(r, "pa_bm_query")
+    return int(r)
+
+
+def pa_copy_blocks(k_cache, v_cache, pairs, status=None, stream=None) -> None:
+    """Copy physical block pairs[i,0] onto pairs[i,1] in both pools (in place).
+
+    pairs: int32 CUDA tensor [n, 2]; status: optional uint32-sized CUDA tensor
+    that receives PA_STATUS_BAD_BLOCK for an out-of-range id."""
+    import torch
+
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("pairs", pairs)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if pairs.dtype != torch.int32 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise TypeError("pairs must be an int32 tensor [n, 2]")
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must match")
+    P, bs, Hkv, d = k_cache.shape
+    shape = pa_shape(0, Hkv, Hkv, d, bs, 1, P, _dtype_code(k_cache))
+    rc = lib().pa_copy_blocks(ctypes.byref(shape), _ptr(k_cache), _ptr(v_cache), _ptr(pairs),
+                              int(pairs.shape[0]), _ptr(status), _stream(stream))
+    _check(rc, "pa_copy_blocks")
 
 
 def pa_version() -> int:

@@ -661,6 +661,8 @@ const char* pa_status_string(int code) {
     case PA_ERR_SCRATCH_LIMIT:
       return "problem needs more scratch than the built-in static buffer "
              "(PA_STATIC_SCRATCH_BYTES) of pa_decode_noalloc holds";
+    case PA_ERR_STATE: return "block manager: invalid handle, id, index or request";
+    case PA_ERR_NO_BLOCKS: return "block manager: not enough free blocks";
     default: break;
   }
   if (code > 0) {
