@@ -9,7 +9,7 @@ from libm); this module compiles it with gcc on first use and marshals numpy
 arrays.  Every function cites the page passage it follows in the C source.
 
 Functions with no pin beyond the tests in ``tests/test_oracle_pins.py``:
-none -- decode, partial/combine and append are all pinned there.
+none -- decode, decode_multi, partial/combine and append are all pinned there.
 """
 from __future__ import annotations
 
@@ -66,6 +66,9 @@ def _load():
     i = ctypes.c_int
     lib.pa_oracle_decode.argtypes = [i] * 8 + [P, P, P, P, P, ctypes.c_double, i, P, P, i]
     lib.pa_oracle_decode.restype = i
+    lib.pa_oracle_decode_multi.argtypes = ([i] * 8 + [P, i, P, i, P, P, P, P, ctypes.c_double,
+                                            i, P, P, i])
+    lib.pa_oracle_decode_multi.restype = i
     lib.pa_oracle_partial.argtypes = ([i] * 8 + [P, P, P, P, P, ctypes.c_double]
                                       + [i, i, i, i, P, P, P])
     lib.pa_oracle_partial.restype = i
@@ -143,6 +146,40 @@ def decode(q, k_cache, v_cache, block_table, cache_seqlens, scale, dtype,
     rc = lib.pa_oracle_decode(B, H, Hkv, d, bs, maxblk, P, _dtype_code(dtype),
                               _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(sl),
                               float(scale), n, pp, _ptr(out), int(n_threads))
+    _check(rc)
+    return out
+
+
+def decode_multi(q, cu_q, causal, k_cache, v_cache, block_table, cache_seqlens, scale, dtype,
+                 pairs=None, n_threads: int = 0) -> np.ndarray:
+    """Float64 attention of packed query rows q [total_q, H, d]; sequence b
+    owns rows cu_q[b] .. cu_q[b+1]-1 and its keys are its cache_seqlens[b]
+    cached tokens (query i of n_q sees keys t < k_len - n_q + i + 1 when
+    causal).  Returns [total_q, H, d] float64, or [n, d] for (row, h) pairs."""
+    lib = _load()
+    q = _bits(q)
+    k_cache = _bits(k_cache)
+    v_cache = _bits(v_cache)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_q, dtype=np.int32)
+    total_q, H, d = q.shape
+    P, bs, Hkv, d2 = k_cache.shape
+    B = sl.shape[0]
+    if d2 != d or v_cache.shape != k_cache.shape or cu.shape != (B + 1,):
+        raise ValueError("q/k/v/cu_q shapes disagree")
+    maxblk = bt.shape[1] if bt.ndim == 2 else 0
+    if pairs is None:
+        out = np.zeros((total_q, H, d), dtype=np.float64)
+        n, pp = -1, None
+    else:
+        pairs = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+        out = np.zeros((pairs.shape[0], d), dtype=np.float64)
+        n, pp = pairs.shape[0], _ptr(pairs)
+    rc = lib.pa_oracle_decode_multi(B, H, Hkv, d, bs, maxblk, P, _dtype_code(dtype), _ptr(q),
+                                    total_q, _ptr(cu), int(bool(causal)), _ptr(k_cache),
+                                    _ptr(v_cache), _ptr(bt), _ptr(sl), float(scale), n, pp,
+                                    _ptr(out), int(n_threads))
     _check(rc)
     return out
 

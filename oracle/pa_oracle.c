@@ -35,6 +35,10 @@
  * "Paged Attention Kernel Architecture for BI-V100", section 2, Level 1 and
  * Level 3.
  *
+ * Several query tokens per sequence (pa_oracle_decode_multi) follow the
+ * varlen indexing of the Hugging Face page (cumulative query lengths) with
+ * the query tokens taken as the last positions of the key sequence.
+ *
  * Cache append (pa_oracle_append) follows the decoding-path example of the
  * Hugging Face page: the new token of a sequence with len cached tokens goes
  * to row len % bs of physical block block_table[b][len / bs].
@@ -133,12 +137,11 @@ static int check_sequence(const shape_t* s, const int32_t* block_table,
 /* One (b, h) output row by the plain definition, over tokens [t0, t1).
  * Writes the softmax-normalised result into out[d].  scratch holds t1-t0
  * doubles. */
-static void attend_one(const shape_t* s, const uint16_t* q, const uint16_t* k_cache,
+static void attend_one(const shape_t* s, const uint16_t* qrow, const uint16_t* k_cache,
                        const uint16_t* v_cache, const int32_t* block_table, int b, int h,
                        int t0, int t1, double scale, double* scores, double* out) {
   int G = s->H / s->Hkv;
   int j = h / G;
-  const uint16_t* qrow = q + ((int64_t)b * s->H + h) * s->d;
   int n = t1 - t0;
   for (int k = 0; k < s->d; ++k) out[k] = 0.0;
   if (n <= 0) return;
@@ -210,13 +213,112 @@ int pa_oracle_decode(int B, int H, int Hkv, int d, int bs, int maxblk, int P, in
       for (int64_t i = 0; i < count; ++i) {
         int b = pairs ? pairs[2 * i] : (int)(i / H);
         int h = pairs ? pairs[2 * i + 1] : (int)(i % H);
-        attend_one(&s, q, k_cache, v_cache, block_table, b, h, 0, cache_seqlens[b], scale,
-                   scores, out + i * d);
+        attend_one(&s, q + ((int64_t)b * H + h) * d, k_cache, v_cache, block_table, b, h, 0,
+                   cache_seqlens[b], scale, scores, out + i * d);
       }
       free(scores);
     }
   }
   (void)n_threads;
+  return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/*
+ * pa_oracle_decode_multi: several query tokens per sequence over the paged
+ * cache (chunked decode).
+ *
+ * Query rows are packed as in the varlen path of the Hugging Face "Paged
+ * attention" page: sequence b owns rows cu_q[b] .. cu_q[b+1]-1 of
+ * q [total_q, H, d] (cumulative query lengths, cu_seq_lens_q), so row r
+ * belongs to the b with cu_q[b] <= r < cu_q[b+1].  Its keys are the
+ * k_len = cache_seqlens[b] tokens of the paged cache (block_table as in
+ * pa_oracle_decode), the new tokens already included.  The n_q query tokens
+ * are the last n_q positions of the key sequence, so query i (0-based within
+ * its sequence) sees
+ *   causal != 0:  keys t < clamp(k_len - n_q + i + 1, 0, k_len)
+ *   causal == 0:  keys t < k_len
+ * and its output is the plain softmax-weighted sum of those V rows; a query
+ * that sees no key gets 0 (as an empty sequence does), and so does a row
+ * that belongs to no sequence.  out is [total_q, H, d], or [n_pairs, d] for
+ * the (row, h) pairs given.
+ * Returns ORACLE_ERR_RANGE when cu_q is not non-decreasing within
+ * [0, total_q] or a pair is out of range, and the pa_oracle_decode codes for
+ * a bad length or table entry of a sequence that owns a requested row.
+ */
+int pa_oracle_decode_multi(int B, int H, int Hkv, int d, int bs, int maxblk, int P, int dtype,
+                           const uint16_t* q, int total_q, const int32_t* cu_q, int causal,
+                           const uint16_t* k_cache, const uint16_t* v_cache,
+                           const int32_t* block_table, const int32_t* cache_seqlens,
+                           double scale, int n_pairs, const int32_t* pairs, double* out,
+                           int n_threads) {
+  shape_t s = {B, H, Hkv, d, bs, maxblk, P, dtype};
+  int rc = check_shape(&s);
+  if (rc) return rc;
+  if (total_q < 0) return ORACLE_ERR_SHAPE;
+  if (B > 0 && (cu_q[0] < 0 || cu_q[B] > total_q)) return ORACLE_ERR_RANGE;
+  for (int b = 0; b < B; ++b)
+    if (cu_q[b + 1] < cu_q[b]) return ORACLE_ERR_RANGE;
+  int64_t count = (pairs == NULL || n_pairs < 0) ? (int64_t)total_q * H : n_pairs;
+  int32_t* owner = (int32_t*)malloc(sizeof(int32_t) * (size_t)(count > 0 ? count : 1));
+  if (!owner) return ORACLE_ERR_NOMEM;
+  /* the sequence of every requested row (-1: none); validate those sequences */
+  for (int64_t i = 0; i < count; ++i) {
+    int r = pairs ? pairs[2 * i] : (int)(i / H);
+    int h = pairs ? pairs[2 * i + 1] : (int)(i % H);
+    if (r < 0 || r >= total_q || h < 0 || h >= H) {
+      free(owner);
+      return ORACLE_ERR_RANGE;
+    }
+    owner[i] = -1;
+    for (int b = 0; b < B; ++b)
+      if (cu_q[b] <= r && r < cu_q[b + 1]) owner[i] = b;
+    if (owner[i] >= 0) {
+      rc = check_sequence(&s, block_table, cache_seqlens, owner[i]);
+      if (rc) {
+        free(owner);
+        return rc;
+      }
+    }
+  }
+  int maxlen = 0;
+  for (int b = 0; b < B; ++b)
+    if (cache_seqlens[b] > maxlen) maxlen = cache_seqlens[b];
+  int failed = 0;
+#ifdef _OPENMP
+  if (n_threads <= 0) n_threads = omp_get_max_threads();
+#pragma omp parallel num_threads(n_threads)
+#endif
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+    if (!scores) {
+      failed = 1;
+    } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+      for (int64_t i = 0; i < count; ++i) {
+        int r = pairs ? pairs[2 * i] : (int)(i / H);
+        int h = pairs ? pairs[2 * i + 1] : (int)(i % H);
+        int b = owner[i];
+        int visible = 0;
+        if (b >= 0) {
+          int k_len = cache_seqlens[b];
+          int n_q = cu_q[b + 1] - cu_q[b];
+          int qi = r - cu_q[b];
+          visible = k_len;
+          if (causal) {
+            int64_t lim = (int64_t)k_len - n_q + qi + 1;
+            visible = lim < 0 ? 0 : (lim > k_len ? k_len : (int)lim);
+          }
+        }
+        attend_one(&s, q + ((int64_t)r * H + h) * d, k_cache, v_cache, block_table,
+                   b < 0 ? 0 : b, h, 0, visible, scale, scores, out + i * d);
+      }
+      free(scores);
+    }
+  }
+  (void)n_threads;
+  free(owner);
   return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
 

@@ -411,3 +411,123 @@ def test_pairs_subset_matches_full_output():
                         "bf16", pairs=pairs)
     for i, (b, h) in enumerate(pairs):
         assert np.array_equal(sub[i], full[b, h])
+
+
+# ------------------------------------------- several query tokens per sequence
+
+VARLEN = os.path.join(os.path.dirname(__file__), "golden", "hf_varlen_example.json")
+
+
+def varlen_example(dtype):
+    g = json.load(open(VARLEN))["facts_from_the_page"]
+    H, Hkv, d, bs = 4, 2, 64, 16
+    cu_q = np.array(g["cu_seq_lens_q"], np.int32)
+    cu_k = np.array(g["cu_seq_lens_k"], np.int32)
+    lens = np.diff(cu_k).astype(np.int32)
+    table = np.array([[-1], [1], [2]], np.int32)
+    P = 3
+    k = np.zeros((P, bs, Hkv, d), np.uint16)  # +0.0
+    vals = np.zeros((P, bs, Hkv, d), np.float32)
+    sign = np.where(np.arange(d) % 2 == 0, 1.0, -1.0)
+    for kidx, req in enumerate(g["k_request_index"]):
+        t = kidx - cu_k[req]                      # position inside its request
+        blk = table[req, t // bs]
+        for j in range(Hkv):
+            vals[blk, t % bs, j] = sign * (kidx + 1) * 2.0 ** j
+    v = wl.to_bits(vals, dtype)
+    rng = np.random.default_rng(5)
+    q = wl.to_bits(rng.standard_normal((int(cu_q[-1]), H, d)).astype(np.float32), dtype)
+    return g, q, cu_q, k, v, table, lens, H, Hkv, d
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_example_assigns_rows_to_the_pages_requests(dtype, causal):
+    g, q, cu_q, k, v, table, lens, H, Hkv, d = varlen_example(dtype)
+    gold = json.load(open(VARLEN))
+    assert q.shape[0] == g["q_shape_tokens"] and int(lens.sum()) == g["k_shape_tokens"]
+    out = oracle.decode_multi(q, cu_q, causal, k, v, table, lens, 0.125, dtype)
+    want = gold["expected_tag_per_row_causal" if causal else "expected_tag_per_row_noncausal"]
+    G = H // Hkv
+    sign = np.where(np.arange(d) % 2 == 0, 1.0, -1.0)
+    for r in range(q.shape[0]):
+        for h in range(H):
+            np.testing.assert_allclose(out[r, h], sign * want[r] * 2.0 ** (h // G), rtol=1e-12,
+                                       atol=0)
+    if not causal:
+        # the row -> request map the page draws, read back from the tags
+        tag_of_request = {0: 0, 1: 1, 2: 5}
+        got = [next(b for b, t in tag_of_request.items() if t == want[r]) for r in range(14)]
+        assert got == g["q_request_index"]
+
+
+def packed_queries(rng, lens_q, H, d, dtype):
+    cu = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    q = wl.to_bits(rng.standard_normal((int(cu[-1]), H, d)).astype(np.float32), dtype)
+    return cu, q
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,Hkv,d", [(8, 2, 64), (6, 3, 128), (8, 1, 64)])
+def test_multi_matches_torch_sdpa_with_an_explicit_mask(causal, H, Hkv, d):
+    rng = np.random.default_rng(H * 10 + d + causal)
+    bs, dtype = 16, "bf16"
+    lens_k = [37, 5, 64, 1]
+    lens_q = [4, 5, 3, 2]       # sequence 1 and 3 have more queries than the
+    w = contiguous_workload(lens_k, H, Hkv, d, bs, dtype, seed=7)  # early ones can see
+    cu, q = packed_queries(rng, lens_q, H, d, dtype)
+    out = oracle.decode_multi(q, cu, causal, w.k_cache, w.v_cache, w.block_table,
+                              w.cache_seqlens, w.scale, dtype)
+    G = H // Hkv
+    qf = torch.from_numpy(wl.from_bits(q, dtype)).double()
+    for b, (nk, nq) in enumerate(zip(lens_k, lens_q)):
+        kf = torch.from_numpy(wl.from_bits(
+            w.k_cache[w.block_table[b]].reshape(-1, Hkv, d)[:nk], dtype)).double()
+        vf = torch.from_numpy(wl.from_bits(
+            w.v_cache[w.block_table[b]].reshape(-1, Hkv, d)[:nk], dtype)).double()
+        qq = qf[cu[b]:cu[b + 1]].permute(1, 0, 2)              # [H, nq, d]
+        kk = kf.permute(1, 0, 2).repeat_interleave(G, dim=0)   # [H, nk, d]
+        vv = vf.permute(1, 0, 2).repeat_interleave(G, dim=0)
+        i = torch.arange(nq)[:, None]
+        t = torch.arange(nk)[None, :]
+        mask = (t < nk - nq + i + 1) if causal else torch.ones(nq, nk, dtype=torch.bool)
+        seen = mask.any(dim=1)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qq[:, seen], kk, vv, attn_mask=mask[seen], scale=w.scale)
+        got = torch.from_numpy(out[cu[b]:cu[b + 1]]).permute(1, 0, 2)
+        np.testing.assert_allclose(got[:, seen].numpy(), ref.numpy(), rtol=1e-10, atol=1e-12)
+        assert (got[:, ~seen] == 0).all()  # queries that see no key give 0
+
+
+def test_causal_query_equals_a_single_token_decode_on_the_prefix():
+    # query i of n_q attends to exactly the first k_len - n_q + i + 1 tokens
+    rng = np.random.default_rng(17)
+    w = wl.random_workload([70, 33], H=8, Hkv=2, d=64, bs=16, dtype="f16", seed=9)
+    lens_q = [6, 4]
+    cu, q = packed_queries(rng, lens_q, w.H, w.d, "f16")
+    out = oracle.decode_multi(q, cu, True, w.k_cache, w.v_cache, w.block_table,
+                              w.cache_seqlens, w.scale, "f16")
+    for b in range(2):
+        for i in range(lens_q[b]):
+            r = cu[b] + i
+            n = int(w.cache_seqlens[b]) - lens_q[b] + i + 1
+            one = oracle.decode(q[r][None], w.k_cache, w.v_cache, w.block_table[[b]],
+                                np.array([n], np.int32), w.scale, "f16")
+            np.testing.assert_array_equal(out[r], one[0])
+
+
+def test_multi_rejects_bad_cumulative_lengths_and_rows_outside_sequences_are_zero():
+    w = wl.random_workload([20, 9], H=4, Hkv=2, d=64, bs=16, dtype="f16", seed=3)
+    rng = np.random.default_rng(1)
+    q = wl.to_bits(rng.standard_normal((6, 4, 64)).astype(np.float32), "f16")
+    for bad in ([0, 3, 2], [0, 3, 7], [-1, 2, 4]):
+        with pytest.raises(oracle.OracleError):
+            oracle.decode_multi(q, bad, True, w.k_cache, w.v_cache, w.block_table,
+                                w.cache_seqlens, w.scale, "f16")
+    out = oracle.decode_multi(q, [1, 3, 4], False, w.k_cache, w.v_cache, w.block_table,
+                              w.cache_seqlens, w.scale, "f16")
+    assert (out[0] == 0).all() and (out[4:] == 0).all() and (out[1:4] != 0).any()
+    pairs = np.array([[2, 3], [4, 0], [1, 1]], np.int32)
+    sub = oracle.decode_multi(q, [1, 3, 4], False, w.k_cache, w.v_cache, w.block_table,
+                              w.cache_seqlens, w.scale, "f16", pairs=pairs)
+    np.testing.assert_array_equal(sub, out[pairs[:, 0], pairs[:, 1]])
