@@ -190,22 +190,56 @@ def make_room_for_next_token(w):
         w.num_blocks += extra
 
 
-def make_workload(name):
+def make_workload(name, query_tokens=0):
+    """The named workload; query_tokens > 0 gives every sequence that many
+    query tokens (its last positions, causal)."""
     from paged_gqa_decode_pa_gb300 import workloads as wl
 
-    return wl.make(name)
+    w = wl.make(name)
+    if query_tokens > 0:
+        w = wl.with_query_tokens(w, np.full(w.B, query_tokens), seed=w.seed + 2000,
+                                 name=f"{w.name}+q{query_tokens}")
+    return w
+
+
+def query_rows(w) -> int:
+    """Output rows of a step: B, or the packed query rows."""
+    return w.B if w.cu_q is None else int(w.q.shape[0])
+
+
+def row_sequences(w) -> np.ndarray:
+    """The sequence each output row belongs to (-1: none)."""
+    if w.cu_q is None:
+        return np.arange(w.B)
+    seq = np.full(query_rows(w), -1, dtype=np.int64)
+    for b in range(w.B):
+        seq[w.cu_q[b]:w.cu_q[b + 1]] = b
+    return seq
+
+
+def oracle_outputs(w, pairs):
+    """The oracle's outputs for (row, head) pairs of the workload."""
+    import oracle
+
+    if w.cu_q is None:
+        return oracle.decode(w.q, w.k_cache, w.v_cache, w.block_table, w.cache_seqlens,
+                             w.scale, w.dtype, pairs=pairs)
+    return oracle.decode_multi(w.q, w.cu_q, w.causal, w.k_cache, w.v_cache, w.block_table,
+                               w.cache_seqlens, w.scale, w.dtype, pairs=pairs)
 
 
 def metric_bytes_of_pairs(w, pairs) -> float:
     """The share of the step's metric bytes (unique K/V bytes) that the
-    (b, h) outputs in `pairs` account for: output (b, h) owns 1/G of its
-    sequence's K/V rows of kv head h // G, scaled so that all B * H outputs
-    add up to exactly the step's unique K/V bytes (shared prefix blocks
-    counted once)."""
-    lens = w.cache_seqlens.astype(np.int64)
-    per_pair = lens * w.d * 4 / w.G                     # bytes per output, no sharing
-    total = float(per_pair.sum()) * w.H                  # all outputs
-    return float(per_pair[pairs[:, 0]].sum()) * (w.kv_bytes() / total) if total else 0.0
+    outputs in `pairs` account for: the H * n_q outputs of a sequence with
+    n_q query rows share its K/V rows (output (row, h) owns 1/(G n_q) of kv
+    head h // G), scaled so that all outputs add up to exactly the step's
+    unique K/V bytes (shared prefix blocks counted once)."""
+    seq = row_sequences(w)
+    nq = np.ones(w.B) if w.cu_q is None else np.maximum(np.diff(w.cu_q), 1)
+    lens = w.cache_seqlens.astype(np.float64)
+    per_row = np.where(seq >= 0, lens[seq] * w.d * 4 / w.G / nq[seq], 0.0)
+    total = float(per_row.sum()) * w.H
+    return float(per_row[pairs[:, 0]].sum()) * (w.kv_bytes() / total) if total else 0.0
 
 
 def oracle_sample(w, budget_s: float, seed: int = 0):
@@ -218,13 +252,12 @@ def oracle_sample(w, budget_s: float, seed: int = 0):
     oracle.build()
     threads = oracle.max_threads()
     rng = np.random.default_rng(seed)
-    order = rng.permutation(w.B * w.H)
+    order = rng.permutation(query_rows(w) * w.H)
     pairs_all = np.stack([order // w.H, order % w.H], axis=1).astype(np.int32)
 
     def run(pairs):
         t = time.perf_counter()
-        oracle.decode(w.q, w.k_cache, w.v_cache, w.block_table, w.cache_seqlens, w.scale,
-                      w.dtype, pairs=pairs)
+        oracle_outputs(w, pairs)
         return time.perf_counter() - t
 
     # calibrate on a few outputs, then size the sample for the budget
@@ -248,22 +281,18 @@ def run_reference(args, rank, world):
     """The oracle timed on the host cores (rank 0 only)."""
     if rank != 0:
         return
-    w = make_workload(args.config)
+    w = make_workload(args.config, args.query_tokens)
     per_step = max(0.05, min(1.0, 90.0 / max(1, args.steps + args.warmup)))
     gbs, dt, pairs, threads, _ = oracle_sample(w, per_step)
-    import oracle
-
     for _ in range(args.warmup):
-        oracle.decode(w.q, w.k_cache, w.v_cache, w.block_table, w.cache_seqlens, w.scale,
-                      w.dtype, pairs=pairs)
+        oracle_outputs(w, pairs)
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle.decode(w.q, w.k_cache, w.v_cache, w.block_table, w.cache_seqlens, w.scale,
-                      w.dtype, pairs=pairs)
+        oracle_outputs(w, pairs)
     el = time.perf_counter() - t
-    toks = int(w.cache_seqlens[pairs[:, 0]].astype(np.int64).sum())
+    toks = int(w.cache_seqlens[row_sequences(w)[pairs[:, 0]]].astype(np.int64).sum())
     value = metric_bytes_of_pairs(w, pairs) * args.steps / el / 1e9
-    sample = (f"{len(pairs)} of {w.B * w.H} (sequence, query head) outputs per step, "
+    sample = (f"{len(pairs)} of {query_rows(w) * w.H} (query row, head) outputs per step, "
               f"{toks} cached tokens")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
@@ -288,6 +317,7 @@ def workload_config(w, args):
             "partition_tokens": args.partition_tokens, "compute": args.compute,
             "stages": args.stages, "graph": bool(args.graph),
             "fused_append": bool(args.fused_append),
+            "query_tokens": query_rows(w), "causal": bool(w.causal) if w.cu_q is not None else None,
             "kv_bytes_per_step": w.kv_bytes(),
             "l2": ("inputs larger than L2" if w.kv_bytes() > 2 * L2_BYTES
                    else "L2 flushed between timed steps"),
@@ -301,16 +331,36 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = make_workload(args.config)
+    w = make_workload(args.config, args.query_tokens)
     if args.fused_append:
         make_room_for_next_token(w)
     q, k, v, t, sl = w.torch_tensors(dev)
-    out = torch.empty((w.B, w.H, w.d), dtype=torch.float32, device=dev)
-    opts = pg.options(partition_tokens=args.partition_tokens, compute=args.compute,
-                      stages=args.stages)
-    shape = pg.shape_of(q, k, t)
-    ws = pg.alloc_workspace(shape, opts, dev)
+    multi = w.cu_q is not None
+    if multi and args.fused_append:
+        raise SystemExit("--fused-append is a one-token-per-sequence step")
+    out = torch.empty(tuple(q.shape), dtype=torch.float32, device=dev)
+    opt_kw = dict(partition_tokens=args.partition_tokens, compute=args.compute,
+                  stages=args.stages)
+    opts = pg.options(**opt_kw)
+    opts_split = pg.options(**opt_kw, phase=pg.PA_PHASE_SPLIT)
+    opts_merge = pg.options(**opt_kw, phase=pg.PA_PHASE_MERGE)
+    if multi:
+        cu = torch.from_numpy(w.cu_q).to(dev)
+        shape = pg.shape_multi(q, k, t)
+        ws = pg.alloc_workspace_multi(shape, w.max_q, opts, dev)
+    else:
+        cu = None
+        shape = pg.shape_of(q, k, t)
+        ws = pg.alloc_workspace(shape, opts, dev)
     stream = torch.cuda.current_stream(dev)
+
+    def attend(o):
+        """One step of the path through the C ABI (o selects the phases)."""
+        if multi:
+            pg.pa_decode_multi(q, cu, w.max_q, w.causal, k, v, t, sl, w.scale, out, ws, o)
+        else:
+            pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, o)
+
     kv_bytes = w.kv_bytes()
     flush = kv_bytes <= 2 * L2_BYTES
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
@@ -318,9 +368,9 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.warmup):
         if flush:
             scratch.fill_(1.0)
-        pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
-    pg.pa_decode_split(q, k, v, t, sl, w.scale, out, ws, opts)
-    pg.pa_decode_merge(q, k, v, t, sl, w.scale, out, ws, opts)
+        attend(opts)
+    attend(opts_split)
+    attend(opts_merge)
     torch.cuda.synchronize()
     if pg.pa_read_status(ws) != 0:
         raise RuntimeError("device status bits set during warm-up")
@@ -343,7 +393,7 @@ def run_ours(args, rank, world, local_rank):
             pg.pa_decode_append(q, kn, vn, k, v, t, sl, w.scale, out, ws, opts)
     else:
         def decode_step():
-            pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+            attend(opts)
 
     graph = None
     if args.graph:
@@ -395,9 +445,9 @@ def run_ours(args, rank, world, local_rank):
         if flush:
             scratch.fill_(1.0)
         ev3[i][0].record(stream)
-        pg.pa_decode_split(q, k, v, t, sl, w.scale, out, ws, opts)
+        attend(opts_split)
         ev3[i][1].record(stream)
-        pg.pa_decode_merge(q, k, v, t, sl, w.scale, out, ws, opts)
+        attend(opts_merge)
         ev3[i][2].record(stream)
     torch.cuda.synchronize()
     split_ms = [ev3[i][0].elapsed_time(ev3[i][1]) for i in range(K)]
@@ -411,11 +461,13 @@ def run_ours(args, rank, world, local_rank):
     t_h = t.cpu().pin_memory()
     sl_h = sl.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = q_h.numel() * q_h.element_size() + t_h.numel() * 4 + sl_h.numel() * 4
+    cu_h = cu.cpu().pin_memory() if multi else None
+    h2d = (q_h.numel() * q_h.element_size() + t_h.numel() * 4 + sl_h.numel() * 4
+           + (cu_h.numel() * 4 if multi else 0))
     d2h = out_h.numel() * 4
     for _ in range(2):
         q.copy_(q_h, non_blocking=True)
-        pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+        attend(opts)
         out_h.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -428,7 +480,9 @@ def run_ours(args, rank, world, local_rank):
         q.copy_(q_h, non_blocking=True)
         t.copy_(t_h, non_blocking=True)
         sl.copy_(sl_h, non_blocking=True)
-        pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, opts)
+        if multi:
+            cu.copy_(cu_h, non_blocking=True)
+        attend(opts)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
     e1.record(stream)
@@ -450,18 +504,16 @@ def run_ours(args, rank, world, local_rank):
     cpu = None
     parity = None
     if args.cpu_baseline_s > 0 and world == 1:
-        import oracle
-
         gbs, dt, pairs, threads, passes = oracle_sample(w, args.cpu_baseline_s)
-        toks = int(w.cache_seqlens[pairs[:, 0]].astype(np.int64).sum())
+        toks = int(w.cache_seqlens[row_sequences(w)[pairs[:, 0]]].astype(np.int64).sum())
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{len(pairs)} of {w.B * w.H} (sequence, query head) outputs, "
+               "sample": f"{len(pairs)} of {query_rows(w) * w.H} (query row, head) outputs, "
                          f"{toks} cached tokens, {passes} pass(es), {dt:.1f} s; GB/s counts "
-                         f"each output's 1/G share of the step's unique K/V bytes"}
+                         f"each output's share (1/G of its kv head, split over its "
+                         f"sequence's query rows) of the step's unique K/V bytes"}
         # the timed kernels' last output against the oracle on that sample
         chk = pairs[:256]
-        ref = oracle.decode(w.q, w.k_cache, w.v_cache, w.block_table, w.cache_seqlens, w.scale,
-                            w.dtype, pairs=chk)
+        ref = oracle_outputs(w, chk)
         got = out.cpu().numpy().astype(np.float64)[chk[:, 0], chk[:, 1]]
         err = np.abs(got - ref)
         parity = {"pairs": int(len(chk)), "max_abs_err": float(err.max()),
@@ -470,7 +522,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "us_per_step": round(ms_per_step * 1e3, 2),
-        "tokens_per_s": round(world * w.B / (ms_per_step * 1e-3), 1),
+        "tokens_per_s": round(world * int(q.shape[0]) / (ms_per_step * 1e-3), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic", "config": workload_config(w, args),
         "gpu_launches": 2 * K,
@@ -500,6 +552,8 @@ def main():
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--compute", default="mma", choices=["mma", "simt", "auto"])
     ap.add_argument("--stages", type=int, default=0, help="pipeline stages (0 = library choice)")
+    ap.add_argument("--query-tokens", type=int, default=0,
+                    help="query tokens per sequence (0 = the workload's own: one in decode)")
     ap.add_argument("--fused-append", action="store_true",
                     help="time pa_decode_append (write the new token, attend over len+1)")
     ap.add_argument("--graph", action="store_true",

@@ -125,7 +125,16 @@ typedef struct pa_options {
                         pa_workspace_size independent of the device. */
   int32_t stages;    /* TMA ring slots per warp (16-token K/V stages,
                         1..8); 0 = library choice */
+  int32_t phase;     /* pa_decode / pa_decode_append / pa_decode_multi:
+                        PA_PHASE_BOTH (0) runs both kernels; PA_PHASE_SPLIT
+                        only phase 1, PA_PHASE_MERGE only phase 2 (which must
+                        follow phase 1 of the same step on the same stream),
+                        e.g. to time the kernels apart */
 } pa_options;
+
+#define PA_PHASE_BOTH 0
+#define PA_PHASE_SPLIT 1
+#define PA_PHASE_MERGE 2
 
 /* Bytes of workspace pa_decode / pa_decode_split / pa_decode_merge /
  * pa_cache_append need for this shape and these options (NULL = defaults).
@@ -184,6 +193,42 @@ int pa_decode_append(const pa_shape* shape, const pa_options* options, const voi
                      const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                      const int32_t* block_table, const int32_t* cache_seqlens, float scale,
                      float* out, void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* Several query tokens per sequence over the paged cache (chunked decode,
+ * e.g. verifying draft tokens).  Query rows are packed as in the varlen path
+ * of the Hugging Face "Paged attention" page: sequence b owns rows
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q [total_q, H, d] (the page's
+ * cu_seq_lens_q, a DEVICE int32 array [B+1]), and out [total_q, H, d] fp32
+ * gets the same rows.  The keys are the cache_seqlens[b] tokens of the paged
+ * cache (block_table as in pa_decode), the query tokens themselves included:
+ * the n_q query tokens of a sequence are its last n_q key positions, so
+ * query i (0-based within its sequence) sees
+ *   causal != 0:  keys t < clamp(cache_seqlens[b] - n_q + i + 1, 0, cache_seqlens[b])
+ *   causal == 0:  all cache_seqlens[b] keys
+ * and a query that sees no key gets 0.
+ *   max_q:   host bound on n_q (the page's max_length_q), 1..PA_MAX_QUERY_TOKENS;
+ *            it fixes the launch shape, so a captured graph stays valid while
+ *            the lengths change under it.
+ *   total_q: rows of q and out (host); the library reads and writes no row
+ *            at or beyond it.
+ * A sequence whose span is not non-decreasing within [0, total_q], or holds
+ * more than max_q tokens, is skipped (its rows are not written) and sets
+ * PA_STATUS_BAD_SEQLEN; an invalid cache_seqlens[b] makes its rows NaN and
+ * sets the same bit; bad table entries as in pa_decode.  Rows that belong
+ * to no sequence are not written.  The workspace must hold
+ * pa_workspace_size_multi(shape, options, max_q) bytes (zero-filled once, as
+ * for pa_decode).  Tensor-core path only (options->compute SIMT is
+ * PA_ERR_OPTION).  Up to 16 (token, head) pairs of one kv head share one pass
+ * over its K/V (8 at d = 256): a sequence with n_q * G above that is read
+ * ceil(n_q * G / 16) times. */
+#define PA_MAX_QUERY_TOKENS 4096
+int pa_workspace_size_multi(const pa_shape* shape, const pa_options* options, int32_t max_q,
+                            size_t* bytes);
+int pa_decode_multi(const pa_shape* shape, const pa_options* options, const void* q,
+                    const int32_t* cu_seqlens_q, int32_t total_q, int32_t max_q, int32_t causal,
+                    const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    const int32_t* cache_seqlens, float scale, float* out, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream);
 
 /* Append one new token per sequence to the paged cache, in place: for every
  * b and kv head j, k_new[b,j,:] and v_new[b,j,:] are copied bit for bit to

@@ -27,6 +27,8 @@ PA_ERR_SCRATCH_LIMIT = -7
 PA_ERR_STATE = -8
 PA_ERR_NO_BLOCKS = -9
 
+PA_MAX_QUERY_TOKENS = 4096
+
 PA_BM_FREE_BLOCKS = 0
 PA_BM_REF_COUNT = 1
 PA_BM_SEQ_BLOCKS = 2
@@ -50,7 +52,8 @@ EXPORTS = ("pa_workspace_size", "pa_decode", "pa_decode_split", "pa_decode_merge
            "pa_plan_merge", "pa_version", "pa_decode_noalloc", "pa_decode_append",
            "pa_bm_create", "pa_bm_destroy", "pa_bm_allocate", "pa_bm_free_sequence",
            "pa_bm_share_prefix", "pa_bm_copy_on_write", "pa_bm_reserve_slot",
-           "pa_bm_block_table", "pa_bm_query", "pa_copy_blocks")
+           "pa_bm_block_table", "pa_bm_query", "pa_copy_blocks", "pa_decode_multi",
+           "pa_workspace_size_multi")
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -70,15 +73,21 @@ class pa_shape(ctypes.Structure):
                 ("num_blocks", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
+PA_PHASE_BOTH = 0
+PA_PHASE_SPLIT = 1
+PA_PHASE_MERGE = 2
+
+
 class pa_options(ctypes.Structure):
     _fields_ = [("partition_tokens", ctypes.c_int32), ("compute", ctypes.c_int32),
-                ("num_ctas", ctypes.c_int32), ("stages", ctypes.c_int32)]
+                ("num_ctas", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("phase", ctypes.c_int32)]
 
 
 def options(partition_tokens: int = 0, compute: str = "auto", num_ctas: int = 0,
-            stages: int = 0) -> pa_options:
+            stages: int = 0, phase: int = PA_PHASE_BOTH) -> pa_options:
     return pa_options(int(partition_tokens), _COMPUTE[compute] if isinstance(compute, str)
-                      else int(compute), int(num_ctas), int(stages))
+                      else int(compute), int(num_ctas), int(stages), int(phase))
 
 
 _lib = None
@@ -140,6 +149,11 @@ def lib():
             getattr(L, name).restype = ctypes.c_int
         L.pa_copy_blocks.argtypes = [SP, P, P, P, i32, P, P]
         L.pa_copy_blocks.restype = ctypes.c_int
+        L.pa_workspace_size_multi.argtypes = [SP, OP, i32, ctypes.POINTER(ctypes.c_size_t)]
+        L.pa_workspace_size_multi.restype = ctypes.c_int
+        L.pa_decode_multi.argtypes = [SP, OP, P, P, i32, i32, i32, P, P, P, P, ctypes.c_float, P,
+                                      P, ctypes.c_size_t, P]
+        L.pa_decode_multi.restype = ctypes.c_int
         L.pa_version.argtypes = []
         L.pa_version.restype = ctypes.c_int
         _lib = L
@@ -207,7 +221,7 @@ def _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out):
     if block_table.dtype != torch.int32 or cache_seqlens.dtype != torch.int32:
         raise TypeError("block_table and cache_seqlens must be int32")
     if out is not None and (out.dtype != torch.float32 or tuple(out.shape) != tuple(q.shape)):
-        raise TypeError("out must be float32 with q's shape [B, H, d]")
+        raise TypeError("out must be float32 with q's shape")
 
 
 def pa_workspace_size(shape: pa_shape, opts: Optional[pa_options] = None) -> int:
@@ -224,6 +238,57 @@ def alloc_workspace(shape: pa_shape, opts: Optional[pa_options] = None, device=N
 
     return torch.zeros(pa_workspace_size(shape, opts), dtype=torch.uint8,
                        device=device if device is not None else "cuda")
+
+
+def shape_multi(q, k_cache, block_table) -> pa_shape:
+    """pa_shape of a call with several query tokens per sequence: q is the
+    packed [total_q, H, d]; B is the number of block-table rows."""
+    _, H, d = q.shape
+    P, bs, Hkv, d2 = k_cache.shape
+    if d2 != d:
+        raise ValueError("inconsistent q / k_cache shapes")
+    return pa_shape(block_table.shape[0], H, Hkv, d, bs, block_table.shape[1], P, _dtype_code(q))
+
+
+def pa_workspace_size_multi(shape: pa_shape, max_q: int,
+                            opts: Optional[pa_options] = None) -> int:
+    n = ctypes.c_size_t(0)
+    rc = lib().pa_workspace_size_multi(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                                       int(max_q), ctypes.byref(n))
+    _check(rc, "pa_workspace_size_multi")
+    return int(n.value)
+
+
+def alloc_workspace_multi(shape: pa_shape, max_q: int, opts: Optional[pa_options] = None,
+                          device=None):
+    """Zero-filled device workspace for pa_decode_multi (torch uint8)."""
+    import torch
+
+    return torch.zeros(pa_workspace_size_multi(shape, max_q, opts), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def pa_decode_multi(q, cu_seqlens_q, max_q, causal, k_cache, v_cache, block_table,
+                    cache_seqlens, scale, out, workspace, opts: Optional[pa_options] = None,
+                    stream=None) -> None:
+    """out[total_q,H,d] (fp32) = attention of the packed query rows q
+    [total_q,H,d]; sequence b owns rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+    (see include/pagedgqa.h)."""
+    import torch
+
+    _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out)
+    if not cu_seqlens_q.is_cuda or cu_seqlens_q.dtype != torch.int32:
+        raise TypeError("cu_seqlens_q must be an int32 CUDA tensor")
+    if tuple(cu_seqlens_q.shape) != (block_table.shape[0] + 1,):
+        raise ValueError("cu_seqlens_q must be [B + 1]")
+    shape = shape_multi(q, k_cache, block_table)
+    rc = lib().pa_decode_multi(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                               _ptr(q), _ptr(cu_seqlens_q), int(q.shape[0]), int(max_q),
+                               int(bool(causal)), _ptr(k_cache), _ptr(v_cache),
+                               _ptr(block_table), _ptr(cache_seqlens), float(scale), _ptr(out),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream))
+    _check(rc, "pa_decode_multi")
 
 
 def _decode_call(name, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,

@@ -33,7 +33,7 @@ namespace {
 // then warp w accumulates pieces w, w+4, ... of the batch, lanes over the 64
 // dims as float2, with 8 pieces' loads issued before they are used.
 __device__ __forceinline__ void merge_segment_chunk(const MergeArgs& a, const MergeSeg& ms, int g,
-                                                    int c) {
+                                                    int c, int64_t out_row) {
   constexpr int NW = kMergeThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   __shared__ float red[NW];
@@ -41,7 +41,7 @@ __device__ __forceinline__ void merge_segment_chunk(const MergeArgs& a, const Me
   __shared__ float2 wacc[NW][32];
   // pass 1: M = max_p m_p
   float m = -INFINITY;
-  for (int p = tid; p < ms.np; p += kMergeThreads) m = fmaxf(m, a.ws_ml[(ms.slot(p) * a.G + g) * 2]);
+  for (int p = tid; p < ms.np; p += kMergeThreads) m = fmaxf(m, a.ws_ml[(ms.slot(p) * a.C + g) * 2]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if (lane == 0) red[w] = m;
@@ -58,8 +58,8 @@ __device__ __forceinline__ void merge_segment_chunk(const MergeArgs& a, const Me
     int64_t s_lane = 0;
     if (lane < nb) {
       s_lane = ms.slot(p0 + lane);
-      const float mp = a.ws_ml[(s_lane * a.G + g) * 2];
-      const float lp = a.ws_ml[(s_lane * a.G + g) * 2 + 1];
+      const float mp = a.ws_ml[(s_lane * a.C + g) * 2];
+      const float lp = a.ws_ml[(s_lane * a.C + g) * 2 + 1];
       e_lane = ex2(mp - M);
       if (w == 0) l = fmaf(e_lane, lp, l);  // each piece's l counted once
     }
@@ -72,7 +72,7 @@ __device__ __forceinline__ void merge_segment_chunk(const MergeArgs& a, const Me
         const int kk = k < nb ? k : 0;
         const int64_t s = __shfl_sync(0xffffffffu, s_lane, kk);
         e[u] = __shfl_sync(0xffffffffu, e_lane, kk);
-        x[u] = k < nb ? *reinterpret_cast<const float2*>(a.ws_acc + (s * a.G + g) * a.D + c * 64 + 2 * lane)
+        x[u] = k < nb ? *reinterpret_cast<const float2*>(a.ws_acc + (s * a.C + g) * a.D + c * 64 + 2 * lane)
                       : make_float2(0.f, 0.f);
         if (k >= nb) e[u] = 0.f;
       }
@@ -99,8 +99,9 @@ __device__ __forceinline__ void merge_segment_chunk(const MergeArgs& a, const Me
       o.x += wacc[v][lane].x;
       o.y += wacc[v][lane].y;
     }
-    float* dst = a.out + ((int64_t)ms.b * a.H + (int64_t)ms.j * a.G + g) * a.D + c * 64 + 2 * lane;
-    *reinterpret_cast<float2*>(dst) = make_float2(o.x / L, o.y / L);
+    float* dst = a.out + out_row * a.D + c * 64 + 2 * lane;
+    // a column that saw no key (causal limit 0) gets 0; NaN passes through
+    *reinterpret_cast<float2*>(dst) = L == 0.f ? make_float2(0.f, 0.f) : make_float2(o.x / L, o.y / L);
   }
 }
 
@@ -114,9 +115,20 @@ __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs
   if (a.part_blocks == 0) desc = a.ws_desc[seg];
   const MergeSeg ms = merge_segment(sched, seg, desc.x, desc.y, desc.z, desc.w, a.ws_pre);
   if (ms.np == 0) return;
+  // the output row of column g: head j*G + g of sequence b (decode), or
+  // token grp*tq + g/G, head j*G + g%G of the row's sequence
+  int64_t out_row = (int64_t)ms.b * a.H + (int64_t)ms.j * a.G + g;
+  if (a.cu_q) {
+    const int seq = ms.b / a.nqg, grp = ms.b - seq * a.nqg;
+    int32_t q0, nq;
+    query_span(a.cu_q, seq, a.total_q, a.max_q, q0, nq);
+    const int tok = grp * a.tq + g / a.G;
+    if (tok >= nq) return;  // the column holds no query (uniform over the block)
+    out_row = (int64_t)(q0 + tok) * a.H + (int64_t)ms.j * a.G + g % a.G;
+  }
   // gridDim.z == D/64: one chunk per block; gridDim.z == 1: all chunks here
   for (int cc = c; cc < a.D / 64; cc += gridDim.z) {
-    merge_segment_chunk(a, ms, g, cc);
+    merge_segment_chunk(a, ms, g, cc, out_row);
     __syncthreads();  // shared scratch reuse
   }
 }
@@ -198,11 +210,15 @@ int check_options(const pa_shape* s, const pa_options* o) {
   if (o->compute < PA_COMPUTE_AUTO || o->compute > PA_COMPUTE_MMA) return PA_ERR_OPTION;
   if (o->num_ctas < 0 || o->num_ctas > (1 << 20)) return PA_ERR_OPTION;
   if (o->stages < 0 || o->stages > kMaxSlots / kMaxWarps) return PA_ERR_OPTION;
+  if (o->phase < PA_PHASE_BOTH || o->phase > PA_PHASE_MERGE) return PA_ERR_OPTION;
   return PA_OK;
 }
 
 struct Plan {
   int D, G, bs, mode, warps, ring;
+  int C;              // query columns per row (G in decode)
+  int rows;           // rows of the schedule (B in decode, B * nqg with several tokens)
+  int nqg, tq;        // several query tokens: groups per sequence, tokens per group
   int part_blocks;
   int grid;  // split kernel CTAs
   size_t smem;
@@ -220,9 +236,8 @@ int choose_mode(const pa_options* o) {
 // Ring slots per warp: 2 by default (measured best for every head dimension:
 // one tile computing, one in flight), fewer when shared memory does not hold
 // them; at most what fits in the per-block limit.
-int choose_ring(const pa_shape* s, const pa_options* o, int mode, int W) {
-  const int G = s->num_heads / s->num_kv_heads;
-  const SmemLayout L0 = split_smem_layout(s->head_dim, G, s->batch, W, 0, mode);
+int choose_ring(const pa_shape* s, const pa_options* o, int mode, int W, int C, int rows) {
+  const SmemLayout L0 = split_smem_layout(s->head_dim, C, rows, W, 0, mode);
   int fit = (kMaxDynamicSmem - (int)L0.total) / (W * (int)L0.stage_bytes);
   if (fit > kMaxSlots / W) fit = kMaxSlots / W;
   if (o && o->stages > 0) return o->stages <= fit ? o->stages : -1;
@@ -233,7 +248,8 @@ int choose_ring(const pa_shape* s, const pa_options* o, int mode, int W) {
 const void* kernel_for(int dtype, int D, int mode) {
 #define PA_PICK(T, DD)                                                                 \
   if (D == DD) return mode == kSimt ? split_kernel_ptr<T, DD, kSimt>()                \
-                                    : split_kernel_ptr<T, DD, kMma>();
+                      : mode == kMmaQ ? split_kernel_ptr<T, DD, kMmaQ>()              \
+                                      : split_kernel_ptr<T, DD, kMma>();
   if (dtype == PA_BF16) {
     PA_PICK(__nv_bfloat16, 64)
     PA_PICK(__nv_bfloat16, 128)
@@ -291,7 +307,8 @@ int device_sms(int* dev_out, int* sms_out) {
 
 // Sizes and offsets of everything one call needs.  `need_device` = false
 // only when options->num_ctas fixes the grid (pure host computation).
-int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p) {
+// max_q > 0: several query tokens per sequence, at most max_q each.
+int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p, int max_q = 0) {
   int rc = check_shape(s);
   if (rc) return rc;
   rc = check_options(s, o);
@@ -301,10 +318,24 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
   p->bs = s->block_size;
   p->mode = choose_mode(o);
   p->warps = split_warps(p->D);
-  p->ring = choose_ring(s, o, p->mode, p->warps);
+  p->C = p->G;
+  p->rows = s->batch;
+  p->nqg = 1;
+  p->tq = 1;
+  if (max_q > 0) {
+    if (max_q > PA_MAX_QUERY_TOKENS) return PA_ERR_SHAPE;
+    if (p->mode == kSimt) return PA_ERR_OPTION;  // tensor-core path only
+    p->mode = kMmaQ;
+    p->tq = 8 * mma_blocks(p->D, kMmaQ) / p->G;
+    p->nqg = (max_q + p->tq - 1) / p->tq;
+    p->C = p->tq * p->G;
+    if ((int64_t)s->batch * p->nqg > PA_MAX_BATCH) return PA_ERR_SHAPE;
+    p->rows = s->batch * p->nqg;
+  }
+  p->ring = choose_ring(s, o, p->mode, p->warps, p->C, p->rows);
   if (p->ring < 1) return (o && o->stages > 0) ? PA_ERR_OPTION : PA_ERR_SHAPE;
   p->part_blocks = (o && o->partition_tokens > 0) ? o->partition_tokens / s->block_size : 0;
-  const SmemLayout L = split_smem_layout(p->D, p->G, s->batch, p->warps, p->ring, p->mode);
+  const SmemLayout L = split_smem_layout(p->D, p->C, p->rows, p->warps, p->ring, p->mode);
   p->smem = L.total;
   if (p->smem > (size_t)kMaxDynamicSmem) return PA_ERR_SHAPE;
   const bool fixed_grid = o && o->num_ctas > 0;
@@ -323,17 +354,17 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
     p->slots = 2 * (int64_t)p->grid;
   } else {
     const int64_t nparts = (s->max_blocks_per_seq + p->part_blocks - 1) / p->part_blocks;
-    p->slots = (int64_t)s->batch * s->num_kv_heads * nparts;
+    p->slots = (int64_t)p->rows * s->num_kv_heads * nparts;
   }
   size_t off = kHeaderBytes;
   p->off_pre = off;
-  off = round256(off + sizeof(int32_t) * (size_t)(s->batch + 1));
+  off = round256(off + sizeof(int32_t) * (size_t)(p->rows + 1));
   p->off_desc = off;
   off = round256(off + sizeof(int4) * (size_t)p->grid);
   p->off_ml = off;
-  off = round256(off + sizeof(float) * 2 * (size_t)p->slots * p->G);
+  off = round256(off + sizeof(float) * 2 * (size_t)p->slots * p->C);
   p->off_acc = off;
-  off = round256(off + sizeof(float) * (size_t)p->slots * p->G * p->D);
+  off = round256(off + sizeof(float) * (size_t)p->slots * p->C * p->D);
   p->total = off;
   return PA_OK;
 }
@@ -379,7 +410,7 @@ struct Call {
 int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k_cache,
             const void* v_cache, const int32_t* block_table, const int32_t* cache_seqlens,
             float scale, float* out, void* workspace, size_t workspace_bytes, bool need_kv,
-            Call* c) {
+            Call* c, int max_q = 0) {
   int rc = check_shape(s);
   if (rc) return rc;
   if (!block_table || !cache_seqlens || !out || !workspace) return PA_ERR_NULL;
@@ -390,12 +421,12 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   if (need_kv && (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)))
     return PA_ERR_ALIGN;
   if (!(scale == scale)) return PA_ERR_SHAPE;  // NaN scale
-  rc = make_plan(s, o, false, &c->plan);
+  rc = make_plan(s, o, false, &c->plan, max_q);
   if (rc) return rc;
   if (workspace_bytes < c->plan.total) return PA_ERR_WORKSPACE;
   if (need_kv) {
     // kernel attributes (dynamic shared memory limit) before the first launch
-    rc = make_plan(s, o, true, &c->plan);
+    rc = make_plan(s, o, true, &c->plan, max_q);
     if (rc) return rc;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -410,7 +441,7 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.ws_pre = reinterpret_cast<int32_t*>(ws + p.off_pre);
   a.ws_desc = reinterpret_cast<int4*>(ws + p.off_desc);
   a.status = reinterpret_cast<uint32_t*>(ws);
-  a.B = s->batch;
+  a.B = p.rows;
   a.H = s->num_heads;
   a.Hkv = s->num_kv_heads;
   a.G = p.G;
@@ -424,6 +455,13 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.len_add = 0;
   a.k_new = a.v_new = nullptr;
   a.k_pool = a.v_pool = nullptr;
+  a.C = p.C;
+  a.cu_q = nullptr;
+  a.nqg = p.nqg;
+  a.tq = p.tq;
+  a.causal = 0;
+  a.total_q = 0;
+  a.max_q = max_q;
   MergeArgs& m = c->ma;
   m.seqlens = cache_seqlens;
   m.out = out;
@@ -440,6 +478,12 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   m.maxblk = a.maxblk;
   m.part_blocks = a.part_blocks;
   m.num_ctas = p.grid;
+  m.C = p.C;
+  m.cu_q = nullptr;
+  m.nqg = p.nqg;
+  m.tq = p.tq;
+  m.total_q = 0;
+  m.max_q = max_q;
   return PA_OK;
 }
 
@@ -491,10 +535,12 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
   if (rc) return rc;
   const Plan& p = c->plan;
   cudaError_t e = cudaErrorInvalidValue;
-#define PA_LAUNCH(T, DD)                                                                      \
-  if (p.D == DD)                                                                              \
-    e = p.mode == kSimt                                                                       \
-            ? launch_split<T, DD, kSimt>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream)   \
+#define PA_LAUNCH(T, DD)                                                                        \
+  if (p.D == DD)                                                                                \
+    e = p.mode == kSimt                                                                         \
+            ? launch_split<T, DD, kSimt>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream)     \
+        : p.mode == kMmaQ                                                                       \
+            ? launch_split<T, DD, kMmaQ>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream)     \
             : launch_split<T, DD, kMma>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream);
   if (s->dtype == PA_BF16) {
     PA_LAUNCH(__nv_bfloat16, 64)
@@ -517,7 +563,7 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   const int nseg = p.part_blocks == 0 ? p.grid : c->sa.B * c->sa.Hkv;
   cudaLaunchConfig_t cfg = {};
   // long heads get one block per 64-dim chunk (few segments, many pieces)
-  cfg.gridDim = dim3(nseg, p.G, p.D == 256 ? p.D / 64 : 1);
+  cfg.gridDim = dim3(nseg, p.C, p.D == 256 ? p.D / 64 : 1);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -528,6 +574,19 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   cfg.numAttrs = overlap ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, pa_merge_kernel, c->ma);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Both phases (the merge as a programmatic dependent of the split), or the
+// one options->phase names.
+int run_phases(const pa_shape* s, const pa_options* o, const void* k_cache, const void* v_cache,
+               Call* c, cudaStream_t st) {
+  const int phase = o ? o->phase : PA_PHASE_BOTH;
+  if (phase != PA_PHASE_MERGE) {
+    const int rc = launch_split_phase(s, k_cache, v_cache, c, st);
+    if (rc) return rc;
+  }
+  if (phase == PA_PHASE_SPLIT) return PA_OK;
+  return launch_merge_phase(c, st, phase == PA_PHASE_BOTH);
 }
 
 }  // namespace
@@ -578,10 +637,7 @@ int pa_decode(const pa_shape* shape, const pa_options* options, const void* q,
   int rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                    workspace, workspace_bytes, true, &c);
   if (rc) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  rc = launch_split_phase(shape, k_cache, v_cache, &c, st);
-  if (rc) return rc;
-  return launch_merge_phase(&c, st, true);
+  return run_phases(shape, options, k_cache, v_cache, &c, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int pa_decode_append(const pa_shape* shape, const pa_options* options, const void* q,
@@ -600,10 +656,40 @@ int pa_decode_append(const pa_shape* shape, const pa_options* options, const voi
   c.sa.v_new = static_cast<const uint16_t*>(v_new);
   c.sa.k_pool = static_cast<uint16_t*>(k_cache);
   c.sa.v_pool = static_cast<uint16_t*>(v_cache);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  rc = launch_split_phase(shape, k_cache, v_cache, &c, st);
+  return run_phases(shape, options, k_cache, v_cache, &c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_workspace_size_multi(const pa_shape* shape, const pa_options* options, int32_t max_q,
+                            size_t* bytes) {
+  if (!shape || !bytes) return PA_ERR_NULL;
+  if (max_q < 1) return PA_ERR_SHAPE;
+  Plan p;
+  int rc = make_plan(shape, options, false, &p, max_q);
   if (rc) return rc;
-  return launch_merge_phase(&c, st, true);
+  *bytes = p.total;
+  return PA_OK;
+}
+
+int pa_decode_multi(const pa_shape* shape, const pa_options* options, const void* q,
+                    const int32_t* cu_seqlens_q, int32_t total_q, int32_t max_q, int32_t causal,
+                    const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    const int32_t* cache_seqlens, float scale, float* out, void* workspace,
+                    size_t workspace_bytes, pa_stream_t stream) {
+  if (max_q < 1 || total_q < 0) return PA_ERR_SHAPE;
+  if (shape && shape->batch == 0 && check_shape(shape) == PA_OK) return PA_OK;
+  if (!cu_seqlens_q) return PA_ERR_NULL;
+  if (!aligned16(cu_seqlens_q)) return PA_ERR_ALIGN;
+  if (total_q == 0) return PA_OK;
+  Call c;
+  int rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                   workspace, workspace_bytes, true, &c, max_q);
+  if (rc) return rc;
+  c.sa.cu_q = cu_seqlens_q;
+  c.sa.causal = causal ? 1 : 0;
+  c.sa.total_q = total_q;
+  c.ma.cu_q = cu_seqlens_q;
+  c.ma.total_q = total_q;
+  return run_phases(shape, options, k_cache, v_cache, &c, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int pa_cache_append(const pa_shape* shape, const void* k_new, const void* v_new, void* k_cache,
@@ -695,7 +781,8 @@ int pa_plan_pieces(const pa_shape* shape, const pa_options* options,
   const SchedShape sched{B, shape->num_kv_heads, shape->block_size, shape->max_blocks_per_seq,
                          part_blocks, num_ctas};
   PieceIter it;
-  it.init(pre, cache_seqlens_host, sched, cta);
+  it.init(pre, HostLens{cache_seqlens_host, 0, shape->block_size, shape->max_blocks_per_seq},
+          sched, cta);
   Piece pc;
   int n = 0;
   while (it.next(pc)) {

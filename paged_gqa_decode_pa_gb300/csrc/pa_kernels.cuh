@@ -18,10 +18,18 @@ constexpr int kMaxWarps = 8;   // warps per split CTA (each runs its own TMA rin
 PA_HD constexpr int split_warps(int D) { return D == 256 ? 4 : kMaxWarps; }
 constexpr int kMaxSlots = 64;  // warps x ring slots
 constexpr int kGMax = 8;       // query heads per kv head handled by one CTA
+constexpr int kColMax = 16;    // query columns (token, head) per row: two mma n-blocks
 constexpr int kTile = 16;      // tokens per pipeline stage (one mma row tile)
 constexpr int kMergeThreads = 128;
 
-enum Mode { kSimt = 1, kMma = 2 };
+// kSimt / kMma: one query token per sequence (decode).  kMmaQ: several query
+// tokens per sequence; a row is a group of one sequence's query tokens whose
+// (token, head) pairs fill up to mma_blocks(D) x 8 columns.
+enum Mode { kSimt = 1, kMma = 2, kMmaQ = 3 };
+
+// mma n-blocks of 8 query columns a warp keeps (registers allow two below
+// d = 256).
+PA_HD constexpr int mma_blocks(int D, int mode) { return (mode == kMmaQ && D <= 128) ? 2 : 1; }
 
 struct SplitArgs {
   const uint16_t* q;        // [B, H, D] raw 16-bit patterns
@@ -45,6 +53,57 @@ struct SplitArgs {
   const uint16_t* v_new;
   uint16_t* k_pool;         // the pools, writable (fused append only)
   uint16_t* v_pool;
+  // columns of one row: G heads in decode; tq tokens x G heads with several
+  // query tokens per sequence
+  int32_t C;
+  // several query tokens per sequence (kMmaQ): B counts rows = sequences x
+  // nqg groups of tq tokens; q and out are packed [total_q, H, D] rows and
+  // sequence s owns rows cu_q[s] .. cu_q[s+1]-1
+  const int32_t* cu_q;
+  int32_t nqg, tq, causal, total_q, max_q;
+};
+
+// Query rows [q0, q0 + nq) of sequence s, or false when cu_q is not a valid
+// span there (then nothing of s is read or written).
+__device__ __forceinline__ bool query_span(const int32_t* cu_q, int32_t s, int32_t total_q,
+                                           int32_t max_q, int32_t& q0, int32_t& nq) {
+  const int32_t a = __ldg(cu_q + s), b = __ldg(cu_q + s + 1);
+  const bool ok = a >= 0 && a <= b && b <= total_q && b - a <= max_q;
+  q0 = ok ? a : 0;
+  nq = ok ? b - a : 0;
+  return ok;
+}
+
+// Decode rows: the stored length (plus the appended token).
+struct DecodeLen {
+  const int32_t* seqlens;
+  int32_t add, bs, maxblk;
+  __device__ __forceinline__ int32_t operator()(int32_t b) const {
+    return eff_len(__ldg(seqlens + b), add, bs, maxblk);
+  }
+};
+
+// Rows of several query tokens: row r = group r % nqg of sequence r / nqg.
+// The group's tokens are the sequence's query tokens [g*tq, g*tq + tq); a
+// query token i of nq sees keys t < k_len - nq + i + 1 (causal) or all k_len
+// keys, so the row reads up to the limit of its last token.  -1: the
+// sequence's key length is invalid; 0: nothing to read.
+struct MultiLen {
+  const int32_t* seqlens;
+  const int32_t* cu_q;
+  int32_t nqg, tq, causal, total_q, max_q, bs, maxblk;
+  __device__ __forceinline__ int32_t operator()(int32_t r) const {
+    const int32_t s = r / nqg, g = r - s * nqg;
+    const int32_t klen = __ldg(seqlens + s);
+    if (!seq_len_valid(klen, bs, maxblk)) return -1;
+    int32_t q0, nq;
+    if (!query_span(cu_q, s, total_q, max_q, q0, nq)) return 0;
+    const int32_t first = g * tq;
+    if (first >= nq) return 0;
+    if (!causal) return klen;
+    const int32_t last = min(nq, first + tq) - 1;
+    return max(0, min(klen, klen - nq + last + 1));
+  }
 };
 
 struct MergeArgs {
@@ -57,6 +116,9 @@ struct MergeArgs {
   int32_t B, H, Hkv, G, D, bs, maxblk;
   int32_t part_blocks;
   int32_t num_ctas;  // grid of the split kernel
+  int32_t C;         // columns per row (G in decode)
+  const int32_t* cu_q;  // non-null: rows of several query tokens (see SplitArgs)
+  int32_t nqg, tq, total_q, max_q;
 };
 
 struct AppendArgs {
@@ -77,7 +139,8 @@ struct SmemLayout {
   uint32_t stage;                   // [W][R] stages: K chunks | V chunks, 16 rows each
   uint32_t stage_bytes;
   uint32_t mo, mm, ml, mbad;        // per-warp partial states for the CTA combine
-  uint32_t qs;                      // [G][D+4] fp32 q * scale * log2(e) of the current piece
+  uint32_t qs;                      // [C][D+4] fp32 q * scale * log2(e) of the current piece
+  uint32_t qlim;                    // [kColMax] int32 key limit per column (several tokens)
   uint32_t zrow;                    // one all-zero K/V row (D x 2 bytes)
   uint32_t nrow;                    // per warp: the appended token's K and V rows
   uint32_t ps;                      // CUDA-core path: p per warp
@@ -87,7 +150,8 @@ struct SmemLayout {
 
 PA_HD uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-PA_HD SmemLayout split_smem_layout(int D, int G, int B, int W, int R, int mode) {
+// C = query columns per row (G in decode), B = rows.
+PA_HD SmemLayout split_smem_layout(int D, int C, int B, int W, int R, int mode) {
   SmemLayout L;
   L.full = 0;
   L.info = 8 * kMaxSlots;
@@ -95,18 +159,20 @@ PA_HD SmemLayout split_smem_layout(int D, int G, int B, int W, int R, int mode) 
   L.stage_bytes = 4u * (uint32_t)D * (uint32_t)kTile;  // K + V tiles, 2 bytes each
   uint32_t off = L.stage + (uint32_t)(W * R) * L.stage_bytes;
   L.mo = off;
-  off += (uint32_t)(W * G * (D + 4)) * 4u;
+  off += (uint32_t)(W * C * (D + 4)) * 4u;
   L.mm = off;
-  off += (uint32_t)W * kGMax * 4u;
+  off += (uint32_t)W * kColMax * 4u;
   L.ml = off;
-  off += (uint32_t)W * kGMax * 4u;
+  off += (uint32_t)W * kColMax * 4u;
   L.mbad = off;
   off += (uint32_t)W * 4u;
-  L.abort_flag = off;  // followed by the current piece's stored length
-  off += 8u;
+  L.abort_flag = off;  // followed by the current piece's stored length, q0, nq
+  off += 16u;
+  L.qlim = off;
+  off += (uint32_t)kColMax * 4u;
   off = align_up(off, 16);
   L.qs = off;
-  off += (uint32_t)(G * (D + 4)) * 4u;
+  off += (uint32_t)(C * (D + 4)) * 4u;
   L.zrow = off;
   off += (uint32_t)D * 2u;
   L.nrow = off;

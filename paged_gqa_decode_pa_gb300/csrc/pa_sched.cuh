@@ -3,8 +3,10 @@
 // Compiled for host and device so that pa_plan_pieces (host) and the kernels
 // run the very same code.
 //
-// Work unit: one physical block of one (sequence b, kv head j) "segment".
-// Segment (b, j) holds nblk_b = ceil(len_b / bs) units.
+// Work unit: one physical block of one (row b, kv head j) "segment".
+// Segment (b, j) holds nblk_b = ceil(len_b / bs) units.  A row is one
+// sequence in decode; with several query tokens per sequence it is one
+// group of a sequence's query tokens, and len_b the keys that group reads.
 //
 // Balanced split (partition_tokens == 0): units are ordered (b, j, block);
 // CTA c of C_eff owns units [floor(U c / C_eff), floor(U (c+1) / C_eff)),
@@ -103,10 +105,19 @@ struct Piece {
   int32_t slot;              // partial-state slot, or -1 = whole segment
 };
 
-// Iterates the pieces one CTA processes, in processing order.
-struct PieceIter {
+// Row lengths from a host array of stored lengths (plus `add`).
+struct HostLens {
+  const int32_t* lens;
+  int32_t add, bs, maxblk;
+  PA_HD int32_t operator()(int32_t b) const { return eff_len(lens[b], add, bs, maxblk); }
+};
+
+// Iterates the pieces one CTA processes, in processing order.  LenOf maps a
+// row to the length it attends to (the fixed split needs nblk per row).
+template <class LenOf>
+struct PieceIterT {
   const int32_t* pre;     // [B+1] prefix sums of seq_count
-  const int32_t* lens;    // [B] (fixed split needs nblk per sequence)
+  LenOf len_of;
   SchedShape s;
   int32_t cta;
   // balanced state
@@ -115,10 +126,10 @@ struct PieceIter {
   // fixed state
   int64_t item, items;
 
-  PA_HD void init(const int32_t* pre_, const int32_t* lens_, const SchedShape& s_,
+  PA_HD void init(const int32_t* pre_, const LenOf& len_of_, const SchedShape& s_,
                   int32_t cta_) {
     pre = pre_;
-    lens = lens_;
+    len_of = len_of_;
     s = s_;
     cta = cta_;
     if (s.part_blocks == 0) {
@@ -167,7 +178,7 @@ struct PieceIter {
     int64_t r = item - (int64_t)s.Hkv * pre[b];
     int32_t part = (int32_t)(r / s.Hkv);
     int32_t j = (int32_t)(r % s.Hkv);
-    int32_t nb = seq_blocks(eff_len(lens[b], s.len_add, s.bs, s.maxblk), s.bs, s.maxblk);
+    int32_t nb = seq_blocks(len_of(b), s.bs, s.maxblk);
     int32_t np = pre[b + 1] - pre[b];
     p.b = b;
     p.j = j;
@@ -178,6 +189,8 @@ struct PieceIter {
     return true;
   }
 };
+
+using PieceIter = PieceIterT<HostLens>;
 
 // Balanced split: the segment that begins inside CTA c and continues past
 // its range, if any.  Returns false when CTA c has none.  On success gives

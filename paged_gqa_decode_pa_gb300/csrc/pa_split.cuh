@@ -37,6 +37,8 @@
 
 #include <math.h>
 
+#include <type_traits>
+
 #include "pa_kernels.cuh"
 #include "pa_ptx.cuh"
 
@@ -57,16 +59,17 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t unit) {
 
 // ------------------------------------------------------------------ prologue
 
-// Prefix sums of the per-sequence counts into pre[0..B] (shared memory).
-__device__ __forceinline__ void build_prefix(const SplitArgs& a, int32_t* pre, int32_t* scratch) {
+// Prefix sums of the per-row counts into pre[0..B] (shared memory).
+template <class LenOf>
+__device__ __forceinline__ void build_prefix(const SplitArgs& a, const LenOf& len_of, int32_t* pre,
+                                             int32_t* scratch) {
   const int tid = threadIdx.x;
   const int T = blockDim.x;
   const int per = (a.B + T - 1) / T;
   const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
   int local = 0;
   for (int b = b0; b < b1; ++b)
-    local += seq_count(seq_blocks(eff_len(__ldg(a.seqlens + b), a.len_add, a.bs, a.maxblk), a.bs, a.maxblk),
-                       a.part_blocks);
+    local += seq_count(seq_blocks(len_of(b), a.bs, a.maxblk), a.part_blocks);
   // inclusive scan of `local` over the block
   const int lane = tid & 31, warp = tid >> 5;
   int x = local;
@@ -90,69 +93,83 @@ __device__ __forceinline__ void build_prefix(const SplitArgs& a, int32_t* pre, i
   int run = scratch[warp] + x - local;
   for (int b = b0; b < b1; ++b) {
     pre[b] = run;
-    run += seq_count(seq_blocks(eff_len(__ldg(a.seqlens + b), a.len_add, a.bs, a.maxblk), a.bs, a.maxblk),
-                     a.part_blocks);
+    run += seq_count(seq_blocks(len_of(b), a.bs, a.maxblk), a.part_blocks);
   }
   __syncthreads();
 }
 
 // ------------------------------------------------------------- consumer state
 
-template <typename T, int D>
+template <typename T, int D, int NB, bool kQ>
 struct MmaState {
-  uint32_t qh[D / 16][2], ql[D / 16][2];  // B fragments of Q' (hi / lo)
-  float o[D / 16][4];                     // O^T accumulators
-  float m0, m1, l0, l1;                   // heads 2t and 2t+1 of this lane
+  uint32_t qh[NB][D / 16][2], ql[NB][D / 16][2];  // B fragments of Q' (hi / lo)
+  float o[NB][D / 16][4];                         // O^T accumulators
+  float m[NB][2], l[NB][2];                       // columns 8nb + 2t, 8nb + 2t + 1 of this lane
+  int32_t lim[NB][2];                             // kQ: key limit of those columns
   bool bad;
 
-  // B fragments of q' = q * scale * log2(e) for the 8 head columns, from
-  // the CTA's shared fp32 copy qs [G][D+4] (heads >= G are zero columns).
-  __device__ __forceinline__ void load_q(const float* qs, int G) {
+  // B fragments of q' = q * scale * log2(e) for the 8 NB columns, from the
+  // CTA's shared fp32 copy qs [C][D+4] (columns >= C are zero).  kQ: also
+  // the columns' key limits (tokens t < lim are visible).
+  __device__ __forceinline__ void load_q(const float* qs, int C, const int32_t* qlim) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const bool live = g < G;
-    const float* qrow = qs + (live ? g : 0) * (D + 4);
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
+    for (int nb = 0; nb < NB; ++nb) {
+      const int col = nb * 8 + g;
+      const bool live = col < C;
+      const float* qrow = qs + (live ? col : 0) * (D + 4);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t hi = 0, lo = 0;
-        if (live) {
-          const float2 x = *reinterpret_cast<const float2*>(qrow + ks * 16 + half * 8 + 2 * t);
-          hi = Cvt<T>::pack(x.x, x.y);
-          lo = Cvt<T>::pack(x.x - Cvt<T>::low(hi), x.y - Cvt<T>::high(hi));
+      for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t hi = 0, lo = 0;
+          if (live) {
+            const float2 x = *reinterpret_cast<const float2*>(qrow + ks * 16 + half * 8 + 2 * t);
+            hi = Cvt<T>::pack(x.x, x.y);
+            lo = Cvt<T>::pack(x.x - Cvt<T>::low(hi), x.y - Cvt<T>::high(hi));
+          }
+          qh[nb][ks][half] = hi;
+          ql[nb][ks][half] = lo;
         }
-        qh[ks][half] = hi;
-        ql[ks][half] = lo;
+      }
+      if constexpr (kQ) {
+        lim[nb][0] = qlim[nb * 8 + 2 * t];
+        lim[nb][1] = qlim[nb * 8 + 2 * t + 1];
       }
     }
   }
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
-    for (int i = 0; i < D / 16; ++i)
+    for (int nb = 0; nb < NB; ++nb) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) o[i][c] = 0.f;
-    m0 = m1 = -INFINITY;
-    l0 = l1 = 0.f;
+      for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[nb][i][c] = 0.f;
+      m[nb][0] = m[nb][1] = -INFINITY;
+      l[nb][0] = l[nb][1] = 0.f;
+    }
     bad = false;
   }
 
-  // One 16-token tile, `valid` (1..16) of its rows real; K chunks at kb, V
-  // chunks at vb, each chunk a 128B-swizzled [16][64] tile of 2 KB.
+  // One 16-token tile, `valid` (1..16) of its rows real, tok0 = index of its
+  // first token in the sequence; K chunks at kb, V chunks at vb, each chunk a
+  // 128B-swizzled [16][64] tile of 2 KB.
   //
   // ldmatrix takes one row address per lane, so two kinds of rows are read
   // from outside the TMA stage (which no thread ever writes): V rows past the
   // sequence end read the CTA's zero row, and row `new_r` (the token being
   // appended, or -1) reads the warp's copy of the new K/V rows at nk / nv.
   // Those buffers are unswizzled: 64-dim chunk c, unit u at c*128 + u*16.
-  __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int valid, int new_r, uint32_t nk,
-                                       uint32_t nv, uint32_t zrow) {
+  // Each K and V fragment feeds the NB column blocks.
+  __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int valid, int tok0, int new_r,
+                                       uint32_t nk, uint32_t nv, uint32_t zrow) {
     const int lane = threadIdx.x & 31;
     constexpr uint32_t chunk = kTile * 128u;
-    // ---- S^T = K . Q'^T  (rows: the 16 tokens, cols: heads); four
-    // independent accumulator chains (hi/lo x even/odd k-step)
-    float acc4[4][4] = {};
+    // ---- S^T = K . Q'^T  (rows: the 16 tokens, cols: query columns); four
+    // independent accumulator chains per block (hi/lo x even/odd k-step)
+    float acc4[NB][4][4] = {};
     {
       const uint32_t tok = (lane & 7) + ((lane >> 3) & 1) * 8;
       const uint32_t uh = (uint32_t)(lane >> 4);
@@ -164,49 +181,67 @@ struct MmaState {
         const uint32_t addr = knew ? nk + (uint32_t)(ks >> 2) * 128u + unit * 16u
                                    : kb + (uint32_t)(ks >> 2) * chunk + swz(tok, unit);
         ldmatrix_x4(addr, a0, a1, a2, a3);
-        mma_16816<T>(acc4[ks & 1], a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
-        mma_16816<T>(acc4[2 + (ks & 1)], a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          mma_16816<T>(acc4[nb][ks & 1], a0, a1, a2, a3, qh[nb][ks][0], qh[nb][ks][1]);
+          mma_16816<T>(acc4[nb][2 + (ks & 1)], a0, a1, a2, a3, ql[nb][ks][0], ql[nb][ks][1]);
+        }
       }
     }
     const int tr = lane >> 2;
-    float s0 = (acc4[0][0] + acc4[1][0]) + (acc4[2][0] + acc4[3][0]);
-    float s1 = (acc4[0][1] + acc4[1][1]) + (acc4[2][1] + acc4[3][1]);
-    float s2 = (acc4[0][2] + acc4[1][2]) + (acc4[2][2] + acc4[3][2]);
-    float s3 = (acc4[0][3] + acc4[1][3]) + (acc4[2][3] + acc4[3][3]);
-    if (tr >= valid) s0 = s1 = -INFINITY;
-    if (tr + 8 >= valid) s2 = s3 = -INFINITY;
-    // ---- online softmax update for heads 2t, 2t+1
-    float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+    uint32_t bh0[NB], bh1[NB], bl0[NB], bl1[NB];
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
-    }
-    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-    const float u0 = (n0 == -INFINITY) ? 0.f : n0;
-    const float u1 = (n1 == -INFINITY) ? 0.f : n1;
-    const float al0 = ex2(m0 - u0), al1 = ex2(m1 - u1);
-    const float p0 = ex2(s0 - u0), p1 = ex2(s1 - u1), p2 = ex2(s2 - u0), p3 = ex2(s3 - u1);
-    l0 = l0 * al0 + (p0 + p2);
-    l1 = l1 * al1 + (p1 + p3);
-    m0 = n0;
-    m1 = n1;
-    // rescale the accumulator only when some running max moved
-    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-      for (int dt = 0; dt < D / 16; ++dt) {
-        o[dt][0] *= al0;
-        o[dt][1] *= al1;
-        o[dt][2] *= al0;
-        o[dt][3] *= al1;
+    for (int nb = 0; nb < NB; ++nb) {
+      float s0 = (acc4[nb][0][0] + acc4[nb][1][0]) + (acc4[nb][2][0] + acc4[nb][3][0]);
+      float s1 = (acc4[nb][0][1] + acc4[nb][1][1]) + (acc4[nb][2][1] + acc4[nb][3][1]);
+      float s2 = (acc4[nb][0][2] + acc4[nb][1][2]) + (acc4[nb][2][2] + acc4[nb][3][2]);
+      float s3 = (acc4[nb][0][3] + acc4[nb][1][3]) + (acc4[nb][2][3] + acc4[nb][3][3]);
+      if (tr >= valid) s0 = s1 = -INFINITY;
+      if (tr + 8 >= valid) s2 = s3 = -INFINITY;
+      if constexpr (kQ) {
+        // per-column visibility: token tok0 + row is seen by a column only
+        // below its limit
+        const int r0 = tok0 + tr, r1 = r0 + 8;
+        if (r0 >= lim[nb][0]) s0 = -INFINITY;
+        if (r0 >= lim[nb][1]) s1 = -INFINITY;
+        if (r1 >= lim[nb][0]) s2 = -INFINITY;
+        if (r1 >= lim[nb][1]) s3 = -INFINITY;
       }
+      // ---- online softmax update for the lane's two columns
+      float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+      }
+      const float n0 = fmaxf(m[nb][0], x0), n1 = fmaxf(m[nb][1], x1);
+      const float u0 = (n0 == -INFINITY) ? 0.f : n0;
+      const float u1 = (n1 == -INFINITY) ? 0.f : n1;
+      const float al0 = ex2(m[nb][0] - u0), al1 = ex2(m[nb][1] - u1);
+      const float p0 = ex2(s0 - u0), p1 = ex2(s1 - u1), p2 = ex2(s2 - u0), p3 = ex2(s3 - u1);
+      l[nb][0] = l[nb][0] * al0 + (p0 + p2);
+      l[nb][1] = l[nb][1] * al1 + (p1 + p3);
+      m[nb][0] = n0;
+      m[nb][1] = n1;
+      // rescale the accumulator only when some running max moved
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt) {
+          o[nb][dt][0] *= al0;
+          o[nb][dt][1] *= al1;
+          o[nb][dt][2] *= al0;
+          o[nb][dt][3] *= al1;
+        }
+      }
+      // ---- P^T fragments (k = tokens, n = columns), hi + lo parts
+      const uint32_t h01 = Cvt<T>::pack(p0, p1), h23 = Cvt<T>::pack(p2, p3);
+      const uint32_t e01 = Cvt<T>::pack(p0 - Cvt<T>::low(h01), p1 - Cvt<T>::high(h01));
+      const uint32_t e23 = Cvt<T>::pack(p2 - Cvt<T>::low(h23), p3 - Cvt<T>::high(h23));
+      bh0[nb] = movmatrix_trans(h01);
+      bh1[nb] = movmatrix_trans(h23);
+      bl0[nb] = movmatrix_trans(e01);
+      bl1[nb] = movmatrix_trans(e23);
     }
-    // ---- P^T fragments (k = tokens, n = heads), hi + lo parts
-    const uint32_t h01 = Cvt<T>::pack(p0, p1), h23 = Cvt<T>::pack(p2, p3);
-    const uint32_t e01 = Cvt<T>::pack(p0 - Cvt<T>::low(h01), p1 - Cvt<T>::high(h01));
-    const uint32_t e23 = Cvt<T>::pack(p2 - Cvt<T>::low(h23), p3 - Cvt<T>::high(h23));
-    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-    const uint32_t bl0 = movmatrix_trans(e01), bl1 = movmatrix_trans(e23);
     // ---- O^T += V^T . P^T  (rows past the end read zeros, so p = 0 adds 0
     // even where the pool holds NaN)
     {
@@ -221,41 +256,48 @@ struct MmaState {
         const uint32_t addr = vplain ? vrow + (uint32_t)(dt >> 2) * 128u + unit * 16u
                                      : vb + (uint32_t)(dt >> 2) * chunk + swz(tok, unit);
         ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-        mma_16816<T>(o[dt], a0, a1, a2, a3, bh0, bh1);
-        mma_16816<T>(o[dt], a0, a1, a2, a3, bl0, bl1);
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          mma_16816<T>(o[nb][dt], a0, a1, a2, a3, bh0[nb], bh1[nb]);
+          mma_16816<T>(o[nb][dt], a0, a1, a2, a3, bl0[nb], bl1[nb]);
+        }
       }
     }
   }
 
   // Publish this warp's state for the CTA-level combine.
-  __device__ __forceinline__ void publish(uint8_t* smem, const SmemLayout& L, int w, int G) {
+  __device__ __forceinline__ void publish(uint8_t* smem, const SmemLayout& L, int w, int C) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
+    float* mm = reinterpret_cast<float*>(smem + L.mm) + w * kColMax;
+    float* ml = reinterpret_cast<float*>(smem + L.ml) + w * kColMax;
+    float* mo = reinterpret_cast<float*>(smem + L.mo) + (size_t)w * C * (D + 4);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-    float* mm = reinterpret_cast<float*>(smem + L.mm) + w * kGMax;
-    float* ml = reinterpret_cast<float*>(smem + L.ml) + w * kGMax;
-    if (g == 0) {
-      mm[2 * t] = m0;
-      mm[2 * t + 1] = m1;
-      ml[2 * t] = l0;
-      ml[2 * t + 1] = l1;
-    }
-    float* mo = reinterpret_cast<float*>(smem + L.mo) + (size_t)w * G * (D + 4);
-    const int h0 = 2 * t, h1 = 2 * t + 1;
+    for (int nb = 0; nb < NB; ++nb) {
+      float l0 = l[nb][0], l1 = l[nb][1];
 #pragma unroll
-    for (int dt = 0; dt < D / 16; ++dt) {
-      const int dim = dt * 16 + g;
-      if (h0 < G) {
-        mo[h0 * (D + 4) + dim] = o[dt][0];
-        mo[h0 * (D + 4) + dim + 8] = o[dt][2];
+      for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
       }
-      if (h1 < G) {
-        mo[h1 * (D + 4) + dim] = o[dt][1];
-        mo[h1 * (D + 4) + dim + 8] = o[dt][3];
+      const int c0 = nb * 8 + 2 * t, c1 = c0 + 1;
+      if (g == 0) {
+        mm[c0] = m[nb][0];
+        mm[c1] = m[nb][1];
+        ml[c0] = l0;
+        ml[c1] = l1;
+      }
+#pragma unroll
+      for (int dt = 0; dt < D / 16; ++dt) {
+        const int dim = dt * 16 + g;
+        if (c0 < C) {
+          mo[c0 * (D + 4) + dim] = o[nb][dt][0];
+          mo[c0 * (D + 4) + dim + 8] = o[nb][dt][2];
+        }
+        if (c1 < C) {
+          mo[c1 * (D + 4) + dim] = o[nb][dt][1];
+          mo[c1 * (D + 4) + dim + 8] = o[nb][dt][3];
+        }
       }
     }
     if (lane == 0) reinterpret_cast<int*>(smem + L.mbad)[w] = bad ? 1 : 0;
@@ -388,8 +430,8 @@ struct SimtState {
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) l[g] += __shfl_xor_sync(0xffffffffu, l[g], off);
     }
-    float* mm = reinterpret_cast<float*>(smem + L.mm) + w * kGMax;
-    float* ml = reinterpret_cast<float*>(smem + L.ml) + w * kGMax;
+    float* mm = reinterpret_cast<float*>(smem + L.mm) + w * kColMax;
+    float* ml = reinterpret_cast<float*>(smem + L.ml) + w * kColMax;
     if (lane == 0) {
 #pragma unroll
       for (int g = 0; g < kGMax; ++g) {
@@ -412,11 +454,30 @@ struct SimtState {
   }
 };
 
-// CTA-level combine of the W warp states of one piece (all threads).
-template <int D>
+// Where column c of a piece's row goes: its output row (or -1 when the
+// column holds no query) -- decode: head j*G + c of sequence b; several
+// query tokens: token g*tq + c/G of the row's sequence, head j*G + c%G.
+template <bool kQ>
+__device__ __forceinline__ int64_t column_out(const SplitArgs& a, int row, int j, int c, int q0,
+                                              int nq) {
+  if constexpr (!kQ) {
+    return (int64_t)row * a.H + (int64_t)j * a.G + c;
+  } else {
+    const int g = row % a.nqg;
+    const int tok = g * a.tq + c / a.G;
+    if (tok >= nq) return -1;
+    return (int64_t)(q0 + tok) * a.H + (int64_t)j * a.G + c % a.G;
+  }
+}
+
+// CTA-level combine of the W warp states of one piece (all threads).  A
+// column that saw no key (l = 0: a query token whose causal limit is 0)
+// gets 0, as an empty sequence does.
+// q0, nq: the query rows of the piece's sequence (several query tokens).
+template <int D, bool kQ>
 __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem, const SmemLayout& L,
-                                              const Piece& pc, int W) {
-  const int G = a.G;
+                                              const Piece& pc, int W, int q0, int nq) {
+  const int C = a.C;
   const float* mm = reinterpret_cast<const float*>(smem + L.mm);
   const float* ml = reinterpret_cast<const float*>(smem + L.ml);
   const float* mo = reinterpret_cast<const float*>(smem + L.mo);
@@ -424,25 +485,25 @@ __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem,
   bool bad = false;
   for (int w = 0; w < W; ++w) bad |= (mbad[w] != 0);
   const float qnan = __int_as_float(0x7fc00000);
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int g = idx / D, dim = idx % D;
+  for (int idx = threadIdx.x; idx < C * D; idx += blockDim.x) {
+    const int c = idx / D, dim = idx % D;
     float M = -INFINITY;
-    for (int w = 0; w < W; ++w) M = fmaxf(M, mm[w * kGMax + g]);
+    for (int w = 0; w < W; ++w) M = fmaxf(M, mm[w * kColMax + c]);
     float Lsum = 0.f, o = 0.f;
     for (int w = 0; w < W; ++w) {
-      const float mw = mm[w * kGMax + g];
+      const float mw = mm[w * kColMax + c];
       const float e = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-      Lsum = fmaf(e, ml[w * kGMax + g], Lsum);
-      o = fmaf(e, mo[(w * G + g) * (D + 4) + dim], o);
+      Lsum = fmaf(e, ml[w * kColMax + c], Lsum);
+      o = fmaf(e, mo[(w * C + c) * (D + 4) + dim], o);
     }
     if (pc.slot < 0) {
-      float* dst = a.out + ((int64_t)pc.b * a.H + (int64_t)pc.j * G + g) * D + dim;
-      *dst = bad ? qnan : o / Lsum;
+      const int64_t r = column_out<kQ>(a, pc.b, pc.j, c, q0, nq);
+      if (r >= 0) a.out[r * D + dim] = bad ? qnan : (Lsum == 0.f ? 0.f : o / Lsum);
     } else {
-      a.ws_acc[((int64_t)pc.slot * G + g) * D + dim] = bad ? qnan : o;
+      a.ws_acc[((int64_t)pc.slot * C + c) * D + dim] = bad ? qnan : o;
       if (dim == 0) {
-        a.ws_ml[((int64_t)pc.slot * G + g) * 2 + 0] = M;
-        a.ws_ml[((int64_t)pc.slot * G + g) * 2 + 1] = bad ? qnan : Lsum;
+        a.ws_ml[((int64_t)pc.slot * C + c) * 2 + 0] = M;
+        a.ws_ml[((int64_t)pc.slot * C + c) * 2 + 1] = bad ? qnan : Lsum;
       }
     }
   }
@@ -460,30 +521,33 @@ __device__ __forceinline__ int warp_tiles(const Piece& pc, int sl, int w) {
 // computing side and loads each tile into the ring slot the computing side
 // has just freed.  Block-table entries are read 32 tiles at a time, one
 // window ahead.
-struct Issuer {
-  PieceIter it;
+template <class LenOf>
+struct IssuerT {
+  PieceIterT<LenOf> it;
   Piece pc;
   int i, cnt;        // next tile index (of this warp) in pc, and their count
   int win;           // first tile index of the current table window
   int32_t entry;     // this lane's entry of the current window (tile win + lane)
   int32_t entry_next;  // ... of the next window (tile win + 32 + lane)
-  int32_t len;       // cache_seqlens[pc.b]
+  int32_t len;       // the length row pc.b attends to
+  int32_t seq;       // the row's sequence (its block-table row)
   uint32_t issued;   // tiles issued so far
   bool done;
 };
 
 template <int W>
-__device__ __forceinline__ int32_t table_entry(const SplitArgs& a, const Piece& pc, int cnt, int ii,
-                                               int sl, int w) {
+__device__ __forceinline__ int32_t table_entry(const SplitArgs& a, const Piece& pc, int seq, int cnt,
+                                               int ii, int sl, int w) {
   if (ii >= cnt) return 0;
   const int t = w + W * ii;
-  return __ldg(a.table + (int64_t)pc.b * a.maxblk + pc.blk0 + (t >> sl));
+  return __ldg(a.table + (int64_t)seq * a.maxblk + pc.blk0 + (t >> sl));
 }
 
-template <int D, int W>
-__device__ __forceinline__ void issue_next(Issuer& is, const SplitArgs& a, const CUtensorMap* tmk,
-                                           const CUtensorMap* tmv, uint32_t base,
-                                           const SmemLayout& L, int w, uint32_t slot, int sl) {
+template <int D, int W, class LenOf>
+__device__ __forceinline__ void issue_next(IssuerT<LenOf>& is, const SplitArgs& a,
+                                           const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                           uint32_t base, const SmemLayout& L, int w,
+                                           uint32_t slot, int sl) {
   const int lane = threadIdx.x & 31;
   while (!is.done && is.i >= is.cnt) {
     if (!is.it.next(is.pc)) {
@@ -493,15 +557,16 @@ __device__ __forceinline__ void issue_next(Issuer& is, const SplitArgs& a, const
     is.i = 0;
     is.cnt = warp_tiles<W>(is.pc, sl, w);
     is.win = 0;
-    is.len = eff_len(__ldg(a.seqlens + is.pc.b), a.len_add, a.bs, a.maxblk);
-    is.entry = table_entry<W>(a, is.pc, is.cnt, lane, sl, w);
-    is.entry_next = table_entry<W>(a, is.pc, is.cnt, 32 + lane, sl, w);
+    is.len = is.it.len_of(is.pc.b);
+    is.seq = a.nqg > 1 ? is.pc.b / a.nqg : is.pc.b;
+    is.entry = table_entry<W>(a, is.pc, is.seq, is.cnt, lane, sl, w);
+    is.entry_next = table_entry<W>(a, is.pc, is.seq, is.cnt, 32 + lane, sl, w);
   }
   if (is.done) return;
   if (is.i >= is.win + 32) {
     is.win += 32;
     is.entry = is.entry_next;
-    is.entry_next = table_entry<W>(a, is.pc, is.cnt, is.win + 32 + lane, sl, w);
+    is.entry_next = table_entry<W>(a, is.pc, is.seq, is.cnt, is.win + 32 + lane, sl, w);
   }
   const int32_t phys = __shfl_sync(0xffffffffu, is.entry, is.i - is.win);
   if (lane == 0) {
@@ -528,37 +593,78 @@ __device__ __forceinline__ void issue_next(Issuer& is, const SplitArgs& a, const
   ++is.issued;
 }
 
-// q' = q * scale * log2(e) of piece pc's G heads into the shared fp32 buffer
-// (all threads).  The loads are issued first; `finish` stores them.
-template <int D>
+// q' = q * scale * log2(e) of piece pc's C query columns into the shared
+// fp32 buffer (all threads).  The loads are issued first; `finish` stores
+// them.  kQ: column c is token g*tq + c/G (head c%G) of the row's sequence,
+// and `finish` also writes each column's key limit and the row's query span.
+template <int D, int NB, bool kQ>
 struct QPrefetch {
-  static constexpr int kPer = (kGMax * D / 2 + 32 * 4 - 1) / (32 * 4);  // words per thread, >= 4 warps
+  // words per thread, for >= 4 warps
+  static constexpr int kPer = (kGMax * NB * D / 2 + 32 * 4 - 1) / (32 * 4);
   uint32_t v[kPer];
-  int32_t len;  // stored cache_seqlens of the piece's sequence (thread 0)
+  int32_t len;         // stored cache_seqlens of the piece's sequence
+  int32_t q0, nq, grp; // kQ: the sequence's query rows, the row's group
   __device__ __forceinline__ void start(const SplitArgs& a, const Piece& pc) {
-    if (threadIdx.x == 0) len = __ldg(a.seqlens + pc.b);
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(
-        a.q + ((int64_t)pc.b * a.H + (int64_t)pc.j * a.G) * D);
-    const int nw = a.G * D / 2;
+    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q);
+    const int nw = a.C * D / 2;
+    if constexpr (!kQ) {
+      if (threadIdx.x == 0) len = __ldg(a.seqlens + pc.b);
+      const uint32_t* src = q32 + ((int64_t)pc.b * a.H + (int64_t)pc.j * a.G) * (D / 2);
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * blockDim.x;
-      v[k] = (i < nw) ? __ldg(src + i) : 0u;
+      for (int k = 0; k < kPer; ++k) {
+        const int i = threadIdx.x + k * blockDim.x;
+        v[k] = (i < nw) ? __ldg(src + i) : 0u;
+      }
+    } else {
+      const int seq = pc.b / a.nqg;
+      grp = pc.b - seq * a.nqg;
+      len = __ldg(a.seqlens + seq);
+      query_span(a.cu_q, seq, a.total_q, a.max_q, q0, nq);
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = threadIdx.x + k * blockDim.x;
+        uint32_t x = 0u;
+        if (i < nw) {
+          const int c = (2 * i) / D, d = (2 * i) % D;
+          const int tok = grp * a.tq + c / a.G;
+          if (tok < nq)
+            x = __ldg(q32 + (((int64_t)(q0 + tok) * a.H + (int64_t)pc.j * a.G + c % a.G) * D + d) / 2);
+        }
+        v[k] = x;
+      }
     }
   }
   template <typename T>
-  __device__ __forceinline__ void finish(const SplitArgs& a, float* qs, int32_t* len_out) {
-    if (threadIdx.x == 0) *len_out = len;
-    const int nw = a.G * D / 2;
+  __device__ __forceinline__ void finish(const SplitArgs& a, float* qs, int32_t* info,
+                                         int32_t* qlim) {
+    if (threadIdx.x == 0) {
+      info[1] = len;
+      if constexpr (kQ) {
+        info[2] = q0;
+        info[3] = nq;
+      }
+    }
+    if constexpr (kQ) {
+      // the key limit of every column: tokens t < limit are visible; columns
+      // that hold no query see everything (their q is zero)
+      const int c = threadIdx.x;
+      if (c < kColMax) {
+        int32_t lim = 0x7fffffff;
+        const int tok = grp * a.tq + c / a.G;
+        if (c < a.C && tok < nq && a.causal) lim = max(0, min(len, len - nq + tok + 1));
+        qlim[c] = lim;
+      }
+    }
+    const int nw = a.C * D / 2;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
       if (i < nw) {
-        const int g = (2 * i) / D, d = (2 * i) % D;
+        const int c = (2 * i) / D, d = (2 * i) % D;
         float2 x;
         x.x = Cvt<T>::low(v[k]) * a.qscale;
         x.y = Cvt<T>::high(v[k]) * a.qscale;
-        *reinterpret_cast<float2*>(qs + g * (D + 4) + d) = x;
+        *reinterpret_cast<float2*>(qs + c * (D + 4) + d) = x;
       }
     }
   }
@@ -569,20 +675,31 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     pa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                     const SplitArgs a) {
   constexpr int W = split_warps(D);
+  constexpr bool kQ = MODE == kMmaQ;
+  constexpr int NB = mma_blocks(D, MODE);
+  using RowLen = typename std::conditional<kQ, MultiLen, DecodeLen>::type;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
   const int R = a.ring;
-  const SmemLayout L = split_smem_layout(D, a.G, a.B, W, R, MODE);
+  const SmemLayout L = split_smem_layout(D, a.C, a.B, W, R, MODE);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   int32_t* pre = reinterpret_cast<int32_t*>(smem + L.pre);
   float* qs = reinterpret_cast<float*>(smem + L.qs);
-  int32_t* piece_len = reinterpret_cast<int32_t*>(smem + L.abort_flag + 4);
+  int32_t* piece_info = reinterpret_cast<int32_t*>(smem + L.abort_flag);  // [1] len, [2] q0, [3] nq
+  int32_t* qlim = reinterpret_cast<int32_t*>(smem + L.qlim);
   __shared__ int32_t scan_scratch[kMaxWarps];
+
+  RowLen len_of;
+  if constexpr (kQ) {
+    len_of = MultiLen{a.seqlens, a.cu_q, a.nqg, a.tq, a.causal, a.total_q, a.max_q, a.bs, a.maxblk};
+  } else {
+    len_of = DecodeLen{a.seqlens, a.len_add, a.bs, a.maxblk};
+  }
 
   if (tid == 0) {
     for (int s = 0; s < W * R; ++s) mbar_init(base + L.full + 8 * s, 1);
@@ -594,23 +711,36 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
   }
-  build_prefix(a, pre, scan_scratch);  // contains __syncthreads
+  build_prefix(a, len_of, pre, scan_scratch);  // contains __syncthreads
   // The merge kernel may be scheduled now; it waits for this grid to finish.
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, (int32_t)gridDim.x, a.len_add};
   const int cta = blockIdx.x;
 
-  // Sequences with no cached token: out = 0; invalid length: NaN + status
-  // (with the fused append also "no slot": nothing is written for them).
+  // Rows with no key to read: out = 0; invalid length: NaN + status (with
+  // the fused append also "no slot": nothing is written for them).
   for (int b = cta; b < a.B; b += gridDim.x) {
-    const int32_t len = eff_len(__ldg(a.seqlens + b), a.len_add, a.bs, a.maxblk);
+    const int32_t len = len_of(b);
     if (seq_blocks(len, a.bs, a.maxblk) != 0) continue;
-    const bool ok = seq_len_valid(len, a.bs, a.maxblk);
+    const bool ok = len >= 0;
     const float v = ok ? 0.f : __int_as_float(0x7fc00000);
-    float* row = a.out + (int64_t)b * a.H * D;
-    for (int i = tid; i < a.H * D; i += blockDim.x) row[i] = v;
-    if (!ok && tid == 0) atomicOr(a.status, kStatusBadSeqlen | (a.len_add ? kStatusNoSlot : 0u));
+    if constexpr (!kQ) {
+      float* row = a.out + (int64_t)b * a.H * D;
+      for (int i = tid; i < a.H * D; i += blockDim.x) row[i] = v;
+      if (!ok && tid == 0) atomicOr(a.status, kStatusBadSeqlen | (a.len_add ? kStatusNoSlot : 0u));
+    } else {
+      // the row's query tokens are consecutive packed rows of out
+      const int seq = b / a.nqg, grp = b - seq * a.nqg;
+      int32_t q0, nq;
+      const bool span = query_span(a.cu_q, seq, a.total_q, a.max_q, q0, nq);
+      if ((!span || !ok) && grp == 0 && tid == 0) atomicOr(a.status, kStatusBadSeqlen);
+      const int first = grp * a.tq;
+      if (!span || first >= nq) continue;
+      const int cnt = min(a.tq, nq - first);
+      float* rows = a.out + (int64_t)(q0 + first) * a.H * D;
+      for (int i = tid; i < cnt * a.H * D; i += blockDim.x) rows[i] = v;
+    }
   }
   if (tid == 0) {
     if (cta == 0) {
@@ -631,35 +761,36 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   constexpr uint32_t chunk = kTile * 128u;
 
   // ---- the warp's issuing side: prime the ring with the first R tiles
-  Issuer is;
-  is.it.init(pre, a.seqlens, sched, cta);
+  IssuerT<RowLen> is;
+  is.it.init(pre, len_of, sched, cta);
   is.i = is.cnt = 0;
   is.win = 0;
   is.entry = is.entry_next = 0;
   is.len = 0;
+  is.seq = 0;
   is.issued = 0;
   is.done = false;
   for (int r = 0; r < R; ++r) issue_next<D, W>(is, a, &tmk, &tmv, base, L, w, (uint32_t)r, sl);
 
   // ---- the computing side
-  PieceIter it;
-  it.init(pre, a.seqlens, sched, cta);
+  PieceIterT<RowLen> it;
+  it.init(pre, len_of, sched, cta);
   Piece pc;
   bool have = it.next(pc);
   if (have) {
-    QPrefetch<D> qp;
+    QPrefetch<D, NB, kQ> qp;
     qp.start(a, pc);
-    qp.template finish<T>(a, qs, piece_len);
+    qp.template finish<T>(a, qs, piece_info, qlim);
   }
   __syncthreads();
   uint32_t slot = 0, phase = 0;  // ring slot to consume next; per-slot parity bits
   uint32_t consumed = 0;
-  MmaState<T, D> mst;
+  MmaState<T, D, NB, kQ> mst;
   SimtState<T, D> sst;
   float* ps = reinterpret_cast<float*>(smem + L.ps) + w * kTile * kGMax;
   while (have) {
-    if constexpr (MODE == kMma) {
-      mst.load_q(qs, a.G);
+    if constexpr (MODE != kSimt) {
+      mst.load_q(qs, a.C, qlim);
       mst.reset();
     } else {
       sst.reset();
@@ -671,7 +802,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     int32_t new_pos = -1;
     uint4 nk = make_uint4(0u, 0u, 0u, 0u), nv = nk;
     if (a.len_add) {
-      const int32_t p0 = *reinterpret_cast<volatile int32_t*>(piece_len);
+      const int32_t p0 = *reinterpret_cast<volatile int32_t*>(piece_info + 1);
       const int rel = p0 - pc.blk0 * a.bs;
       if (rel >= 0 && rel < (pc.blk1 - pc.blk0) * a.bs && ((rel >> 4) % W) == w) {
         new_pos = p0;
@@ -698,14 +829,14 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       } else if (valid > 0) {
         const uint32_t kb = base + L.stage + gslot * L.stage_bytes;
         const uint32_t vb = kb + NC * chunk;
+        const int t = w + W * i;
+        const int tok0 = (pc.blk0 + (t >> sl)) * a.bs + (t & ((1 << sl) - 1)) * kTile;
         int new_r = -1;
         const uint32_t nkr = base + L.nrow + (uint32_t)w * 4u * D, nvr = nkr + 2u * D;
         if (new_pos >= 0) {
           // The tile holding the new token: its row comes from the warp's
           // copy of k_new/v_new, which also goes to the pool slot (no other
           // CTA reads this row).
-          const int t = w + W * i;
-          const int tok0 = (pc.blk0 + (t >> sl)) * a.bs + (t & ((1 << sl) - 1)) * kTile;
           const int r = new_pos - tok0;
           if (r >= 0 && r < kTile) {
             const int32_t phys = (int32_t)(info64 >> 32);
@@ -720,8 +851,8 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
             new_r = r;
           }
         }
-        if constexpr (MODE == kMma) {
-          mst.tile(kb, vb, valid, new_r, nkr, nvr, base + L.zrow);
+        if constexpr (MODE != kSimt) {
+          mst.tile(kb, vb, valid, tok0, new_r, nkr, nvr, base + L.zrow);
         } else {
           sst.tile(kb, vb, valid, qs, ps, a.G, new_r, nkr, nvr);
         }
@@ -732,22 +863,25 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       issue_next<D, W>(is, a, &tmk, &tmv, base, L, w, slot, sl);
       slot = (slot + 1 == (uint32_t)R) ? 0u : slot + 1;
     }
-    if constexpr (MODE == kMma) {
+    if constexpr (MODE != kSimt) {
       mst.bad |= bad;
-      mst.publish(smem, L, w, a.G);
+      mst.publish(smem, L, w, a.C);
     } else {
       sst.bad |= bad;
       sst.publish(smem, L, w, a.G);
     }
+    // this piece's query span, read before the next piece's `finish` may
+    // overwrite it
+    const int q0 = kQ ? piece_info[2] : 0, nq = kQ ? piece_info[3] : 0;
     named_bar_sync(1, blockDim.x);
     // start loading the next piece's q while this piece is being combined
     Piece next;
-    PieceIter peek = it;
+    PieceIterT<RowLen> peek = it;
     const bool more = peek.next(next);
-    QPrefetch<D> qp;
+    QPrefetch<D, NB, kQ> qp;
     if (more) qp.start(a, next);
-    combine_piece<D>(a, smem, L, pc, W);
-    if (more) qp.template finish<T>(a, qs, piece_len);
+    combine_piece<D, kQ>(a, smem, L, pc, W, q0, nq);
+    if (more) qp.template finish<T>(a, qs, piece_info, qlim);
     named_bar_sync(1, blockDim.x);
     have = it.next(pc);
   }

@@ -1,0 +1,5 @@
+// Instantiation of the split kernel for several query tokens per sequence,
+// bf16 storage, head_dim 256.
+#include "pa_split.cuh"
+
+PA_INSTANTIATE_SPLIT(__nv_bfloat16, 256, pa::kMmaQ)

@@ -1,0 +1,5 @@
+// Instantiation of the split kernel for several query tokens per sequence,
+// f16 storage, head_dim 128.
+#include "pa_split.cuh"
+
+PA_INSTANTIATE_SPLIT(__half, 128, pa::kMmaQ)

@@ -65,6 +65,14 @@ class Workload:
     v_cache: np.ndarray  # [P, bs, Hkv, d] uint16
     partition_tokens: int = 0  # the split size the setting names (0 = none)
     seed: int = 0
+    # several query tokens per sequence: q is packed [total_q, H, d] and
+    # sequence b owns rows cu_q[b] .. cu_q[b+1]-1 (None: one token each)
+    cu_q: Optional[np.ndarray] = None
+    causal: bool = True
+
+    @property
+    def max_q(self) -> int:
+        return 1 if self.cu_q is None else max(1, int(np.diff(self.cu_q).max(initial=0)))
 
     @property
     def G(self) -> int:
@@ -287,6 +295,38 @@ def serving_mix_b32_g4_d128(seed: int = 5, poison: bool = False) -> Workload:
     return serving_mix_b256_g4_d128(seed, poison, B=32)
 
 
+def with_query_tokens(w: Workload, lens_q, seed: int = 0, causal: bool = True,
+                      name: Optional[str] = None) -> Workload:
+    """The same cache with lens_q[b] query tokens for sequence b, packed
+    (cumulative counts in cu_q) and drawn like q.  The cache lengths already
+    count the query tokens: they are the last positions of each sequence."""
+    rng = np.random.default_rng(seed)
+    lens_q = np.asarray(lens_q, dtype=np.int32)
+    if lens_q.shape != (w.B,):
+        raise ValueError("one query count per sequence")
+    cu = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    w.q = _normal_bits(rng, (int(cu[-1]), w.H, w.d), w.dtype)
+    w.cu_q = cu
+    w.causal = bool(causal)
+    if name:
+        w.name = name
+    return w
+
+
+def serving_mix_b256_q4_g4_d128(seed: int = 5, poison: bool = False) -> Workload:
+    """The serving mix verifying 4 tokens per sequence (3 drafted + 1), causal."""
+    w = serving_mix_b256_g4_d128(seed, poison)
+    return with_query_tokens(w, np.full(w.B, 4), seed=seed + 2000,
+                             name="serving_mix_b256_q4_g4_d128")
+
+
+def prefix_share_b64_q2_g8_d128(seed: int = 4, poison: bool = False) -> Workload:
+    """Prefix sharing with 2 query tokens per sequence, causal."""
+    w = prefix_share_b64_g8_d128(seed, poison)
+    return with_query_tokens(w, np.full(w.B, 2), seed=seed + 2000,
+                             name="prefix_share_b64_q2_g8_d128")
+
+
 WORKLOADS = {
     "p5_example": p5_example,
     "qwen2_b8_g7_d64": qwen2_b8_g7_d64,
@@ -294,6 +334,8 @@ WORKLOADS = {
     "prefix_share_b64_g8_d128": prefix_share_b64_g8_d128,
     "serving_mix_b256_g4_d128": serving_mix_b256_g4_d128,
     "serving_mix_b32_g4_d128": serving_mix_b32_g4_d128,
+    "serving_mix_b256_q4_g4_d128": serving_mix_b256_q4_g4_d128,
+    "prefix_share_b64_q2_g8_d128": prefix_share_b64_q2_g8_d128,
 }
 
 
