@@ -21,96 +21,124 @@ namespace {
 // ------------------------------------------------------------------ merge
 
 // Phase 2: combine the partial states of every segment the split kernel cut
-// across CTAs (balanced split) or partitions (fixed split).  Block
-// (seg, g) merges head g of merge index seg (pa_sched.cuh, merge_segment):
-// warp w folds pieces w, w+4, ... with the combine op, lanes over the head
-// dimension; the four warp states are folded the same way in a fixed order,
-// so the result is deterministic.  Combine op: "Paged Attention Kernel
-// Architecture for BI-V100", section 2, Level 1 binary op / Level 3.
-// Block (seg, g, c) folds head g, dims [64c, 64c+64) of merge index seg.
-// Pieces are taken 32 at a time: lane k of every warp loads (m, l) of piece
-// k of the batch, so the batch's weights 2^(m_p - M) need one round trip;
-// then warp w accumulates pieces w, w+4, ... of the batch, lanes over the 64
-// dims as float2, with 8 pieces' loads issued before they are used.
-__device__ __forceinline__ void merge_segment_chunk(const MergeArgs& a, const MergeSeg& ms, int g,
-                                                    int c, int64_t out_row) {
+// across CTAs (balanced split) or partitions (fixed split).  Block (seg, g)
+// folds column g (a query head, or a (token, head) pair) of merge index seg
+// (pa_sched.cuh, merge_segment) with the combine op ("Paged Attention Kernel
+// Architecture for BI-V100", section 2, Level 1 binary op / Level 3): warp w
+// folds pieces w, w+4, ... in order, each lane holding D/32 of the dims; the
+// four warp states are then folded in a fixed order, so the result is
+// deterministic.  The loads of up to kMergeBatch pieces are issued before
+// any of them is folded, so a segment of many pieces costs few round trips.
+constexpr int kMergeBatch = 8;
+
+template <int V>
+struct Vec {
+  float v[V];
+};
+
+template <int V>
+__device__ __forceinline__ Vec<V> load_vec(const float* p) {
+  Vec<V> r;
+  if constexpr (V % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < V; i += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(p + i);
+      r.v[i] = x.x;
+      r.v[i + 1] = x.y;
+      r.v[i + 2] = x.z;
+      r.v[i + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; i += 2) {
+      const float2 x = *reinterpret_cast<const float2*>(p + i);
+      r.v[i] = x.x;
+      r.v[i + 1] = x.y;
+    }
+  }
+  return r;
+}
+
+template <int D>
+__device__ __forceinline__ void merge_column(const MergeArgs& a, const MergeSeg& ms, int g,
+                                             int64_t out_row) {
   constexpr int NW = kMergeThreads / 32;
+  constexpr int V = D / 32;  // dims per lane
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  __shared__ float red[NW];
-  __shared__ float wl[NW];
-  __shared__ float2 wacc[NW][32];
-  // pass 1: M = max_p m_p
-  float m = -INFINITY;
-  for (int p = tid; p < ms.np; p += kMergeThreads) m = fmaxf(m, a.ws_ml[(ms.slot(p) * a.C + g) * 2]);
+  __shared__ float wm[NW], wl[NW];
+  __shared__ __align__(16) float wacc[NW][D];
+  float m = -INFINITY, l = 0.f;
+  float acc[V];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) red[w] = m;
-  __syncthreads();
-  float M = red[0];
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  for (int p0 = w; p0 < ms.np; p0 += NW * kMergeBatch) {
+    float mp[kMergeBatch], lp[kMergeBatch];
+    Vec<V> x[kMergeBatch];
 #pragma unroll
-  for (int v = 1; v < NW; ++v) M = fmaxf(M, red[v]);
-  // pass 2
-  float l = 0.f;
-  float2 acc = make_float2(0.f, 0.f);
-  for (int p0 = 0; p0 < ms.np; p0 += 32) {
-    const int nb = min(32, ms.np - p0);
-    float e_lane = 0.f;
-    int64_t s_lane = 0;
-    if (lane < nb) {
-      s_lane = ms.slot(p0 + lane);
-      const float mp = a.ws_ml[(s_lane * a.C + g) * 2];
-      const float lp = a.ws_ml[(s_lane * a.C + g) * 2 + 1];
-      e_lane = ex2(mp - M);
-      if (w == 0) l = fmaf(e_lane, lp, l);  // each piece's l counted once
-    }
-    for (int k0 = w; k0 < nb; k0 += 8 * NW) {
-      float2 x[8];
-      float e[8];
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int p = p0 + u * NW;
+      mp[u] = -INFINITY;
+      lp[u] = 0.f;
+      if (p < ms.np) {
+        const int64_t s = ms.slot(p);
+        mp[u] = a.ws_ml[(s * a.C + g) * 2];
+        lp[u] = a.ws_ml[(s * a.C + g) * 2 + 1];
+        x[u] = load_vec<V>(a.ws_acc + (s * a.C + g) * D + lane * V);
+      } else {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int k = k0 + u * NW;
-        const int kk = k < nb ? k : 0;
-        const int64_t s = __shfl_sync(0xffffffffu, s_lane, kk);
-        e[u] = __shfl_sync(0xffffffffu, e_lane, kk);
-        x[u] = k < nb ? *reinterpret_cast<const float2*>(a.ws_acc + (s * a.C + g) * a.D + c * 64 + 2 * lane)
-                      : make_float2(0.f, 0.f);
-        if (k >= nb) e[u] = 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        acc.x = fmaf(e[u], x[u].x, acc.x);
-        acc.y = fmaf(e[u], x[u].y, acc.y);
+        for (int i = 0; i < V; ++i) x[u].v[i] = 0.f;
       }
     }
-  }
-  // the l partial sums live in warp 0's lanes
-  if (w == 0) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-  }
-  if (lane == 0) wl[w] = l;
-  wacc[w][lane] = acc;
-  __syncthreads();
-  if (w == 0) {
-    const float L = wl[0];
-    float2 o = wacc[0][lane];
+    for (int u = 0; u < kMergeBatch; ++u) {
+      // an empty state (m = -inf) gets weight 0: the identity, except that a
+      // NaN it carries (a bad piece) still reaches the result
+      const float nm = fmaxf(m, mp[u]);
+      const float sa = (m == -INFINITY) ? 0.f : ex2(m - nm);
+      const float sb = (mp[u] == -INFINITY) ? 0.f : ex2(mp[u] - nm);
+      l = l * sa + lp[u] * sb;
 #pragma unroll
-    for (int v = 1; v < NW; ++v) {
-      o.x += wacc[v][lane].x;
-      o.y += wacc[v][lane].y;
+      for (int i = 0; i < V; ++i) acc[i] = acc[i] * sa + x[u].v[i] * sb;
+      m = nm;
     }
-    float* dst = a.out + out_row * a.D + c * 64 + 2 * lane;
+  }
+  if (lane == 0) {
+    wm[w] = m;
+    wl[w] = l;
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i) wacc[w][lane * V + i] = acc[i];
+  __syncthreads();
+  // warp 0 folds the four warp states in order and writes the column
+  if (w == 0) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int v = 0; v < NW; ++v) M = fmaxf(M, wm[v]);
+    float L = 0.f;
+    float o[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) o[i] = 0.f;
+#pragma unroll
+    for (int v = 0; v < NW; ++v) {
+      const float e = (wm[v] == -INFINITY) ? 0.f : ex2(wm[v] - M);
+      L = fmaf(e, wl[v], L);
+#pragma unroll
+      for (int i = 0; i < V; ++i) o[i] = fmaf(e, wacc[v][lane * V + i], o[i]);
+    }
     // a column that saw no key (causal limit 0) gets 0; NaN passes through
-    *reinterpret_cast<float2*>(dst) = L == 0.f ? make_float2(0.f, 0.f) : make_float2(o.x / L, o.y / L);
+    float* dst = a.out + out_row * D + lane * V;
+#pragma unroll
+    for (int i = 0; i < V; ++i) dst[i] = L == 0.f ? 0.f : o[i] / L;
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs a) {
   // With programmatic dependent launch this grid may start while the split
   // kernel is finishing: wait until its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int seg = blockIdx.x, g = blockIdx.y, c = blockIdx.z;
-  const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas};
+  const int seg = blockIdx.x, g = blockIdx.y;
+  const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas, 0, 0};
   int4 desc = make_int4(-1, 0, 0, 0);
   if (a.part_blocks == 0) desc = a.ws_desc[seg];
   const MergeSeg ms = merge_segment(sched, seg, desc.x, desc.y, desc.z, desc.w, a.ws_pre);
@@ -126,11 +154,7 @@ __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs
     if (tok >= nq) return;  // the column holds no query (uniform over the block)
     out_row = (int64_t)(q0 + tok) * a.H + (int64_t)ms.j * a.G + g % a.G;
   }
-  // gridDim.z == D/64: one chunk per block; gridDim.z == 1: all chunks here
-  for (int cc = c; cc < a.D / 64; cc += gridDim.z) {
-    merge_segment_chunk(a, ms, g, cc, out_row);
-    __syncthreads();  // shared scratch reuse
-  }
+  merge_column<D>(a, ms, g, out_row);
 }
 
 // --------------------------------------------------------------- append
@@ -449,6 +473,7 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.maxblk = s->max_blocks_per_seq;
   a.P = s->num_blocks;
   a.part_blocks = p.part_blocks;
+  a.piece_k = p.part_blocks == 0 ? piece_units(s->block_size, s->head_dim) : 0;
   a.warps = p.warps;
   a.ring = p.ring;
   a.qscale = scale * 1.4426950408889634f;  // log2(e)
@@ -562,8 +587,7 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   const Plan& p = c->plan;
   const int nseg = p.part_blocks == 0 ? p.grid : c->sa.B * c->sa.Hkv;
   cudaLaunchConfig_t cfg = {};
-  // long heads get one block per 64-dim chunk (few segments, many pieces)
-  cfg.gridDim = dim3(nseg, p.C, p.D == 256 ? p.D / 64 : 1);
+  cfg.gridDim = dim3(nseg, p.C, 1);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -572,7 +596,10 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, pa_merge_kernel, c->ma);
+  cudaError_t e = cudaErrorInvalidValue;
+  if (p.D == 64) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<64>, c->ma);
+  if (p.D == 128) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<128>, c->ma);
+  if (p.D == 256) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<256>, c->ma);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -772,14 +799,15 @@ int pa_plan_pieces(const pa_shape* shape, const pa_options* options,
   const int B = shape->batch;
   const int part_blocks =
       (options && options->partition_tokens > 0) ? options->partition_tokens / shape->block_size : 0;
+  const int K = part_blocks == 0 ? piece_units(shape->block_size, shape->head_dim) : 0;
   int32_t* pre = new int32_t[B + 1];
   pre[0] = 0;
   for (int b = 0; b < B; ++b)
     pre[b + 1] = pre[b] + seq_count(seq_blocks(cache_seqlens_host[b], shape->block_size,
                                                shape->max_blocks_per_seq),
-                                    part_blocks);
-  const SchedShape sched{B, shape->num_kv_heads, shape->block_size, shape->max_blocks_per_seq,
-                         part_blocks, num_ctas};
+                                    part_blocks, K);
+  const SchedShape sched{B,           shape->num_kv_heads, shape->block_size, shape->max_blocks_per_seq,
+                         part_blocks, num_ctas,            0,                 K};
   PieceIter it;
   it.init(pre, HostLens{cache_seqlens_host, 0, shape->block_size, shape->max_blocks_per_seq},
           sched, cta);
@@ -813,14 +841,15 @@ int pa_plan_merge(const pa_shape* shape, const pa_options* options,
       (options && options->partition_tokens > 0) ? options->partition_tokens / shape->block_size : 0;
   const int nseg = part_blocks == 0 ? num_ctas : B * shape->num_kv_heads;
   if (seg >= nseg) return PA_ERR_OPTION;
+  const int K = part_blocks == 0 ? piece_units(shape->block_size, shape->head_dim) : 0;
   int32_t* pre = new int32_t[B + 1];
   pre[0] = 0;
   for (int b = 0; b < B; ++b)
     pre[b + 1] = pre[b] + seq_count(seq_blocks(cache_seqlens_host[b], shape->block_size,
                                                shape->max_blocks_per_seq),
-                                    part_blocks);
-  const SchedShape sched{B, shape->num_kv_heads, shape->block_size, shape->max_blocks_per_seq,
-                         part_blocks, num_ctas};
+                                    part_blocks, K);
+  const SchedShape sched{B,           shape->num_kv_heads, shape->block_size, shape->max_blocks_per_seq,
+                         part_blocks, num_ctas,            0,                 K};
   int32_t db = -1, dj = 0, dlast = 0, dslot = 0;
   if (part_blocks == 0 && !balanced_split_segment(pre, sched, seg, db, dj, dlast, dslot)) db = -1;
   const MergeSeg ms = merge_segment(sched, seg, db, dj, dlast, dslot, pre);

@@ -43,6 +43,7 @@ struct SplitArgs {
   uint32_t* status;         // sticky PA_STATUS_* bits
   int32_t B, H, Hkv, G, bs, maxblk, P;
   int32_t part_blocks;      // 0 = balanced split
+  int32_t piece_k;          // balanced split: overhead units per segment (pa_sched.cuh)
   int32_t warps;            // warps per CTA (= blockDim.x / 32)
   int32_t ring;             // TMA ring slots per warp
   float qscale;             // scale * log2(e): scores are kept in log2 units

@@ -8,13 +8,19 @@
 // sequence in decode; with several query tokens per sequence it is one
 // group of a sequence's query tokens, and len_b the keys that group reads.
 //
-// Balanced split (partition_tokens == 0): units are ordered (b, j, block);
-// CTA c of C_eff owns units [floor(U c / C_eff), floor(U (c+1) / C_eff)),
-// U = Hkv * sum_b nblk_b.  A CTA's range cuts at most two segments (its first
-// and its last piece), so each CTA writes at most two partial states:
-// slot 2c (the piece that starts at the CTA's first unit) and slot 2c+1 (the
-// CTA's last piece, when it is partial and not also the first).  A segment
-// that lies inside one CTA is finished there and written straight to `out`.
+// Balanced split (partition_tokens == 0): every non-empty segment is
+// charged K extra "overhead units" ahead of its blocks -- a piece costs a
+// fixed amount (publishing, folding and writing the warp states, loading the
+// next q) on top of its blocks, so a CTA that holds many short segments must
+// get fewer blocks.  Units are ordered (b, j, [K overhead units, blocks]);
+// CTA c of C_eff owns units [floor(V c / C_eff), floor(V (c+1) / C_eff)),
+// V = Hkv * sum_b (nblk_b + K [nblk_b > 0]), and processes the blocks in its
+// range.  A CTA's range cuts at most two segments (its first and its last
+// piece), so each CTA writes at most two partial states: slot 2c (its first
+// piece, when that continues a segment begun in an earlier CTA) and slot
+// 2c+1 (its last piece, when that begins here and continues past the range).
+// A segment that lies inside one CTA is finished there and written straight
+// to `out`.
 //
 // Fixed split (partition_tokens > 0, part_blocks = partition_tokens / bs):
 // segment (b, j) has np_b = ceil(nblk_b / part_blocks) partitions; items are
@@ -43,7 +49,17 @@ struct SchedShape {
   int32_t part_blocks;  // 0 = balanced
   int32_t num_ctas;     // launched persistent grid
   int32_t len_add;      // 1 when the step also appends each sequence's new token
+  int32_t K;            // balanced split: overhead units charged per segment
 };
+
+// Overhead units per segment of the balanced split: a piece's fixed cost
+// (about 3.5 us on GB300) in units of one block of one kv head (4 bs D bytes
+// of K and V, streamed at a CTA's ~44 GB/s share of HBM): about 160 KB worth.
+PA_HD int32_t piece_units(int32_t bs, int32_t D) {
+  const int32_t unit = 4 * bs * D;
+  const int32_t k = (160 * 1024 + unit / 2) / unit;
+  return k < 1 ? 1 : k;
+}
 
 // Blocks of a sequence; lengths outside [0, maxblk*bs] count as empty (the
 // kernels flag them separately).
@@ -64,9 +80,11 @@ PA_HD int32_t eff_len(int32_t stored, int32_t add, int32_t bs, int32_t maxblk) {
   return e > (int64_t)maxblk * bs ? -1 : (int32_t)e;
 }
 
-// Per-sequence count that the prefix sums run over.
-PA_HD int32_t seq_count(int32_t nblk, int32_t part_blocks) {
-  return part_blocks > 0 ? (nblk + part_blocks - 1) / part_blocks : nblk;
+// Per-row count that the prefix sums run over: partitions (fixed split), or
+// blocks plus the K overhead units of a non-empty segment (balanced split).
+PA_HD int32_t seq_count(int32_t nblk, int32_t part_blocks, int32_t K) {
+  if (part_blocks > 0) return (nblk + part_blocks - 1) / part_blocks;
+  return nblk > 0 ? nblk + K : 0;
 }
 
 // Largest b in [0, B) with mult * pre[b] <= x, for x < mult * pre[B]
@@ -156,20 +174,26 @@ struct PieceIterT {
     if (s.part_blocks == 0) {
       if (u >= u_end) return false;
       int32_t b = find_seq(pre, s.B, s.Hkv, u);
-      int32_t n = pre[b + 1] - pre[b];
+      int32_t n = pre[b + 1] - pre[b];  // K + blocks of each segment of row b
       int64_t r = u - (int64_t)s.Hkv * pre[b];
       int32_t j = (int32_t)(r / n);
-      int32_t blk0 = (int32_t)(r % n);
+      int32_t off = (int32_t)(r % n);
+      if (off < s.K) {  // the segment's overhead units: on to its first block
+        u += s.K - off;
+        off = s.K;
+        if (u >= u_end) return false;
+      }
+      const int32_t nb = n - s.K;
+      const int32_t blk0 = off - s.K;
       int64_t avail = u_end - u;
-      int32_t cnt = (int64_t)(n - blk0) < avail ? (n - blk0) : (int32_t)avail;
+      int32_t cnt = (int64_t)(nb - blk0) < avail ? (nb - blk0) : (int32_t)avail;
       p.b = b;
       p.j = j;
       p.blk0 = blk0;
       p.blk1 = blk0 + cnt;
-      if (blk0 == 0 && cnt == n)
-        p.slot = -1;
-      else
-        p.slot = 2 * cta + (u == u_begin ? 0 : 1);
+      const bool cont = blk0 > 0;          // begun in an earlier CTA
+      const bool past = blk0 + cnt < nb;   // continues in a later one
+      p.slot = (cont || past) ? 2 * cta + (cont ? 0 : 1) : -1;
       u += cnt;
       return true;
     }
@@ -212,11 +236,12 @@ PA_HD bool balanced_split_segment(const int32_t* pre, const SchedShape& s, int32
   int64_t r = last - (int64_t)s.Hkv * pre[b];
   j = (int32_t)(r / n);
   int64_t seg_begin = (int64_t)s.Hkv * pre[b] + (int64_t)j * n;
+  int64_t first_blk = seg_begin + s.K;  // unit of the segment's first block
   int64_t seg_end = seg_begin + n;
   if (seg_end <= u1) return false;     // finishes inside c
-  if (seg_begin < u0) return false;    // began in an earlier CTA
+  if (first_blk < u0 || first_blk >= u1) return false;  // its blocks do not begin in c
   c_last = balanced_cta_of(U, Ce, seg_end - 1);
-  slot = 2 * c + (seg_begin == u0 ? 0 : 1);
+  slot = 2 * c + 1;
   return true;
 }
 
@@ -232,7 +257,7 @@ struct MergeSeg {
   int64_t fbase;      // fixed: slot of partition 0
 
   PA_HD int64_t slot(int32_t p) const {
-    if (balanced) return p == 0 ? slot0 : 2 * (int64_t)(seg + p);
+    if (balanced) return p == 0 ? slot0 : 2 * (int64_t)(seg + p);  // slot0 = 2 seg + 1
     return fbase + (int64_t)p * Hkv;
   }
 };

@@ -69,7 +69,7 @@ __device__ __forceinline__ void build_prefix(const SplitArgs& a, const LenOf& le
   const int b0 = min(a.B, tid * per), b1 = min(a.B, b0 + per);
   int local = 0;
   for (int b = b0; b < b1; ++b)
-    local += seq_count(seq_blocks(len_of(b), a.bs, a.maxblk), a.part_blocks);
+    local += seq_count(seq_blocks(len_of(b), a.bs, a.maxblk), a.part_blocks, a.piece_k);
   // inclusive scan of `local` over the block
   const int lane = tid & 31, warp = tid >> 5;
   int x = local;
@@ -93,7 +93,7 @@ __device__ __forceinline__ void build_prefix(const SplitArgs& a, const LenOf& le
   int run = scratch[warp] + x - local;
   for (int b = b0; b < b1; ++b) {
     pre[b] = run;
-    run += seq_count(seq_blocks(len_of(b), a.bs, a.maxblk), a.part_blocks);
+    run += seq_count(seq_blocks(len_of(b), a.bs, a.maxblk), a.part_blocks, a.piece_k);
   }
   __syncthreads();
 }
@@ -715,7 +715,8 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   // The merge kernel may be scheduled now; it waits for this grid to finish.
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, (int32_t)gridDim.x, a.len_add};
+  const SchedShape sched{a.B,           a.Hkv,      a.bs,     a.maxblk,
+                         a.part_blocks, (int32_t)gridDim.x, a.len_add, a.piece_k};
   const int cta = blockIdx.x;
 
   // Rows with no key to read: out = 0; invalid length: NaN + status (with

@@ -160,11 +160,38 @@ def test_work_split_on_the_page_example():
         check_schedule([30, 32, 70], 2, 32, 4, 32, C)
 
 
+K_UNITS = {(16, 256): 10, (32, 128): 10, (16, 128): 20, (16, 64): 40}  # 160 KB / (4 bs d)
+
+
 def test_balanced_split_is_even():
+    # one long sequence: every CTA gets the same blocks, except that the CTA
+    # where a segment begins is also charged the segment's overhead units
     lens = [100_000]
     s = shape(B=1, H=24, Hkv=4, d=256, bs=16, maxblk=6250, P=6250, dtype=pg.PA_BF16)
     C = 304
     sizes = [sum(k1 - k0 for (_, _, k0, k1, _) in pg.pa_plan_pieces(s, None, lens, C, c))
              for c in range(C)]
     assert sum(sizes) == 4 * 6250
-    assert max(sizes) - min(sizes) <= 1
+    K = K_UNITS[(16, 256)]
+    assert max(sizes) - min(sizes) <= K + 1
+    assert sorted(sizes)[4] >= max(sizes) - 1  # only the 4 segment starts are short
+
+
+def test_balanced_split_charges_each_segment_its_overhead():
+    # 64 short sequences then one long one, 8 CTAs: the CTAs holding many
+    # segment starts get fewer blocks, and every CTA's blocks plus K units per
+    # segment it starts add up to the same load within one block
+    lens = [64] * 64 + [40_000]
+    s = shape(B=65, H=8, Hkv=1, d=128, bs=16, maxblk=2500, P=8000, dtype=pg.PA_BF16)
+    K = K_UNITS[(16, 128)]
+    C = 8
+    loads = []
+    for c in range(C):
+        pieces = pg.pa_plan_pieces(s, None, lens, C, c)
+        blocks = sum(k1 - k0 for (_, _, k0, k1, _) in pieces)
+        starts = sum(1 for (_, _, k0, _, _) in pieces if k0 == 0)
+        loads.append(blocks + K * starts)
+    assert max(loads) - min(loads) <= K + 1
+    first = sum(k1 - k0 for (_, _, k0, k1, _) in pg.pa_plan_pieces(s, None, lens, C, 0))
+    last = sum(k1 - k0 for (_, _, k0, k1, _) in pg.pa_plan_pieces(s, None, lens, C, C - 1))
+    assert first < last - 5 * K
