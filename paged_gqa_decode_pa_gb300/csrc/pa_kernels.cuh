@@ -142,6 +142,7 @@ struct SmemLayout {
   uint32_t mo, mm, ml, mbad;        // per-warp partial states for the CTA combine
   uint32_t qs;                      // [C][D+4] fp32 q * scale * log2(e) of the current piece
   uint32_t qlim;                    // [kColMax] int32 key limit per column (several tokens)
+  uint32_t qraw;                    // [C][D] raw 16-bit q of the next piece (cp.async target)
   uint32_t zrow;                    // one all-zero K/V row (D x 2 bytes)
   uint32_t nrow;                    // per warp: the appended token's K and V rows
   uint32_t ps;                      // CUDA-core path: p per warp
@@ -174,6 +175,8 @@ PA_HD SmemLayout split_smem_layout(int D, int C, int B, int W, int R, int mode) 
   off = align_up(off, 16);
   L.qs = off;
   off += (uint32_t)(C * (D + 4)) * 4u;
+  L.qraw = off;
+  off += (uint32_t)(C * D) * 2u;
   L.zrow = off;
   off += (uint32_t)D * 2u;
   L.nrow = off;

@@ -485,17 +485,24 @@ __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem,
   bool bad = false;
   for (int w = 0; w < W; ++w) bad |= (mbad[w] != 0);
   const float qnan = __int_as_float(0x7fc00000);
+  const int lane = threadIdx.x & 31, wl = lane & 7;
+  // The 32 elements a warp takes in one step share their column (D is a
+  // multiple of 32): lane w (w < W) computes warp w's weight 2^(m_w - M)
+  // once and the lanes share it by shuffles.
   for (int idx = threadIdx.x; idx < C * D; idx += blockDim.x) {
     const int c = idx / D, dim = idx % D;
-    float M = -INFINITY;
-    for (int w = 0; w < W; ++w) M = fmaxf(M, mm[w * kColMax + c]);
-    float Lsum = 0.f, o = 0.f;
-    for (int w = 0; w < W; ++w) {
-      const float mw = mm[w * kColMax + c];
-      const float e = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-      Lsum = fmaf(e, ml[w * kColMax + c], Lsum);
-      o = fmaf(e, mo[(w * C + c) * (D + 4) + dim], o);
-    }
+    const float mw = wl < W ? mm[wl * kColMax + c] : -INFINITY;
+    const float lw = wl < W ? ml[wl * kColMax + c] : 0.f;
+    float M = mw;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float e = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+    float Lsum = wl < W ? e * lw : 0.f;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
+    float o = 0.f;
+    for (int w = 0; w < W; ++w)
+      o = fmaf(__shfl_sync(0xffffffffu, e, w), mo[(w * C + c) * (D + 4) + dim], o);
     if (pc.slot < 0) {
       const int64_t r = column_out<kQ>(a, pc.b, pc.j, c, q0, nq);
       if (r >= 0) a.out[r * D + dim] = bad ? qnan : (Lsum == 0.f ? 0.f : o / Lsum);
@@ -593,49 +600,58 @@ __device__ __forceinline__ void issue_next(IssuerT<LenOf>& is, const SplitArgs& 
   ++is.issued;
 }
 
-// q' = q * scale * log2(e) of piece pc's C query columns into the shared
-// fp32 buffer (all threads).  The loads are issued first; `finish` stores
-// them.  kQ: column c is token g*tq + c/G (head c%G) of the row's sequence,
-// and `finish` also writes each column's key limit and the row's query span.
-template <int D, int NB, bool kQ>
-struct QPrefetch {
-  // words per thread, for >= 4 warps
-  static constexpr int kPer = (kGMax * NB * D / 2 + 32 * 4 - 1) / (32 * 4);
-  uint32_t v[kPer];
-  int32_t len;         // stored cache_seqlens of the piece's sequence
-  int32_t q0, nq, grp; // kQ: the sequence's query rows, the row's group
-  __device__ __forceinline__ void start(const SplitArgs& a, const Piece& pc) {
-    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q);
-    const int nw = a.C * D / 2;
+// The next piece's q, fetched while the current piece runs: its raw 16-bit
+// values are copied (cp.async) into the shared staging buffer qraw -- at
+// the start of the current piece in decode, after its tiles with several
+// query tokens (whose rows need the sequence's query span first) -- and at
+// the piece boundary `finish` turns them into q' = q * scale * log2(e) in
+// the fp32 buffer qs.  kQ: column c is token g*tq + c/G (head c%G) of the
+// row's sequence; `finish` also writes each column's key limit and the
+// row's query span.
+template <int D, bool kQ>
+struct QStage {
+  int32_t len;          // stored cache_seqlens of the piece's sequence
+  int32_t q0, nq, grp;  // kQ: the sequence's query rows, the row's group
+
+  __device__ __forceinline__ void start(const SplitArgs& a, const Piece& pc, uint32_t qraw) {
     if constexpr (!kQ) {
-      if (threadIdx.x == 0) len = __ldg(a.seqlens + pc.b);
-      const uint32_t* src = q32 + ((int64_t)pc.b * a.H + (int64_t)pc.j * a.G) * (D / 2);
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = threadIdx.x + k * blockDim.x;
-        v[k] = (i < nw) ? __ldg(src + i) : 0u;
-      }
+      len = __ldg(a.seqlens + pc.b);
+      const char* src =
+          reinterpret_cast<const char*>(a.q + ((int64_t)pc.b * a.H + (int64_t)pc.j * a.G) * D);
+      const int chunks = a.C * D / 8;  // 16-byte pieces of G contiguous rows
+      for (int i = threadIdx.x; i < chunks; i += blockDim.x)
+        cp_async16(qraw + 16u * i, src + 16 * (int64_t)i, 16u);
+      cp_async_commit();
     } else {
       const int seq = pc.b / a.nqg;
       grp = pc.b - seq * a.nqg;
       len = __ldg(a.seqlens + seq);
       query_span(a.cu_q, seq, a.total_q, a.max_q, q0, nq);
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const int i = threadIdx.x + k * blockDim.x;
-        uint32_t x = 0u;
-        if (i < nw) {
-          const int c = (2 * i) / D, d = (2 * i) % D;
-          const int tok = grp * a.tq + c / a.G;
-          if (tok < nq)
-            x = __ldg(q32 + (((int64_t)(q0 + tok) * a.H + (int64_t)pc.j * a.G + c % a.G) * D + d) / 2);
-        }
-        v[k] = x;
-      }
     }
   }
+
+  // kQ: the copies, once the span is known (columns without a query are
+  // zero-filled).
+  __device__ __forceinline__ void issue_copies(const SplitArgs& a, const Piece& pc, uint32_t qraw) {
+    constexpr int per_col = D / 8;
+    const int chunks = a.C * per_col;
+    for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
+      const int c = i / per_col, k = i - c * per_col;
+      const int tok = grp * a.tq + c / a.G;
+      const bool valid = tok < nq;
+      const char* src =
+          valid ? reinterpret_cast<const char*>(
+                      a.q + ((int64_t)(q0 + tok) * a.H + (int64_t)pc.j * a.G + c % a.G) * D) +
+                      16 * k
+                : reinterpret_cast<const char*>(a.q);
+      cp_async16(qraw + 16u * i, src, valid ? 16u : 0u);
+    }
+    cp_async_commit();
+  }
+
+  // After every thread's copies are complete and a barrier.
   template <typename T>
-  __device__ __forceinline__ void finish(const SplitArgs& a, float* qs, int32_t* info,
+  __device__ __forceinline__ void finish(const SplitArgs& a, uint32_t qraw, float* qs, int32_t* info,
                                          int32_t* qlim) {
     if (threadIdx.x == 0) {
       info[1] = len;
@@ -656,16 +672,13 @@ struct QPrefetch {
       }
     }
     const int nw = a.C * D / 2;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * blockDim.x;
-      if (i < nw) {
-        const int c = (2 * i) / D, d = (2 * i) % D;
-        float2 x;
-        x.x = Cvt<T>::low(v[k]) * a.qscale;
-        x.y = Cvt<T>::high(v[k]) * a.qscale;
-        *reinterpret_cast<float2*>(qs + c * (D + 4) + d) = x;
-      }
+    for (int i = threadIdx.x; i < nw; i += blockDim.x) {
+      const int c = (2 * i) / D, d = (2 * i) % D;
+      const uint32_t v = lds32(qraw + 4u * i);
+      float2 x;
+      x.x = Cvt<T>::low(v) * a.qscale;
+      x.y = Cvt<T>::high(v) * a.qscale;
+      *reinterpret_cast<float2*>(qs + c * (D + 4) + d) = x;
     }
   }
 };
@@ -778,11 +791,15 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   it.init(pre, len_of, sched, cta);
   Piece pc;
   bool have = it.next(pc);
+  const uint32_t qraw = base + L.qraw;
+  QStage<D, kQ> qn;
   if (have) {
-    QPrefetch<D, NB, kQ> qp;
-    qp.start(a, pc);
-    qp.template finish<T>(a, qs, piece_info, qlim);
+    qn.start(a, pc, qraw);
+    if constexpr (kQ) qn.issue_copies(a, pc, qraw);
+    cp_async_wait_all();
   }
+  __syncthreads();
+  if (have) qn.template finish<T>(a, qraw, qs, piece_info, qlim);
   __syncthreads();
   uint32_t slot = 0, phase = 0;  // ring slot to consume next; per-slot parity bits
   uint32_t consumed = 0;
@@ -796,6 +813,14 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     } else {
       sst.reset();
     }
+    // the next piece's q starts on its way now
+    Piece next;
+    bool more;
+    {
+      PieceIterT<RowLen> peek = it;
+      more = peek.next(next);
+    }
+    if (more) qn.start(a, next, qraw);
     bool bad = false;
     const int cnt = warp_tiles<W>(pc, sl, w);
     // fused append: the position of this sequence's new token; the warp
@@ -864,6 +889,9 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       issue_next<D, W>(is, a, &tmk, &tmv, base, L, w, slot, sl);
       slot = (slot + 1 == (uint32_t)R) ? 0u : slot + 1;
     }
+    if constexpr (kQ) {
+      if (more) qn.issue_copies(a, next, qraw);
+    }
     if constexpr (MODE != kSimt) {
       mst.bad |= bad;
       mst.publish(smem, L, w, a.C);
@@ -874,15 +902,10 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     // this piece's query span, read before the next piece's `finish` may
     // overwrite it
     const int q0 = kQ ? piece_info[2] : 0, nq = kQ ? piece_info[3] : 0;
+    cp_async_wait_all();  // this thread's copies of the next q have landed
     named_bar_sync(1, blockDim.x);
-    // start loading the next piece's q while this piece is being combined
-    Piece next;
-    PieceIterT<RowLen> peek = it;
-    const bool more = peek.next(next);
-    QPrefetch<D, NB, kQ> qp;
-    if (more) qp.start(a, next);
     combine_piece<D, kQ>(a, smem, L, pc, W, q0, nq);
-    if (more) qp.template finish<T>(a, qs, piece_info, qlim);
+    if (more) qn.template finish<T>(a, qraw, qs, piece_info, qlim);
     named_bar_sync(1, blockDim.x);
     have = it.next(pc);
   }
