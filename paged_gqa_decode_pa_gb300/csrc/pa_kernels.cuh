@@ -107,6 +107,10 @@ struct MultiLen {
   }
 };
 
+// Shared-memory room for a copy of SplitArgs.
+constexpr uint32_t kArgsBytes = 256;
+static_assert(sizeof(SplitArgs) <= kArgsBytes && sizeof(SplitArgs) % 4 == 0, "SplitArgs copy");
+
 struct MergeArgs {
   const int32_t* seqlens;
   float* out;
@@ -143,6 +147,7 @@ struct SmemLayout {
   uint32_t qs;                      // [C][D+4] fp32 q * scale * log2(e) of the current piece
   uint32_t qlim;                    // [kColMax] int32 key limit per column (several tokens)
   uint32_t qraw;                    // [C][D] raw 16-bit q of the next piece (cp.async target)
+  uint32_t args;                    // a copy of the SplitArgs, read by the once-per-piece code
   uint32_t zrow;                    // one all-zero K/V row (D x 2 bytes)
   uint32_t nrow;                    // per warp: the appended token's K and V rows
   uint32_t ps;                      // CUDA-core path: p per warp
@@ -177,6 +182,8 @@ PA_HD SmemLayout split_smem_layout(int D, int C, int B, int W, int R, int mode) 
   off += (uint32_t)(C * (D + 4)) * 4u;
   L.qraw = off;
   off += (uint32_t)(C * D) * 2u;
+  L.args = off;
+  off += kArgsBytes;
   L.zrow = off;
   off += (uint32_t)D * 2u;
   L.nrow = off;

@@ -550,11 +550,13 @@ __device__ __forceinline__ int32_t table_entry(const SplitArgs& a, const Piece& 
   return __ldg(a.table + (int64_t)seq * a.maxblk + pc.blk0 + (t >> sl));
 }
 
+// a: the arguments in the constant bank (read for every tile); pa: their
+// shared-memory copy (read when the issuer moves to the next piece).
 template <int D, int W, class LenOf>
 __device__ __forceinline__ void issue_next(IssuerT<LenOf>& is, const SplitArgs& a,
-                                           const CUtensorMap* tmk, const CUtensorMap* tmv,
-                                           uint32_t base, const SmemLayout& L, int w,
-                                           uint32_t slot, int sl) {
+                                           const SplitArgs& pa, const CUtensorMap* tmk,
+                                           const CUtensorMap* tmv, uint32_t base,
+                                           const SmemLayout& L, int w, uint32_t slot, int sl) {
   const int lane = threadIdx.x & 31;
   while (!is.done && is.i >= is.cnt) {
     if (!is.it.next(is.pc)) {
@@ -565,15 +567,15 @@ __device__ __forceinline__ void issue_next(IssuerT<LenOf>& is, const SplitArgs& 
     is.cnt = warp_tiles<W>(is.pc, sl, w);
     is.win = 0;
     is.len = is.it.len_of(is.pc.b);
-    is.seq = a.nqg > 1 ? is.pc.b / a.nqg : is.pc.b;
-    is.entry = table_entry<W>(a, is.pc, is.seq, is.cnt, lane, sl, w);
-    is.entry_next = table_entry<W>(a, is.pc, is.seq, is.cnt, 32 + lane, sl, w);
+    is.seq = pa.nqg > 1 ? is.pc.b / pa.nqg : is.pc.b;
+    is.entry = table_entry<W>(pa, is.pc, is.seq, is.cnt, lane, sl, w);
+    is.entry_next = table_entry<W>(pa, is.pc, is.seq, is.cnt, 32 + lane, sl, w);
   }
   if (is.done) return;
   if (is.i >= is.win + 32) {
     is.win += 32;
     is.entry = is.entry_next;
-    is.entry_next = table_entry<W>(a, is.pc, is.seq, is.cnt, is.win + 32 + lane, sl, w);
+    is.entry_next = table_entry<W>(pa, is.pc, is.seq, is.cnt, is.win + 32 + lane, sl, w);
   }
   const int32_t phys = __shfl_sync(0xffffffffu, is.entry, is.i - is.win);
   if (lane == 0) {
@@ -686,7 +688,7 @@ struct QStage {
 template <typename T, int D, int MODE>
 __global__ void __launch_bounds__(32 * split_warps(D), 1)
     pa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                    const SplitArgs a) {
+                    const __grid_constant__ SplitArgs a) {
   constexpr int W = split_warps(D);
   constexpr bool kQ = MODE == kMmaQ;
   constexpr int NB = mma_blocks(D, MODE);
@@ -719,6 +721,12 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // The code that runs once per piece reads the arguments from this shared
+  // copy: read from the constant bank after a long run of tiles, they can
+  // miss in the constant cache and wait microseconds behind the HBM stream.
+  SplitArgs* sa = reinterpret_cast<SplitArgs*>(smem + L.args);
+  for (int i = tid; i < (int)(sizeof(SplitArgs) / 4); i += blockDim.x)
+    reinterpret_cast<uint32_t*>(sa)[i] = reinterpret_cast<const uint32_t*>(&a)[i];
   for (int i = tid; i < D / 8; i += blockDim.x) sts128(base + L.zrow + 16u * i, make_uint4(0u, 0u, 0u, 0u));
   if (lane == 0) {
     tma_prefetch_desc(&tmk);
@@ -784,7 +792,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   is.seq = 0;
   is.issued = 0;
   is.done = false;
-  for (int r = 0; r < R; ++r) issue_next<D, W>(is, a, &tmk, &tmv, base, L, w, (uint32_t)r, sl);
+  for (int r = 0; r < R; ++r) issue_next<D, W>(is, a, *sa, &tmk, &tmv, base, L, w, (uint32_t)r, sl);
 
   // ---- the computing side
   PieceIterT<RowLen> it;
@@ -794,12 +802,12 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   const uint32_t qraw = base + L.qraw;
   QStage<D, kQ> qn;
   if (have) {
-    qn.start(a, pc, qraw);
-    if constexpr (kQ) qn.issue_copies(a, pc, qraw);
+    qn.start(*sa, pc, qraw);
+    if constexpr (kQ) qn.issue_copies(*sa, pc, qraw);
     cp_async_wait_all();
   }
   __syncthreads();
-  if (have) qn.template finish<T>(a, qraw, qs, piece_info, qlim);
+  if (have) qn.template finish<T>(*sa, qraw, qs, piece_info, qlim);
   __syncthreads();
   uint32_t slot = 0, phase = 0;  // ring slot to consume next; per-slot parity bits
   uint32_t consumed = 0;
@@ -820,7 +828,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       PieceIterT<RowLen> peek = it;
       more = peek.next(next);
     }
-    if (more) qn.start(a, next, qraw);
+    if (more) qn.start(*sa, next, qraw);
     bool bad = false;
     const int cnt = warp_tiles<W>(pc, sl, w);
     // fused append: the position of this sequence's new token; the warp
@@ -886,11 +894,11 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       __syncwarp();
       phase ^= 1u << slot;
       ++consumed;
-      issue_next<D, W>(is, a, &tmk, &tmv, base, L, w, slot, sl);
+      issue_next<D, W>(is, a, *sa, &tmk, &tmv, base, L, w, slot, sl);
       slot = (slot + 1 == (uint32_t)R) ? 0u : slot + 1;
     }
     if constexpr (kQ) {
-      if (more) qn.issue_copies(a, next, qraw);
+      if (more) qn.issue_copies(*sa, next, qraw);
     }
     if constexpr (MODE != kSimt) {
       mst.bad |= bad;
@@ -904,8 +912,8 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     const int q0 = kQ ? piece_info[2] : 0, nq = kQ ? piece_info[3] : 0;
     cp_async_wait_all();  // this thread's copies of the next q have landed
     named_bar_sync(1, blockDim.x);
-    combine_piece<D, kQ>(a, smem, L, pc, W, q0, nq);
-    if (more) qn.template finish<T>(a, qraw, qs, piece_info, qlim);
+    combine_piece<D, kQ>(*sa, smem, L, pc, W, q0, nq);
+    if (more) qn.template finish<T>(*sa, qraw, qs, piece_info, qlim);
     named_bar_sync(1, blockDim.x);
     have = it.next(pc);
   }
