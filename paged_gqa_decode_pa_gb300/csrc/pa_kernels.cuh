@@ -107,8 +107,10 @@ struct MultiLen {
   }
 };
 
-// Shared-memory room for a copy of SplitArgs.
+// Shared-memory room for a copy of SplitArgs, at a fixed offset after the
+// mbarriers and stage infos.
 constexpr uint32_t kArgsBytes = 256;
+constexpr uint32_t kArgsOffset = 1024;
 static_assert(sizeof(SplitArgs) <= kArgsBytes && sizeof(SplitArgs) % 4 == 0, "SplitArgs copy");
 
 struct MergeArgs {
@@ -162,7 +164,8 @@ PA_HD SmemLayout split_smem_layout(int D, int C, int B, int W, int R, int mode) 
   SmemLayout L;
   L.full = 0;
   L.info = 8 * kMaxSlots;
-  L.stage = 1024;
+  L.args = kArgsOffset;  // fixed, so it can be filled before the layout is known
+  L.stage = 2048;
   L.stage_bytes = 4u * (uint32_t)D * (uint32_t)kTile;  // K + V tiles, 2 bytes each
   uint32_t off = L.stage + (uint32_t)(W * R) * L.stage_bytes;
   L.mo = off;
@@ -182,8 +185,6 @@ PA_HD SmemLayout split_smem_layout(int D, int C, int B, int W, int R, int mode) 
   off += (uint32_t)(C * (D + 4)) * 4u;
   L.qraw = off;
   off += (uint32_t)(C * D) * 2u;
-  L.args = off;
-  off += kArgsBytes;
   L.zrow = off;
   off += (uint32_t)D * 2u;
   L.nrow = off;

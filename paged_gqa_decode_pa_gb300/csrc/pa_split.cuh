@@ -697,10 +697,19 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw_addr);
-  const int R = a.ring;
-  const SmemLayout L = split_smem_layout(D, a.C, a.B, W, R, MODE);
-
   const int tid = threadIdx.x;
+  // The code that runs once per piece reads the arguments -- and the layout
+  // offsets derived from them -- from this shared copy: read from the
+  // constant bank after a long run of tiles, they miss in the constant cache
+  // and wait microseconds behind the HBM stream.
+  SplitArgs* sa = reinterpret_cast<SplitArgs*>(smem + kArgsOffset);
+  for (int i = tid; i < (int)(sizeof(SplitArgs) / 4); i += blockDim.x)
+    reinterpret_cast<uint32_t*>(sa)[i] = reinterpret_cast<const uint32_t*>(&a)[i];
+  __syncthreads();
+  const SplitArgs& A = *sa;
+  const int R = a.ring;
+  const SmemLayout L = split_smem_layout(D, A.C, A.B, W, A.ring, MODE);
+
   const int warp = tid >> 5, lane = tid & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   int32_t* pre = reinterpret_cast<int32_t*>(smem + L.pre);
@@ -721,12 +730,6 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // The code that runs once per piece reads the arguments from this shared
-  // copy: read from the constant bank after a long run of tiles, they can
-  // miss in the constant cache and wait microseconds behind the HBM stream.
-  SplitArgs* sa = reinterpret_cast<SplitArgs*>(smem + L.args);
-  for (int i = tid; i < (int)(sizeof(SplitArgs) / 4); i += blockDim.x)
-    reinterpret_cast<uint32_t*>(sa)[i] = reinterpret_cast<const uint32_t*>(&a)[i];
   for (int i = tid; i < D / 8; i += blockDim.x) sts128(base + L.zrow + 16u * i, make_uint4(0u, 0u, 0u, 0u));
   if (lane == 0) {
     tma_prefetch_desc(&tmk);
@@ -816,7 +819,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   float* ps = reinterpret_cast<float*>(smem + L.ps) + w * kTile * kGMax;
   while (have) {
     if constexpr (MODE != kSimt) {
-      mst.load_q(qs, a.C, qlim);
+      mst.load_q(qs, A.C, qlim);
       mst.reset();
     } else {
       sst.reset();
@@ -902,7 +905,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     }
     if constexpr (MODE != kSimt) {
       mst.bad |= bad;
-      mst.publish(smem, L, w, a.C);
+      mst.publish(smem, L, w, A.C);
     } else {
       sst.bad |= bad;
       sst.publish(smem, L, w, a.G);
