@@ -425,6 +425,38 @@ int make_pool_map(CUtensorMap* map, const void* pool, const pa_shape* s) {
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// One 5-D map over both pools, for one copy per tile: dims (64, bs, D/64,
+// P*bs*Hkv, 2) with strides (row Hkv*D*2, chunk 128, "slot" D*2, pool
+// distance).  Coordinate (0, row, 0, phys*bs*Hkv + j, 0) with box (64, 16,
+// D/64, 1, 2) lands 16 rows of kv head j of block phys from the lower pool,
+// then the same rows from the other one -- the K chunks then the V chunks
+// of a stage, or V then K when the V pool has the lower address (*swap).
+// The slot and row dimensions alias (slot index phys*bs*Hkv + j plus row *
+// Hkv is the row's index in the pool), which only addresses rows of the
+// pools.  PA_ERR_SHAPE when the pools cannot be described this way (the
+// same buffer, a distance of 2^40 bytes or more, a slot index past int32).
+int make_kv_map(CUtensorMap* map, const void* k_pool, const void* v_pool, const pa_shape* s,
+                int* swap) {
+  const uint64_t D = (uint64_t)s->head_dim, Hkv = (uint64_t)s->num_kv_heads;
+  const uint64_t bs = (uint64_t)s->block_size, P = (uint64_t)s->num_blocks;
+  const uintptr_t k = reinterpret_cast<uintptr_t>(k_pool), v = reinterpret_cast<uintptr_t>(v_pool);
+  if (k == v) return PA_ERR_SHAPE;
+  const uint64_t dist = k < v ? v - k : k - v;
+  if (dist % 16 != 0 || dist >= (1ull << 40)) return PA_ERR_SHAPE;
+  if (P * bs * Hkv >= (1ull << 31)) return PA_ERR_SHAPE;
+  *swap = v < k ? 1 : 0;
+  cuuint64_t dims[5] = {64, bs, D / 64, P * bs * Hkv, 2};
+  cuuint64_t strides[4] = {Hkv * D * 2, 128, D * 2, dist};
+  cuuint32_t box[5] = {64, (cuuint32_t)kTile, (cuuint32_t)(D / 64), 1, 2};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUtensorMapDataType dt =
+      s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = g_encode(map, dt, 5, reinterpret_cast<void*>(k < v ? k : v), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_SHAPE;
+}
+
 struct Call {
   Plan plan;
   SplitArgs sa;
@@ -516,36 +548,49 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
 // work of a few microseconds per map, and a decode loop reuses its pools.
 struct MapEntry {
   const void* pool;
+  const void* pool2;  // the other pool of a map over both (nullptr: one pool)
   int32_t D, Hkv, bs, P, dtype;
+  int32_t rc, swap;   // encode result (a map over both pools may be impossible)
   alignas(64) CUtensorMap map;
 };
 constexpr int kMapCache = 32;
 MapEntry g_maps[kMapCache];
 int g_nmaps = 0, g_next_map = 0;
 
-int pool_map(CUtensorMap* out, const void* pool, const pa_shape* s) {
+// pool2 == nullptr: the map of one pool; otherwise the map over both pools
+// (make_kv_map), whose result code is cached too.
+int pool_map(CUtensorMap* out, const void* pool, const void* pool2, const pa_shape* s,
+             int* swap) {
   std::lock_guard<std::mutex> lk(g_mu);
   for (int i = 0; i < g_nmaps; ++i) {
     const MapEntry& e = g_maps[i];
-    if (e.pool == pool && e.D == s->head_dim && e.Hkv == s->num_kv_heads &&
+    if (e.pool == pool && e.pool2 == pool2 && e.D == s->head_dim && e.Hkv == s->num_kv_heads &&
         e.bs == s->block_size && e.P == s->num_blocks && e.dtype == s->dtype) {
-      *out = e.map;
-      return PA_OK;
+      if (e.rc == PA_OK) {
+        *out = e.map;
+        if (swap) *swap = e.swap;
+      }
+      return e.rc;
     }
   }
   MapEntry e;
   e.pool = pool;
+  e.pool2 = pool2;
   e.D = s->head_dim;
   e.Hkv = s->num_kv_heads;
   e.bs = s->block_size;
   e.P = s->num_blocks;
   e.dtype = s->dtype;
-  const int rc = make_pool_map(&e.map, pool, s);
-  if (rc) return rc;
+  e.swap = 0;
+  e.rc = pool2 ? make_kv_map(&e.map, pool, pool2, s, &e.swap) : make_pool_map(&e.map, pool, s);
+  if (e.rc != PA_OK && e.rc != PA_ERR_SHAPE) return e.rc;  // encoder failure: not cached
   const int slot = g_nmaps < kMapCache ? g_nmaps++ : (g_next_map++ % kMapCache);
   g_maps[slot] = e;
-  *out = e.map;
-  return PA_OK;
+  if (e.rc == PA_OK) {
+    *out = e.map;
+    if (swap) *swap = e.swap;
+  }
+  return e.rc;
 }
 
 int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cache, Call* c,
@@ -554,10 +599,20 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
   if (rc) return rc;
   alignas(64) CUtensorMap tmk;
   alignas(64) CUtensorMap tmv;
-  rc = pool_map(&tmk, k_cache, s);
-  if (rc) return rc;
-  rc = pool_map(&tmv, v_cache, s);
-  if (rc) return rc;
+  int swap = 0;
+  if (pool_map(&tmk, k_cache, v_cache, s, &swap) == PA_OK) {
+    // one copy per tile for K and V
+    c->sa.kv_fused = 1;
+    c->sa.kv_swap = swap;
+    tmv = tmk;
+  } else {
+    c->sa.kv_fused = 0;
+    c->sa.kv_swap = 0;
+    rc = pool_map(&tmk, k_cache, nullptr, s, nullptr);
+    if (rc) return rc;
+    rc = pool_map(&tmv, v_cache, nullptr, s, nullptr);
+    if (rc) return rc;
+  }
   const Plan& p = c->plan;
   cudaError_t e = cudaErrorInvalidValue;
 #define PA_LAUNCH(T, DD)                                                                        \

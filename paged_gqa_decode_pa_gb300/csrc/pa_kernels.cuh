@@ -57,6 +57,10 @@ struct SplitArgs {
   // columns of one row: G heads in decode; tq tokens x G heads with several
   // query tokens per sequence
   int32_t C;
+  // 1: one tensor map covers both pools (its last dimension, extent 2, steps
+  // from one pool to the other), so a tile's K and V rows come in one copy;
+  // kv_swap: the map starts at the V pool (V lands first in the stage)
+  int32_t kv_fused, kv_swap;
   // several query tokens per sequence (kMmaQ): B counts rows = sequences x
   // nqg groups of tq tokens; q and out are packed [total_q, H, D] rows and
   // sequence s owns rows cu_q[s] .. cu_q[s+1]-1

@@ -594,8 +594,13 @@ __device__ __forceinline__ void issue_next(IssuerT<LenOf>& is, const SplitArgs& 
       constexpr uint32_t chunk = kTile * 128u;
       mbar_arrive_expect_tx(full, L.stage_bytes);
       const uint32_t kdst = base + L.stage + gslot * L.stage_bytes;
-      tma_load_5d(kdst, tmk, full, 0, h * kTile, 0, is.pc.j, phys);
-      tma_load_5d(kdst + (D / 64) * chunk, tmv, full, 0, h * kTile, 0, is.pc.j, phys);
+      if (a.kv_fused) {
+        // one copy: (64 dims, 16 rows, D/64 chunks, one (block, kv head) slot, K and V)
+        tma_load_5d(kdst, tmk, full, 0, h * kTile, 0, phys * a.bs * a.Hkv + is.pc.j, 0);
+      } else {
+        tma_load_5d(kdst, tmk, full, 0, h * kTile, 0, is.pc.j, phys);
+        tma_load_5d(kdst + (D / 64) * chunk, tmv, full, 0, h * kTile, 0, is.pc.j, phys);
+      }
     }
   }
   ++is.i;
@@ -864,8 +869,9 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
           is.done = true;  // stop issuing after a timeout
         }
       } else if (valid > 0) {
-        const uint32_t kb = base + L.stage + gslot * L.stage_bytes;
-        const uint32_t vb = kb + NC * chunk;
+        const uint32_t sb = base + L.stage + gslot * L.stage_bytes;
+        const uint32_t kb = sb + (a.kv_swap ? NC * chunk : 0u);
+        const uint32_t vb = sb + (a.kv_swap ? 0u : NC * chunk);
         const int t = w + W * i;
         const int tok0 = (pc.blk0 + (t >> sl)) * a.bs + (t & ((1 << sl) - 1)) * kTile;
         int new_r = -1;

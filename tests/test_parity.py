@@ -131,6 +131,32 @@ def test_poison_and_determinism_on_ragged_batch(mode):
     assert np.array_equal(clean[5], np.zeros_like(clean[5]))  # empty sequence
 
 
+@pytest.mark.parametrize("layout", ["v_below_k", "same_buffer"])
+def test_pool_placement_does_not_matter(layout):
+    # K and V normally come in one copy per tile through a map spanning both
+    # pools; it must give the same result when the V pool sits below the K
+    # pool, and the two-map path must serve K and V sharing one buffer.
+    w = wl.random_workload([300, 77, 1, 512], H=8, Hkv=2, d=128, bs=32, dtype="bf16", seed=31)
+    ref_w = wl.random_workload([300, 77, 1, 512], H=8, Hkv=2, d=128, bs=32, dtype="bf16", seed=31)
+    if layout == "same_buffer":
+        w.v_cache = w.k_cache.copy()
+        ref_w.v_cache = ref_w.k_cache.copy()
+    q, k, v, t, sl = w.torch_tensors("cuda")
+    if layout == "v_below_k":
+        both = torch.empty((2,) + tuple(k.shape), dtype=k.dtype, device="cuda")
+        both[0].copy_(v)
+        both[1].copy_(k)
+        v, k = both[0], both[1]
+        assert v.data_ptr() < k.data_ptr()
+    else:
+        v = k
+    out = torch.full((w.B, w.H, w.d), float("nan"), dtype=torch.float32, device="cuda")
+    ws = pg.alloc_workspace(pg.shape_of(q, k, t))
+    pg.pa_decode(q, k, v, t, sl, w.scale, out, ws)
+    assert pg.pa_read_status(ws) == 0
+    assert_close(out.cpu().numpy().astype(np.float64), run_oracle(ref_w), layout)
+
+
 def test_empty_and_full_sequences():
     # all empty; and one sequence that fills every table column
     w = wl.random_workload([0, 0, 0], H=8, Hkv=2, d=64, bs=16, dtype="f16", seed=7, maxblk=3)
