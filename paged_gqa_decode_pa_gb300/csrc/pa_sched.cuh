@@ -52,12 +52,13 @@ struct SchedShape {
   int32_t K;            // balanced split: overhead units charged per segment
 };
 
-// Overhead units per segment of the balanced split: a piece's fixed cost
-// (about 3.5 us on GB300) in units of one block of one kv head (4 bs D bytes
-// of K and V, streamed at a CTA's ~44 GB/s share of HBM): about 160 KB worth.
+// Overhead units per segment of the balanced split: a piece's fixed cost in
+// units of one block of one kv head (4 bs D bytes of K and V).  Measured
+// best on GB300 at about 200 KB worth (a sweep of 0 to 320 KB on the serving
+// and prefix-sharing steps).
 PA_HD int32_t piece_units(int32_t bs, int32_t D) {
   const int32_t unit = 4 * bs * D;
-  const int32_t k = (160 * 1024 + unit / 2) / unit;
+  const int32_t k = (200 * 1024 + unit / 2) / unit;
   return k < 1 ? 1 : k;
 }
 

@@ -160,7 +160,7 @@ def test_work_split_on_the_page_example():
         check_schedule([30, 32, 70], 2, 32, 4, 32, C)
 
 
-K_UNITS = {(16, 256): 10, (32, 128): 10, (16, 128): 20, (16, 64): 40}  # 160 KB / (4 bs d)
+K_UNITS = {(16, 256): 13, (32, 128): 13, (16, 128): 25, (16, 64): 50}  # 200 KB / (4 bs d)
 
 
 def test_balanced_split_is_even():
