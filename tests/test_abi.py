@@ -180,7 +180,8 @@ def test_balanced_split_is_even():
 def test_balanced_split_charges_each_segment_its_overhead():
     # 64 short sequences then one long one, 8 CTAs: the CTAs holding many
     # segment starts get fewer blocks, and every CTA's blocks plus K units per
-    # segment it starts add up to the same load within one block
+    # segment it starts add up to the same load -- within 2K + 1, since a
+    # range may begin or end inside a segment's overhead units
     lens = [64] * 64 + [40_000]
     s = shape(B=65, H=8, Hkv=1, d=128, bs=16, maxblk=2500, P=8000, dtype=pg.PA_BF16)
     K = K_UNITS[(16, 128)]
@@ -191,7 +192,7 @@ def test_balanced_split_charges_each_segment_its_overhead():
         blocks = sum(k1 - k0 for (_, _, k0, k1, _) in pieces)
         starts = sum(1 for (_, _, k0, _, _) in pieces if k0 == 0)
         loads.append(blocks + K * starts)
-    assert max(loads) - min(loads) <= K + 1
+    assert max(loads) - min(loads) <= 2 * K + 1
     first = sum(k1 - k0 for (_, _, k0, k1, _) in pg.pa_plan_pieces(s, None, lens, C, 0))
     last = sum(k1 - k0 for (_, _, k0, k1, _) in pg.pa_plan_pieces(s, None, lens, C, C - 1))
     assert first < last - 5 * K
