@@ -751,8 +751,8 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   // Rows with no key to read: out = 0; invalid length: NaN + status (with
   // the fused append also "no slot": nothing is written for them).
   for (int b = cta; b < a.B; b += gridDim.x) {
+    if (pre[b + 1] != pre[b]) continue;  // has blocks: no global read needed
     const int32_t len = len_of(b);
-    if (seq_blocks(len, a.bs, a.maxblk) != 0) continue;
     const bool ok = len >= 0;
     const float v = ok ? 0.f : __int_as_float(0x7fc00000);
     if constexpr (!kQ) {
@@ -772,11 +772,10 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       for (int i = tid; i < cnt * a.H * D; i += blockDim.x) rows[i] = v;
     }
   }
+  // prefix sums for the merge kernel (only the fixed split's merge reads them)
+  if (cta == 0 && a.part_blocks > 0)
+    for (int b = tid; b <= a.B; b += blockDim.x) a.ws_pre[b] = pre[b];
   if (tid == 0) {
-    if (cta == 0) {
-      // prefix sums for the merge kernel
-      for (int b = 0; b <= a.B; ++b) a.ws_pre[b] = pre[b];
-    }
     if (a.part_blocks == 0) {
       int32_t b, j, c_last, slot;
       int4 desc = make_int4(-1, 0, 0, 0);
@@ -789,6 +788,19 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   const int sl = a.bs == 16 ? 0 : (a.bs == 32 ? 1 : 2);  // log2(16-token tiles per block)
   constexpr int NC = D / 64;
   constexpr uint32_t chunk = kTile * 128u;
+
+  // ---- the first piece's q: its copy starts first, so that its latency
+  // overlaps the block-table reads of the ring's first tiles
+  PieceIterT<RowLen> it;
+  it.init(pre, len_of, sched, cta);
+  Piece pc;
+  bool have = it.next(pc);
+  const uint32_t qraw = base + L.qraw;
+  QStage<D, kQ> qn;
+  if (have) {
+    qn.start(*sa, pc, qraw);
+    if constexpr (kQ) qn.issue_copies(*sa, pc, qraw);
+  }
 
   // ---- the warp's issuing side: prime the ring with the first R tiles
   IssuerT<RowLen> is;
@@ -803,17 +815,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   for (int r = 0; r < R; ++r) issue_next<D, W>(is, a, *sa, &tmk, &tmv, base, L, w, (uint32_t)r, sl);
 
   // ---- the computing side
-  PieceIterT<RowLen> it;
-  it.init(pre, len_of, sched, cta);
-  Piece pc;
-  bool have = it.next(pc);
-  const uint32_t qraw = base + L.qraw;
-  QStage<D, kQ> qn;
-  if (have) {
-    qn.start(*sa, pc, qraw);
-    if constexpr (kQ) qn.issue_copies(*sa, pc, qraw);
-    cp_async_wait_all();
-  }
+  if (have) cp_async_wait_all();
   __syncthreads();
   if (have) qn.template finish<T>(*sa, qraw, qs, piece_info, qlim);
   __syncthreads();
