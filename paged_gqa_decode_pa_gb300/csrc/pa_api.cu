@@ -29,7 +29,7 @@ namespace {
 // four warp states are then folded in a fixed order, so the result is
 // deterministic.  The loads of up to kMergeBatch pieces are issued before
 // any of them is folded, so a segment of many pieces costs few round trips.
-constexpr int kMergeBatch = 8;
+constexpr int kMergeBatch = 16;
 
 template <int V>
 struct Vec {
