@@ -150,7 +150,7 @@ struct SmemLayout {
   uint32_t stage;                   // [W][R] stages: K chunks | V chunks, 16 rows each
   uint32_t stage_bytes;
   uint32_t mo, mm, ml, mbad;        // per-warp partial states for the CTA combine
-  uint32_t qs;                      // [C][D+4] fp32 q * scale * log2(e) of the current piece
+  uint32_t qs;                      // [C][D+4] fp32 q of the current piece (x scale*log2(e): CUDA cores)
   uint32_t qlim;                    // [kColMax] int32 key limit per column (several tokens)
   uint32_t qraw;                    // [C][D] raw 16-bit q of the next piece (cp.async target)
   uint32_t args;                    // a copy of the SplitArgs, read by the once-per-piece code

@@ -102,18 +102,22 @@ __device__ __forceinline__ void build_prefix(const SplitArgs& a, const LenOf& le
 
 template <typename T, int D, int NB, bool kQ>
 struct MmaState {
-  uint32_t qh[NB][D / 16][2], ql[NB][D / 16][2];  // B fragments of Q' (hi / lo)
+  uint32_t qf[NB][D / 16][2];  // B fragments of q (the 16-bit values, exact)
+  float qsc;                   // scale * log2(e), applied to the fp32 scores
   float o[NB][D / 16][4];                         // O^T accumulators
   float m[NB][2], l[NB][2];                       // columns 8nb + 2t, 8nb + 2t + 1 of this lane
   int32_t lim[NB][2];                             // kQ: key limit of those columns
   bool bad;
 
-  // B fragments of q' = q * scale * log2(e) for the 8 NB columns, from the
-  // CTA's shared fp32 copy qs [C][D+4] (columns >= C are zero).  kQ: also
-  // the columns' key limits (tokens t < lim are visible).
-  __device__ __forceinline__ void load_q(const float* qs, int C, const int32_t* qlim) {
+  // B fragments of q for the 8 NB columns, from the CTA's shared fp32 copy
+  // qs [C][D+4] of the 16-bit values (columns >= C are zero); packing them
+  // back to 16 bits is exact, so the scores K.q come out of the mma with fp32
+  // accumulation and only then take the factor scale * log2(e).  kQ: also the
+  // columns' key limits (tokens t < lim are visible).
+  __device__ __forceinline__ void load_q(const float* qs, int C, const int32_t* qlim, float qscale) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
+    qsc = qscale;
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
       const int col = nb * 8 + g;
@@ -123,14 +127,12 @@ struct MmaState {
       for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          uint32_t hi = 0, lo = 0;
+          uint32_t v = 0;
           if (live) {
             const float2 x = *reinterpret_cast<const float2*>(qrow + ks * 16 + half * 8 + 2 * t);
-            hi = Cvt<T>::pack(x.x, x.y);
-            lo = Cvt<T>::pack(x.x - Cvt<T>::low(hi), x.y - Cvt<T>::high(hi));
+            v = Cvt<T>::pack(x.x, x.y);
           }
-          qh[nb][ks][half] = hi;
-          ql[nb][ks][half] = lo;
+          qf[nb][ks][half] = v;
         }
       }
       if constexpr (kQ) {
@@ -167,8 +169,8 @@ struct MmaState {
                                        uint32_t nk, uint32_t nv, uint32_t zrow) {
     const int lane = threadIdx.x & 31;
     constexpr uint32_t chunk = kTile * 128u;
-    // ---- S^T = K . Q'^T  (rows: the 16 tokens, cols: query columns); four
-    // independent accumulator chains per block (hi/lo x even/odd k-step)
+    // ---- S^T = K . q^T  (rows: the 16 tokens, cols: query columns); four
+    // independent accumulator chains per block (k-step mod 4)
     float acc4[NB][4][4] = {};
     {
       const uint32_t tok = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -183,8 +185,7 @@ struct MmaState {
         ldmatrix_x4(addr, a0, a1, a2, a3);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          mma_16816<T>(acc4[nb][ks & 1], a0, a1, a2, a3, qh[nb][ks][0], qh[nb][ks][1]);
-          mma_16816<T>(acc4[nb][2 + (ks & 1)], a0, a1, a2, a3, ql[nb][ks][0], ql[nb][ks][1]);
+          mma_16816<T>(acc4[nb][ks & 3], a0, a1, a2, a3, qf[nb][ks][0], qf[nb][ks][1]);
         }
       }
     }
@@ -192,10 +193,10 @@ struct MmaState {
     uint32_t bh0[NB], bh1[NB], bl0[NB], bl1[NB];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-      float s0 = (acc4[nb][0][0] + acc4[nb][1][0]) + (acc4[nb][2][0] + acc4[nb][3][0]);
-      float s1 = (acc4[nb][0][1] + acc4[nb][1][1]) + (acc4[nb][2][1] + acc4[nb][3][1]);
-      float s2 = (acc4[nb][0][2] + acc4[nb][1][2]) + (acc4[nb][2][2] + acc4[nb][3][2]);
-      float s3 = (acc4[nb][0][3] + acc4[nb][1][3]) + (acc4[nb][2][3] + acc4[nb][3][3]);
+      float s0 = ((acc4[nb][0][0] + acc4[nb][1][0]) + (acc4[nb][2][0] + acc4[nb][3][0])) * qsc;
+      float s1 = ((acc4[nb][0][1] + acc4[nb][1][1]) + (acc4[nb][2][1] + acc4[nb][3][1])) * qsc;
+      float s2 = ((acc4[nb][0][2] + acc4[nb][1][2]) + (acc4[nb][2][2] + acc4[nb][3][2])) * qsc;
+      float s3 = ((acc4[nb][0][3] + acc4[nb][1][3]) + (acc4[nb][2][3] + acc4[nb][3][3])) * qsc;
       if (tr >= valid) s0 = s1 = -INFINITY;
       if (tr + 8 >= valid) s2 = s3 = -INFINITY;
       if constexpr (kQ) {
@@ -611,8 +612,9 @@ __device__ __forceinline__ void issue_next(IssuerT<LenOf>& is, const SplitArgs& 
 // values are copied (cp.async) into the shared staging buffer qraw -- at
 // the start of the current piece in decode, after its tiles with several
 // query tokens (whose rows need the sequence's query span first) -- and at
-// the piece boundary `finish` turns them into q' = q * scale * log2(e) in
-// the fp32 buffer qs.  kQ: column c is token g*tq + c/G (head c%G) of the
+// the piece boundary `finish` widens them to fp32 in the buffer qs (times
+// scale * log2(e) on the CUDA-core path; the tensor-core path applies that
+// factor to the scores).  kQ: column c is token g*tq + c/G (head c%G) of the
 // row's sequence; `finish` also writes each column's key limit and the
 // row's query span.
 template <int D, bool kQ>
@@ -657,7 +659,7 @@ struct QStage {
   }
 
   // After every thread's copies are complete and a barrier.
-  template <typename T>
+  template <typename T, bool kScaled>
   __device__ __forceinline__ void finish(const SplitArgs& a, uint32_t qraw, float* qs, int32_t* info,
                                          int32_t* qlim) {
     if (threadIdx.x == 0) {
@@ -683,8 +685,12 @@ struct QStage {
       const int c = (2 * i) / D, d = (2 * i) % D;
       const uint32_t v = lds32(qraw + 4u * i);
       float2 x;
-      x.x = Cvt<T>::low(v) * a.qscale;
-      x.y = Cvt<T>::high(v) * a.qscale;
+      x.x = Cvt<T>::low(v);
+      x.y = Cvt<T>::high(v);
+      if constexpr (kScaled) {
+        x.x *= a.qscale;
+        x.y *= a.qscale;
+      }
       *reinterpret_cast<float2*>(qs + c * (D + 4) + d) = x;
     }
   }
@@ -817,7 +823,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   // ---- the computing side
   if (have) cp_async_wait_all();
   __syncthreads();
-  if (have) qn.template finish<T>(*sa, qraw, qs, piece_info, qlim);
+  if (have) qn.template finish<T, MODE == kSimt>(*sa, qraw, qs, piece_info, qlim);
   __syncthreads();
   uint32_t slot = 0, phase = 0;  // ring slot to consume next; per-slot parity bits
   uint32_t consumed = 0;
@@ -826,7 +832,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   float* ps = reinterpret_cast<float*>(smem + L.ps) + w * kTile * kGMax;
   while (have) {
     if constexpr (MODE != kSimt) {
-      mst.load_q(qs, A.C, qlim);
+      mst.load_q(qs, A.C, qlim, A.qscale);
       mst.reset();
     } else {
       sst.reset();
@@ -924,7 +930,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     cp_async_wait_all();  // this thread's copies of the next q have landed
     named_bar_sync(1, blockDim.x);
     combine_piece<D, kQ>(*sa, smem, L, pc, W, q0, nq);
-    if (more) qn.template finish<T>(*sa, qraw, qs, piece_info, qlim);
+    if (more) qn.template finish<T, MODE == kSimt>(*sa, qraw, qs, piece_info, qlim);
     named_bar_sync(1, blockDim.x);
     have = it.next(pc);
   }
