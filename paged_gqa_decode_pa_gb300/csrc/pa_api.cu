@@ -8,6 +8,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pa_kernels.cuh"
@@ -132,15 +133,71 @@ __device__ __forceinline__ void merge_column(const MergeArgs& a, const MergeSeg&
   }
 }
 
+// Balanced split: which segment merge CTA `blockIdx.x` takes.  The segments
+// with more than one piece are the split CTAs whose descriptor is set; the
+// CTA takes the k-th of them in CTA order, k = blockIdx.x / C, so the CTAs
+// that have work are the first ones of the grid and start in its first wave.
+// Returns false when fewer than k + 1 segments have pieces to merge.
+__device__ __forceinline__ bool find_segment(const MergeArgs& a, int k, int& seg, int4& desc) {
+  constexpr int NW = kMergeThreads / 32;
+  constexpr int kPre = 4;  // descriptor chunks loaded before the scan
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  __shared__ int wcount[NW];
+  __shared__ int found_seg;
+  __shared__ int4 found_desc;
+  if (tid == 0) found_seg = -1;
+  int4 pre[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int c = i * kMergeThreads + tid;
+    pre[i] = c < a.num_ctas ? a.ws_desc[c] : make_int4(-1, 0, 0, 0);
+  }
+  int base = 0;  // segments found in the chunks before
+  for (int i = 0; i * kMergeThreads < a.num_ctas; ++i) {
+    const int c = i * kMergeThreads + tid;
+    int4 d = make_int4(-1, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < kPre; ++u)
+      if (u == i) d = pre[u];
+    if (i >= kPre && c < a.num_ctas) d = a.ws_desc[c];
+    const bool has = d.x >= 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, has);
+    if (lane == 0) wcount[w] = __popc(bal);
+    __syncthreads();
+    int before = base, total = 0;
+#pragma unroll
+    for (int v = 0; v < NW; ++v) {
+      before += v < w ? wcount[v] : 0;
+      total += wcount[v];
+    }
+    if (has && before + __popc(bal & ((1u << lane) - 1u)) == k) {
+      found_seg = c;
+      found_desc = d;
+    }
+    __syncthreads();  // found_* written; wcount free for the next chunk
+    base += total;
+    if (base > k) break;  // uniform over the block
+  }
+  seg = found_seg;
+  desc = found_desc;
+  return seg >= 0;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs a) {
   // With programmatic dependent launch this grid may start while the split
   // kernel is finishing: wait until its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int seg = blockIdx.x, g = blockIdx.y;
   const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas, 0, 0};
+  int seg, g;
   int4 desc = make_int4(-1, 0, 0, 0);
-  if (a.part_blocks == 0) desc = a.ws_desc[seg];
+  if (a.part_blocks == 0) {
+    g = blockIdx.x % a.C;
+    if (!find_segment(a, blockIdx.x / a.C, seg, desc)) return;
+  } else {
+    seg = blockIdx.x;  // segment (b, j) = (seg / Hkv, seg % Hkv)
+    g = blockIdx.y;
+  }
   const MergeSeg ms = merge_segment(sched, seg, desc.x, desc.y, desc.z, desc.w, a.ws_pre);
   if (ms.np == 0) return;
   // the output row of column g: head j*G + g of sequence b (decode), or
@@ -640,9 +697,12 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
 // split kernel drains; griddepcontrol.wait orders the reads).
 int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   const Plan& p = c->plan;
-  const int nseg = p.part_blocks == 0 ? p.grid : c->sa.B * c->sa.Hkv;
+  // balanced split: one CTA per (segment with pieces to merge, column); such
+  // segments continue past a split CTA, so there are fewer than the split
+  // CTAs and at most one per row.  Fixed split: one per (row, column).
+  const int rows = c->sa.B * c->sa.Hkv;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nseg, p.C, 1);
+  cfg.gridDim = p.part_blocks == 0 ? dim3(std::min(p.grid, rows) * p.C, 1, 1) : dim3(rows, p.C, 1);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

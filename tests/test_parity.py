@@ -117,6 +117,23 @@ def test_reduced_settings(name, kw, mode):
         assert_close(got, ref, f"{name} {mode} part={part} ctas={ctas}")
 
 
+def test_more_merged_segments_than_the_preloaded_descriptors():
+    """With many short rows and a large grid, most rows continue past a split
+    CTA: more than 512 segments have pieces to merge, so the merge CTAs'
+    search for their segment runs past the descriptor chunks it preloads."""
+    rng = np.random.default_rng(77)
+    lens = rng.integers(600, 1200, 400).astype(np.int32)
+    w = wl.random_workload(lens, H=4, Hkv=2, d=64, bs=16, dtype="f16", seed=78)
+    o = pg.options(num_ctas=1200)
+    s = pg.pa_shape(w.B, w.H, w.Hkv, w.d, w.block_size, w.max_blocks_per_seq, w.num_blocks,
+                    pg.PA_F16)
+    merged = sum(pg.pa_plan_merge(s, o, lens, 1200, c) is not None for c in range(1200))
+    assert merged > 512
+    got, st = run_gpu(w, o)
+    assert st == 0
+    assert_close(got, run_oracle(w), "1200 CTAs")
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_poison_and_determinism_on_ragged_batch(mode):
     lens = [1, 15, 16, 17, 100, 0, 255, 1024]
