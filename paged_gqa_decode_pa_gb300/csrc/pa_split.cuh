@@ -593,14 +593,15 @@ __device__ __forceinline__ void issue_next(IssuerT<LenOf>& is, const SplitArgs& 
       mbar_arrive(full);
     } else {
       constexpr uint32_t chunk = kTile * 128u;
+      const uint64_t pol = l2_evict_first_policy();  // K/V rows are read once per step
       mbar_arrive_expect_tx(full, L.stage_bytes);
       const uint32_t kdst = base + L.stage + gslot * L.stage_bytes;
       if (a.kv_fused) {
         // one copy: (64 dims, 16 rows, D/64 chunks, one (block, kv head) slot, K and V)
-        tma_load_5d(kdst, tmk, full, 0, h * kTile, 0, phys * a.bs * a.Hkv + is.pc.j, 0);
+        tma_load_5d(kdst, tmk, full, 0, h * kTile, 0, phys * a.bs * a.Hkv + is.pc.j, 0, pol);
       } else {
-        tma_load_5d(kdst, tmk, full, 0, h * kTile, 0, is.pc.j, phys);
-        tma_load_5d(kdst + (D / 64) * chunk, tmv, full, 0, h * kTile, 0, is.pc.j, phys);
+        tma_load_5d(kdst, tmk, full, 0, h * kTile, 0, is.pc.j, phys, pol);
+        tma_load_5d(kdst + (D / 64) * chunk, tmv, full, 0, h * kTile, 0, is.pc.j, phys, pol);
       }
     }
   }
