@@ -418,15 +418,22 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.mark_begin()
+    # With the L2 flushed between steps, each step is bracketed by its own
+    # events (the flush stays outside); otherwise only the first and the
+    # last, so that consecutive steps stay back to back on the stream (the
+    # split kernel is a programmatic dependent of the previous merge, and an
+    # event in between would serialise them).
     for i in range(K):
         if flush:
             scratch.fill_(1.0)
-        ev[i][0].record(stream)
+        if flush or i == 0:
+            ev[i][0].record(stream)
         if graph is not None:
             graph.replay()
         else:
             decode_step()
-        ev[i][1].record(stream)
+        if flush or i == K - 1:
+            ev[i][1].record(stream)
     torch.cuda.synchronize()
     sampler.mark_end()
     if world > 1:

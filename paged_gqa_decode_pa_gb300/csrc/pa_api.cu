@@ -185,6 +185,9 @@ __device__ __forceinline__ bool find_segment(const MergeArgs& a, int k, int& seg
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs a) {
+  // The next kernel on the stream (the next step's split kernel) may be
+  // scheduled now: it waits for this grid to finish before touching memory.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // With programmatic dependent launch this grid may start while the split
   // kernel is finishing: wait until its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");

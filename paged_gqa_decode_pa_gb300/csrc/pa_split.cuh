@@ -747,6 +747,13 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
   }
+  // Launched as a programmatic dependent of the kernel before it on the
+  // stream, this grid may be resident while that kernel finishes: nothing
+  // above touches global memory; from here on, that kernel's writes (q,
+  // tables, lengths, the pools; the previous merge's reads of the workspace
+  // are done) are complete and visible.  Without such a launch this returns
+  // at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   build_prefix(a, len_of, pre, scan_scratch);  // contains __syncthreads
   // The merge kernel may be scheduled now; it waits for this grid to finish.
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -951,8 +958,20 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
 template <typename T, int D, int MODE>
 cudaError_t launch_split(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a,
                          int grid, int threads, size_t smem, cudaStream_t stream) {
-  pa_split_kernel<T, D, MODE><<<grid, threads, smem, stream>>>(tmk, tmv, a);
-  return cudaGetLastError();
+  // a programmatic dependent of the previous kernel on the stream: its CTAs
+  // may be scheduled (and run up to griddepcontrol.wait) while that kernel
+  // drains, which hides the launch gap between consecutive decode steps
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pa_split_kernel<T, D, MODE>, tmk, tmv, a);
 }
 
 template <typename T, int D, int MODE>
