@@ -39,7 +39,9 @@
  *       out            [B, H, d]            float32
  *       k_new, v_new   [B, Hkv, d]          dt
  *   - Supported: d in {64, 128, 256}; bs in {16, 32, 64}; H % Hkv == 0 and
- *     G = H / Hkv <= 8; 0 <= B <= PA_MAX_BATCH (B == 0 is a no-op).
+ *     G = H / Hkv <= 8; 0 <= B <= PA_MAX_BATCH (B == 0 is a no-op);
+ *     max_blocks_per_seq * bs, B * max_blocks_per_seq and
+ *     Hkv * (max_blocks_per_seq + 64) below 2^31 (else PA_ERR_SHAPE).
  *   - Work is enqueued on `stream` (NULL = legacy default stream).  No entry
  *     point synchronises, allocates, or picks a launch shape from device
  *     data, so pa_decode and pa_cache_append can be captured in a CUDA graph

@@ -283,6 +283,8 @@ int check_shape(const pa_shape* s) {
   if (s->max_blocks_per_seq < 1 || s->num_blocks < 1) return PA_ERR_SHAPE;
   if ((int64_t)s->max_blocks_per_seq * s->block_size > INT32_MAX) return PA_ERR_SHAPE;
   if ((int64_t)s->batch * s->max_blocks_per_seq > INT32_MAX) return PA_ERR_SHAPE;
+  // the balanced schedule counts a row's (kv head, block) units in 32 bits
+  if ((int64_t)s->num_kv_heads * (s->max_blocks_per_seq + 64) > INT32_MAX) return PA_ERR_SHAPE;
   if (s->dtype != PA_F16 && s->dtype != PA_BF16) return PA_ERR_SHAPE;
   return PA_OK;
 }

@@ -176,9 +176,11 @@ struct PieceIterT {
       if (u >= u_end) return false;
       int32_t b = find_seq(pre, s.B, s.Hkv, u);
       int32_t n = pre[b + 1] - pre[b];  // K + blocks of each segment of row b
-      int64_t r = u - (int64_t)s.Hkv * pre[b];
-      int32_t j = (int32_t)(r / n);
-      int32_t off = (int32_t)(r % n);
+      // r < Hkv * n fits in 32 bits (the counts of one row), so the division
+      // is a 32-bit one
+      const int32_t r = (int32_t)(u - (int64_t)s.Hkv * pre[b]);
+      int32_t j = r / n;
+      int32_t off = r - j * n;
       if (off < s.K) {  // the segment's overhead units: on to its first block
         u += s.K - off;
         off = s.K;

@@ -475,35 +475,38 @@ __device__ __forceinline__ int64_t column_out(const SplitArgs& a, int row, int j
 // column that saw no key (l = 0: a query token whose causal limit is 0)
 // gets 0, as an empty sequence does.
 // q0, nq: the query rows of the piece's sequence (several query tokens).
-template <int D, bool kQ>
+template <int D, int W, bool kQ>
 __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem, const SmemLayout& L,
-                                              const Piece& pc, int W, int q0, int nq) {
+                                              const Piece& pc, int q0, int nq) {
   const int C = a.C;
   const float* mm = reinterpret_cast<const float*>(smem + L.mm);
   const float* ml = reinterpret_cast<const float*>(smem + L.ml);
   const float* mo = reinterpret_cast<const float*>(smem + L.mo);
   const int* mbad = reinterpret_cast<const int*>(smem + L.mbad);
   bool bad = false;
+#pragma unroll
   for (int w = 0; w < W; ++w) bad |= (mbad[w] != 0);
   const float qnan = __int_as_float(0x7fc00000);
-  const int lane = threadIdx.x & 31, wl = lane & 7;
-  // The 32 elements a warp takes in one step share their column (D is a
-  // multiple of 32): lane w (w < W) computes warp w's weight 2^(m_w - M)
-  // once and the lanes share it by shuffles.
+  // Each thread folds its element from the W warp states directly: the
+  // column's maxima and sums are read by every lane of the warp (the 32
+  // elements a warp takes share their column, D being a multiple of 32, so
+  // these are broadcast loads), with no shuffles on the way.
   for (int idx = threadIdx.x; idx < C * D; idx += blockDim.x) {
     const int c = idx / D, dim = idx % D;
-    const float mw = wl < W ? mm[wl * kColMax + c] : -INFINITY;
-    const float lw = wl < W ? ml[wl * kColMax + c] : 0.f;
-    float M = mw;
+    float mw[W];
+    float M = -INFINITY;
 #pragma unroll
-    for (int off = 1; off < 8; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float e = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-    float Lsum = wl < W ? e * lw : 0.f;
+    for (int w = 0; w < W; ++w) {
+      mw[w] = mm[w * kColMax + c];
+      M = fmaxf(M, mw[w]);
+    }
+    float Lsum = 0.f, o = 0.f;
 #pragma unroll
-    for (int off = 1; off < 8; off <<= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
-    float o = 0.f;
-    for (int w = 0; w < W; ++w)
-      o = fmaf(__shfl_sync(0xffffffffu, e, w), mo[(w * C + c) * (D + 4) + dim], o);
+    for (int w = 0; w < W; ++w) {
+      const float e = (mw[w] == -INFINITY) ? 0.f : ex2(mw[w] - M);
+      Lsum = fmaf(e, ml[w * kColMax + c], Lsum);
+      o = fmaf(e, mo[(w * C + c) * (D + 4) + dim], o);
+    }
     if (pc.slot < 0) {
       const int64_t r = column_out<kQ>(a, pc.b, pc.j, c, q0, nq);
       if (r >= 0) a.out[r * D + dim] = bad ? qnan : (Lsum == 0.f ? 0.f : o / Lsum);
@@ -937,7 +940,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     const int q0 = kQ ? piece_info[2] : 0, nq = kQ ? piece_info[3] : 0;
     cp_async_wait_all();  // this thread's copies of the next q have landed
     named_bar_sync(1, blockDim.x);
-    combine_piece<D, kQ>(*sa, smem, L, pc, W, q0, nq);
+    combine_piece<D, W, kQ>(*sa, smem, L, pc, q0, nq);
     if (more) qn.template finish<T, MODE == kSimt>(*sa, qraw, qs, piece_info, qlim);
     named_bar_sync(1, blockDim.x);
     have = it.next(pc);
