@@ -21,6 +21,8 @@ constexpr int kGMax = 8;       // query heads per kv head handled by one CTA
 constexpr int kColMax = 16;    // query columns (token, head) per row: two mma n-blocks
 constexpr int kTile = 16;      // tokens per pipeline stage (one mma row tile)
 constexpr int kMergeThreads = 128;
+// Slack of the lazy running max in the tensor-core tile (log2 units): p <= 2^8.
+constexpr float kLazyMax = 8.f;
 
 // kSimt / kMma: one query token per sequence (decode).  kMmaQ: several query
 // tokens per sequence; a row is a group of one sequence's query tokens whose

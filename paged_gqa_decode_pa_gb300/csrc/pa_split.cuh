@@ -9,10 +9,11 @@
 // holding the K and V rows (kv head j) of one 16-token tile.  The warp loads
 // the tile's physical block id from the block table (32 ids per warp-wide
 // load, "Paged Attention Kernel Architecture for BI-V100", section 3: the
-// table indirection), checks it, and lane 0 issues 4-D TMA tensor loads (box
-// = 64 dims x 16 rows, 128-byte swizzle) that complete on the stage's
-// mbarrier.  After computing tile n the warp refills the same stage with
-// tile n + R, so loads of R tiles are always in flight per warp.
+// table indirection), checks it, and lane 0 issues the tile's 5-D TMA tensor
+// copy (64 dims x 16 rows x d/64 chunks, 128-byte swizzle; one copy for K and
+// V when one tensor map spans both pools, else one each) that completes on
+// the stage's mbarrier.  After computing tile n the warp refills the same
+// stage with tile n + R, so loads of R tiles are always in flight per warp.
 //
 // A warp keeps the online-softmax state (running max, exp-sum, weighted-V
 // accumulator; "v10_triton_paged_gqa", Core Principle) of ALL G query heads
@@ -22,15 +23,15 @@
 // 1-2) and written as the final output or as a partial state for the merge
 // kernel (section 2, Level 3).
 //
-// Scores are kept in log2 units (q is pre-multiplied by scale*log2(e)) so
-// every exponential is one ex2 instruction; the merge kernel uses the same
-// units.
+// Scores are kept in log2 units (times scale*log2(e)) so every exponential
+// is one ex2 instruction; the merge kernel uses the same units.
 //
 // Tensor-core variant (kMma): per 16-token tile, S^T[16 tokens x 8 heads] =
-// K[16 x d] . Q'^T[d x 8] and O^T[d x 8] += V^T[d x 16] . P^T[16 x 8] with
-// mma.sync m16n8k16 (fp32 accumulate).  Q' and P are split into a high and a
-// low 16-bit part (x = hi + lo) so that both products keep ~16 significant
-// bits; heads beyond G are zero columns.
+// K[16 x d] . q^T[d x 8] (the raw 16-bit q, exact; the fp32 scores then take
+// the factor scale*log2(e)) and O^T[d x 8] += V^T[d x 16] . P^T[16 x 8] with
+// mma.sync m16n8k16 (fp32 accumulate).  P is split into a high and a low
+// 16-bit part (p = hi + lo) so that the product keeps ~16 significant bits;
+// heads beyond G are zero columns.
 // CUDA-core variant (kSimt): lane <-> token for q.k (fp32 FMA), lane <->
 // dimension pair for p.V.
 #pragma once
@@ -215,7 +216,13 @@ struct MmaState {
         x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
         x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
       }
-      const float n0 = fmaxf(m[nb][0], x0), n1 = fmaxf(m[nb][1], x1);
+      // Lazy running max: a column's max moves only when the tile's max is
+      // above it by more than kLazyMax (log2 units).  Otherwise p is taken
+      // against the stale max and stays below 2^kLazyMax, and the
+      // accumulator is not rescaled; the state (m, l, o) is consistent for
+      // any m, so the folds downstream are unchanged.
+      const float n0 = (x0 > m[nb][0] + kLazyMax) ? x0 : m[nb][0];
+      const float n1 = (x1 > m[nb][1] + kLazyMax) ? x1 : m[nb][1];
       const float u0 = (n0 == -INFINITY) ? 0.f : n0;
       const float u1 = (n1 == -INFINITY) ? 0.f : n1;
       const float al0 = ex2(m[nb][0] - u0), al1 = ex2(m[nb][1] - u1);
