@@ -557,7 +557,7 @@ def main():
     ap.add_argument("--config", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--partition-tokens", type=int, default=0)
-    ap.add_argument("--compute", default="mma", choices=["mma", "simt", "auto"])
+    ap.add_argument("--compute", default="mma", choices=["mma", "simt", "tc", "auto"])
     ap.add_argument("--stages", type=int, default=0, help="pipeline stages (0 = library choice)")
     ap.add_argument("--query-tokens", type=int, default=0,
                     help="query tokens per sequence (0 = the workload's own: one in decode)")

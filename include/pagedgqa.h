@@ -100,7 +100,10 @@ typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
 typedef enum {
   PA_COMPUTE_AUTO = 0, /* library choice (tensor-core mma) */
   PA_COMPUTE_SIMT = 1, /* fp32 FMA on CUDA cores */
-  PA_COMPUTE_MMA = 2   /* mma.sync m16n8k16 tensor-core products, fp32 accumulate */
+  PA_COMPUTE_MMA = 2,  /* mma.sync m16n8k16 tensor-core products, fp32 accumulate */
+  PA_COMPUTE_TC = 3    /* tcgen05 tensor cores, accumulators in tensor memory,
+                          128-token tiles: head_dim 128 only (else
+                          PA_ERR_OPTION); not with pa_decode_append */
 } pa_compute;
 
 typedef struct pa_shape {
@@ -126,7 +129,8 @@ typedef struct pa_options {
                         CTAs on the current device.  Setting it makes
                         pa_workspace_size independent of the device. */
   int32_t stages;    /* TMA ring slots per warp (16-token K/V stages,
-                        1..8); 0 = library choice */
+                        1..8); with PA_COMPUTE_TC the CTA's 128-token V
+                        slots (2..4); 0 = library choice */
   int32_t phase;     /* pa_decode / pa_decode_append / pa_decode_multi:
                         PA_PHASE_BOTH (0) runs both kernels; PA_PHASE_SPLIT
                         only phase 1, PA_PHASE_MERGE only phase 2 (which must

@@ -44,7 +44,9 @@ PA_BF16 = 1
 PA_COMPUTE_AUTO = 0
 PA_COMPUTE_SIMT = 1
 PA_COMPUTE_MMA = 2
-_COMPUTE = {"auto": PA_COMPUTE_AUTO, "simt": PA_COMPUTE_SIMT, "mma": PA_COMPUTE_MMA}
+PA_COMPUTE_TC = 3
+_COMPUTE = {"auto": PA_COMPUTE_AUTO, "simt": PA_COMPUTE_SIMT, "mma": PA_COMPUTE_MMA,
+            "tc": PA_COMPUTE_TC}
 
 # Every symbol include/pagedgqa.h declares.
 EXPORTS = ("pa_workspace_size", "pa_decode", "pa_decode_split", "pa_decode_merge",

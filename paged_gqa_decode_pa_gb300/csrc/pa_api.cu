@@ -293,7 +293,7 @@ int check_options(const pa_shape* s, const pa_options* o) {
   if (!o) return PA_OK;
   if (o->partition_tokens < 0) return PA_ERR_OPTION;
   if (o->partition_tokens > 0 && o->partition_tokens % s->block_size != 0) return PA_ERR_OPTION;
-  if (o->compute < PA_COMPUTE_AUTO || o->compute > PA_COMPUTE_MMA) return PA_ERR_OPTION;
+  if (o->compute < PA_COMPUTE_AUTO || o->compute > PA_COMPUTE_TC) return PA_ERR_OPTION;
   if (o->num_ctas < 0 || o->num_ctas > (1 << 20)) return PA_ERR_OPTION;
   if (o->stages < 0 || o->stages > kMaxSlots / kMaxWarps) return PA_ERR_OPTION;
   if (o->phase < PA_PHASE_BOTH || o->phase > PA_PHASE_MERGE) return PA_ERR_OPTION;
@@ -301,7 +301,8 @@ int check_options(const pa_shape* s, const pa_options* o) {
 }
 
 struct Plan {
-  int D, G, bs, mode, warps, ring;
+  int D, G, bs, mode, warps, ring;  // kTc: ring = the CTA's 128-token stages
+  int multi;          // several query tokens per sequence
   int C;              // query columns per row (G in decode)
   int rows;           // rows of the schedule (B in decode, B * nqg with several tokens)
   int nqg, tq;        // several query tokens: groups per sequence, tokens per group
@@ -316,7 +317,7 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 int choose_mode(const pa_options* o) {
   const int c = o ? o->compute : PA_COMPUTE_AUTO;
-  return c == PA_COMPUTE_SIMT ? kSimt : kMma;
+  return c == PA_COMPUTE_SIMT ? kSimt : (c == PA_COMPUTE_TC ? kTc : kMma);
 }
 
 // Ring slots per warp: 2 by default (measured best for every head dimension:
@@ -331,7 +332,13 @@ int choose_ring(const pa_shape* s, const pa_options* o, int mode, int W, int C, 
   return fit < want ? fit : want;
 }
 
-const void* kernel_for(int dtype, int D, int mode) {
+const void* kernel_for(int dtype, int D, int mode, int multi) {
+  if (mode == kTc) {
+    if (D != kTcD) return nullptr;
+    if (dtype == PA_BF16)
+      return multi ? split_tc_kernel_ptr<__nv_bfloat16, true>() : split_tc_kernel_ptr<__nv_bfloat16, false>();
+    return multi ? split_tc_kernel_ptr<__half, true>() : split_tc_kernel_ptr<__half, false>();
+  }
 #define PA_PICK(T, DD)                                                                 \
   if (D == DD) return mode == kSimt ? split_kernel_ptr<T, DD, kSimt>()                \
                       : mode == kMmaQ ? split_kernel_ptr<T, DD, kMmaQ>()              \
@@ -403,26 +410,42 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
   p->G = s->num_heads / s->num_kv_heads;
   p->bs = s->block_size;
   p->mode = choose_mode(o);
-  p->warps = split_warps(p->D);
+  if (p->mode == kTc && p->D != kTcD) return PA_ERR_OPTION;
+  p->warps = p->mode == kTc ? kTcThreads / 32 : split_warps(p->D);
   p->C = p->G;
   p->rows = s->batch;
   p->nqg = 1;
   p->tq = 1;
+  p->multi = max_q > 0;
   if (max_q > 0) {
     if (max_q > PA_MAX_QUERY_TOKENS) return PA_ERR_SHAPE;
     if (p->mode == kSimt) return PA_ERR_OPTION;  // tensor-core path only
-    p->mode = kMmaQ;
-    p->tq = 8 * mma_blocks(p->D, kMmaQ) / p->G;
+    // groups of up to 16 (token, head) columns; the tcgen05 kernel keeps the
+    // mma kernel's grouping (N = 16)
+    if (p->mode != kTc) p->mode = kMmaQ;
+    p->tq = (p->mode == kTc ? kTcN : 8 * mma_blocks(p->D, kMmaQ)) / p->G;
     p->nqg = (max_q + p->tq - 1) / p->tq;
     p->C = p->tq * p->G;
     if ((int64_t)s->batch * p->nqg > PA_MAX_BATCH) return PA_ERR_SHAPE;
     p->rows = s->batch * p->nqg;
   }
-  p->ring = choose_ring(s, o, p->mode, p->warps, p->C, p->rows);
-  if (p->ring < 1) return (o && o->stages > 0) ? PA_ERR_OPTION : PA_ERR_SHAPE;
+  if (p->mode == kTc) {
+    const int fit = tc_stages(p->rows, kMaxDynamicSmem);
+    if (fit < 2) return PA_ERR_SHAPE;
+    if (o && o->stages > 0) {
+      if (o->stages < 2 || o->stages > fit) return PA_ERR_OPTION;
+      p->ring = o->stages;
+    } else {
+      p->ring = fit;  // V slots: as many as fit (4 at 256 rows)
+    }
+    p->smem = tc_smem_layout(p->rows, p->ring).total;
+  } else {
+    p->ring = choose_ring(s, o, p->mode, p->warps, p->C, p->rows);
+    if (p->ring < 1) return (o && o->stages > 0) ? PA_ERR_OPTION : PA_ERR_SHAPE;
+    const SmemLayout L = split_smem_layout(p->D, p->C, p->rows, p->warps, p->ring, p->mode);
+    p->smem = L.total;
+  }
   p->part_blocks = (o && o->partition_tokens > 0) ? o->partition_tokens / s->block_size : 0;
-  const SmemLayout L = split_smem_layout(p->D, p->C, p->rows, p->warps, p->ring, p->mode);
-  p->smem = L.total;
   if (p->smem > (size_t)kMaxDynamicSmem) return PA_ERR_SHAPE;
   const bool fixed_grid = o && o->num_ctas > 0;
   if (fixed_grid) p->grid = o->num_ctas;
@@ -430,7 +453,7 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
     int dev, sms, occ;
     rc = device_sms(&dev, &sms);
     if (rc) return rc;
-    const void* fn = kernel_for(s->dtype, p->D, p->mode);
+    const void* fn = kernel_for(s->dtype, p->D, p->mode, p->multi);
     if (!fn) return PA_ERR_SHAPE;
     rc = occupancy(fn, dev, p->smem, 32 * p->warps, &occ);
     if (rc) return rc;
@@ -472,12 +495,15 @@ int get_encoder() {
 // element, row, 64-dim chunk, kv head and block strides; box (64, 16, D/64,
 // 1, 1), 128-byte swizzle.  One box = 16 rows of one kv head of one physical
 // block, landing in shared memory as D/64 chunk tiles of [16][64].
-int make_pool_map(CUtensorMap* map, const void* pool, const pa_shape* s) {
+// One pool as (64 dims, bs rows, D/64 chunks, Hkv, P).  The box is a 16-row
+// tile of all chunks of one kv head, or (tc) all bs rows of one 64-dim chunk
+// of one block, for the tcgen05 kernel's 128-row stage chunks.
+int make_pool_map(CUtensorMap* map, const void* pool, const pa_shape* s, bool tc) {
   const uint64_t D = (uint64_t)s->head_dim, Hkv = (uint64_t)s->num_kv_heads;
   const uint64_t bs = (uint64_t)s->block_size, P = (uint64_t)s->num_blocks;
   cuuint64_t dims[5] = {64, bs, D / 64, Hkv, P};
   cuuint64_t strides[4] = {Hkv * D * 2, 128, D * 2, bs * Hkv * D * 2};
-  cuuint32_t box[5] = {64, (cuuint32_t)kTile, (cuuint32_t)(D / 64), 1, 1};
+  cuuint32_t box[5] = {64, tc ? (cuuint32_t)bs : (cuuint32_t)kTile, tc ? 1u : (cuuint32_t)(D / 64), 1, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUtensorMapDataType dt =
       s->dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -612,6 +638,7 @@ struct MapEntry {
   const void* pool;
   const void* pool2;  // the other pool of a map over both (nullptr: one pool)
   int32_t D, Hkv, bs, P, dtype;
+  int32_t tc;         // the tcgen05 kernel's box (make_pool_map)
   int32_t rc, swap;   // encode result (a map over both pools may be impossible)
   alignas(64) CUtensorMap map;
 };
@@ -622,12 +649,12 @@ int g_nmaps = 0, g_next_map = 0;
 // pool2 == nullptr: the map of one pool; otherwise the map over both pools
 // (make_kv_map), whose result code is cached too.
 int pool_map(CUtensorMap* out, const void* pool, const void* pool2, const pa_shape* s,
-             int* swap) {
+             int* swap, bool tc = false) {
   std::lock_guard<std::mutex> lk(g_mu);
   for (int i = 0; i < g_nmaps; ++i) {
     const MapEntry& e = g_maps[i];
     if (e.pool == pool && e.pool2 == pool2 && e.D == s->head_dim && e.Hkv == s->num_kv_heads &&
-        e.bs == s->block_size && e.P == s->num_blocks && e.dtype == s->dtype) {
+        e.bs == s->block_size && e.P == s->num_blocks && e.dtype == s->dtype && e.tc == (int)tc) {
       if (e.rc == PA_OK) {
         *out = e.map;
         if (swap) *swap = e.swap;
@@ -643,8 +670,9 @@ int pool_map(CUtensorMap* out, const void* pool, const void* pool2, const pa_sha
   e.bs = s->block_size;
   e.P = s->num_blocks;
   e.dtype = s->dtype;
+  e.tc = tc;
   e.swap = 0;
-  e.rc = pool2 ? make_kv_map(&e.map, pool, pool2, s, &e.swap) : make_pool_map(&e.map, pool, s);
+  e.rc = pool2 ? make_kv_map(&e.map, pool, pool2, s, &e.swap) : make_pool_map(&e.map, pool, s, tc);
   if (e.rc != PA_OK && e.rc != PA_ERR_SHAPE) return e.rc;  // encoder failure: not cached
   const int slot = g_nmaps < kMapCache ? g_nmaps++ : (g_next_map++ % kMapCache);
   g_maps[slot] = e;
@@ -661,6 +689,23 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
   if (rc) return rc;
   alignas(64) CUtensorMap tmk;
   alignas(64) CUtensorMap tmv;
+  const Plan& p = c->plan;
+  if (p.mode == kTc) {
+    rc = pool_map(&tmk, k_cache, nullptr, s, nullptr, true);
+    if (rc) return rc;
+    rc = pool_map(&tmv, v_cache, nullptr, s, nullptr, true);
+    if (rc) return rc;
+    c->sa.kv_fused = 0;
+    c->sa.kv_swap = 0;
+    cudaError_t e;
+    if (s->dtype == PA_BF16)
+      e = p.multi ? launch_split_tc<__nv_bfloat16, true>(tmk, tmv, c->sa, p.grid, p.smem, stream)
+                  : launch_split_tc<__nv_bfloat16, false>(tmk, tmv, c->sa, p.grid, p.smem, stream);
+    else
+      e = p.multi ? launch_split_tc<__half, true>(tmk, tmv, c->sa, p.grid, p.smem, stream)
+                  : launch_split_tc<__half, false>(tmk, tmv, c->sa, p.grid, p.smem, stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
   int swap = 0;
   if (pool_map(&tmk, k_cache, v_cache, s, &swap) == PA_OK) {
     // one copy per tile for K and V
@@ -675,7 +720,6 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
     rc = pool_map(&tmv, v_cache, nullptr, s, nullptr);
     if (rc) return rc;
   }
-  const Plan& p = c->plan;
   cudaError_t e = cudaErrorInvalidValue;
 #define PA_LAUNCH(T, DD)                                                                        \
   if (p.D == DD)                                                                                \
@@ -794,6 +838,7 @@ int pa_decode_append(const pa_shape* shape, const pa_options* options, const voi
   if (shape && shape->batch == 0 && check_shape(shape) == PA_OK) return PA_OK;
   if (!k_new || !v_new) return PA_ERR_NULL;
   if (!aligned16(k_new) || !aligned16(v_new)) return PA_ERR_ALIGN;
+  if (options && options->compute == PA_COMPUTE_TC) return PA_ERR_OPTION;  // not with the append
   Call c;
   int rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                    workspace, workspace_bytes, true, &c);

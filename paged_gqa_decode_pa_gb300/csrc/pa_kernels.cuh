@@ -27,7 +27,7 @@ constexpr float kLazyMax = 8.f;
 // kSimt / kMma: one query token per sequence (decode).  kMmaQ: several query
 // tokens per sequence; a row is a group of one sequence's query tokens whose
 // (token, head) pairs fill up to mma_blocks(D) x 8 columns.
-enum Mode { kSimt = 1, kMma = 2, kMmaQ = 3 };
+enum Mode { kSimt = 1, kMma = 2, kMmaQ = 3, kTc = 4 };  // kTc: the tcgen05 kernel (pa_split_tc.cuh)
 
 // mma n-blocks of 8 query columns a warp keeps (registers allow two below
 // d = 256).
@@ -208,6 +208,89 @@ PA_HD SmemLayout split_smem_layout(int D, int C, int B, int W, int R, int mode) 
   return L;
 }
 
+// ---- the tcgen05 split kernel (pa_split_tc.cuh): constants and shared-memory
+// layout, computed identically on host and device.
+
+constexpr int kTcTile = 128;                        // tokens per tile (MMA M)
+constexpr int kTcD = 128;                           // head dimension of this kernel
+constexpr int kTcN = 16;                            // MMA N: query columns (C <= 16)
+constexpr int kTcThreads = 224;                     // 4 softmax warps, K producer, MMA, V producer
+constexpr uint32_t kTcChunk = kTcTile * 128u;       // [128 rows][64 dims] swizzled: 16 KB
+constexpr uint32_t kTcHalfBytes = 2u * kTcChunk;    // a tile's K (or V): 2 chunks, 32 KB
+constexpr uint32_t kTcOpBytes = kTcN * 128u * 2u;   // q: [16 rows][128] 16-bit, two 2 KB chunks
+constexpr uint32_t kTcPBytes = 2u * kTcOpBytes;     // P: [32 rows (high, low)][128], two 4 KB chunks
+constexpr uint32_t kTcTmemCols = 64;                // S0 at 0, S1 at 16, O (high, low) at 32, 48
+constexpr int kTcKStages = 2;                       // K slots: freed when the scores are done
+constexpr int kTcMaxVStages = 4;                    // V slots: freed when O is updated
+
+// Byte offsets in the kernel's dynamic shared memory (base 1024-aligned).
+struct TcLayout {
+  uint32_t k;       // [kTcKStages] K slots
+  uint32_t v;       // [NV] V slots
+  uint32_t p;       // [2 buffers] P operands (rows 0-15 high parts, 16-31 low)
+  uint32_t q;       // [2] q operands (piece parity)
+  uint32_t bars;    // mbarriers (see TcBars)
+  uint32_t red;     // [4 warps][16] fp32 reduction scratch
+  uint32_t tbase;   // TMEM base address (written by tcgen05.alloc)
+  uint32_t abort_flag;
+  uint32_t args;    // the SplitArgs copy
+  uint32_t pre;     // [rows + 1] prefix sums
+  uint32_t total;
+};
+
+// mbarrier offsets inside TcLayout::bars (8 bytes each).
+struct TcBars {
+  static PA_HD uint32_t full_k(int s) { return 8u * (uint32_t)s; }
+  static PA_HD uint32_t empty_k(int s) { return 8u * (uint32_t)(kTcKStages + s); }
+  static PA_HD uint32_t full_v(int s) { return 8u * (uint32_t)(2 * kTcKStages + s); }
+  static PA_HD uint32_t empty_v(int s) { return 8u * (uint32_t)(2 * kTcKStages + kTcMaxVStages + s); }
+  static constexpr int kRest = 2 * kTcKStages + 2 * kTcMaxVStages;
+  static PA_HD uint32_t s_full(int b) { return 8u * (uint32_t)(kRest + b); }
+  static PA_HD uint32_t s_free(int b) { return 8u * (uint32_t)(kRest + 2 + b); }
+  static PA_HD uint32_t p_full(int b) { return 8u * (uint32_t)(kRest + 4 + b); }
+  static PA_HD uint32_t p_free(int b) { return 8u * (uint32_t)(kRest + 6 + b); }
+  static PA_HD uint32_t q_ready() { return 8u * (uint32_t)(kRest + 8); }
+  static PA_HD uint32_t o_free() { return 8u * (uint32_t)(kRest + 9); }
+  static PA_HD uint32_t drain() { return 8u * (uint32_t)(kRest + 10); }
+  static constexpr uint32_t kBytes = 8u * (kRest + 11);
+};
+
+// NV: V slots.
+PA_HD TcLayout tc_smem_layout(int rows, int NV) {
+  TcLayout L;
+  uint32_t off = 0;
+  L.k = off;
+  off += (uint32_t)kTcKStages * kTcHalfBytes;
+  L.v = off;
+  off += (uint32_t)NV * kTcHalfBytes;
+  L.p = off;
+  off += 2u * kTcPBytes;
+  L.q = off;
+  off += 2u * kTcOpBytes;
+  L.bars = off;
+  off += TcBars::kBytes;
+  L.red = align_up(off, 16);
+  off = L.red;
+  off += 4u * kTcN * 4u;
+  L.tbase = off;
+  off += 16u;
+  L.abort_flag = off;
+  off += 16u;
+  L.args = off;
+  off += kArgsBytes;
+  L.pre = off;
+  off += (uint32_t)(rows + 1) * 4u;
+  L.total = align_up(off, 16) + 1024;  // slack to align the base to 1024 bytes
+  return L;
+}
+
+// V slots that fit next to everything else (>= 2 needed), at most kTcMaxVStages.
+PA_HD int tc_stages(int rows, int max_smem) {
+  for (int nv = kTcMaxVStages; nv >= 2; --nv)
+    if ((int)tc_smem_layout(rows, nv).total <= max_smem) return nv;
+  return 0;
+}
+
 // Launchers (explicitly instantiated in pa_split_*.cu).
 template <typename T, int D, int MODE>
 cudaError_t launch_split(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a,
@@ -215,5 +298,14 @@ cudaError_t launch_split(const CUtensorMap& tmk, const CUtensorMap& tmv, const S
 
 template <typename T, int D, int MODE>
 const void* split_kernel_ptr();
+
+// The tcgen05 split kernel (pa_split_tc.cuh; head_dim 128; kQ: several
+// query tokens per sequence), instantiated in pa_split_tc_*.cu.
+template <typename T, bool kQ>
+cudaError_t launch_split_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a,
+                            int grid, size_t smem, cudaStream_t stream);
+
+template <typename T, bool kQ>
+const void* split_tc_kernel_ptr();
 
 }  // namespace pa

@@ -707,6 +707,52 @@ struct QStage {
   }
 };
 
+// Prologue of a split CTA after the prefix sums (all threads): rows with no
+// key to read get out = 0, rows with an invalid length NaN + a status bit
+// (with the fused append also "no slot": nothing is written for them); CTA 0
+// stores the prefix sums (only the fixed split's merge reads them), and every
+// CTA stores the descriptor of the segment that begins in it and continues
+// past it (balanced split).
+template <int D, bool kQ, class LenOf>
+__device__ __forceinline__ void rows_without_keys_and_descriptors(const SplitArgs& a,
+                                                                  const LenOf& len_of,
+                                                                  const int32_t* pre,
+                                                                  const SchedShape& sched, int cta) {
+  const int tid = threadIdx.x;
+  for (int b = cta; b < a.B; b += gridDim.x) {
+    if (pre[b + 1] != pre[b]) continue;  // has blocks: no global read needed
+    const int32_t len = len_of(b);
+    const bool ok = len >= 0;
+    const float v = ok ? 0.f : __int_as_float(0x7fc00000);
+    if constexpr (!kQ) {
+      float* row = a.out + (int64_t)b * a.H * D;
+      for (int i = tid; i < a.H * D; i += blockDim.x) row[i] = v;
+      if (!ok && tid == 0) atomicOr(a.status, kStatusBadSeqlen | (a.len_add ? kStatusNoSlot : 0u));
+    } else {
+      // the row's query tokens are consecutive packed rows of out
+      const int seq = b / a.nqg, grp = b - seq * a.nqg;
+      int32_t q0, nq;
+      const bool span = query_span(a.cu_q, seq, a.total_q, a.max_q, q0, nq);
+      if ((!span || !ok) && grp == 0 && tid == 0) atomicOr(a.status, kStatusBadSeqlen);
+      const int first = grp * a.tq;
+      if (!span || first >= nq) continue;
+      const int cnt = min(a.tq, nq - first);
+      float* rows = a.out + (int64_t)(q0 + first) * a.H * D;
+      for (int i = tid; i < cnt * a.H * D; i += blockDim.x) rows[i] = v;
+    }
+  }
+  if (cta == 0 && a.part_blocks > 0)
+    for (int b = tid; b <= a.B; b += blockDim.x) a.ws_pre[b] = pre[b];
+  if (tid == 0) {
+    if (a.part_blocks == 0) {
+      int32_t b, j, c_last, slot;
+      int4 desc = make_int4(-1, 0, 0, 0);
+      if (balanced_split_segment(pre, sched, cta, b, j, c_last, slot)) desc = make_int4(b, j, c_last, slot);
+      a.ws_desc[cta] = desc;
+    }
+  }
+}
+
 template <typename T, int D, int MODE>
 __global__ void __launch_bounds__(32 * split_warps(D), 1)
     pa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -772,41 +818,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
                          a.part_blocks, (int32_t)gridDim.x, a.len_add, a.piece_k};
   const int cta = blockIdx.x;
 
-  // Rows with no key to read: out = 0; invalid length: NaN + status (with
-  // the fused append also "no slot": nothing is written for them).
-  for (int b = cta; b < a.B; b += gridDim.x) {
-    if (pre[b + 1] != pre[b]) continue;  // has blocks: no global read needed
-    const int32_t len = len_of(b);
-    const bool ok = len >= 0;
-    const float v = ok ? 0.f : __int_as_float(0x7fc00000);
-    if constexpr (!kQ) {
-      float* row = a.out + (int64_t)b * a.H * D;
-      for (int i = tid; i < a.H * D; i += blockDim.x) row[i] = v;
-      if (!ok && tid == 0) atomicOr(a.status, kStatusBadSeqlen | (a.len_add ? kStatusNoSlot : 0u));
-    } else {
-      // the row's query tokens are consecutive packed rows of out
-      const int seq = b / a.nqg, grp = b - seq * a.nqg;
-      int32_t q0, nq;
-      const bool span = query_span(a.cu_q, seq, a.total_q, a.max_q, q0, nq);
-      if ((!span || !ok) && grp == 0 && tid == 0) atomicOr(a.status, kStatusBadSeqlen);
-      const int first = grp * a.tq;
-      if (!span || first >= nq) continue;
-      const int cnt = min(a.tq, nq - first);
-      float* rows = a.out + (int64_t)(q0 + first) * a.H * D;
-      for (int i = tid; i < cnt * a.H * D; i += blockDim.x) rows[i] = v;
-    }
-  }
-  // prefix sums for the merge kernel (only the fixed split's merge reads them)
-  if (cta == 0 && a.part_blocks > 0)
-    for (int b = tid; b <= a.B; b += blockDim.x) a.ws_pre[b] = pre[b];
-  if (tid == 0) {
-    if (a.part_blocks == 0) {
-      int32_t b, j, c_last, slot;
-      int4 desc = make_int4(-1, 0, 0, 0);
-      if (balanced_split_segment(pre, sched, cta, b, j, c_last, slot)) desc = make_int4(b, j, c_last, slot);
-      a.ws_desc[cta] = desc;
-    }
-  }
+  rows_without_keys_and_descriptors<D, kQ>(a, len_of, pre, sched, cta);
 
   const int w = warp;
   const int sl = a.bs == 16 ? 0 : (a.bs == 32 ? 1 : 2);  // log2(16-token tiles per block)
