@@ -22,9 +22,12 @@ namespace {
 // ------------------------------------------------------------------ merge
 
 // Phase 2: combine the partial states of every segment the split kernel cut
-// across CTAs (balanced split) or partitions (fixed split).  Block (seg, g)
-// folds column g (a query head, or a (token, head) pair) of merge index seg
-// (pa_sched.cuh, merge_segment) with the combine op ("Paged Attention Kernel
+// across CTAs (balanced split) or partitions (fixed split).  A block folds
+// one column (a query head, or a (token, head) pair) of one merge index
+// (pa_sched.cuh, merge_segment): with the balanced split, block i takes
+// column i % C of the (i / C)-th segment that has pieces to merge
+// (find_segment); with the fixed split, block (seg, g) takes column g of
+// segment seg.  The fold uses the combine op ("Paged Attention Kernel
 // Architecture for BI-V100", section 2, Level 1 binary op / Level 3): warp w
 // folds pieces w, w+4, ... in order, each lane holding D/32 of the dims; the
 // four warp states are then folded in a fixed order, so the result is
