@@ -28,6 +28,7 @@ PA_ERR_STATE = -8
 PA_ERR_NO_BLOCKS = -9
 
 PA_MAX_QUERY_TOKENS = 4096
+PA_MAX_BATCH = 8192  # include/pagedgqa.h: sequences per call
 
 PA_BM_FREE_BLOCKS = 0
 PA_BM_REF_COUNT = 1

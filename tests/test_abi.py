@@ -196,3 +196,12 @@ def test_balanced_split_charges_each_segment_its_overhead():
     first = sum(k1 - k0 for (_, _, k0, k1, _) in pg.pa_plan_pieces(s, None, lens, C, 0))
     last = sum(k1 - k0 for (_, _, k0, k1, _) in pg.pa_plan_pieces(s, None, lens, C, C - 1))
     assert first < last - 5 * K
+
+
+def test_batch_limit_matches_the_header():
+    s = pg.pa_shape(pg.PA_MAX_BATCH, 8, 2, 128, 16, 4, 64, pg.PA_BF16)
+    assert pg.pa_workspace_size(s, pg.options(num_ctas=8)) > 0
+    s.batch = pg.PA_MAX_BATCH + 1
+    with pytest.raises(pg.PagedGQAError) as e:
+        pg.pa_workspace_size(s, pg.options(num_ctas=8))
+    assert e.value.code == pg.PA_ERR_SHAPE
