@@ -285,8 +285,10 @@ int pa_decode_noalloc(const pa_shape* shape, const pa_options* options, const vo
                       const int32_t* cache_seqlens, float scale, float* out, uint32_t* status,
                       pa_stream_t stream);
 
-/* Host replica of the device work split, for inspection and tests.  Given
- * host lengths, lists the pieces CTA `cta` of a grid of `num_ctas` processes:
+/* Host replica of the device work split of pa_decode (one query token per
+ * sequence; pa_decode_multi charges each segment a larger overhead in its
+ * balanced split), for inspection and tests.  Given host lengths, lists the
+ * pieces CTA `cta` of a grid of `num_ctas` processes:
  * pieces[5*i .. 5*i+4] = (b, kv_head, first_block, end_block, slot) where
  * slot is the workspace slot of its partial state, or -1 when the piece is a
  * whole sequence/kv-head whose output the CTA writes directly.  Returns the

@@ -596,7 +596,9 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.maxblk = s->max_blocks_per_seq;
   a.P = s->num_blocks;
   a.part_blocks = p.part_blocks;
-  a.piece_k = p.part_blocks == 0 ? piece_units(s->block_size, s->head_dim) : 0;
+  a.piece_k = p.part_blocks == 0
+                  ? piece_units(s->block_size, s->head_dim, p.multi ? kPieceKbMulti : kPieceKb)
+                  : 0;
   a.warps = p.warps;
   a.ring = p.ring;
   a.qscale = scale * 1.4426950408889634f;  // log2(e)

@@ -54,11 +54,16 @@ struct SchedShape {
 
 // Overhead units per segment of the balanced split: a piece's fixed cost in
 // units of one block of one kv head (4 bs D bytes of K and V).  Measured
-// best on GB300 at about 200 KB worth (a sweep of 0 to 320 KB on the serving
-// and prefix-sharing steps).
-PA_HD int32_t piece_units(int32_t bs, int32_t D) {
+// best on GB300 at about 200 KB worth (sweeps of 0 to 320 KB on the serving
+// and prefix-sharing steps).  With several query tokens per sequence a
+// piece's fold and prefix cover up to 16 columns and cost more: measured best
+// at about 440 KB (sweeps of 200 to 1400 KB on steps of 2, 4 and 8 query
+// tokens per sequence; 400 to 480 within 1%).
+constexpr int32_t kPieceKb = 200;
+constexpr int32_t kPieceKbMulti = 440;
+PA_HD int32_t piece_units(int32_t bs, int32_t D, int32_t kb = kPieceKb) {
   const int32_t unit = 4 * bs * D;
-  const int32_t k = (200 * 1024 + unit / 2) / unit;
+  const int32_t k = (kb * 1024 + unit / 2) / unit;
   return k < 1 ? 1 : k;
 }
 
