@@ -10,9 +10,10 @@ metric  : K/V-read HBM GB/s = unique K/V bytes a step must read / step time
           (unit GB/s, higher is better); us per step and tokens/s ride along.
 value   : device-timed with CUDA events on the launching stream, inputs
           resident in HBM; K steps between barrier + synchronize, max over ranks.
-e2e     : the same metric through pa_decode with the step's inputs (q, block
-          table, lengths) copied from pinned host memory -- one staging buffer,
-          one copy -- and the output read back every step.
+e2e     : the same metric through the host-buffer call (pa_decode_host /
+          pa_decode_multi_host): every step copies q, the block table and the
+          lengths from pinned host memory, attends, and copies the output and
+          the call's status back before the call returns.
 roofline: the split kernel alone (CUDA events around phase 1 in the same timed
           loop) against the measured HBM copy bandwidth.
 cpu_baseline / --impl reference: the float64 oracle on the host cores, on a
@@ -462,55 +463,62 @@ def run_ours(args, rank, world, local_rank):
     if pg.pa_read_status(ws) != 0:
         raise RuntimeError("device status bits set during the timed steps")
 
-    # ---- e2e: host buffers, copies inside the timed region.  The step's
-    # inputs (q, block table, lengths, query counts) travel as one pinned
-    # staging buffer, one host-to-device copy per step, whose device copy
-    # the call reads through aligned views; the output comes back as one
-    # device-to-host copy.
+    # ---- e2e: host buffers, transfers inside the timed region.  Every step
+    # is one call of the library's host-buffer entry point (bound once to
+    # the step's buffers, as a serving loop would): it moves q, the block
+    # table and the lengths (and the query offsets) from pinned host memory
+    # into the workspace's staging, runs both phases with the output written
+    # to pinned host memory, publishes the call's status there too, and
+    # waits for the stream.
     Ke = max(3, min(K, 200))
-    parts = [("q", q), ("t", t), ("sl", sl)] + ([("cu", cu)] if multi else [])
-    offs, total = {}, 0
-    for name, x in parts:
-        offs[name] = total
-        total += (x.numel() * x.element_size() + 255) // 256 * 256
-    stage_h = torch.empty(total, dtype=torch.uint8).pin_memory()
-    stage_d = torch.empty(total, dtype=torch.uint8, device=dev)
-    views = {}
-    for name, x in parts:
-        nb = x.numel() * x.element_size()
-        stage_h[offs[name]:offs[name] + nb].copy_(x.cpu().contiguous().view(-1).view(torch.uint8))
-        views[name] = stage_d[offs[name]:offs[name] + nb].view(x.dtype).view(x.shape)
+    q_h, t_h, sl_h = (x.cpu().contiguous().pin_memory() for x in (q, t, sl))
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for _, x in parts)
-    d2h = out_h.numel() * 4
+    parts = [q_h, t_h, sl_h]
+    if multi:
+        cu_h = cu.cpu().contiguous().pin_memory()
+        parts.append(cu_h)
+        shape_h = pg.shape_multi(q, k, t)
+        ws_h = pg.alloc_workspace_multi_host(shape_h, w.max_q, q.shape[0], opts, dev)
 
-    def attend_staged():
-        qe, te, sle = views["q"], views["t"], views["sl"]
-        if multi:
-            pg.pa_decode_multi(qe, views["cu"], w.max_q, w.causal, k, v, te, sle, w.scale, out, ws,
-                               opts)
-        else:
-            pg.pa_decode(qe, k, v, te, sle, w.scale, out, ws, opts)
+        attend_host = pg.bind_decode_multi_host(q_h, cu_h, w.max_q, w.causal, k, v, t_h, sl_h,
+                                                w.scale, out_h, ws_h, opts, stream)
+    else:
+        ws_h = pg.alloc_workspace_host(pg.shape_of(q, k, t), opts, dev)
+        attend_host = pg.bind_decode_host(q_h, k, v, t_h, sl_h, w.scale, out_h, ws_h, opts,
+                                          stream)
+    h2d = sum(x.numel() * x.element_size() for x in parts)
+    d2h = out_h.numel() * 4 + 4  # the output and the call's status word
 
     for _ in range(2):
-        stage_d.copy_(stage_h, non_blocking=True)
-        attend_staged()
-        out_h.copy_(out, non_blocking=True)
+        attend_host()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(Ke):
-        stage_d.copy_(stage_h, non_blocking=True)
-        attend_staged()
-        out_h.copy_(out, non_blocking=True)
-        stream.synchronize()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / Ke
+    e2e_status = 0
+    if flush:
+        # L2 flushed before every step, outside its events
+        eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+        for i in range(Ke):
+            scratch.fill_(1.0)
+            eve[i][0].record(stream)
+            e2e_status |= attend_host()
+            eve[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = float(sum(eve[i][0].elapsed_time(eve[i][1]) for i in range(Ke))) / Ke
+    else:
+        e0.record(stream)
+        for _ in range(Ke):
+            e2e_status |= attend_host()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / Ke
+    if e2e_status != 0:
+        raise RuntimeError(f"device status bits {e2e_status:#x} during the end-to-end steps")
+    if not torch.equal(out_h, out.cpu()):
+        raise RuntimeError("the end-to-end output differs from the device-buffer output")
 
     # ---- max over ranks
     total_ms, e2e_ms, split_avg_ms, merge_avg_ms = max_over_ranks(

@@ -236,6 +236,47 @@ int pa_decode_multi(const pa_shape* shape, const pa_options* options, const void
                     const int32_t* cache_seqlens, float scale, float* out, void* workspace,
                     size_t workspace_bytes, pa_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * End to end from host buffers.
+ *
+ * pa_decode_host is pa_decode for a caller whose step inputs and result live
+ * in host memory: q_host [B, H, d], block_table_host [B, max_blocks_per_seq]
+ * and cache_seqlens_host [B] are copied into device staging inside the
+ * workspace, both phases run on the staged copies, and out_host [B, H, d]
+ * fp32 receives the result; the call then waits for `stream` and returns.
+ * The pools stay on the device (k_cache, v_cache: device pointers, as in
+ * pa_decode).  Host buffers need no alignment; page-locked ones
+ * (cudaHostAlloc / cudaHostRegister) let the copies run asynchronously at
+ * full speed, pageable ones work but are staged by the driver.  The
+ * workspace (device, 16-byte aligned, zero-filled once) must hold
+ * pa_workspace_size_host bytes: pa_workspace_size's plus the staging.
+ * status_host: if not NULL, receives this call's device status bits (0 when
+ * all went well; the workspace's own status word is left untouched); if
+ * NULL, the bits accumulate in the workspace's status word as for pa_decode
+ * (read them with pa_read_status).  options->phase must be PA_PHASE_BOTH.
+ * Returns PA_OK or PA_ERR_*; argument errors are found before anything is
+ * enqueued.  Not capturable in a CUDA graph (it synchronises). */
+int pa_workspace_size_host(const pa_shape* shape, const pa_options* options, size_t* bytes);
+int pa_decode_host(const pa_shape* shape, const pa_options* options, const void* q_host,
+                   const void* k_cache, const void* v_cache, const int32_t* block_table_host,
+                   const int32_t* cache_seqlens_host, float scale, float* out_host,
+                   uint32_t* status_host, void* workspace, size_t workspace_bytes,
+                   pa_stream_t stream);
+
+/* pa_decode_multi from host buffers, as pa_decode_host: q_host
+ * [total_q, H, d], cu_seqlens_q_host [B + 1], block_table_host,
+ * cache_seqlens_host in; out_host [total_q, H, d] fp32 back.  The workspace
+ * must hold pa_workspace_size_multi_host(shape, options, max_q, M) bytes
+ * for some M >= total_q (PA_ERR_WORKSPACE otherwise). */
+int pa_workspace_size_multi_host(const pa_shape* shape, const pa_options* options, int32_t max_q,
+                                 int32_t max_total_q, size_t* bytes);
+int pa_decode_multi_host(const pa_shape* shape, const pa_options* options, const void* q_host,
+                         const int32_t* cu_seqlens_q_host, int32_t total_q, int32_t max_q,
+                         int32_t causal, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table_host, const int32_t* cache_seqlens_host,
+                         float scale, float* out_host, uint32_t* status_host, void* workspace,
+                         size_t workspace_bytes, pa_stream_t stream);
+
 /* Append one new token per sequence to the paged cache, in place: for every
  * b and kv head j, k_new[b,j,:] and v_new[b,j,:] are copied bit for bit to
  * row (cache_seqlens[b] % bs) of physical block

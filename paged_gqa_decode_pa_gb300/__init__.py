@@ -14,7 +14,10 @@ from ._binding import (  # noqa: F401
     BlockManager, pa_bm_create, pa_bm_destroy, pa_bm_allocate, pa_bm_free_sequence,
     pa_bm_share_prefix, pa_bm_copy_on_write, pa_bm_reserve_slot, pa_bm_block_table, pa_bm_query,
     pa_copy_blocks, pa_decode_multi, pa_workspace_size_multi, alloc_workspace_multi,
-    shape_multi, PA_MAX_QUERY_TOKENS, PA_MAX_BATCH, PA_PHASE_BOTH, PA_PHASE_SPLIT, PA_PHASE_MERGE, PA_ERR_STATE, PA_ERR_NO_BLOCKS, PA_BM_FREE_BLOCKS, PA_BM_REF_COUNT,
+    shape_multi, pa_decode_host, pa_workspace_size_host, alloc_workspace_host,
+    pa_decode_multi_host, pa_workspace_size_multi_host, alloc_workspace_multi_host,
+    bind_decode_host, bind_decode_multi_host,
+    PA_MAX_QUERY_TOKENS, PA_MAX_BATCH, PA_PHASE_BOTH, PA_PHASE_SPLIT, PA_PHASE_MERGE, PA_ERR_STATE, PA_ERR_NO_BLOCKS, PA_BM_FREE_BLOCKS, PA_BM_REF_COUNT,
     PA_BM_SEQ_BLOCKS,
     PA_OK, PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_ALIGN, PA_ERR_WORKSPACE, PA_ERR_CUDA,
     PA_ERR_OPTION, PA_ERR_SCRATCH_LIMIT, PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_SEQLEN, PA_STATUS_TIMEOUT,

@@ -56,7 +56,8 @@ EXPORTS = ("pa_workspace_size", "pa_decode", "pa_decode_split", "pa_decode_merge
            "pa_bm_create", "pa_bm_destroy", "pa_bm_allocate", "pa_bm_free_sequence",
            "pa_bm_share_prefix", "pa_bm_copy_on_write", "pa_bm_reserve_slot",
            "pa_bm_block_table", "pa_bm_query", "pa_copy_blocks", "pa_decode_multi",
-           "pa_workspace_size_multi")
+           "pa_workspace_size_multi", "pa_decode_host", "pa_workspace_size_host",
+           "pa_decode_multi_host", "pa_workspace_size_multi_host")
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -157,6 +158,17 @@ def lib():
         L.pa_decode_multi.argtypes = [SP, OP, P, P, i32, i32, i32, P, P, P, P, ctypes.c_float, P,
                                       P, ctypes.c_size_t, P]
         L.pa_decode_multi.restype = ctypes.c_int
+        L.pa_workspace_size_host.argtypes = [SP, OP, ctypes.POINTER(ctypes.c_size_t)]
+        L.pa_workspace_size_host.restype = ctypes.c_int
+        L.pa_decode_host.argtypes = [SP, OP, P, P, P, P, P, ctypes.c_float, P, P, P,
+                                     ctypes.c_size_t, P]
+        L.pa_decode_host.restype = ctypes.c_int
+        L.pa_workspace_size_multi_host.argtypes = [SP, OP, i32, i32,
+                                                   ctypes.POINTER(ctypes.c_size_t)]
+        L.pa_workspace_size_multi_host.restype = ctypes.c_int
+        L.pa_decode_multi_host.argtypes = [SP, OP, P, P, i32, i32, i32, P, P, P, P,
+                                           ctypes.c_float, P, P, P, ctypes.c_size_t, P]
+        L.pa_decode_multi_host.restype = ctypes.c_int
         L.pa_version.argtypes = []
         L.pa_version.restype = ctypes.c_int
         _lib = L
@@ -292,6 +304,178 @@ def pa_decode_multi(q, cu_seqlens_q, max_q, causal, k_cache, v_cache, block_tabl
                                _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _stream(stream))
     _check(rc, "pa_decode_multi")
+
+
+def _check_host(q, block_table, cache_seqlens, out, k_cache, v_cache, extra=()):
+    import torch
+
+    for name, t in (("q", q), ("block_table", block_table), ("cache_seqlens", cache_seqlens),
+                    ("out", out)) + tuple(extra):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host (CPU) tensor")
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype or v_cache.shape != k_cache.shape:
+        raise ValueError("q, k_cache and v_cache must share dtype; k/v shapes must match")
+    if block_table.dtype != torch.int32 or cache_seqlens.dtype != torch.int32:
+        raise TypeError("block_table and cache_seqlens must be int32")
+    if out.dtype != torch.float32 or tuple(out.shape) != tuple(q.shape):
+        raise TypeError("out must be float32 with q's shape")
+
+
+_tls = threading.local()
+
+
+def _status_word():
+    """This thread's page-locked host word that the host-buffer calls have
+    the device publish their status into (no copy back needed), and a numpy
+    view of it for reading."""
+    import torch
+
+    word = getattr(_tls, "status", None)
+    if word is None:
+        t = torch.zeros(1, dtype=torch.int32).pin_memory()
+        word = (t, t.numpy().view("uint32"))
+        _tls.status = word
+    return word
+
+
+def pa_workspace_size_host(shape: pa_shape, opts: Optional[pa_options] = None) -> int:
+    n = ctypes.c_size_t(0)
+    rc = lib().pa_workspace_size_host(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                                      ctypes.byref(n))
+    _check(rc, "pa_workspace_size_host")
+    return int(n.value)
+
+
+def alloc_workspace_host(shape: pa_shape, opts: Optional[pa_options] = None, device=None):
+    """Zero-filled device workspace for pa_decode_host (torch uint8)."""
+    import torch
+
+    return torch.zeros(pa_workspace_size_host(shape, opts), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def pa_decode_host(q, k_cache, v_cache, block_table, cache_seqlens, scale, out, workspace,
+                   opts: Optional[pa_options] = None, stream=None) -> int:
+    """pa_decode with q, block_table, cache_seqlens and out in host memory
+    (CPU tensors; pinned ones copy fastest) and the pools on the device.
+    Returns after out is filled; the result is this call's device status
+    bits (0 = all well).  See include/pagedgqa.h."""
+    _check_host(q, block_table, cache_seqlens, out, k_cache, v_cache)
+    shape = shape_of(q, k_cache, block_table)
+    st, view = _status_word()
+    rc = lib().pa_decode_host(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                              _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                              _ptr(cache_seqlens), float(scale), _ptr(out), st.data_ptr(),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              _stream(stream))
+    _check(rc, "pa_decode_host")
+    return int(view[0])
+
+
+def pa_workspace_size_multi_host(shape: pa_shape, max_q: int, max_total_q: int,
+                                 opts: Optional[pa_options] = None) -> int:
+    n = ctypes.c_size_t(0)
+    rc = lib().pa_workspace_size_multi_host(ctypes.byref(shape),
+                                            ctypes.byref(opts) if opts else None, int(max_q),
+                                            int(max_total_q), ctypes.byref(n))
+    _check(rc, "pa_workspace_size_multi_host")
+    return int(n.value)
+
+
+def alloc_workspace_multi_host(shape: pa_shape, max_q: int, max_total_q: int,
+                               opts: Optional[pa_options] = None, device=None):
+    """Zero-filled device workspace for pa_decode_multi_host (torch uint8)."""
+    import torch
+
+    return torch.zeros(pa_workspace_size_multi_host(shape, max_q, max_total_q, opts),
+                       dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+def pa_decode_multi_host(q, cu_seqlens_q, max_q, causal, k_cache, v_cache, block_table,
+                         cache_seqlens, scale, out, workspace, opts: Optional[pa_options] = None,
+                         stream=None) -> int:
+    """pa_decode_multi with q, cu_seqlens_q, block_table, cache_seqlens and out
+    in host memory; returns this call's device status bits."""
+    import torch
+
+    _check_host(q, block_table, cache_seqlens, out, k_cache, v_cache,
+                (("cu_seqlens_q", cu_seqlens_q),))
+    if cu_seqlens_q.dtype != torch.int32 or tuple(cu_seqlens_q.shape) != (block_table.shape[0] + 1,):
+        raise TypeError("cu_seqlens_q must be int32 [B + 1]")
+    shape = shape_multi(q, k_cache, block_table)
+    st, view = _status_word()
+    rc = lib().pa_decode_multi_host(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                                    _ptr(q), _ptr(cu_seqlens_q), int(q.shape[0]), int(max_q),
+                                    int(bool(causal)), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(block_table), _ptr(cache_seqlens), float(scale),
+                                    _ptr(out), st.data_ptr(), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "pa_decode_multi_host")
+    return int(view[0])
+
+
+class _BoundCall:
+    """One library entry point with its arguments marshalled once; calling
+    it runs that entry point again on the same buffers (whose contents may
+    have changed) and returns the call's device status bits.  Holds
+    references to every tensor it points at."""
+
+    def __init__(self, fn, name, args, keep, status):
+        self._fn, self._name, self._args, self._keep = fn, name, args, keep
+        self._status = status
+
+    def __call__(self) -> int:
+        rc = self._fn(*self._args)
+        if rc != PA_OK:
+            raise PagedGQAError(rc, self._name)
+        return int(self._status[1][0])
+
+
+def bind_decode_host(q, k_cache, v_cache, block_table, cache_seqlens, scale, out, workspace,
+                     opts: Optional[pa_options] = None, stream=None) -> _BoundCall:
+    """pa_decode_host on these buffers, checked and marshalled once: the
+    returned callable runs one step per call (a serving loop rewrites q, the
+    table and the lengths in place between steps) and returns its status."""
+    _check_host(q, block_table, cache_seqlens, out, k_cache, v_cache)
+    shape = shape_of(q, k_cache, block_table)
+    st = _status_word()
+    V = ctypes.c_void_p
+    opt = pa_options.from_buffer_copy(opts) if opts else None
+    args = (ctypes.byref(shape), ctypes.byref(opt) if opt else None, V(_ptr(q)), V(_ptr(k_cache)),
+            V(_ptr(v_cache)), V(_ptr(block_table)), V(_ptr(cache_seqlens)),
+            ctypes.c_float(scale), V(_ptr(out)), V(st[0].data_ptr()), V(_ptr(workspace)),
+            ctypes.c_size_t(workspace.numel() * workspace.element_size()), V(_stream(stream)))
+    keep = (shape, opt, q, k_cache, v_cache, block_table, cache_seqlens, out, workspace, st)
+    return _BoundCall(lib().pa_decode_host, "pa_decode_host", args, keep, st)
+
+
+def bind_decode_multi_host(q, cu_seqlens_q, max_q, causal, k_cache, v_cache, block_table,
+                           cache_seqlens, scale, out, workspace,
+                           opts: Optional[pa_options] = None, stream=None) -> _BoundCall:
+    """pa_decode_multi_host on these buffers, checked and marshalled once
+    (as bind_decode_host; total_q is q's row count)."""
+    import torch
+
+    _check_host(q, block_table, cache_seqlens, out, k_cache, v_cache,
+                (("cu_seqlens_q", cu_seqlens_q),))
+    if cu_seqlens_q.dtype != torch.int32 or tuple(cu_seqlens_q.shape) != (block_table.shape[0] + 1,):
+        raise TypeError("cu_seqlens_q must be int32 [B + 1]")
+    shape = shape_multi(q, k_cache, block_table)
+    st = _status_word()
+    V = ctypes.c_void_p
+    i32 = ctypes.c_int32
+    opt = pa_options.from_buffer_copy(opts) if opts else None
+    args = (ctypes.byref(shape), ctypes.byref(opt) if opt else None, V(_ptr(q)),
+            V(_ptr(cu_seqlens_q)), i32(q.shape[0]), i32(max_q), i32(int(bool(causal))),
+            V(_ptr(k_cache)), V(_ptr(v_cache)), V(_ptr(block_table)), V(_ptr(cache_seqlens)),
+            ctypes.c_float(scale), V(_ptr(out)), V(st[0].data_ptr()), V(_ptr(workspace)),
+            ctypes.c_size_t(workspace.numel() * workspace.element_size()), V(_stream(stream)))
+    keep = (shape, opt, q, cu_seqlens_q, k_cache, v_cache, block_table, cache_seqlens, out,
+            workspace, st)
+    return _BoundCall(lib().pa_decode_multi_host, "pa_decode_multi_host", args, keep, st)
 
 
 def _decode_call(name, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,

@@ -186,6 +186,33 @@ __device__ __forceinline__ bool find_segment(const MergeArgs& a, int k, int& seg
   return seg >= 0;
 }
 
+// Staging of a host-buffer call's inputs by the SMs (see StageArgs): each
+// thread moves 16-byte chunks, four in flight, then the parts' 4-byte tails.
+// Dependents (the split kernel) may be scheduled at once; they wait for this
+// grid before reading what it writes.
+constexpr int kStageThreads = 256;
+__global__ void __launch_bounds__(kStageThreads) pa_stage_in_kernel(const StageArgs s) {
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nth = (int64_t)gridDim.x * blockDim.x;
+  if (tid == 0 && s.status) *s.status = 0u;
+  for (int p = 0; p < s.n; ++p) {
+    const int64_t n16 = s.words[p] / 4;
+    const uint4* src = reinterpret_cast<const uint4*>(s.src[p]);
+    uint4* dst = reinterpret_cast<uint4*>(s.dst[p]);
+    int64_t i = tid;
+    for (; i + 3 * nth < n16; i += 4 * nth) {
+      const uint4 x0 = src[i], x1 = src[i + nth], x2 = src[i + 2 * nth], x3 = src[i + 3 * nth];
+      dst[i] = x0;
+      dst[i + nth] = x1;
+      dst[i + 2 * nth] = x2;
+      dst[i + 3 * nth] = x3;
+    }
+    for (; i < n16; i += nth) dst[i] = src[i];
+    for (int64_t k = 4 * n16 + tid; k < s.words[p]; k += nth) s.dst[p][k] = s.src[p][k];
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs a) {
   // The next kernel on the stream (the next step's split kernel) may be
@@ -194,6 +221,11 @@ __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs
   // With programmatic dependent launch this grid may start while the split
   // kernel is finishing: wait until its writes are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (a.status_out && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    volatile uint32_t* st = a.status;
+    *a.status_out = *st;
+    *st = 0u;
+  }
   const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas, 0, 0};
   int seg, g;
   int4 desc = make_int4(-1, 0, 0, 0);
@@ -634,6 +666,8 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   m.tq = p.tq;
   m.total_q = 0;
   m.max_q = max_q;
+  m.status = a.status;
+  m.status_out = nullptr;
   return PA_OK;
 }
 
@@ -785,6 +819,127 @@ int run_phases(const pa_shape* s, const pa_options* o, const void* k_cache, cons
   return launch_merge_phase(c, st, phase == PA_PHASE_BOTH);
 }
 
+// Device staging that the host-buffer calls add after a plan's workspace:
+// the step's block table, lengths, query offsets, the call's status words
+// (accumulated, published), then out and q for `rows` query rows (last, so a
+// call with fewer rows than the workspace was sized for still fits).
+struct HostLayout {
+  size_t table, lens, cu, status, out, q, total;
+  size_t table_bytes, lens_bytes, cu_bytes, out_bytes, q_bytes;
+};
+
+HostLayout host_layout(const Plan& p, const pa_shape* s, int64_t rows, bool multi) {
+  HostLayout h;
+  const size_t B = (size_t)s->batch, row = (size_t)s->num_heads * s->head_dim;
+  h.table_bytes = sizeof(int32_t) * B * (size_t)s->max_blocks_per_seq;
+  h.lens_bytes = sizeof(int32_t) * B;
+  h.cu_bytes = multi ? sizeof(int32_t) * (B + 1) : 0;
+  h.out_bytes = sizeof(float) * (size_t)rows * row;
+  h.q_bytes = 2 * (size_t)rows * row;
+  size_t off = round256(p.total);
+  h.table = off;
+  off = round256(off + h.table_bytes);
+  h.lens = off;
+  off = round256(off + h.lens_bytes);
+  h.cu = off;
+  off = round256(off + h.cu_bytes);
+  h.status = off;
+  off = round256(off + 2 * sizeof(uint32_t));
+  h.out = off;
+  off = round256(off + h.out_bytes);
+  h.q = off;
+  h.total = off + h.q_bytes;
+  return h;
+}
+
+// The device address of page-locked host memory that this device maps
+// (cudaHostAlloc, cudaHostRegister), if `p` is such memory and aligned to
+// `align` bytes; otherwise null (pageable or device memory: the caller
+// copies instead).
+void* mapped_host(const void* p, uintptr_t align) {
+  if (!p || (reinterpret_cast<uintptr_t>(p) & (align - 1))) return nullptr;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+  if (reinterpret_cast<uintptr_t>(at.devicePointer) & (align - 1)) return nullptr;
+  return at.devicePointer;
+}
+
+struct HostBuffers {
+  const void* q;
+  const int32_t* cu;  // several query tokens only
+  const int32_t* table;
+  const int32_t* lens;
+  float* out;
+  uint32_t* status;
+};
+
+// Where the kernels write out: the caller's buffer itself when the device
+// maps it, else the staging (copied back at the end).
+float* host_out_target(const HostLayout& h, uint8_t* ws, float* out_host) {
+  void* d = mapped_host(out_host, 16);
+  return d ? static_cast<float*>(d) : reinterpret_cast<float*>(ws + h.out);
+}
+
+// One step from host buffers, after every argument check has passed: stage
+// the inputs (by the SMs from page-locked memory the device maps, by copies
+// otherwise), run both phases, bring out and the call's status back, wait
+// for the stream.  `c` was prepared on the staged inputs and on the output
+// target host_out_target chose.
+int run_host_step(const pa_shape* s, const pa_options* o, const HostLayout& h, uint8_t* ws,
+                  const HostBuffers& hb, const void* k_cache, const void* v_cache, Call* c,
+                  cudaStream_t st) {
+  StageArgs sa = {};
+  auto part = [&](const void* host, size_t off, size_t bytes) {
+    if (bytes == 0) return PA_OK;
+    const void* d = mapped_host(host, 16);
+    if (d && bytes % 4 == 0) {
+      sa.src[sa.n] = static_cast<const uint32_t*>(d);
+      sa.dst[sa.n] = reinterpret_cast<uint32_t*>(ws + off);
+      sa.words[sa.n] = (int64_t)(bytes / 4);
+      ++sa.n;
+      return PA_OK;
+    }
+    return cudaMemcpyAsync(ws + off, host, bytes, cudaMemcpyHostToDevice, st) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+  };
+  int rc = part(hb.q, h.q, h.q_bytes);
+  if (!rc) rc = part(hb.table, h.table, h.table_bytes);
+  if (!rc) rc = part(hb.lens, h.lens, h.lens_bytes);
+  if (!rc && hb.cu) rc = part(hb.cu, h.cu, h.cu_bytes);
+  if (rc) return rc;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(ws + h.status);
+  uint32_t* published = nullptr;
+  if (hb.status) {
+    // this call's bits: a fresh word, published by the merge kernel
+    sa.status = slot;
+    c->sa.status = slot;
+    c->ma.status = slot;
+    published = static_cast<uint32_t*>(mapped_host(hb.status, 4));
+    c->ma.status_out = published ? published : slot + 1;
+  }
+  int64_t vec = 0;
+  for (int i = 0; i < sa.n; ++i) vec += sa.words[i] / 4;
+  const int64_t want = (vec + kStageThreads * 4 - 1) / (kStageThreads * 4);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 2 * (int64_t)c->plan.grid));
+  pa_stage_in_kernel<<<grid, kStageThreads, 0, st>>>(sa);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  rc = run_phases(s, o, k_cache, v_cache, c, st);
+  if (rc) return rc;
+  const cudaMemcpyKind back = cudaMemcpyDeviceToHost;
+  if (c->sa.out == reinterpret_cast<float*>(ws + h.out) &&
+      cudaMemcpyAsync(hb.out, ws + h.out, h.out_bytes, back, st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (hb.status && !published &&
+      cudaMemcpyAsync(hb.status, slot + 1, sizeof(uint32_t), back, st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -887,6 +1042,99 @@ int pa_decode_multi(const pa_shape* shape, const pa_options* options, const void
   c.ma.cu_q = cu_seqlens_q;
   c.ma.total_q = total_q;
   return run_phases(shape, options, k_cache, v_cache, &c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_workspace_size_host(const pa_shape* shape, const pa_options* options, size_t* bytes) {
+  if (!shape || !bytes) return PA_ERR_NULL;
+  Plan p;
+  int rc = make_plan(shape, options, false, &p);
+  if (rc) return rc;
+  *bytes = host_layout(p, shape, shape->batch, false).total;
+  return PA_OK;
+}
+
+int pa_decode_host(const pa_shape* shape, const pa_options* options, const void* q_host,
+                   const void* k_cache, const void* v_cache, const int32_t* block_table_host,
+                   const int32_t* cache_seqlens_host, float scale, float* out_host,
+                   uint32_t* status_host, void* workspace, size_t workspace_bytes,
+                   pa_stream_t stream) {
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (options && options->phase != PA_PHASE_BOTH) return PA_ERR_OPTION;
+  if (shape->batch == 0) {  // a no-op, as for pa_decode
+    if (status_host) *status_host = 0;
+    return PA_OK;
+  }
+  if (!q_host || !block_table_host || !cache_seqlens_host || !out_host || !workspace)
+    return PA_ERR_NULL;
+  Plan p;
+  rc = make_plan(shape, options, false, &p);
+  if (rc) return rc;
+  const HostLayout h = host_layout(p, shape, shape->batch, false);
+  if (workspace_bytes < h.total) return PA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Call c;
+  rc = prepare(shape, options, ws + h.q, k_cache, v_cache,
+               reinterpret_cast<const int32_t*>(ws + h.table),
+               reinterpret_cast<const int32_t*>(ws + h.lens), scale,
+               host_out_target(h, ws, out_host), workspace, p.total, true, &c);
+  if (rc) return rc;
+  const HostBuffers hb{q_host, nullptr, block_table_host, cache_seqlens_host, out_host,
+                       status_host};
+  return run_host_step(shape, options, h, ws, hb, k_cache, v_cache, &c,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pa_workspace_size_multi_host(const pa_shape* shape, const pa_options* options, int32_t max_q,
+                                 int32_t max_total_q, size_t* bytes) {
+  if (!shape || !bytes) return PA_ERR_NULL;
+  if (max_q < 1 || max_total_q < 0) return PA_ERR_SHAPE;
+  Plan p;
+  int rc = make_plan(shape, options, false, &p, max_q);
+  if (rc) return rc;
+  *bytes = host_layout(p, shape, max_total_q, true).total;
+  return PA_OK;
+}
+
+int pa_decode_multi_host(const pa_shape* shape, const pa_options* options, const void* q_host,
+                         const int32_t* cu_seqlens_q_host, int32_t total_q, int32_t max_q,
+                         int32_t causal, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table_host, const int32_t* cache_seqlens_host,
+                         float scale, float* out_host, uint32_t* status_host, void* workspace,
+                         size_t workspace_bytes, pa_stream_t stream) {
+  if (max_q < 1 || total_q < 0) return PA_ERR_SHAPE;
+  int rc = check_shape(shape);
+  if (rc) return rc;
+  if (options && options->phase != PA_PHASE_BOTH) return PA_ERR_OPTION;
+  if (shape->batch == 0 || total_q == 0) {  // nothing to attend
+    if (status_host) *status_host = 0;
+    return PA_OK;
+  }
+  if (!q_host || !cu_seqlens_q_host || !block_table_host || !cache_seqlens_host || !out_host ||
+      !workspace)
+    return PA_ERR_NULL;
+  Plan p;
+  rc = make_plan(shape, options, false, &p, max_q);
+  if (rc) return rc;
+  const HostLayout h = host_layout(p, shape, total_q, true);
+  if (workspace_bytes < h.total) return PA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Call c;
+  rc = prepare(shape, options, ws + h.q, k_cache, v_cache,
+               reinterpret_cast<const int32_t*>(ws + h.table),
+               reinterpret_cast<const int32_t*>(ws + h.lens), scale,
+               host_out_target(h, ws, out_host), workspace, p.total, true, &c, max_q);
+  if (rc) return rc;
+  const int32_t* cu = reinterpret_cast<const int32_t*>(ws + h.cu);
+  c.sa.cu_q = cu;
+  c.sa.causal = causal ? 1 : 0;
+  c.sa.total_q = total_q;
+  c.ma.cu_q = cu;
+  c.ma.total_q = total_q;
+  const HostBuffers hb{q_host, cu_seqlens_q_host, block_table_host, cache_seqlens_host, out_host,
+                       status_host};
+  return run_host_step(shape, options, h, ws, hb, k_cache, v_cache, &c,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 int pa_cache_append(const pa_shape* shape, const void* k_new, const void* v_new, void* k_cache,

@@ -132,6 +132,21 @@ struct MergeArgs {
   int32_t C;         // columns per row (G in decode)
   const int32_t* cu_q;  // non-null: rows of several query tokens (see SplitArgs)
   int32_t nqg, tq, total_q, max_q;
+  // status_out non-null: once the split grid is done, CTA 0 copies the status
+  // word the split kernel accumulated (*status) to *status_out and clears it
+  uint32_t* status;
+  uint32_t* status_out;
+};
+
+// Host-to-device staging by the SMs: n parts of `words` 4-byte words each,
+// read from page-locked host memory the device maps (src) and written to
+// device memory (dst); `status`, if not null, is cleared first.
+struct StageArgs {
+  const uint32_t* src[4];
+  uint32_t* dst[4];
+  int64_t words[4];
+  int32_t n;
+  uint32_t* status;
 };
 
 struct AppendArgs {

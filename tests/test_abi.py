@@ -205,3 +205,48 @@ def test_batch_limit_matches_the_header():
     with pytest.raises(pg.PagedGQAError) as e:
         pg.pa_workspace_size(s, pg.options(num_ctas=8))
     assert e.value.code == pg.PA_ERR_SHAPE
+
+
+def test_host_buffer_calls_reject_bad_arguments_before_any_cuda_call():
+    L = pg.lib()
+    o = pg.options(num_ctas=8)
+    s = shape()
+    st = ctypes.c_uint32(7)
+
+    def host(s=s, opts=o, q=FAKE, t=FAKE, sl=FAKE, out=FAKE, ws=FAKE, ws_bytes=1 << 30):
+        return L.pa_decode_host(ctypes.byref(s), ctypes.byref(opts) if opts else None, q, FAKE,
+                                FAKE, t, sl, 0.125, out, ctypes.byref(st), ws, ws_bytes, None)
+
+    for kw in (dict(q=None), dict(t=None), dict(sl=None), dict(out=None), dict(ws=None)):
+        assert host(**kw) == pg.PA_ERR_NULL, kw
+    need = pg.pa_workspace_size_host(s, o)
+    assert host(ws_bytes=need - 1) == pg.PA_ERR_WORKSPACE
+    assert host(opts=pg.options(num_ctas=8, phase=pg.PA_PHASE_SPLIT)) == pg.PA_ERR_OPTION
+    assert host(s=shape(d=96)) == pg.PA_ERR_SHAPE
+    # an empty batch is a no-op that needs no pointers and reports a clean status
+    assert host(s=shape(B=0), q=None, t=None, sl=None, out=None, ws=None) == pg.PA_OK
+    assert st.value == 0
+
+    def multi(total_q=5, max_q=2, ws_bytes=1 << 30, cu=FAKE):
+        return L.pa_decode_multi_host(ctypes.byref(s), ctypes.byref(o), FAKE, cu, total_q, max_q,
+                                      1, FAKE, FAKE, FAKE, FAKE, 0.125, FAKE, ctypes.byref(st),
+                                      FAKE, ws_bytes, None)
+
+    assert multi(cu=None) == pg.PA_ERR_NULL
+    assert multi(max_q=0) == pg.PA_ERR_SHAPE
+    assert multi(total_q=-1) == pg.PA_ERR_SHAPE
+    n5 = pg.pa_workspace_size_multi_host(s, 2, 5, o)
+    assert multi(ws_bytes=n5 - 1) == pg.PA_ERR_WORKSPACE
+    st.value = 7
+    assert multi(total_q=0) == pg.PA_OK and st.value == 0
+
+
+def test_host_workspace_adds_the_staging():
+    s = shape(B=256, H=32, Hkv=8, d=128, bs=32, maxblk=1024, P=30000, dtype=pg.PA_BF16)
+    o = pg.options(num_ctas=304)
+    base, host = pg.pa_workspace_size(s, o), pg.pa_workspace_size_host(s, o)
+    staged = 256 * 32 * 128 * (2 + 4) + 256 * 1024 * 4 + 256 * 4 + 4
+    assert staged <= host - base <= staged + 6 * 256
+    m = [pg.pa_workspace_size_multi_host(s, 4, n, o) for n in (0, 1, 1024)]
+    assert m[0] >= pg.pa_workspace_size_multi(s, 4, o) + 256 * 1024 * 4
+    assert m[1] - m[0] >= 32 * 128 * 6 and m[2] - m[0] >= 1024 * 32 * 128 * 6
