@@ -191,15 +191,18 @@ def make_room_for_next_token(w):
         w.num_blocks += extra
 
 
-def make_workload(name, query_tokens=0):
+def make_workload(name, query_tokens=0, group=0):
     """The named workload; query_tokens > 0 gives every sequence that many
-    query tokens (its last positions, causal)."""
+    query tokens (its last positions, causal); group > 0 sets G query heads
+    per kv head over the same cache."""
     from paged_gqa_decode_pa_gb300 import workloads as wl
 
     w = wl.make(name)
     if query_tokens > 0:
         w = wl.with_query_tokens(w, np.full(w.B, query_tokens), seed=w.seed + 2000,
                                  name=f"{w.name}+q{query_tokens}")
+    if group > 0:
+        w = wl.with_group(w, group, seed=w.seed + 3000, name=f"{w.name}+G{group}")
     return w
 
 
@@ -282,7 +285,7 @@ def run_reference(args, rank, world):
     """The oracle timed on the host cores (rank 0 only)."""
     if rank != 0:
         return
-    w = make_workload(args.config, args.query_tokens)
+    w = make_workload(args.config, args.query_tokens, args.group)
     per_step = max(0.05, min(1.0, 90.0 / max(1, args.steps + args.warmup)))
     gbs, dt, pairs, threads, _ = oracle_sample(w, per_step)
     for _ in range(args.warmup):
@@ -318,7 +321,7 @@ def workload_config(w, args):
             "partition_tokens": args.partition_tokens, "compute": args.compute,
             "stages": args.stages, "graph": bool(args.graph),
             "fused_append": bool(args.fused_append),
-            "query_tokens": query_rows(w), "causal": bool(w.causal) if w.cu_q is not None else None,
+            "query_rows_per_step": query_rows(w), "causal": bool(w.causal) if w.cu_q is not None else None,
             "kv_bytes_per_step": w.kv_bytes(),
             "l2": ("inputs larger than L2" if w.kv_bytes() > 2 * L2_BYTES
                    else "L2 flushed between timed steps"),
@@ -332,7 +335,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = make_workload(args.config, args.query_tokens)
+    w = make_workload(args.config, args.query_tokens, args.group)
     if args.fused_append:
         make_room_for_next_token(w)
     q, k, v, t, sl = w.torch_tensors(dev)
@@ -585,6 +588,8 @@ def main():
     ap.add_argument("--stages", type=int, default=0, help="pipeline stages (0 = library choice)")
     ap.add_argument("--query-tokens", type=int, default=0,
                     help="query tokens per sequence (0 = the workload's own: one in decode)")
+    ap.add_argument("--group", type=int, default=0,
+                    help="G query heads per kv head over the same cache (0 = the workload's)")
     ap.add_argument("--fused-append", action="store_true",
                     help="time pa_decode_append (write the new token, attend over len+1)")
     ap.add_argument("--graph", action="store_true",

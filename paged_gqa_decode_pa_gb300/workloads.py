@@ -313,6 +313,21 @@ def with_query_tokens(w: Workload, lens_q, seed: int = 0, causal: bool = True,
     return w
 
 
+def with_group(w: Workload, G: int, seed: int = 0, name: Optional[str] = None) -> Workload:
+    """The same cache, table and lengths with G query heads per kv head
+    (H = G * Hkv), the queries drawn afresh: the K/V a step reads does not
+    change with G, only the heads that share it."""
+    if G < 1:
+        raise ValueError("G >= 1")
+    rng = np.random.default_rng(seed)
+    w.H = G * w.Hkv
+    rows = w.B if w.cu_q is None else int(w.cu_q[-1])
+    w.q = _normal_bits(rng, (rows, w.H, w.d), w.dtype)
+    if name:
+        w.name = name
+    return w
+
+
 def serving_mix_b256_q4_g4_d128(seed: int = 5, poison: bool = False) -> Workload:
     """The serving mix verifying 4 tokens per sequence (3 drafted + 1), causal."""
     w = serving_mix_b256_g4_d128(seed, poison)

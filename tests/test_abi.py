@@ -250,3 +250,19 @@ def test_host_workspace_adds_the_staging():
     m = [pg.pa_workspace_size_multi_host(s, 4, n, o) for n in (0, 1, 1024)]
     assert m[0] >= pg.pa_workspace_size_multi(s, 4, o) + 256 * 1024 * 4
     assert m[1] - m[0] >= 32 * 128 * 6 and m[2] - m[0] >= 1024 * 32 * 128 * 6
+
+
+def test_with_group_keeps_the_cache_and_draws_new_queries():
+    from paged_gqa_decode_pa_gb300 import workloads as wl
+
+    a = wl.random_workload([5, 40, 0], H=8, Hkv=2, d=64, bs=16, dtype="f16", seed=3)
+    k, v, t, sl = a.k_cache.copy(), a.v_cache.copy(), a.block_table.copy(), a.cache_seqlens.copy()
+    b = wl.with_group(a, 3, seed=9)
+    assert b.H == 6 and b.G == 3 and b.q.shape == (3, 6, 64)
+    assert np.array_equal(b.k_cache, k) and np.array_equal(b.v_cache, v)
+    assert np.array_equal(b.block_table, t) and np.array_equal(b.cache_seqlens, sl)
+    c = wl.with_group(wl.random_workload([5, 40, 0], H=8, Hkv=2, d=64, bs=16, dtype="f16",
+                                         seed=3), 3, seed=9)
+    assert np.array_equal(b.q, c.q)  # seeded
+    with pytest.raises(ValueError):
+        wl.with_group(c, 0)

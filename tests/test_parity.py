@@ -185,6 +185,20 @@ def test_empty_and_full_sequences():
     assert_close(got, run_oracle(w), "full table row")
 
 
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 6, 7, 8])
+def test_every_group_size_over_one_cache(G):
+    """The same cache, table and lengths read by G = 1..8 query heads per kv
+    head: every group size the library takes, odd ones included."""
+    base = wl.random_workload([1, 15, 16, 17, 300, 0, 1000, 129], H=8, Hkv=4, d=128, bs=16,
+                              dtype="bf16", seed=41, poison=True, outlier_frac=0.02)
+    w = wl.with_group(base, G, seed=50 + G)
+    assert w.H == 4 * G
+    for opts in (None, pg.options(num_ctas=7)):
+        got, st = run_gpu(w, opts)
+        assert st == 0
+        assert_close(got, run_oracle(w), f"G={G}")
+
+
 def test_simt_and_mma_agree():
     w = wl.random_workload([3000, 1, 77], H=24, Hkv=4, d=256, bs=16, dtype="bf16", seed=9)
     a, _ = run_gpu(w, pg.options(compute="mma"))
