@@ -224,9 +224,9 @@ int pa_decode_append(const pa_shape* shape, const pa_options* options, const voi
  * to no sequence are not written.  The workspace must hold
  * pa_workspace_size_multi(shape, options, max_q) bytes (zero-filled once, as
  * for pa_decode).  Tensor-core path only (options->compute SIMT is
- * PA_ERR_OPTION).  Up to 16 (token, head) pairs of one kv head share one pass
- * over its K/V (8 at d = 256): a sequence with n_q * G above that is read
- * ceil(n_q * G / 16) times. */
+ * PA_ERR_OPTION).  Up to 32 (token, head) pairs of one kv head share one pass
+ * over its K/V (16 at d = 256, and with PA_COMPUTE_TC): a sequence with
+ * n_q * G above that is read ceil(n_q * G / 32) times (16). */
 #define PA_MAX_QUERY_TOKENS 4096
 int pa_workspace_size_multi(const pa_shape* shape, const pa_options* options, int32_t max_q,
                             size_t* bytes);

@@ -355,15 +355,17 @@ int choose_mode(const pa_options* o) {
   return c == PA_COMPUTE_SIMT ? kSimt : (c == PA_COMPUTE_TC ? kTc : kMma);
 }
 
-// Ring slots per warp: 2 by default (measured best for every head dimension:
-// one tile computing, one in flight), fewer when shared memory does not hold
-// them; at most what fits in the per-block limit.
+// Ring slots per tile stream: 2 by default (measured best for every head
+// dimension: one tile computing, one in flight), 4 for a warp pair's stream
+// (the same stages per CTA), fewer when shared memory does not hold them; at
+// most what fits in the per-block limit.
 int choose_ring(const pa_shape* s, const pa_options* o, int mode, int W, int C, int rows) {
+  const int streams = split_streams(W, mode);
   const SmemLayout L0 = split_smem_layout(s->head_dim, C, rows, W, 0, mode);
-  int fit = (kMaxDynamicSmem - (int)L0.total) / (W * (int)L0.stage_bytes);
-  if (fit > kMaxSlots / W) fit = kMaxSlots / W;
+  int fit = (kMaxDynamicSmem - (int)L0.total) / (streams * (int)L0.stage_bytes);
+  if (fit > kMaxSlots / streams) fit = kMaxSlots / streams;
   if (o && o->stages > 0) return o->stages <= fit ? o->stages : -1;
-  const int want = 2;
+  const int want = mode == kMmaP ? 4 : 2;
   return fit < want ? fit : want;
 }
 
@@ -377,6 +379,7 @@ const void* kernel_for(int dtype, int D, int mode, int multi) {
 #define PA_PICK(T, DD)                                                                 \
   if (D == DD) return mode == kSimt ? split_kernel_ptr<T, DD, kSimt>()                \
                       : mode == kMmaQ ? split_kernel_ptr<T, DD, kMmaQ>()              \
+                      : mode == kMmaP ? split_kernel_ptr<T, DD, kMmaP>()              \
                                       : split_kernel_ptr<T, DD, kMma>();
   if (dtype == PA_BF16) {
     PA_PICK(__nv_bfloat16, 64)
@@ -455,10 +458,12 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
   if (max_q > 0) {
     if (max_q > PA_MAX_QUERY_TOKENS) return PA_ERR_SHAPE;
     if (p->mode == kSimt) return PA_ERR_OPTION;  // tensor-core path only
-    // groups of up to 16 (token, head) columns; the tcgen05 kernel keeps the
-    // mma kernel's grouping (N = 16)
-    if (p->mode != kTc) p->mode = kMmaQ;
-    p->tq = (p->mode == kTc ? kTcN : 8 * mma_blocks(p->D, kMmaQ)) / p->G;
+    // groups of (token, head) columns: a warp keeps cw = 8 x mma_blocks of
+    // them; rows wider than that go to warp pairs (2 cw columns, one read of
+    // the K/V).  The tcgen05 kernel keeps groups of N = 16.
+    const int cw = 8 * mma_blocks(p->D, kMmaQ);
+    if (p->mode != kTc) p->mode = (int64_t)max_q * p->G > cw ? kMmaP : kMmaQ;
+    p->tq = (p->mode == kTc ? kTcN : (p->mode == kMmaP ? 2 * cw : cw)) / p->G;
     p->nqg = (max_q + p->tq - 1) / p->tq;
     p->C = p->tq * p->G;
     if ((int64_t)s->batch * p->nqg > PA_MAX_BATCH) return PA_ERR_SHAPE;
@@ -766,6 +771,8 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
             ? launch_split<T, DD, kSimt>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream)     \
         : p.mode == kMmaQ                                                                       \
             ? launch_split<T, DD, kMmaQ>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream)     \
+        : p.mode == kMmaP                                                                       \
+            ? launch_split<T, DD, kMmaP>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream)     \
             : launch_split<T, DD, kMma>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream);
   if (s->dtype == PA_BF16) {
     PA_LAUNCH(__nv_bfloat16, 64)

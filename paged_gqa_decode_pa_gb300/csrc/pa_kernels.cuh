@@ -18,7 +18,8 @@ constexpr int kMaxWarps = 8;   // warps per split CTA (each runs its own TMA rin
 PA_HD constexpr int split_warps(int D) { return D == 256 ? 4 : kMaxWarps; }
 constexpr int kMaxSlots = 64;  // warps x ring slots
 constexpr int kGMax = 8;       // query heads per kv head handled by one CTA
-constexpr int kColMax = 16;    // query columns (token, head) per row: two mma n-blocks
+constexpr int kColMax = 16;    // query columns (token, head) of a warp state: two mma n-blocks
+constexpr int kRowCols = 32;   // query columns of a row: a warp pair's two states
 constexpr int kTile = 16;      // tokens per pipeline stage (one mma row tile)
 constexpr int kMergeThreads = 128;
 // Slack of the lazy running max in the tensor-core tile (log2 units): p <= 2^8.
@@ -26,12 +27,19 @@ constexpr float kLazyMax = 8.f;
 
 // kSimt / kMma: one query token per sequence (decode).  kMmaQ: several query
 // tokens per sequence; a row is a group of one sequence's query tokens whose
-// (token, head) pairs fill up to mma_blocks(D) x 8 columns.
-enum Mode { kSimt = 1, kMma = 2, kMmaQ = 3, kTc = 4 };  // kTc: the tcgen05 kernel (pa_split_tc.cuh)
+// (token, head) pairs fill up to mma_blocks(D) x 8 columns.  kMmaP: the same
+// with warp pairs -- warps w and w + W/2 consume the same tiles (stream
+// w % (W/2)), each for its own half of the row's columns ([0, 8 NB) and
+// [8 NB, C)), so a row of up to 16 NB columns reads its K/V once; the lower
+// warp loads the tiles, the upper one releases each ring slot through the
+// slot's "empty" mbarrier.
+enum Mode { kSimt = 1, kMma = 2, kMmaQ = 3, kTc = 4, kMmaP = 5 };  // kTc: pa_split_tc.cuh
+
+PA_HD constexpr bool several_tokens(int mode) { return mode == kMmaQ || mode == kMmaP; }
 
 // mma n-blocks of 8 query columns a warp keeps (registers allow two below
 // d = 256).
-PA_HD constexpr int mma_blocks(int D, int mode) { return (mode == kMmaQ && D <= 128) ? 2 : 1; }
+PA_HD constexpr int mma_blocks(int D, int mode) { return (several_tokens(mode) && D <= 128) ? 2 : 1; }
 
 struct SplitArgs {
   const uint16_t* q;        // [B, H, D] raw 16-bit patterns
@@ -118,6 +126,9 @@ struct MultiLen {
 constexpr uint32_t kArgsBytes = 256;
 constexpr uint32_t kArgsOffset = 1024;
 static_assert(sizeof(SplitArgs) <= kArgsBytes && sizeof(SplitArgs) % 4 == 0, "SplitArgs copy");
+// Warp pairs: one "empty" mbarrier per ring slot, after the SplitArgs copy.
+constexpr uint32_t kEmptyOffset = kArgsOffset + kArgsBytes;
+static_assert(kEmptyOffset + 8u * kMaxSlots <= 2048u, "empty barriers below the stages");
 
 struct MergeArgs {
   const int32_t* seqlens;
@@ -164,11 +175,12 @@ struct AppendArgs {
 // a 1024-byte aligned base.
 struct SmemLayout {
   uint32_t full, info, abort_flag;  // per slot: mbarrier, (phys << 32 | bad | valid rows)
-  uint32_t stage;                   // [W][R] stages: K chunks | V chunks, 16 rows each
+  uint32_t empty;                   // per slot (warp pairs): released by the upper warp
+  uint32_t stage;                   // [streams][R] stages: K chunks | V chunks, 16 rows each
   uint32_t stage_bytes;
   uint32_t mo, mm, ml, mbad;        // per-warp partial states for the CTA combine
   uint32_t qs;                      // [C][D+4] fp32 q of the current piece (x scale*log2(e): CUDA cores)
-  uint32_t qlim;                    // [kColMax] int32 key limit per column (several tokens)
+  uint32_t qlim;                    // [kRowCols] int32 key limit per column (several tokens)
   uint32_t qraw;                    // [C][D] raw 16-bit q of the next piece (cp.async target)
   uint32_t args;                    // a copy of the SplitArgs, read by the once-per-piece code
   uint32_t zrow;                    // one all-zero K/V row (D x 2 bytes)
@@ -180,17 +192,27 @@ struct SmemLayout {
 
 PA_HD uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// C = query columns per row (G in decode), B = rows.
+// Tile streams of a CTA: one per warp, or one per warp pair (kMmaP).
+PA_HD constexpr int split_streams(int W, int mode) { return mode == kMmaP ? W / 2 : W; }
+
+// Columns of the row a warp keeps (the stride of its published state).
+PA_HD constexpr int warp_columns(int D, int C, int mode) {
+  return mode == kMmaP ? 8 * mma_blocks(D, mode) : C;
+}
+
+// C = query columns per row (G in decode), B = rows, R = ring slots per
+// tile stream.
 PA_HD SmemLayout split_smem_layout(int D, int C, int B, int W, int R, int mode) {
   SmemLayout L;
   L.full = 0;
   L.info = 8 * kMaxSlots;
   L.args = kArgsOffset;  // fixed, so it can be filled before the layout is known
+  L.empty = kEmptyOffset;
   L.stage = 2048;
   L.stage_bytes = 4u * (uint32_t)D * (uint32_t)kTile;  // K + V tiles, 2 bytes each
-  uint32_t off = L.stage + (uint32_t)(W * R) * L.stage_bytes;
+  uint32_t off = L.stage + (uint32_t)(split_streams(W, mode) * R) * L.stage_bytes;
   L.mo = off;
-  off += (uint32_t)(W * C * (D + 4)) * 4u;
+  off += (uint32_t)(W * warp_columns(D, C, mode) * (D + 4)) * 4u;
   L.mm = off;
   off += (uint32_t)W * kColMax * 4u;
   L.ml = off;
@@ -200,7 +222,7 @@ PA_HD SmemLayout split_smem_layout(int D, int C, int B, int W, int R, int mode) 
   L.abort_flag = off;  // followed by the current piece's stored length, q0, nq
   off += 16u;
   L.qlim = off;
-  off += (uint32_t)kColMax * 4u;
+  off += (uint32_t)kRowCols * 4u;
   off = align_up(off, 16);
   L.qs = off;
   off += (uint32_t)(C * (D + 4)) * 4u;

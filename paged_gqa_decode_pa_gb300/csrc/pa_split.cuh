@@ -273,13 +273,15 @@ struct MmaState {
     }
   }
 
-  // Publish this warp's state for the CTA-level combine.
-  __device__ __forceinline__ void publish(uint8_t* smem, const SmemLayout& L, int w, int C) {
+  // Publish this warp's state for the CTA-level combine: its C columns, in
+  // a slot of `stride` columns.
+  __device__ __forceinline__ void publish(uint8_t* smem, const SmemLayout& L, int w, int C,
+                                          int stride) {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     float* mm = reinterpret_cast<float*>(smem + L.mm) + w * kColMax;
     float* ml = reinterpret_cast<float*>(smem + L.ml) + w * kColMax;
-    float* mo = reinterpret_cast<float*>(smem + L.mo) + (size_t)w * C * (D + 4);
+    float* mo = reinterpret_cast<float*>(smem + L.mo) + (size_t)w * stride * (D + 4);
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
       float l0 = l[nb][0], l1 = l[nb][1];
@@ -482,10 +484,14 @@ __device__ __forceinline__ int64_t column_out(const SplitArgs& a, int row, int j
 // column that saw no key (l = 0: a query token whose causal limit is 0)
 // gets 0, as an empty sequence does.
 // q0, nq: the query rows of the piece's sequence (several query tokens).
-template <int D, int W, bool kQ>
+// kPair: warp pairs, warps [0, W/2) hold columns [0, cw) and warps
+// [W/2, W) columns [cw, C), each state with cw columns; otherwise every warp
+// holds all C columns.
+template <int D, int W, bool kQ, bool kPair>
 __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem, const SmemLayout& L,
-                                              const Piece& pc, int q0, int nq) {
+                                              const Piece& pc, int q0, int nq, int cw) {
   const int C = a.C;
+  const int stride = kPair ? cw : C;  // columns of one published warp state
   const float* mm = reinterpret_cast<const float*>(smem + L.mm);
   const float* ml = reinterpret_cast<const float*>(smem + L.ml);
   const float* mo = reinterpret_cast<const float*>(smem + L.mo);
@@ -500,19 +506,27 @@ __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem,
   // these are broadcast loads), with no shuffles on the way.
   for (int idx = threadIdx.x; idx < C * D; idx += blockDim.x) {
     const int c = idx / D, dim = idx % D;
-    float mw[W];
+    // the warps holding column c, and its index in their states
+    constexpr int NW = kPair ? W / 2 : W;  // warps holding a column
+    int w0 = 0, lc = c;
+    if constexpr (kPair) {
+      const int cg = c >= cw ? 1 : 0;
+      w0 = cg * NW;
+      lc = c - cg * cw;
+    }
+    float mw[NW];
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      mw[w] = mm[w * kColMax + c];
+    for (int w = 0; w < NW; ++w) {
+      mw[w] = mm[(w0 + w) * kColMax + lc];
       M = fmaxf(M, mw[w]);
     }
     float Lsum = 0.f, o = 0.f;
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const float e = (mw[w] == -INFINITY) ? 0.f : ex2(mw[w] - M);
-      Lsum = fmaf(e, ml[w * kColMax + c], Lsum);
-      o = fmaf(e, mo[(w * C + c) * (D + 4) + dim], o);
+      Lsum = fmaf(e, ml[(w0 + w) * kColMax + lc], Lsum);
+      o = fmaf(e, mo[((w0 + w) * stride + lc) * (D + 4) + dim], o);
     }
     if (pc.slot < 0) {
       const int64_t r = column_out<kQ>(a, pc.b, pc.j, c, q0, nq);
@@ -527,11 +541,10 @@ __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem,
   }
 }
 
-// Number of the piece's tiles that belong to warp w (tiles t = w, w+W, ...).
-template <int W>
-__device__ __forceinline__ int warp_tiles(const Piece& pc, int sl, int w) {
+// Tiles of stream s of S in a piece: tiles s, s + S, ...
+__device__ __forceinline__ int stream_tiles(const Piece& pc, int sl, int s, int S) {
   const int nt = (pc.blk1 - pc.blk0) << sl;
-  return nt > w ? (nt - w + W - 1) / W : 0;
+  return nt > s ? (nt - s + S - 1) / S : 0;
 }
 
 // The issuing side of one warp's pipeline: walks the warp's tile stream (all
@@ -553,21 +566,23 @@ struct IssuerT {
   bool done;
 };
 
-template <int W>
+// Block-table entry of the ii-th tile of stream s (of S) in piece pc.
 __device__ __forceinline__ int32_t table_entry(const SplitArgs& a, const Piece& pc, int seq, int cnt,
-                                               int ii, int sl, int w) {
+                                               int ii, int sl, int s, int S) {
   if (ii >= cnt) return 0;
-  const int t = w + W * ii;
+  const int t = s + S * ii;
   return __ldg(a.table + (int64_t)seq * a.maxblk + pc.blk0 + (t >> sl));
 }
 
 // a: the arguments in the constant bank (read for every tile); pa: their
 // shared-memory copy (read when the issuer moves to the next piece).
-template <int D, int W, class LenOf>
+// s: the warp's tile stream, of S (one per warp, or one per warp pair).
+template <int D, class LenOf>
 __device__ __forceinline__ void issue_next(IssuerT<LenOf>& is, const SplitArgs& a,
                                            const SplitArgs& pa, const CUtensorMap* tmk,
                                            const CUtensorMap* tmv, uint32_t base,
-                                           const SmemLayout& L, int w, uint32_t slot, int sl) {
+                                           const SmemLayout& L, int s, int S, uint32_t slot,
+                                           int sl) {
   const int lane = threadIdx.x & 31;
   while (!is.done && is.i >= is.cnt) {
     if (!is.it.next(is.pc)) {
@@ -575,26 +590,26 @@ __device__ __forceinline__ void issue_next(IssuerT<LenOf>& is, const SplitArgs& 
       break;
     }
     is.i = 0;
-    is.cnt = warp_tiles<W>(is.pc, sl, w);
+    is.cnt = stream_tiles(is.pc, sl, s, S);
     is.win = 0;
     is.len = is.it.len_of(is.pc.b);
     is.seq = pa.nqg > 1 ? is.pc.b / pa.nqg : is.pc.b;
-    is.entry = table_entry<W>(pa, is.pc, is.seq, is.cnt, lane, sl, w);
-    is.entry_next = table_entry<W>(pa, is.pc, is.seq, is.cnt, 32 + lane, sl, w);
+    is.entry = table_entry(pa, is.pc, is.seq, is.cnt, lane, sl, s, S);
+    is.entry_next = table_entry(pa, is.pc, is.seq, is.cnt, 32 + lane, sl, s, S);
   }
   if (is.done) return;
   if (is.i >= is.win + 32) {
     is.win += 32;
     is.entry = is.entry_next;
-    is.entry_next = table_entry<W>(pa, is.pc, is.seq, is.cnt, is.win + 32 + lane, sl, w);
+    is.entry_next = table_entry(pa, is.pc, is.seq, is.cnt, is.win + 32 + lane, sl, s, S);
   }
   const int32_t phys = __shfl_sync(0xffffffffu, is.entry, is.i - is.win);
   if (lane == 0) {
-    const int t = w + W * is.i;
+    const int t = s + S * is.i;
     const int blk = is.pc.blk0 + (t >> sl), h = t & ((1 << sl) - 1);
     const int valid = max(0, min(kTile, is.len - blk * a.bs - h * kTile));
     const bool bad = phys < 0 || phys >= a.P;
-    const uint32_t gslot = (uint32_t)w * a.ring + slot;
+    const uint32_t gslot = (uint32_t)s * a.ring + slot;
     const uint32_t full = base + L.full + 8 * gslot;
     sts64(base + L.info + 8 * gslot,
           ((uint64_t)(uint32_t)phys << 32) | (uint32_t)valid | (bad ? kInfoBad : 0u));
@@ -684,7 +699,7 @@ struct QStage {
       // the key limit of every column: tokens t < limit are visible; columns
       // that hold no query see everything (their q is zero)
       const int c = threadIdx.x;
-      if (c < kColMax) {
+      if (c < kRowCols) {
         int32_t lim = 0x7fffffff;
         const int tok = grp * a.tq + c / a.G;
         if (c < a.C && tok < nq && a.causal) lim = max(0, min(len, len - nq + tok + 1));
@@ -758,7 +773,8 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     pa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                     const __grid_constant__ SplitArgs a) {
   constexpr int W = split_warps(D);
-  constexpr bool kQ = MODE == kMmaQ;
+  constexpr bool kQ = several_tokens(MODE);
+  constexpr bool kPair = MODE == kMmaP;
   constexpr int NB = mma_blocks(D, MODE);
   using RowLen = typename std::conditional<kQ, MultiLen, DecodeLen>::type;
   extern __shared__ uint8_t smem_raw[];
@@ -775,7 +791,9 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     reinterpret_cast<uint32_t*>(sa)[i] = reinterpret_cast<const uint32_t*>(&a)[i];
   __syncthreads();
   const SplitArgs& A = *sa;
-  const int R = a.ring;
+  const int R = a.ring;  // ring slots per tile stream
+  // tile streams: one per warp, or one per warp pair
+  constexpr int S = split_streams(W, MODE);
   const SmemLayout L = split_smem_layout(D, A.C, A.B, W, A.ring, MODE);
 
   const int warp = tid >> 5, lane = tid & 31;
@@ -794,7 +812,10 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   }
 
   if (tid == 0) {
-    for (int s = 0; s < W * R; ++s) mbar_init(base + L.full + 8 * s, 1);
+    for (int s = 0; s < S * R; ++s) {
+      mbar_init(base + L.full + 8 * s, 1);
+      if (kPair) mbar_init(base + L.empty + 8 * s, 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -821,6 +842,12 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   rows_without_keys_and_descriptors<D, kQ>(a, len_of, pre, sched, cta);
 
   const int w = warp;
+  // the warp's tile stream and column group: with warp pairs, warps w and
+  // w + W/2 take the same tiles, the lower one issuing their copies
+  const int sw = kPair ? w % S : w, cg = kPair ? w / S : 0;
+  const bool issuer = !kPair || cg == 0;
+  const int cw = warp_columns(D, A.C, MODE);           // columns of a warp state
+  const int cl = kPair ? min(cw, A.C - cg * cw) : A.C;  // columns this warp computes
   const int sl = a.bs == 16 ? 0 : (a.bs == 32 ? 1 : 2);  // log2(16-token tiles per block)
   constexpr int NC = D / 64;
   constexpr uint32_t chunk = kTile * 128u;
@@ -848,7 +875,8 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   is.seq = 0;
   is.issued = 0;
   is.done = false;
-  for (int r = 0; r < R; ++r) issue_next<D, W>(is, a, *sa, &tmk, &tmv, base, L, w, (uint32_t)r, sl);
+  if (issuer)
+    for (int r = 0; r < R; ++r) issue_next<D>(is, a, *sa, &tmk, &tmv, base, L, sw, S, (uint32_t)r, sl);
 
   // ---- the computing side
   if (have) cp_async_wait_all();
@@ -856,13 +884,17 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   if (have) qn.template finish<T, MODE == kSimt>(*sa, qraw, qs, piece_info, qlim);
   __syncthreads();
   uint32_t slot = 0, phase = 0;  // ring slot to consume next; per-slot parity bits
+  uint32_t ephase = 0;           // warp pairs, issuer: per-slot parity of the "empty" barriers
   uint32_t consumed = 0;
   MmaState<T, D, NB, kQ> mst;
   SimtState<T, D> sst;
   float* ps = reinterpret_cast<float*>(smem + L.ps) + w * kTile * kGMax;
   while (have) {
     if constexpr (MODE != kSimt) {
-      mst.load_q(qs, A.C, qlim, A.qscale);
+      if constexpr (kPair)
+        mst.load_q(qs + cg * cw * (D + 4), cl, qlim + cg * cw, A.qscale);
+      else
+        mst.load_q(qs, A.C, qlim, A.qscale);
       mst.reset();
     } else {
       sst.reset();
@@ -876,7 +908,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     }
     if (more) qn.start(*sa, next, qraw);
     bool bad = false;
-    const int cnt = warp_tiles<W>(pc, sl, w);
+    const int cnt = stream_tiles(pc, sl, sw, S);
     // fused append: the position of this sequence's new token; the warp
     // whose tile holds it loads the new K/V row now, ahead of that tile
     int32_t new_pos = -1;
@@ -884,7 +916,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     if (a.len_add) {
       const int32_t p0 = *reinterpret_cast<volatile int32_t*>(piece_info + 1);
       const int rel = p0 - pc.blk0 * a.bs;
-      if (rel >= 0 && rel < (pc.blk1 - pc.blk0) * a.bs && ((rel >> 4) % W) == w) {
+      if (rel >= 0 && rel < (pc.blk1 - pc.blk0) * a.bs && ((rel >> 4) % S) == sw) {
         new_pos = p0;
         const int64_t src = ((int64_t)pc.b * a.Hkv + pc.j) * D;
         if (lane < D / 8) {
@@ -894,7 +926,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       }
     }
     for (int i = 0; i < cnt; ++i) {
-      const uint32_t gslot = (uint32_t)w * R + slot;
+      const uint32_t gslot = (uint32_t)sw * R + slot;
       const bool ok = mbar_wait_bounded(base + L.full + 8 * gslot, (phase >> slot) & 1u, abort_flag,
                                         kWaitLimitNs);
       const uint64_t info64 = lds64(base + L.info + 8 * gslot);
@@ -910,7 +942,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
         const uint32_t sb = base + L.stage + gslot * L.stage_bytes;
         const uint32_t kb = sb + (a.kv_swap ? NC * chunk : 0u);
         const uint32_t vb = sb + (a.kv_swap ? 0u : NC * chunk);
-        const int t = w + W * i;
+        const int t = sw + S * i;
         const int tok0 = (pc.blk0 + (t >> sl)) * a.bs + (t & ((1 << sl) - 1)) * kTile;
         int new_r = -1;
         const uint32_t nkr = base + L.nrow + (uint32_t)w * 4u * D, nvr = nkr + 2u * D;
@@ -941,7 +973,21 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       __syncwarp();
       phase ^= 1u << slot;
       ++consumed;
-      issue_next<D, W>(is, a, *sa, &tmk, &tmv, base, L, w, slot, sl);
+      if (issuer) {
+        if constexpr (kPair) {
+          // the partner warp must be done with this slot before it is refilled
+          const bool freed = mbar_wait_bounded(base + L.empty + 8 * gslot, (ephase >> slot) & 1u,
+                                               abort_flag, kWaitLimitNs);
+          ephase ^= 1u << slot;
+          if (!freed) {
+            if (lane == 0) atomicOr(a.status, kStatusTimeout);
+            is.done = true;  // stop issuing
+          }
+        }
+        issue_next<D>(is, a, *sa, &tmk, &tmv, base, L, sw, S, slot, sl);
+      } else if (lane == 0) {
+        mbar_arrive(base + L.empty + 8 * gslot);  // this warp is done with the slot
+      }
       slot = (slot + 1 == (uint32_t)R) ? 0u : slot + 1;
     }
     if constexpr (kQ) {
@@ -949,7 +995,10 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     }
     if constexpr (MODE != kSimt) {
       mst.bad |= bad;
-      mst.publish(smem, L, w, A.C);
+      if constexpr (kPair)
+        mst.publish(smem, L, w, cl, cw);
+      else
+        mst.publish(smem, L, w, A.C, A.C);
     } else {
       sst.bad |= bad;
       sst.publish(smem, L, w, a.G);
@@ -959,7 +1008,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     const int q0 = kQ ? piece_info[2] : 0, nq = kQ ? piece_info[3] : 0;
     cp_async_wait_all();  // this thread's copies of the next q have landed
     named_bar_sync(1, blockDim.x);
-    combine_piece<D, W, kQ>(*sa, smem, L, pc, q0, nq);
+    combine_piece<D, W, kQ, kPair>(*sa, smem, L, pc, q0, nq, kPair ? cw : 0);
     if (more) qn.template finish<T, MODE == kSimt>(*sa, qraw, qs, piece_info, qlim);
     named_bar_sync(1, blockDim.x);
     have = it.next(pc);
@@ -969,7 +1018,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     // still in flight before the CTA may exit.
     volatile int never = 0;
     for (uint32_t kk = consumed; kk < is.issued; ++kk) {
-      mbar_wait_bounded(base + L.full + 8 * ((uint32_t)w * R + slot), (phase >> slot) & 1u, &never,
+      mbar_wait_bounded(base + L.full + 8 * ((uint32_t)sw * R + slot), (phase >> slot) & 1u, &never,
                         kWaitLimitNs / 4);
       phase ^= 1u << slot;
       slot = (slot + 1 == (uint32_t)R) ? 0u : slot + 1;

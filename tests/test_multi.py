@@ -65,8 +65,12 @@ def test_workspace_grows_with_query_groups():
     # fixed partitions: slots scale with the groups per sequence
     of = pg.options(num_ctas=304, partition_tokens=512)
     g1 = pg.pa_workspace_size_multi(s, 4, of)    # 1 group
-    g3 = pg.pa_workspace_size_multi(s, 12, of)   # 3 groups
+    g3 = pg.pa_workspace_size_multi(s, 12, of)   # two rows of 32 columns (warp pairs)
     assert g3 > 2.5 * g1
+    # above 16 columns a row holds 32 (warp pairs): 5 to 8 tokens of G = 4 are one row of 32
+    # columns, 9 tokens are two
+    g5, g8, g9 = (pg.pa_workspace_size_multi(s, n, of) for n in (5, 8, 9))
+    assert g5 == g8 and 1.8 * g1 < g8 < 2.2 * g1 and 1.8 * g8 < g9 < 2.2 * g8
 
 
 # ------------------------------------------------------------------ GPU
@@ -136,6 +140,9 @@ CASES = [
     ([200, 64, 31], [3, 1, 2], 12, 2, 256, 16, "bf16"),                   # d=256: 8 columns
     ([2, 3, 50, 0], [5, 3, 1, 2], 4, 4, 64, 16, "f16"),                   # fewer keys than queries
     ([1000, 2500], [16, 9], 8, 8, 128, 64, "bf16"),                       # G=1: 16 tokens a pass
+    ([500, 77, 1200, 9], [8, 8, 5, 3], 16, 4, 128, 32, "bf16"),          # G=4, 8 tokens: warp pairs
+    ([900, 40], [20, 13], 8, 2, 128, 16, "f16"),                          # pairs, 3 groups of 8 tokens
+    ([300, 64, 2000], [4, 2, 3], 14, 2, 64, 16, "f16"),                   # G=7, d=64: 28 columns
 ]
 
 
