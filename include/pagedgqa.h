@@ -246,8 +246,10 @@ int pa_decode_multi(const pa_shape* shape, const pa_options* options, const void
  * fp32 receives the result; the call then waits for `stream` and returns.
  * The pools stay on the device (k_cache, v_cache: device pointers, as in
  * pa_decode).  Host buffers need no alignment; page-locked ones
- * (cudaHostAlloc / cudaHostRegister) let the copies run asynchronously at
- * full speed, pageable ones work but are staged by the driver.  The
+ * (cudaHostAlloc / cudaHostRegister, 16-byte aligned) are read and written
+ * by the kernels directly, pageable ones are copied (cudaMemcpyAsync, staged
+ * by the driver).  Memory of the current device is accepted too (used in
+ * place, like page-locked memory).  The
  * workspace (device, 16-byte aligned, zero-filled once) must hold
  * pa_workspace_size_host bytes: pa_workspace_size's plus the staging.
  * status_host: if not NULL, receives this call's device status bits (0 when

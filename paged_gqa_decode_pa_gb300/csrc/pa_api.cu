@@ -859,10 +859,11 @@ HostLayout host_layout(const Plan& p, const pa_shape* s, int64_t rows, bool mult
   return h;
 }
 
-// The device address of page-locked host memory that this device maps
-// (cudaHostAlloc, cudaHostRegister), if `p` is such memory and aligned to
-// `align` bytes; otherwise null (pageable or device memory: the caller
-// copies instead).
+// The address at which this device's kernels can use `p` directly, if `p`
+// is page-locked host memory the device maps (cudaHostAlloc,
+// cudaHostRegister) or memory of the current device, and that address is
+// aligned to `align` bytes; otherwise null (pageable memory, another
+// device's memory: the caller copies instead).
 void* mapped_host(const void* p, uintptr_t align) {
   if (!p || (reinterpret_cast<uintptr_t>(p) & (align - 1))) return nullptr;
   cudaPointerAttributes at;
@@ -870,8 +871,14 @@ void* mapped_host(const void* p, uintptr_t align) {
     (void)cudaGetLastError();
     return nullptr;
   }
-  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
-  if (reinterpret_cast<uintptr_t>(at.devicePointer) & (align - 1)) return nullptr;
+  if (at.type == cudaMemoryTypeDevice) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != at.device) return nullptr;
+  } else if (at.type != cudaMemoryTypeHost) {
+    return nullptr;
+  }
+  if (!at.devicePointer || (reinterpret_cast<uintptr_t>(at.devicePointer) & (align - 1)))
+    return nullptr;
   return at.devicePointer;
 }
 
@@ -910,7 +917,7 @@ int run_host_step(const pa_shape* s, const pa_options* o, const HostLayout& h, u
       ++sa.n;
       return PA_OK;
     }
-    return cudaMemcpyAsync(ws + off, host, bytes, cudaMemcpyHostToDevice, st) == cudaSuccess
+    return cudaMemcpyAsync(ws + off, host, bytes, cudaMemcpyDefault, st) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
   };
@@ -937,7 +944,7 @@ int run_host_step(const pa_shape* s, const pa_options* o, const HostLayout& h, u
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   rc = run_phases(s, o, k_cache, v_cache, c, st);
   if (rc) return rc;
-  const cudaMemcpyKind back = cudaMemcpyDeviceToHost;
+  const cudaMemcpyKind back = cudaMemcpyDefault;
   if (c->sa.out == reinterpret_cast<float*>(ws + h.out) &&
       cudaMemcpyAsync(hb.out, ws + h.out, h.out_bytes, back, st) != cudaSuccess)
     return PA_ERR_CUDA;

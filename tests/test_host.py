@@ -225,3 +225,34 @@ def test_bound_host_calls_follow_the_buffers_contents():
     assert step() & pg.PA_STATUS_BAD_BLOCK
     t[1, 0] = t2[1, 0]
     assert step() == 0 and torch.equal(out, ref)
+
+
+@pytest.mark.gpu
+def test_decode_host_accepts_device_buffers():
+    """Memory of the current device is used in place (the C ABI takes any
+    mix of pageable, page-locked and device buffers); the result does not
+    change."""
+    import torch
+
+    from _helpers import run_gpu
+
+    w = wl.random_workload([3, 200, 0, 1500], H=16, Hkv=4, d=128, bs=32, dtype="bf16", seed=23,
+                           poison=True)
+    ref, st = run_gpu(w)
+    assert st == 0
+    qd, k, v, td, sld = w.torch_tensors("cuda")
+    qh, _, _, th, slh = host_inputs(w, True)
+    for mix in range(4):
+        q = qd if mix & 1 else qh
+        t, sl = (td, sld) if mix & 2 else (th, slh)
+        out = (torch.full((w.B, w.H, w.d), float("nan"), device="cuda") if mix & 1
+               else empty_out((w.B, w.H, w.d), True))
+        ws = pg.alloc_workspace_host(pg.shape_of(q, k, t))
+        stw = ctypes.c_uint32(99)
+        shape = pg.shape_of(q, k, t)
+        rc = pg.lib().pa_decode_host(ctypes.byref(shape), None, q.data_ptr(), k.data_ptr(),
+                                     v.data_ptr(), t.data_ptr(), sl.data_ptr(), w.scale,
+                                     out.data_ptr(), ctypes.byref(stw), ws.data_ptr(), ws.numel(),
+                                     pg._binding._stream(None))
+        assert rc == pg.PA_OK and stw.value == 0
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), ref), mix
