@@ -369,12 +369,13 @@ int choose_ring(const pa_shape* s, const pa_options* o, int mode, int W, int C, 
   return fit < want ? fit : want;
 }
 
-const void* kernel_for(int dtype, int D, int mode, int multi) {
+const void* kernel_for(int dtype, int D, int mode, int multi, int C) {
   if (mode == kTc) {
     if (D != kTcD) return nullptr;
     if (dtype == PA_BF16)
-      return multi ? split_tc_kernel_ptr<__nv_bfloat16, true>() : split_tc_kernel_ptr<__nv_bfloat16, false>();
-    return multi ? split_tc_kernel_ptr<__half, true>() : split_tc_kernel_ptr<__half, false>();
+      return multi ? split_tc_kernel_ptr<__nv_bfloat16, true>(C)
+                   : split_tc_kernel_ptr<__nv_bfloat16, false>(C);
+    return multi ? split_tc_kernel_ptr<__half, true>(C) : split_tc_kernel_ptr<__half, false>(C);
   }
 #define PA_PICK(T, DD)                                                                 \
   if (D == DD) return mode == kSimt ? split_kernel_ptr<T, DD, kSimt>()                \
@@ -493,7 +494,7 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
     int dev, sms, occ;
     rc = device_sms(&dev, &sms);
     if (rc) return rc;
-    const void* fn = kernel_for(s->dtype, p->D, p->mode, p->multi);
+    const void* fn = kernel_for(s->dtype, p->D, p->mode, p->multi, p->C);
     if (!fn) return PA_ERR_SHAPE;
     rc = occupancy(fn, dev, p->smem, 32 * p->warps, &occ);
     if (rc) return rc;

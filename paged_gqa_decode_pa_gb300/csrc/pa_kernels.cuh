@@ -343,6 +343,6 @@ cudaError_t launch_split_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, cons
                             int grid, size_t smem, cudaStream_t stream);
 
 template <typename T, bool kQ>
-const void* split_tc_kernel_ptr();
+const void* split_tc_kernel_ptr(int C);  // the variant for C query columns
 
 }  // namespace pa

@@ -304,7 +304,9 @@ __device__ __forceinline__ void tc_mma(const SplitArgs& A, PieceIterT<LenOf> it,
 // tokens so that p = 0 never meets stale data.  At the piece end, read O
 // (thread t = dimension t), reduce the exp-sums and write the output or the
 // partial state.
-template <typename T, bool kQ, class LenOf>
+// NC: the columns that can hold a query (C <= NC <= kTcN); the P rows of
+// the others are zeroed once and never written again.
+template <typename T, bool kQ, int NC, class LenOf>
 __device__ __forceinline__ void tc_softmax(const SplitArgs& A, PieceIterT<LenOf> it, uint32_t base,
                                            uint8_t* smem, const TcLayout& L, int NV, uint32_t tmem,
                                            volatile int* abort_flag) {
@@ -318,6 +320,11 @@ __device__ __forceinline__ void tc_softmax(const SplitArgs& A, PieceIterT<LenOf>
   uint32_t i = 0, piece = 0;
   Piece pc;
   TcColumns<kQ> cols;
+  if constexpr (NC < kTcN) {
+    // both P buffers start at zero: the rows of columns >= NC stay so
+    for (uint32_t off = 16u * (uint32_t)t; off < 2u * kTcPBytes; off += 16u * 128u)
+      sts128(base + L.p + off, make_uint4(0u, 0u, 0u, 0u));
+  }
   bool have = it.next(pc);
   if (have) {
     cols.setup(A, pc);
@@ -337,10 +344,10 @@ __device__ __forceinline__ void tc_softmax(const SplitArgs& A, PieceIterT<LenOf>
     const bool more = nit.next(nx);
     TcColumns<kQ> ncols;
     uint4 nqv[2];
-    int32_t lim[kTcN];
-    float m[kTcN], lp[kTcN];
+    int32_t lim[NC];
+    float m[NC], lp[NC];
 #pragma unroll
-    for (int c = 0; c < kTcN; ++c) {
+    for (int c = 0; c < NC; ++c) {
       lim[c] = cols.limit(A, c);
       m[c] = -INFINITY;
       lp[c] = 0.f;
@@ -380,7 +387,7 @@ __device__ __forceinline__ void tc_softmax(const SplitArgs& A, PieceIterT<LenOf>
       const int tok = tok0 + t;
       bool need = false;
 #pragma unroll
-      for (int c = 0; c < kTcN; ++c) {
+      for (int c = 0; c < NC; ++c) {
         float x = ok ? sc[c] * qscale : -INFINITY;
         if (!in || tok >= lim[c]) x = -INFINITY;
         sc[c] = x;
@@ -389,17 +396,17 @@ __device__ __forceinline__ void tc_softmax(const SplitArgs& A, PieceIterT<LenOf>
       if (named_bar_or(1, 128, need)) {
         // the tile's column maxima: warp trees, then the four warps in order
 #pragma unroll
-        for (int c = 0; c < kTcN; ++c) {
+        for (int c = 0; c < NC; ++c) {
           float v = sc[c];
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
           if (lane == 0) red[warp * kTcN + c] = v;
         }
         named_bar_sync(2, 128);
-        float al[kTcN];
+        float al[NC];
         bool moved = false;
 #pragma unroll
-        for (int c = 0; c < kTcN; ++c) {
+        for (int c = 0; c < NC; ++c) {
           const float tm = fmaxf(fmaxf(red[c], red[kTcN + c]), fmaxf(red[2 * kTcN + c], red[3 * kTcN + c]));
           const float nm = tm > m[c] + tc_lazy_max<T>() ? tm : m[c];
           al[c] = (m[c] == -INFINITY) ? 0.f : ex2(m[c] - nm);
@@ -421,7 +428,7 @@ __device__ __forceinline__ void tc_softmax(const SplitArgs& A, PieceIterT<LenOf>
             tmem_ld16(lanes + 48u, ol);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < kTcN; ++c) {
+            for (int c = 0; c < NC; ++c) {
               oh[c] *= al[c];
               ol[c] *= al[c];
             }
@@ -441,7 +448,7 @@ __device__ __forceinline__ void tc_softmax(const SplitArgs& A, PieceIterT<LenOf>
       }
       const uint32_t pbuf = base + L.p + (uint32_t)sb * kTcPBytes;
 #pragma unroll
-      for (int c = 0; c < kTcN; ++c) {
+      for (int c = 0; c < NC; ++c) {
         const float u = (m[c] == -INFINITY) ? 0.f : m[c];
         const float pv = ex2(sc[c] - u);
         lp[c] += pv;
@@ -497,14 +504,14 @@ __device__ __forceinline__ void tc_softmax(const SplitArgs& A, PieceIterT<LenOf>
       tmem_ld16(lanes + 48u, ol);
       tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < kTcN; ++c) o[c] += ol[c];
+      for (int c = 0; c < NC; ++c) o[c] += ol[c];
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + TcBars::o_free());  // the next piece may overwrite O
     named_bar_sync(2, 128);  // every thread is done with the maxima scratch
 #pragma unroll
-    for (int c = 0; c < kTcN; ++c) {
+    for (int c = 0; c < NC; ++c) {
       float v = lp[c];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -512,7 +519,7 @@ __device__ __forceinline__ void tc_softmax(const SplitArgs& A, PieceIterT<LenOf>
     }
     const bool any_bad = named_bar_or(1, 128, bad || !ok);
 #pragma unroll
-    for (int c = 0; c < kTcN; ++c) {
+    for (int c = 0; c < NC; ++c) {
       if (c >= C) continue;
       const float l = (red[c] + red[kTcN + c]) + (red[2 * kTcN + c] + red[3 * kTcN + c]);
       const int64_t r = cols.row(A, pc, c);
@@ -537,7 +544,7 @@ __device__ __forceinline__ void tc_softmax(const SplitArgs& A, PieceIterT<LenOf>
 
 // ------------------------------------------------------------------ kernel
 
-template <typename T, bool kQ>
+template <typename T, bool kQ, int NC>
 __global__ void __launch_bounds__(kTcThreads, 1)
     pa_split_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ SplitArgs a) {
@@ -604,7 +611,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   it.init(pre, len_of, sched, cta);
   const SplitArgs& A = *sa;
   if (warp < 4) {
-    tc_softmax<T, kQ>(A, it, base, smem, L, NV, tmem, abort_flag);
+    tc_softmax<T, kQ, NC>(A, it, base, smem, L, NV, tmem, abort_flag);
   } else if (warp == 4) {
     tc_producer<kQ, false>(A, it, &tmk, base, L, NV, abort_flag);
   } else if (warp == 6) {
@@ -621,6 +628,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
+// The softmax's live columns for C query columns: several query tokens fill
+// all 16; decode takes 4 or 8 (C = G).
+PA_HD constexpr int tc_live_columns(bool several, int C) {
+  return several ? kTcN : (C <= 4 ? 4 : (C <= 8 ? 8 : kTcN));
+}
+
 template <typename T, bool kQ>
 cudaError_t launch_split_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a,
                             int grid, size_t smem, cudaStream_t stream) {
@@ -634,12 +647,20 @@ cudaError_t launch_split_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pa_split_tc_kernel<T, kQ>, tmk, tmv, a);
+  switch (tc_live_columns(kQ, a.C)) {
+    case 4: return cudaLaunchKernelEx(&cfg, pa_split_tc_kernel<T, kQ, kQ ? kTcN : 4>, tmk, tmv, a);
+    case 8: return cudaLaunchKernelEx(&cfg, pa_split_tc_kernel<T, kQ, kQ ? kTcN : 8>, tmk, tmv, a);
+    default: return cudaLaunchKernelEx(&cfg, pa_split_tc_kernel<T, kQ, kTcN>, tmk, tmv, a);
+  }
 }
 
 template <typename T, bool kQ>
-const void* split_tc_kernel_ptr() {
-  return reinterpret_cast<const void*>(&pa_split_tc_kernel<T, kQ>);
+const void* split_tc_kernel_ptr(int C) {
+  switch (tc_live_columns(kQ, C)) {
+    case 4: return reinterpret_cast<const void*>(&pa_split_tc_kernel<T, kQ, kQ ? kTcN : 4>);
+    case 8: return reinterpret_cast<const void*>(&pa_split_tc_kernel<T, kQ, kQ ? kTcN : 8>);
+    default: return reinterpret_cast<const void*>(&pa_split_tc_kernel<T, kQ, kTcN>);
+  }
 }
 
 }  // namespace pa
@@ -648,4 +669,4 @@ const void* split_tc_kernel_ptr() {
   template cudaError_t pa::launch_split_tc<T, KQ>(const CUtensorMap&, const CUtensorMap&,     \
                                                   const pa::SplitArgs&, int, size_t,          \
                                                   cudaStream_t);                              \
-  template const void* pa::split_tc_kernel_ptr<T, KQ>();
+  template const void* pa::split_tc_kernel_ptr<T, KQ>(int);
