@@ -196,7 +196,9 @@ __global__ void __launch_bounds__(kStageThreads) pa_stage_in_kernel(const StageA
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nth = (int64_t)gridDim.x * blockDim.x;
   if (tid == 0 && s.status) *s.status = 0u;
-  for (int p = 0; p < s.n; ++p) {
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {  // unrolled: the parameter arrays stay in the constant bank
+    if (p >= s.n) break;
     const int64_t n16 = s.words[p] / 4;
     const uint4* src = reinterpret_cast<const uint4*>(s.src[p]);
     uint4* dst = reinterpret_cast<uint4*>(s.dst[p]);

@@ -221,6 +221,19 @@ __device__ __forceinline__ void tc_producer(const SplitArgs& A, PieceIterT<LenOf
 // overwrites O, after the previous piece's O has been read).  Completion is
 // signalled with tcgen05.commit: S ready and K slot free, V slot and P
 // buffer free.
+// tcgen05.mma without a memory clobber: the MMA thread touches shared memory
+// only through the mbarrier operations, which keep their own ordering.  A
+// descriptor's start address (bits 0-13, in 16-byte units) advances by a
+// constant per k-step, so the loops add to one descriptor instead of
+// rebuilding it (addresses stay below 2^18 bytes: no carry out of the field).
+__device__ __forceinline__ void tc_umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
+}
+
 template <typename T, class LenOf>
 __device__ __forceinline__ void tc_mma(const SplitArgs& A, PieceIterT<LenOf> it, uint32_t base,
                                        const TcLayout& L, int NV, uint32_t tmem,
@@ -241,12 +254,11 @@ __device__ __forceinline__ void tc_mma(const SplitArgs& A, PieceIterT<LenOf> it,
       return false;
     tc_fence_after();
     const uint32_t kst = base + L.k + (uint32_t)s * kTcHalfBytes;
+    const uint64_t a0 = sdesc_sw128(kst, 16, 1024), b0 = sdesc_sw128(qop, 16, 1024);
 #pragma unroll
-    for (int ks = 0; ks < kTcD / 16; ++ks)
-      umma_f16(tmem + 16u * sb,
-               sdesc_sw128(kst + (uint32_t)(ks >> 2) * kTcChunk + (uint32_t)(ks & 3) * 32u, 16, 1024),
-               sdesc_sw128(qop + (uint32_t)(ks >> 2) * opc + (uint32_t)(ks & 3) * 32u, 16, 1024), idS,
-               ks > 0);
+    for (int ks = 0; ks < kTcD / 16; ++ks)  // 32 bytes per k-step, 64 dims per chunk
+      tc_umma(tmem + 16u * sb, a0 + (uint64_t)((ks >> 2) * (kTcChunk >> 4) + (ks & 3) * 2),
+              b0 + (uint64_t)((ks >> 2) * (opc >> 4) + (ks & 3) * 2), idS, ks > 0);
     umma_commit(bars + TcBars::s_full(sb));
     umma_commit(bars + TcBars::empty_k(s));
     return true;
@@ -258,13 +270,13 @@ __device__ __forceinline__ void tc_mma(const SplitArgs& A, PieceIterT<LenOf> it,
     tc_fence_after();
     const uint32_t vst = base + L.v + (uint32_t)s * kTcHalfBytes;
     const uint32_t pb = base + L.p + (uint32_t)sb * kTcPBytes;
+    // V^T: 64-dim blocks one chunk apart, 8-token groups 1 KB apart
+    const uint64_t a0 = sdesc_sw128(vst, kTcChunk, 1024), b0 = sdesc_sw128(pb, 16, 1024);
 #pragma unroll
     for (int ks = 0; ks < kTcTile / 16; ++ks)
-      umma_f16(tmem + 32u,
-               // V^T: 64-dim blocks one chunk apart, 8-token groups 1 KB apart
-               sdesc_sw128(vst + (uint32_t)ks * 2048u, kTcChunk, 1024),
-               sdesc_sw128(pb + (uint32_t)(ks >> 2) * (kTcPBytes / 2) + (uint32_t)(ks & 3) * 32u, 16, 1024),
-               idO, (first && ks == 0) ? 0u : 1u);
+      tc_umma(tmem + 32u, a0 + (uint64_t)(ks * (2048 >> 4)),
+              b0 + (uint64_t)((ks >> 2) * ((kTcPBytes / 2) >> 4) + (ks & 3) * 2), idO,
+              (first && ks == 0) ? 0u : 1u);
     umma_commit(bars + TcBars::empty_v(s));
     umma_commit(bars + TcBars::p_free(sb));
     return true;
