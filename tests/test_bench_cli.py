@@ -78,3 +78,30 @@ def test_fewer_than_three_warmup_steps_are_refused():
               "--warmup", "2"])
     assert r.returncode != 0
     assert _json_lines(r.stdout) == []
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("extra", [[], ["--query-tokens", "2"], ["--graph"], ["--fused-append"]])
+def test_bench_line_on_the_gpu(extra):
+    """The GPU arm on a small workload: one JSON line with the contract's keys,
+    the roofline against the measured peak, an end-to-end figure with its
+    byte counts, the clocks, the launch count and the parity sample."""
+    r = _run([BENCH, "--config", "qwen2_b8_g7_d64", "--steps", "20", "--warmup", "3",
+              "--cpu-baseline-s", "0.5"] + extra, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    (d,) = _json_lines(r.stdout)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches"):
+        assert key in d, key
+    assert d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 20 and d["warmup"] == 3
+    rf = d["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
+    assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"], rel=1e-3)
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert e["value"] < d["value"]  # the copies cost time
+    assert d["gpu_launches"] >= 2 * d["steps"]
+    assert d["clocks"]["sm_max_mhz"] > 0
+    assert d["parity_vs_oracle"]["max_abs_err"] <= 2e-3
+    assert d["cpu_baseline"]["kind"] == "oracle"
