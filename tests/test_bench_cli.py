@@ -97,7 +97,7 @@ def test_bench_line_on_the_gpu(extra):
     assert d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 20 and d["warmup"] == 3
     rf = d["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
-    assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"], rel=1e-3)
+    assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"], abs=1e-4)  # rounded to 4 places
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert e["value"] < d["value"]  # the copies cost time
