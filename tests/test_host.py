@@ -140,7 +140,8 @@ MULTI = [
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("case", range(len(MULTI)))
-def test_decode_multi_host_matches_the_oracle_and_the_device_call(case):
+@pytest.mark.parametrize("pinned", [True, False])
+def test_decode_multi_host_matches_the_oracle_and_the_device_call(case, pinned):
     import torch
 
     from _helpers import assert_close
@@ -149,9 +150,11 @@ def test_decode_multi_host_matches_the_oracle_and_the_device_call(case):
     w = wl.random_workload(lens_k, H, Hkv, d, bs, dtype=dtype, seed=100 + case, poison=True,
                            outlier_frac=0.02)
     w = wl.with_query_tokens(w, lens_q, seed=110 + case, causal=causal)
-    q, k, v, t, sl = host_inputs(w, True)
-    cu = torch.from_numpy(w.cu_q).pin_memory()
-    out = empty_out((q.shape[0], w.H, w.d), True)
+    q, k, v, t, sl = host_inputs(w, pinned)
+    cu = torch.from_numpy(w.cu_q)
+    if pinned:
+        cu = cu.pin_memory()
+    out = empty_out((q.shape[0], w.H, w.d), pinned)
     shape = pg.shape_multi(q, k, t)
     # sized for more rows than this call has: the staging of q and out comes last
     ws = pg.alloc_workspace_multi_host(shape, w.max_q, q.shape[0] + 37)
@@ -168,7 +171,7 @@ def test_decode_multi_host_matches_the_oracle_and_the_device_call(case):
     assert pg.pa_read_status(wsd) == 0
     assert np.array_equal(got, outd.cpu().numpy().astype(np.float64))
     # the bound form of the same call gives the same bits
-    out_b = empty_out((q.shape[0], w.H, w.d), True)
+    out_b = empty_out((q.shape[0], w.H, w.d), pinned)
     step = pg.bind_decode_multi_host(q, cu, w.max_q, w.causal, k, v, t, sl, w.scale, out_b, ws)
     assert step() == 0 and step() == 0
     assert np.array_equal(got, out_b.numpy().astype(np.float64))
