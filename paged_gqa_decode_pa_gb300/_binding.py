@@ -438,7 +438,8 @@ def bind_decode_host(q, k_cache, v_cache, block_table, cache_seqlens, scale, out
                      opts: Optional[pa_options] = None, stream=None) -> _BoundCall:
     """pa_decode_host on these buffers, checked and marshalled once: the
     returned callable runs one step per call (a serving loop rewrites q, the
-    table and the lengths in place between steps) and returns its status."""
+    table and the lengths in place between steps) and returns its status.
+    The stream (the current one when None) is taken at bind time."""
     _check_host(q, block_table, cache_seqlens, out, k_cache, v_cache)
     shape = shape_of(q, k_cache, block_table)
     st = _status_word()
@@ -456,7 +457,8 @@ def bind_decode_multi_host(q, cu_seqlens_q, max_q, causal, k_cache, v_cache, blo
                            cache_seqlens, scale, out, workspace,
                            opts: Optional[pa_options] = None, stream=None) -> _BoundCall:
     """pa_decode_multi_host on these buffers, checked and marshalled once
-    (as bind_decode_host; total_q is q's row count)."""
+    (as bind_decode_host; total_q is q's row count, the stream is taken at
+    bind time)."""
     import torch
 
     _check_host(q, block_table, cache_seqlens, out, k_cache, v_cache,
