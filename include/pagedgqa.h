@@ -28,8 +28,10 @@
  *
  * Conventions shared by every entry point
  *   - All tensor arguments are DEVICE pointers to dense, row-major memory the
- *     caller owns; the library allocates nothing and keeps no per-call state.
- *   - Every pointer must be 16-byte aligned.
+ *     caller owns (pa_decode_host / pa_decode_multi_host also take host
+ *     buffers; see there); the library allocates nothing and keeps no
+ *     per-call state.
+ *   - Every device pointer must be 16-byte aligned.
  *   - Layouts (dt = fp16 or bf16, the same for q, k and v):
  *       q              [B, H, d]            dt
  *       k_cache        [P, bs, Hkv, d]      dt   (P = num_blocks)
@@ -43,8 +45,9 @@
  *     max_blocks_per_seq * bs, B * max_blocks_per_seq and
  *     Hkv * (max_blocks_per_seq + 64) below 2^31 (else PA_ERR_SHAPE).
  *   - Work is enqueued on `stream` (NULL = legacy default stream).  No entry
- *     point synchronises, allocates, or picks a launch shape from device
- *     data, so pa_decode and pa_cache_append can be captured in a CUDA graph
+ *     point allocates or picks a launch shape from device data, and none but
+ *     pa_read_status and the host-buffer calls synchronises, so pa_decode and
+ *     pa_cache_append can be captured in a CUDA graph
  *     and replayed after the inputs are changed in place.  The first call on
  *     a device performs one-time host-side setup (kernel attributes,
  *     occupancy query); make it before beginning a stream capture.
