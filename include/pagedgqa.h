@@ -30,7 +30,8 @@
  *   - All tensor arguments are DEVICE pointers to dense, row-major memory the
  *     caller owns (pa_decode_host / pa_decode_multi_host also take host
  *     buffers; see there); the library allocates nothing and keeps no
- *     per-call state.
+ *     per-call state.  The one exception is pa_decode_noalloc, whose scratch
+ *     is a static device array inside the library (see there).
  *   - Every device pointer must be 16-byte aligned.
  *   - Layouts (dt = fp16 or bf16, the same for q, k and v):
  *       q              [B, H, d]            dt
@@ -46,7 +47,9 @@
  *     Hkv * (max_blocks_per_seq + 64) below 2^31 (else PA_ERR_SHAPE).
  *   - Work is enqueued on `stream` (NULL = legacy default stream).  No entry
  *     point allocates or picks a launch shape from device data, and none but
- *     pa_read_status and the host-buffer calls synchronises, so pa_decode and
+ *     pa_read_status and the host-buffer calls synchronises (the first
+ *     pa_decode_noalloc call on a device also enqueues one memset on its
+ *     stream), so pa_decode and
  *     pa_cache_append can be captured in a CUDA graph
  *     and replayed after the inputs are changed in place.  The first call on
  *     a device performs one-time host-side setup (kernel attributes,
@@ -54,7 +57,8 @@
  *   - Host-side errors are reported by the return code before anything is
  *     enqueued.  Data errors found on the device never trap and never wait:
  *     they set a bit in the status word kept at the start of the workspace
- *     and make the affected outputs NaN (see pa_read_status).
+ *     (pa_decode_noalloc: the caller's status word, if given) and make the
+ *     affected outputs NaN (see pa_read_status).
  */
 #ifndef PAGEDGQA_H
 #define PAGEDGQA_H
@@ -314,17 +318,21 @@ const char* pa_status_string(int code);
  * the kernels need lives in one static device array of PA_STATIC_SCRATCH_BYTES
  * that every GPU loading this library holds until the process exits.  A
  * problem whose pa_workspace_size exceeds that size is rejected with
- * PA_ERR_SCRATCH_LIMIT before anything is enqueued (the default balanced
- * split needs well under 4 MiB for B <= PA_MAX_BATCH, G <= 8, d <= 256 on a
- * 152-SM GPU; large fixed partitions may not fit).
+ * PA_ERR_SCRATCH_LIMIT before anything is enqueued.  The default balanced
+ * split fits for B <= PA_MAX_BATCH, G <= 8, d <= 256 whenever the persistent
+ * grid has at most 256 CTAs (a 152-SM GPU runs 152); large fixed partitions
+ * may not fit.
  *   status: device pointer to a uint32 that receives the PA_STATUS_* bits
  *           (OR-ed in; the caller zeroes it), or NULL to drop them.
+ *   options->phase must be PA_PHASE_BOTH (else PA_ERR_OPTION): both kernels
+ *   always run, since the scratch is shared by every call.
  * The first call on each device looks up the array's device address and
- * zeroes its status word (with that device current); make that first call
- * before any stream capture.  All calls share the one array and it keeps
- * the previous call's contents (each call rewrites everything it reads), so
- * two calls that may overlap on the GPU -- on different streams, or from
- * different threads -- race and give wrong results: serialise them. */
+ * zeroes the array's 256-byte header on `stream` (with that device
+ * current); make that first call before any stream capture.  All calls
+ * share the one array and it keeps the previous call's contents (each call
+ * rewrites everything it reads), so two calls that may overlap on the GPU
+ * -- on different streams, or from different threads -- race and give wrong
+ * results: serialise them. */
 #define PA_STATIC_SCRATCH_BYTES (8u << 20)
 int pa_decode_noalloc(const pa_shape* shape, const pa_options* options, const void* q,
                       const void* k_cache, const void* v_cache, const int32_t* block_table,

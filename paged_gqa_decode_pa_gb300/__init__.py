@@ -17,7 +17,7 @@ from ._binding import (  # noqa: F401
     shape_multi, pa_decode_host, pa_workspace_size_host, alloc_workspace_host,
     pa_decode_multi_host, pa_workspace_size_multi_host, alloc_workspace_multi_host,
     bind_decode_host, bind_decode_multi_host,
-    PA_MAX_QUERY_TOKENS, PA_MAX_BATCH, PA_PHASE_BOTH, PA_PHASE_SPLIT, PA_PHASE_MERGE, PA_ERR_STATE, PA_ERR_NO_BLOCKS, PA_BM_FREE_BLOCKS, PA_BM_REF_COUNT,
+    PA_MAX_QUERY_TOKENS, PA_MAX_BATCH, PA_STATIC_SCRATCH_BYTES, PA_PHASE_BOTH, PA_PHASE_SPLIT, PA_PHASE_MERGE, PA_ERR_STATE, PA_ERR_NO_BLOCKS, PA_BM_FREE_BLOCKS, PA_BM_REF_COUNT,
     PA_BM_SEQ_BLOCKS,
     PA_OK, PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_ALIGN, PA_ERR_WORKSPACE, PA_ERR_CUDA,
     PA_ERR_OPTION, PA_ERR_SCRATCH_LIMIT, PA_STATUS_BAD_BLOCK, PA_STATUS_BAD_SEQLEN, PA_STATUS_TIMEOUT,

@@ -29,6 +29,7 @@ PA_ERR_NO_BLOCKS = -9
 
 PA_MAX_QUERY_TOKENS = 4096
 PA_MAX_BATCH = 8192  # include/pagedgqa.h: sequences per call
+PA_STATIC_SCRATCH_BYTES = 8 << 20  # include/pagedgqa.h: pa_decode_noalloc scratch
 
 PA_BM_FREE_BLOCKS = 0
 PA_BM_REF_COUNT = 1
@@ -536,7 +537,17 @@ def pa_decode_noalloc(q, k_cache, v_cache, block_table, cache_seqlens, scale, ou
     scratch lives in a fixed static device array inside the library (see
     include/pagedgqa.h).  `status` is an optional int32/uint32 CUDA tensor of
     one element that receives the device status bits."""
+    import torch
+
     _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out)
+    if status is not None:
+        # the kernels OR bits into this word from the device: it must be
+        # device memory of q's GPU, 4-byte integers, at least one element
+        if (not isinstance(status, torch.Tensor) or not status.is_cuda
+                or status.device != q.device or status.numel() < 1
+                or status.dtype not in (torch.int32, getattr(torch, "uint32", torch.int32))):
+            raise PagedGQAError(PA_ERR_SHAPE, "pa_decode_noalloc: status must be an int32 or "
+                                "uint32 CUDA tensor of at least one element on q's device")
     shape = shape_of(q, k_cache, block_table)
     rc = lib().pa_decode_noalloc(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
                                  _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),

@@ -1317,16 +1317,18 @@ namespace {
 void* g_static_ptr[kMaxDevices];
 
 // Once per device, with that device current: the array's device address.
-// (In host code the array's name is only a host-side stand-in.)
-int static_scratch(void** ptr) {
+// (In host code the array's name is only a host-side stand-in.)  The first
+// call also zeroes the array's header (status word and the split kernel's
+// work counters, which must start at zero) on the caller's stream, so the
+// zeroing is ordered before that call's kernels.
+int static_scratch(void** ptr, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   if (!g_static_ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_pa_static_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
-    // the status word must start at zero
-    if (cudaMemset(p, 0, kHeaderBytes) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaMemsetAsync(p, 0, kHeaderBytes, stream) != cudaSuccess) return PA_ERR_CUDA;
     g_static_ptr[dev] = p;
   }
   *ptr = g_static_ptr[dev];
@@ -1345,19 +1347,22 @@ extern "C" int pa_decode_noalloc(const pa_shape* shape, const pa_options* option
   rc = check_options(shape, options);
   if (rc) return rc;
   if (status && (reinterpret_cast<uintptr_t>(status) & 3u)) return PA_ERR_ALIGN;
+  // both phases always run here: the scratch is not the caller's to carry
+  // from a split-only call to a merge-only one
+  if (options && options->phase != PA_PHASE_BOTH) return PA_ERR_OPTION;
   Plan plan;
   rc = make_plan(shape, options, false, &plan);
   if (rc) return rc;
   if (plan.total > (size_t)PA_STATIC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   void* scratch = nullptr;
-  rc = static_scratch(&scratch);
+  rc = static_scratch(&scratch, st);
   if (rc) return rc;
   Call c;
   rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                scratch, (size_t)PA_STATIC_SCRATCH_BYTES, true, &c);
   if (rc) return rc;
   if (status) c.sa.status = status;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   rc = launch_split_phase(shape, k_cache, v_cache, &c, st);
   if (rc) return rc;
   return launch_merge_phase(&c, st, true);

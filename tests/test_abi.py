@@ -266,3 +266,24 @@ def test_with_group_keeps_the_cache_and_draws_new_queries():
     assert np.array_equal(b.q, c.q)  # seeded
     with pytest.raises(ValueError):
         wl.with_group(c, 0)
+
+
+def test_noalloc_rejects_split_or_merge_phase_before_any_cuda_call():
+    L = pg.lib()
+    s = shape()
+    for phase in (pg.PA_PHASE_SPLIT, pg.PA_PHASE_MERGE):
+        o = pg.options(num_ctas=8, phase=phase)
+        assert L.pa_decode_noalloc(ctypes.byref(s), ctypes.byref(o), FAKE, FAKE, FAKE, FAKE,
+                                   FAKE, 0.125, FAKE, None, None) == pg.PA_ERR_OPTION
+
+
+@pytest.mark.parametrize("grid", [152, 256])
+def test_noalloc_scratch_holds_the_default_split_at_the_largest_shapes(grid):
+    # the bound include/pagedgqa.h states for pa_decode_noalloc: the default
+    # balanced split at B = PA_MAX_BATCH, G = 8, d = 256 fits the static
+    # scratch for any persistent grid of up to 256 CTAs
+    limit = pg.PA_STATIC_SCRATCH_BYTES
+    for dtype in (pg.PA_F16, pg.PA_BF16):
+        s = shape(B=pg.PA_MAX_BATCH, H=64, Hkv=8, d=256, bs=16, maxblk=8192, P=1 << 20,
+                  dtype=dtype)
+        assert pg.pa_workspace_size(s, pg.options(num_ctas=grid)) <= limit

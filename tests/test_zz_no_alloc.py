@@ -46,14 +46,42 @@ def check(got, ref):
     assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS
 
 
+def oracle_of(w):
+    import oracle
+
+    return oracle.decode(w.q, w.k_cache, w.v_cache, w.block_table, w.cache_seqlens, w.scale,
+                         w.dtype)
+
+
 def test_two_calls_in_a_row_match_the_workspace_entry_point():
     # first call: serving-mix shape, split across CTAs (partial states in scratch)
     a = wl.random_workload(list(wl.serving_mix_lengths(5, 24) // 2 + 1), H=32, Hkv=8, d=128,
                            bs=32, dtype="bf16", seed=77, outlier_frac=0.01)
-    check(*both_ways(a))
+    got, ref = both_ways(a)
+    check(got, ref)
+    check(got, oracle_of(a))
     # second call: different shape and fixed 512-token partitions
     b = wl.random_workload([10_007, 3, 700], H=24, Hkv=4, d=256, bs=16, dtype="bf16", seed=78)
-    check(*both_ways(b, pg.options(partition_tokens=512)))
+    got, ref = both_ways(b, pg.options(partition_tokens=512))
+    check(got, ref)
+    check(got, oracle_of(b))
+
+
+def test_status_must_be_a_device_word_of_q_s_gpu():
+    # checked in the binding before the C call: the kernels would OR bits into
+    # whatever address they are given
+    w = wl.random_workload([40, 9], H=8, Hkv=2, d=64, bs=16, dtype="f16", seed=81)
+    q, k, v, t, sl = w.torch_tensors("cuda")
+    out = torch.empty((w.B, w.H, w.d), dtype=torch.float32, device="cuda")
+    for bad in (torch.zeros(1, dtype=torch.int32),                  # host memory
+                torch.zeros(0, dtype=torch.int32, device="cuda"),   # no element
+                torch.zeros(1, dtype=torch.float32, device="cuda")):  # not an integer word
+        with pytest.raises(pg.PagedGQAError):
+            pg.pa_decode_noalloc(q, k, v, t, sl, w.scale, out, bad)
+    with pytest.raises(pg.PagedGQAError) as e:
+        pg.pa_decode_noalloc(q, k, v, t, sl, w.scale, out, None,
+                             pg.options(phase=pg.PA_PHASE_SPLIT))
+    assert e.value.code == pg.PA_ERR_OPTION
 
 
 def test_status_bits_reach_the_callers_word_and_oversize_is_rejected():
