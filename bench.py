@@ -17,7 +17,16 @@ e2e     : the same metric through the host-buffer call (pa_decode_host /
 roofline: the split kernel alone (CUDA events around phase 1 in the same timed
           loop) against the measured HBM copy bandwidth.
 cpu_baseline / --impl reference: the float64 oracle on the host cores, on a
-          bounded sample of the same workload.
+          bounded sample of the same workload (cpu_baseline: all cores, plus a
+          one-core figure).
+repeats : the K-step region repeated for about --repeat-s seconds (spread);
+          the clocks are sampled every 20 ms over the loaded window.
+per_config: with the default workload, the other configurations the metric
+          is quoted on (the tiny page example, Qwen2-style GQA, long context
+          with the default split and with 512-token partitions, prefix
+          sharing), each with device and end-to-end time per step, the split
+          kernel's fraction of the HBM peak, the recorded ncu traffic ratio
+          and an oracle parity sample.
 N > 1   : independent replicas (the path has no exchange step), one per GPU,
           scaling "weak".
 """
@@ -85,11 +94,13 @@ def recorded_traffic(workload: str, opts_key: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms (a read-only
+    query; no GPU setting is touched)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -101,7 +112,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.gpu)],
+                 "-lms", str(self.PERIOD_MS), "-i", str(self.gpu)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -121,17 +132,23 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return None
-        time.sleep(0.25)
+            return
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        inside = [r for (t, r) in self.rows if self.t0 - 0.2 <= t <= self.t1 + 0.2]
+
+    def window(self, t0, t1):
+        """Median SM clock, max clock and active throttle reasons of the
+        samples taken between t0 and t1 (wall clock)."""
+        if self.proc is None:
+            return None
+        inside = [r for (t, r) in self.rows if t0 <= t <= t1]
         if not inside and self.rows:
-            inside = [min(self.rows, key=lambda x: abs(x[0] - self.t1))[1]]
+            inside = [min(self.rows, key=lambda x: abs(x[0] - t1))[1]]
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in inside:
@@ -149,7 +166,8 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "sm_mhz_min": min(sm), "reasons": sorted(reasons), "samples": len(sm),
+                "period_ms": self.PERIOD_MS}
 
 
 def max_over_ranks(values, device="cpu"):
@@ -221,15 +239,16 @@ def row_sequences(w) -> np.ndarray:
     return seq
 
 
-def oracle_outputs(w, pairs):
+def oracle_outputs(w, pairs, n_threads: int = 0):
     """The oracle's outputs for (row, head) pairs of the workload."""
     import oracle
 
     if w.cu_q is None:
         return oracle.decode(w.q, w.k_cache, w.v_cache, w.block_table, w.cache_seqlens,
-                             w.scale, w.dtype, pairs=pairs)
+                             w.scale, w.dtype, pairs=pairs, n_threads=n_threads)
     return oracle.decode_multi(w.q, w.cu_q, w.causal, w.k_cache, w.v_cache, w.block_table,
-                               w.cache_seqlens, w.scale, w.dtype, pairs=pairs)
+                               w.cache_seqlens, w.scale, w.dtype, pairs=pairs,
+                               n_threads=n_threads)
 
 
 def metric_bytes_of_pairs(w, pairs) -> float:
@@ -246,22 +265,23 @@ def metric_bytes_of_pairs(w, pairs) -> float:
     return float(per_row[pairs[:, 0]].sum()) * (w.kv_bytes() / total) if total else 0.0
 
 
-def oracle_sample(w, budget_s: float, seed: int = 0):
+def oracle_sample(w, budget_s: float, seed: int = 0, n_threads: int = 0):
     """Time the oracle on a bounded sample of (b, h) outputs of the workload,
     repeated until about `budget_s` seconds of work have been timed.
+    n_threads = 0: all host cores (OpenMP); 1: one core.
 
     Returns (GB/s in the metric's unit, seconds, pairs, threads, passes)."""
     import oracle
 
     oracle.build()
-    threads = oracle.max_threads()
+    threads = oracle.max_threads() if n_threads <= 0 else n_threads
     rng = np.random.default_rng(seed)
     order = rng.permutation(query_rows(w) * w.H)
     pairs_all = np.stack([order // w.H, order % w.H], axis=1).astype(np.int32)
 
     def run(pairs):
         t = time.perf_counter()
-        oracle_outputs(w, pairs)
+        oracle_outputs(w, pairs, n_threads)
         return time.perf_counter() - t
 
     # calibrate on a few outputs, then size the sample for the budget
@@ -328,230 +348,343 @@ def workload_config(w, args):
             "parallelism": f"replicas x{args.gpus}"}
 
 
-def run_ours(args, rank, world, local_rank):
+class Stepper:
+    """One workload resident on the device, with the calls of one decode step
+    bound through the C ABI: the step itself (both phases), the two phases
+    apart, and the end-to-end host-buffer step."""
+
+    def __init__(self, w, opt_kw, dev, fused_append=False, graph=False, warmup=3):
+        import torch
+
+        import paged_gqa_decode_pa_gb300 as pg
+
+        self.pg, self.w, self.dev = pg, w, dev
+        if fused_append:
+            make_room_for_next_token(w)
+        self.q, self.k, self.v, self.t, self.sl = w.torch_tensors(dev)
+        q, k, t = self.q, self.k, self.t
+        self.multi = w.cu_q is not None
+        if self.multi and fused_append:
+            raise SystemExit("--fused-append is a one-token-per-sequence step")
+        self.out = torch.empty(tuple(q.shape), dtype=torch.float32, device=dev)
+        self.opt_kw = opt_kw
+        self.opts = pg.options(**opt_kw)
+        self.opts_split = pg.options(**opt_kw, phase=pg.PA_PHASE_SPLIT)
+        self.opts_merge = pg.options(**opt_kw, phase=pg.PA_PHASE_MERGE)
+        if self.multi:
+            self.cu = torch.from_numpy(w.cu_q).to(dev)
+            self.ws = pg.alloc_workspace_multi(pg.shape_multi(q, k, t), w.max_q, self.opts, dev)
+        else:
+            self.cu = None
+            self.ws = pg.alloc_workspace(pg.shape_of(q, k, t), self.opts, dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.kv_bytes = w.kv_bytes()
+        self.flush = self.kv_bytes <= 2 * L2_BYTES
+        self.scratch = (torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+                        if self.flush else None)
+        for _ in range(warmup):
+            self.flush_l2()
+            self.attend(self.opts)
+        self.attend(self.opts_split)
+        self.attend(self.opts_merge)
+        torch.cuda.synchronize()
+        if pg.pa_read_status(self.ws) != 0:
+            raise RuntimeError("device status bits set during warm-up")
+        self.decode_step = lambda: self.attend(self.opts)
+        if fused_append:
+            # each step writes a new K/V row at position len and attends over
+            # len + 1 tokens (the lengths are not advanced, so every step
+            # rewrites the same slots)
+            gen = torch.Generator(device=dev).manual_seed(1)
+            self.kn = torch.randn((w.B, w.Hkv, w.d), generator=gen, device=dev).to(k.dtype)
+            self.vn = torch.randn((w.B, w.Hkv, w.d), generator=gen, device=dev).to(k.dtype)
+            self.kv_bytes += w.B * w.Hkv * w.d * 2 * 2  # the appended rows
+            self.decode_step = lambda: pg.pa_decode_append(
+                self.q, self.kn, self.vn, self.k, self.v, self.t, self.sl, w.scale, self.out,
+                self.ws, self.opts)
+        self.graph = None
+        if graph:
+            # one decode step captured once and replayed (host launch cost removed)
+            self.graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(self.stream)
+            with torch.cuda.stream(cap):
+                self.decode_step()
+            cap.synchronize()
+            with torch.cuda.graph(self.graph, stream=cap):
+                self.decode_step()
+            for _ in range(warmup):
+                self.graph.replay()
+            torch.cuda.synchronize()
+
+    def flush_l2(self):
+        if self.flush:
+            self.scratch.fill_(1.0)
+
+    def attend(self, o):
+        """One step of the path through the C ABI (o selects the phases)."""
+        w, pg = self.w, self.pg
+        if self.multi:
+            pg.pa_decode_multi(self.q, self.cu, w.max_q, w.causal, self.k, self.v, self.t,
+                               self.sl, w.scale, self.out, self.ws, o)
+        else:
+            pg.pa_decode(self.q, self.k, self.v, self.t, self.sl, w.scale, self.out, self.ws, o)
+
+    def steps(self, K):
+        """K decode steps; device ms per step.  With the L2 flushed between
+        steps each step is bracketed by its own events (the flush stays
+        outside); otherwise only the first and the last, so that consecutive
+        steps stay back to back on the stream (the split kernel is a
+        programmatic dependent of the previous merge, and an event in between
+        would serialise them)."""
+        import torch
+
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            self.flush_l2()
+            if self.flush or i == 0:
+                ev[i][0].record(self.stream)
+            if self.graph is not None:
+                self.graph.replay()
+            else:
+                self.decode_step()
+            if self.flush or i == K - 1:
+                ev[i][1].record(self.stream)
+        torch.cuda.synchronize()
+        if self.flush:
+            return float(sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))) / K
+        return ev[0][0].elapsed_time(ev[K - 1][1]) / K
+
+    def phases(self, K):
+        """K steps as two phase calls with an event between them: the split
+        kernel's and the merge kernel's own average durations (ms)."""
+        import torch
+
+        ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        torch.cuda.synchronize()
+        for i in range(K):
+            self.flush_l2()
+            ev3[i][0].record(self.stream)
+            self.attend(self.opts_split)
+            ev3[i][1].record(self.stream)
+            self.attend(self.opts_merge)
+            ev3[i][2].record(self.stream)
+        torch.cuda.synchronize()
+        split_ms = [ev3[i][0].elapsed_time(ev3[i][1]) for i in range(K)]
+        merge_ms = [ev3[i][1].elapsed_time(ev3[i][2]) for i in range(K)]
+        if self.pg.pa_read_status(self.ws) != 0:
+            raise RuntimeError("device status bits set during the timed steps")
+        return float(np.mean(split_ms)), float(np.mean(merge_ms))
+
+    def e2e(self, K):
+        """End to end through the host-buffer call: every step is one call of
+        the library's host-buffer entry point (bound once to the step's
+        buffers, as a serving loop would).  It moves q, the block table and
+        the lengths (and the query offsets) from pinned host memory into the
+        workspace's staging, runs both phases with the output written to
+        pinned host memory, publishes the call's status there too, and waits
+        for the stream.  Returns (ms per step, h2d bytes, d2h bytes)."""
+        import torch
+
+        pg, w = self.pg, self.w
+        q, k, v, t, sl, out, dev, stream = (self.q, self.k, self.v, self.t, self.sl, self.out,
+                                            self.dev, self.stream)
+        Ke = max(3, min(K, 200))
+        q_h, t_h, sl_h = (x.cpu().contiguous().pin_memory() for x in (q, t, sl))
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        parts = [q_h, t_h, sl_h]
+        if self.multi:
+            cu_h = self.cu.cpu().contiguous().pin_memory()
+            parts.append(cu_h)
+            ws_h = pg.alloc_workspace_multi_host(pg.shape_multi(q, k, t), w.max_q, q.shape[0],
+                                                 self.opts, dev)
+            attend_host = pg.bind_decode_multi_host(q_h, cu_h, w.max_q, w.causal, k, v, t_h,
+                                                    sl_h, w.scale, out_h, ws_h, self.opts,
+                                                    stream)
+        else:
+            ws_h = pg.alloc_workspace_host(pg.shape_of(q, k, t), self.opts, dev)
+            attend_host = pg.bind_decode_host(q_h, k, v, t_h, sl_h, w.scale, out_h, ws_h,
+                                              self.opts, stream)
+        h2d = sum(x.numel() * x.element_size() for x in parts)
+        d2h = out_h.numel() * 4 + 4  # the output and the call's status word
+        for _ in range(2):
+            attend_host()
+        torch.cuda.synchronize()
+        status = 0
+        if self.flush:
+            # L2 flushed before every step, outside its events
+            eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
+            for i in range(Ke):
+                self.flush_l2()
+                eve[i][0].record(stream)
+                status |= attend_host()
+                eve[i][1].record(stream)
+            torch.cuda.synchronize()
+            ms = float(sum(eve[i][0].elapsed_time(eve[i][1]) for i in range(Ke))) / Ke
+        else:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(Ke):
+                status |= attend_host()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / Ke
+        if status != 0:
+            raise RuntimeError(f"device status bits {status:#x} during the end-to-end steps")
+        if not torch.equal(out_h, out.cpu()):
+            raise RuntimeError("the end-to-end output differs from the device-buffer output")
+        return ms, h2d, d2h
+
+    def parity(self, n, seed=0):
+        """The last output against the oracle on n sampled (row, head) outputs
+        (all of them when the step has at most n)."""
+        w = self.w
+        total = query_rows(w) * w.H
+        order = np.random.default_rng(seed).permutation(total)[:min(n, total)]
+        pairs = np.stack([order // w.H, order % w.H], axis=1).astype(np.int32)
+        ref = oracle_outputs(w, pairs)
+        got = self.out.cpu().numpy().astype(np.float64)[pairs[:, 0], pairs[:, 1]]
+        err = np.abs(got - ref)
+        return {"pairs": int(len(pairs)), "max_abs_err": float(err.max()),
+                "mean_abs_err": float(err.mean()), "tolerance": [2e-3, 2e-4]}
+
+
+def opts_key(kw) -> str:
+    return f"part={kw['partition_tokens']},compute={kw['compute']},stages={kw['stages']}"
+
+
+# The other configurations the metric is quoted on, measured in the same run
+# as the headline (one GPU): (entry name, workload, partition_tokens).
+PER_CONFIG = [
+    ("p5_example", "p5_example", 0),
+    ("qwen2_b8_g7_d64", "qwen2_b8_g7_d64", 0),
+    ("long_ctx_100k_g6_d256", "long_ctx_100k_g6_d256", 0),
+    ("long_ctx_100k_g6_d256_part512", "long_ctx_100k_g6_d256", 512),
+    ("prefix_share_b64_g8_d128", "prefix_share_b64_g8_d128", 0),
+]
+
+
+def per_config_entry(name, part, args, dev, peak):
+    """One configuration at a glance: device and end-to-end time per step,
+    the split kernel's fraction of the HBM peak, the recorded ncu traffic
+    ratio (when taken on the current kernel sources) and the parity sample."""
     import torch
 
-    import paged_gqa_decode_pa_gb300 as pg
+    w = make_workload(name)
+    kw = dict(partition_tokens=part, compute=args.compute, stages=args.stages)
+    st = Stepper(w, kw, dev, warmup=args.warmup)
+    K = max(args.steps, 20)
+    ms = st.steps(K)
+    split_ms, merge_ms = st.phases(K)
+    e2e_ms, _, _ = st.e2e(K)
+    par = st.parity(256)
+    traffic = recorded_traffic(w.name, opts_key(kw))
+    kvb = st.kv_bytes
+    entry = {"workload": w.name, "partition_tokens": part, "steps": K,
+             "us_per_step": round(ms * 1e3, 3), "gbs": round(kvb / (ms * 1e-3) / 1e9, 2),
+             "split_us": round(split_ms * 1e3, 3), "merge_us": round(merge_ms * 1e3, 3),
+             "frac": round(kvb / (split_ms * 1e-3) / 1e9 / peak, 4),
+             "step_frac": round(kvb / (ms * 1e-3) / 1e9 / peak, 4),
+             "e2e_us": round(e2e_ms * 1e3, 3),
+             "kv_bytes_per_step": kvb,
+             "traffic_ratio": round(traffic / kvb, 4) if traffic else None,
+             "l2": ("inputs larger than L2" if not st.flush
+                    else "L2 flushed between timed steps"),
+             "max_abs_err": par["max_abs_err"], "mean_abs_err": par["mean_abs_err"],
+             "parity_outputs": par["pairs"]}
+    del st
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = make_workload(args.config, args.query_tokens, args.group)
-    if args.fused_append:
-        make_room_for_next_token(w)
-    q, k, v, t, sl = w.torch_tensors(dev)
-    multi = w.cu_q is not None
-    if multi and args.fused_append:
-        raise SystemExit("--fused-append is a one-token-per-sequence step")
-    out = torch.empty(tuple(q.shape), dtype=torch.float32, device=dev)
     opt_kw = dict(partition_tokens=args.partition_tokens, compute=args.compute,
                   stages=args.stages)
-    opts = pg.options(**opt_kw)
-    opts_split = pg.options(**opt_kw, phase=pg.PA_PHASE_SPLIT)
-    opts_merge = pg.options(**opt_kw, phase=pg.PA_PHASE_MERGE)
-    if multi:
-        cu = torch.from_numpy(w.cu_q).to(dev)
-        shape = pg.shape_multi(q, k, t)
-        ws = pg.alloc_workspace_multi(shape, w.max_q, opts, dev)
-    else:
-        cu = None
-        shape = pg.shape_of(q, k, t)
-        ws = pg.alloc_workspace(shape, opts, dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def attend(o):
-        """One step of the path through the C ABI (o selects the phases)."""
-        if multi:
-            pg.pa_decode_multi(q, cu, w.max_q, w.causal, k, v, t, sl, w.scale, out, ws, o)
-        else:
-            pg.pa_decode(q, k, v, t, sl, w.scale, out, ws, o)
-
-    kv_bytes = w.kv_bytes()
-    flush = kv_bytes <= 2 * L2_BYTES
-    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
-
-    for _ in range(args.warmup):
-        if flush:
-            scratch.fill_(1.0)
-        attend(opts)
-    attend(opts_split)
-    attend(opts_merge)
-    torch.cuda.synchronize()
-    if pg.pa_read_status(ws) != 0:
-        raise RuntimeError("device status bits set during warm-up")
-
+    st = Stepper(w, opt_kw, dev, fused_append=args.fused_append, graph=args.graph,
+                 warmup=args.warmup)
+    q = st.q
+    kv_bytes = st.kv_bytes
     K = args.steps
     props = torch.cuda.get_device_properties(dev)
     uuid = getattr(props, "uuid", None)
     sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local_rank))
-
-    if args.fused_append:
-        # each step writes a new K/V row at position len and attends over
-        # len + 1 tokens (the lengths are not advanced, so every step
-        # rewrites the same slots)
-        gen = torch.Generator(device=dev).manual_seed(1)
-        kn = torch.randn((w.B, w.Hkv, w.d), generator=gen, device=dev).to(k.dtype)
-        vn = torch.randn((w.B, w.Hkv, w.d), generator=gen, device=dev).to(k.dtype)
-        kv_bytes += w.B * w.Hkv * w.d * 2 * 2  # the appended rows
-
-        def decode_step():
-            pg.pa_decode_append(q, kn, vn, k, v, t, sl, w.scale, out, ws, opts)
-    else:
-        def decode_step():
-            attend(opts)
-
-    graph = None
-    if args.graph:
-        # one decode step captured once and replayed (host launch cost removed)
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.stream(cap):
-            decode_step()
-        cap.synchronize()
-        with torch.cuda.graph(graph, stream=cap):
-            decode_step()
-        for _ in range(args.warmup):
-            graph.replay()
-        torch.cuda.synchronize()
-
-    # ---- timed region 1 (the value): K decode steps through pa_decode
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     sampler.start()
     time.sleep(0.3)
+
+    # ---- timed region 1 (the value): K decode steps through pa_decode
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    sampler.mark_begin()
-    # With the L2 flushed between steps, each step is bracketed by its own
-    # events (the flush stays outside); otherwise only the first and the
-    # last, so that consecutive steps stay back to back on the stream (the
-    # split kernel is a programmatic dependent of the previous merge, and an
-    # event in between would serialise them).
-    for i in range(K):
-        if flush:
-            scratch.fill_(1.0)
-        if flush or i == 0:
-            ev[i][0].record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            decode_step()
-        if flush or i == K - 1:
-            ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    sampler.mark_end()
+    t_load0 = time.time()
+    ms_value = st.steps(K)
     if world > 1:
         torch.distributed.barrier()
-    clocks = sampler.stop()
-    if flush:
-        total_ms = float(sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)))
-    else:
-        total_ms = ev[0][0].elapsed_time(ev[K - 1][1])
-
-    # ---- timed region 2 (the roofline): the same steps as two phase calls
-    # with an event between them, giving the split kernel's own duration
-    ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    torch.cuda.synchronize()
-    for i in range(K):
-        if flush:
-            scratch.fill_(1.0)
-        ev3[i][0].record(stream)
-        attend(opts_split)
-        ev3[i][1].record(stream)
-        attend(opts_merge)
-        ev3[i][2].record(stream)
-    torch.cuda.synchronize()
-    split_ms = [ev3[i][0].elapsed_time(ev3[i][1]) for i in range(K)]
-    merge_ms = [ev3[i][1].elapsed_time(ev3[i][2]) for i in range(K)]
-    if pg.pa_read_status(ws) != 0:
-        raise RuntimeError("device status bits set during the timed steps")
-
-    # ---- e2e: host buffers, transfers inside the timed region.  Every step
-    # is one call of the library's host-buffer entry point (bound once to
-    # the step's buffers, as a serving loop would): it moves q, the block
-    # table and the lengths (and the query offsets) from pinned host memory
-    # into the workspace's staging, runs both phases with the output written
-    # to pinned host memory, publishes the call's status there too, and
-    # waits for the stream.
-    Ke = max(3, min(K, 200))
-    q_h, t_h, sl_h = (x.cpu().contiguous().pin_memory() for x in (q, t, sl))
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    parts = [q_h, t_h, sl_h]
-    if multi:
-        cu_h = cu.cpu().contiguous().pin_memory()
-        parts.append(cu_h)
-        shape_h = pg.shape_multi(q, k, t)
-        ws_h = pg.alloc_workspace_multi_host(shape_h, w.max_q, q.shape[0], opts, dev)
-
-        attend_host = pg.bind_decode_multi_host(q_h, cu_h, w.max_q, w.causal, k, v, t_h, sl_h,
-                                                w.scale, out_h, ws_h, opts, stream)
-    else:
-        ws_h = pg.alloc_workspace_host(pg.shape_of(q, k, t), opts, dev)
-        attend_host = pg.bind_decode_host(q_h, k, v, t_h, sl_h, w.scale, out_h, ws_h, opts,
-                                          stream)
-    h2d = sum(x.numel() * x.element_size() for x in parts)
-    d2h = out_h.numel() * 4 + 4  # the output and the call's status word
-
-    for _ in range(2):
-        attend_host()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    # ---- the same K-step region repeated (run-to-run spread; a longer
+    # loaded window for the clock samples)
+    reps = []
+    t_rep = time.time()
+    while len(reps) < 3 or (time.time() - t_rep < args.repeat_s and len(reps) < 200):
+        reps.append(st.steps(K))
+    # ---- timed region 2 (the roofline): the split kernel's own duration
+    split_ms, merge_ms = st.phases(K)
+    t_load1 = time.time()
+    clocks = sampler.window(t_load0, t_load1)
+    # ---- e2e: host buffers, transfers inside the timed region
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    e2e_status = 0
-    if flush:
-        # L2 flushed before every step, outside its events
-        eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
-        for i in range(Ke):
-            scratch.fill_(1.0)
-            eve[i][0].record(stream)
-            e2e_status |= attend_host()
-            eve[i][1].record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = float(sum(eve[i][0].elapsed_time(eve[i][1]) for i in range(Ke))) / Ke
-    else:
-        e0.record(stream)
-        for _ in range(Ke):
-            e2e_status |= attend_host()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / Ke
-    if e2e_status != 0:
-        raise RuntimeError(f"device status bits {e2e_status:#x} during the end-to-end steps")
-    if not torch.equal(out_h, out.cpu()):
-        raise RuntimeError("the end-to-end output differs from the device-buffer output")
+    e2e_ms, h2d, d2h = st.e2e(K)
 
     # ---- max over ranks
+    total_ms = ms_value * K
     total_ms, e2e_ms, split_avg_ms, merge_avg_ms = max_over_ranks(
-        [total_ms, e2e_ms, float(np.mean(split_ms)), float(np.mean(merge_ms))], dev)
+        [total_ms, e2e_ms, split_ms, merge_ms], dev)
+    peak, peak_kind = peaks()
+    cpu = None
+    parity = None
+    per_config = None
+    if rank == 0 and world == 1:
+        if args.cpu_baseline_s > 0:
+            gbs, dt, pairs, threads, passes = oracle_sample(w, args.cpu_baseline_s)
+            toks = int(w.cache_seqlens[row_sequences(w)[pairs[:, 0]]].astype(np.int64).sum())
+            gbs1, dt1, pairs1, _, passes1 = oracle_sample(w, args.cpu_baseline_s / 2,
+                                                          n_threads=1)
+            toks1 = int(w.cache_seqlens[row_sequences(w)[pairs1[:, 0]]].astype(np.int64).sum())
+            cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                   "sample": f"{len(pairs)} of {query_rows(w) * w.H} (query row, head) outputs, "
+                             f"{toks} cached tokens, {passes} pass(es), {dt:.1f} s; GB/s counts "
+                             f"each output's share (1/G of its kv head, split over its "
+                             f"sequence's query rows) of the step's unique K/V bytes",
+                   "one_core": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                                "sample": f"{len(pairs1)} outputs, {toks1} cached tokens, "
+                                          f"{passes1} pass(es), {dt1:.1f} s"}}
+        parity = st.parity(256)
+        if args.per_config == "all" or (args.per_config == "auto" and args.config ==
+                                         DEFAULT_WORKLOAD and not (args.query_tokens or
+                                         args.group or args.fused_append or args.graph)):
+            del st
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            per_config = {}
+            for entry, name, part in PER_CONFIG:
+                t0 = time.time()
+                per_config[entry] = per_config_entry(name, part, args, dev, peak)
+                per_config[entry]["clocks"] = sampler.window(t0, time.time())
+    sampler.stop()
     if rank != 0:
         return
     ms_per_step = total_ms / K
     value = whole_job_gbs(kv_bytes, world, ms_per_step)
     e2e_value = whole_job_gbs(kv_bytes, world, e2e_ms)
-    peak, peak_kind = peaks()
     achieved = kv_bytes / (split_avg_ms * 1e-3) / 1e9
-    opts_key = f"part={args.partition_tokens},compute={args.compute},stages={args.stages}"
-    traffic = recorded_traffic(w.name, opts_key)
-    cpu = None
-    parity = None
-    if args.cpu_baseline_s > 0 and world == 1:
-        gbs, dt, pairs, threads, passes = oracle_sample(w, args.cpu_baseline_s)
-        toks = int(w.cache_seqlens[row_sequences(w)[pairs[:, 0]]].astype(np.int64).sum())
-        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{len(pairs)} of {query_rows(w) * w.H} (query row, head) outputs, "
-                         f"{toks} cached tokens, {passes} pass(es), {dt:.1f} s; GB/s counts "
-                         f"each output's share (1/G of its kv head, split over its "
-                         f"sequence's query rows) of the step's unique K/V bytes"}
-        # the timed kernels' last output against the oracle on that sample
-        chk = pairs[:256]
-        ref = oracle_outputs(w, chk)
-        got = out.cpu().numpy().astype(np.float64)[chk[:, 0], chk[:, 1]]
-        err = np.abs(got - ref)
-        parity = {"pairs": int(len(chk)), "max_abs_err": float(err.max()),
-                  "mean_abs_err": float(err.mean()), "tolerance": [2e-3, 2e-4]}
+    traffic = recorded_traffic(w.name, opts_key(opt_kw))
+    rep_us = sorted(r * 1e3 for r in reps)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -569,9 +702,14 @@ def run_ours(args, rank, world, local_rank):
                      "merge_avg_launch_us": round(merge_avg_ms * 1e3, 3)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_ms * 1e3, 2)},
+        "repeats": {"n": len(rep_us), "steps_each": K,
+                    "us_per_step_min": round(rep_us[0], 2),
+                    "us_per_step_median": round(statistics.median(rep_us), 2),
+                    "us_per_step_max": round(rep_us[-1], 2)},
         "clocks": clocks,
         "cpu_baseline": cpu,
         "parity_vs_oracle": parity,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
 
@@ -595,7 +733,13 @@ def main():
     ap.add_argument("--graph", action="store_true",
                     help="replay one captured CUDA graph of pa_decode per step")
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0,
-                    help="seconds of oracle work for the cpu_baseline sample (0 = skip)")
+                    help="seconds of oracle work for the cpu_baseline sample on all host "
+                         "cores (0 = skip); the one-core sample takes half as long")
+    ap.add_argument("--per-config", default="auto", choices=["auto", "all", "none"],
+                    help="also measure the other configurations (auto: when the headline "
+                         "workload runs with default workload options)")
+    ap.add_argument("--repeat-s", type=float, default=0.3,
+                    help="seconds of repeated K-step regions after the timed one (spread)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -143,6 +143,21 @@ typedef struct pa_options {
                         only phase 1, PA_PHASE_MERGE only phase 2 (which must
                         follow phase 1 of the same step on the same stream),
                         e.g. to time the kernels apart */
+  int32_t wait_limit_us; /* the longest one pipeline wait of the split kernel
+                        may take before the step gives up (sets
+                        PA_STATUS_TIMEOUT, outputs of that step unreliable);
+                        0 = 2 s.  Such a wait is never expected to run out:
+                        copies complete in microseconds.  The copies a CTA
+                        has in flight when it gives up are always waited for
+                        before it exits.  Not used by PA_COMPUTE_TC, whose
+                        waits keep 2 s. */
+  int32_t stall_test; /* testing the timeout path, 0 in normal use.  1: warp 0
+                        of every CTA of the split kernel that has work waits
+                        for its first tile on a barrier that nothing
+                        completes, so that wait runs out after
+                        wait_limit_us; the step then reports
+                        PA_STATUS_TIMEOUT and the next call on the same
+                        workspace is unaffected.  PA_COMPUTE_TC: PA_ERR_OPTION. */
 } pa_options;
 
 #define PA_PHASE_BOTH 0

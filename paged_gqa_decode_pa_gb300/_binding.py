@@ -86,13 +86,16 @@ PA_PHASE_MERGE = 2
 class pa_options(ctypes.Structure):
     _fields_ = [("partition_tokens", ctypes.c_int32), ("compute", ctypes.c_int32),
                 ("num_ctas", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("phase", ctypes.c_int32)]
+                ("phase", ctypes.c_int32), ("wait_limit_us", ctypes.c_int32),
+                ("stall_test", ctypes.c_int32)]
 
 
 def options(partition_tokens: int = 0, compute: str = "auto", num_ctas: int = 0,
-            stages: int = 0, phase: int = PA_PHASE_BOTH) -> pa_options:
+            stages: int = 0, phase: int = PA_PHASE_BOTH, wait_limit_us: int = 0,
+            stall_test: int = 0) -> pa_options:
     return pa_options(int(partition_tokens), _COMPUTE[compute] if isinstance(compute, str)
-                      else int(compute), int(num_ctas), int(stages), int(phase))
+                      else int(compute), int(num_ctas), int(stages), int(phase),
+                      int(wait_limit_us), int(stall_test))
 
 
 _lib = None

@@ -334,6 +334,9 @@ int check_options(const pa_shape* s, const pa_options* o) {
   if (o->num_ctas < 0 || o->num_ctas > (1 << 20)) return PA_ERR_OPTION;
   if (o->stages < 0 || o->stages > kMaxSlots / kMaxWarps) return PA_ERR_OPTION;
   if (o->phase < PA_PHASE_BOTH || o->phase > PA_PHASE_MERGE) return PA_ERR_OPTION;
+  if (o->wait_limit_us < 0) return PA_ERR_OPTION;
+  if (o->stall_test < 0 || o->stall_test > 1) return PA_ERR_OPTION;
+  if (o->stall_test && o->compute == PA_COMPUTE_TC) return PA_ERR_OPTION;
   return PA_OK;
 }
 
@@ -652,6 +655,8 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.causal = 0;
   a.total_q = 0;
   a.max_q = max_q;
+  a.wait_us = o ? o->wait_limit_us : 0;
+  a.stall_test = o ? o->stall_test : 0;
   MergeArgs& m = c->ma;
   m.seqlens = cache_seqlens;
   m.out = out;

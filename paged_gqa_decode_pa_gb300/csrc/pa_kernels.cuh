@@ -76,6 +76,10 @@ struct SplitArgs {
   // sequence s owns rows cu_q[s] .. cu_q[s+1]-1
   const int32_t* cu_q;
   int32_t nqg, tq, causal, total_q, max_q;
+  // the longest a pipeline wait may take before the step gives up (us; 0 =
+  // kWaitLimitNs), and the timeout-path test: 1 = warp 0 of every CTA waits
+  // for its first tile on a barrier that nothing completes
+  int32_t wait_us, stall_test;
 };
 
 // Query rows [q0, q0 + nq) of sequence s, or false when cu_q is not a valid
@@ -129,6 +133,9 @@ static_assert(sizeof(SplitArgs) <= kArgsBytes && sizeof(SplitArgs) % 4 == 0, "Sp
 // Warp pairs: one "empty" mbarrier per ring slot, after the SplitArgs copy.
 constexpr uint32_t kEmptyOffset = kArgsOffset + kArgsBytes;
 static_assert(kEmptyOffset + 8u * kMaxSlots <= 2048u, "empty barriers below the stages");
+// The timeout-path test's barrier (initialised, never arrived on).
+constexpr uint32_t kStallOffset = kEmptyOffset + 8u * kMaxSlots;
+static_assert(kStallOffset + 8u <= 2048u, "stall barrier below the stages");
 
 struct MergeArgs {
   const int32_t* seqlens;

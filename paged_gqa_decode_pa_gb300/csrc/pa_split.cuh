@@ -816,9 +816,11 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       mbar_init(base + L.full + 8 * s, 1);
       if (kPair) mbar_init(base + L.empty + 8 * s, 1);
     }
+    if (a.stall_test) mbar_init(base + kStallOffset, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  const uint64_t wait_ns = a.wait_us > 0 ? (uint64_t)a.wait_us * 1000ull : kWaitLimitNs;
   for (int i = tid; i < D / 8; i += blockDim.x) sts128(base + L.zrow + 16u * i, make_uint4(0u, 0u, 0u, 0u));
   if (lane == 0) {
     tma_prefetch_desc(&tmk);
@@ -886,6 +888,10 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   uint32_t slot = 0, phase = 0;  // ring slot to consume next; per-slot parity bits
   uint32_t ephase = 0;           // warp pairs, issuer: per-slot parity of the "empty" barriers
   uint32_t consumed = 0;
+  // the first of this warp's tiles whose wait gave up: from there on, copies
+  // it issued may still be in flight when the loop ends (see the drain)
+  int64_t first_fail = -1;
+  bool stall = a.stall_test && w == 0;
   MmaState<T, D, NB, kQ> mst;
   SimtState<T, D> sst;
   float* ps = reinterpret_cast<float*>(smem + L.ps) + w * kTile * kGMax;
@@ -927,8 +933,15 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     }
     for (int i = 0; i < cnt; ++i) {
       const uint32_t gslot = (uint32_t)sw * R + slot;
-      const bool ok = mbar_wait_bounded(base + L.full + 8 * gslot, (phase >> slot) & 1u, abort_flag,
-                                        kWaitLimitNs);
+      // the timeout-path test waits on a barrier nothing completes instead
+      const uint32_t wbar = stall ? base + kStallOffset : base + L.full + 8 * gslot;
+      const uint32_t wpar = stall ? 0u : (phase >> slot) & 1u;
+      stall = false;
+      // lanes poll on their own: a give-up seen by one lane counts for the
+      // warp, so the warp-wide mma below runs on all lanes or on none
+      const bool ok =
+          __all_sync(0xffffffffu, mbar_wait_bounded(wbar, wpar, abort_flag, wait_ns));
+      if (!ok && first_fail < 0) first_fail = consumed;
       const uint64_t info64 = lds64(base + L.info + 8 * gslot);
       const uint32_t info = (uint32_t)info64;
       const int valid = (int)(info & 0xffffu);
@@ -976,8 +989,9 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       if (issuer) {
         if constexpr (kPair) {
           // the partner warp must be done with this slot before it is refilled
-          const bool freed = mbar_wait_bounded(base + L.empty + 8 * gslot, (ephase >> slot) & 1u,
-                                               abort_flag, kWaitLimitNs);
+          const bool freed = __all_sync(
+              0xffffffffu, mbar_wait_bounded(base + L.empty + 8 * gslot, (ephase >> slot) & 1u,
+                                             abort_flag, wait_ns));
           ephase ^= 1u << slot;
           if (!freed) {
             if (lane == 0) atomicOr(a.status, kStatusTimeout);
@@ -1013,16 +1027,18 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     named_bar_sync(1, blockDim.x);
     have = it.next(pc);
   }
-  if (*abort_flag && lane == 0) {
+  if (first_fail >= 0 && lane == 0) {
     // Drain: wait (bounded, ignoring the abort flag) for this warp's copies
-    // still in flight before the CTA may exit.
+    // that may still be in flight before the CTA may exit.  Tile n of the
+    // warp's stream sits in ring slot n % R in phase (n / R) & 1.  Before
+    // the first give-up every issued tile was waited for; after it nothing
+    // more was issued, so tiles first_fail .. issued-1 (at most R, one per
+    // slot) are the ones to wait for -- each slot's phase completes once
+    // more at most, so waiting on a tile already consumed returns at once.
     volatile int never = 0;
-    for (uint32_t kk = consumed; kk < is.issued; ++kk) {
-      mbar_wait_bounded(base + L.full + 8 * ((uint32_t)sw * R + slot), (phase >> slot) & 1u, &never,
-                        kWaitLimitNs / 4);
-      phase ^= 1u << slot;
-      slot = (slot + 1 == (uint32_t)R) ? 0u : slot + 1;
-    }
+    for (int64_t kk = first_fail; kk < (int64_t)is.issued; ++kk)
+      mbar_wait_bounded(base + L.full + 8 * ((uint32_t)sw * R + (uint32_t)(kk % R)),
+                        (uint32_t)((kk / R) & 1), &never, kWaitLimitNs / 4);
   }
 }
 
