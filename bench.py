@@ -10,10 +10,13 @@ metric  : K/V-read HBM GB/s = unique K/V bytes a step must read / step time
           (unit GB/s, higher is better); us per step and tokens/s ride along.
 value   : device-timed with CUDA events on the launching stream, inputs
           resident in HBM; K steps between barrier + synchronize, max over ranks.
-e2e     : the same metric through the host-buffer call (pa_decode_host /
-          pa_decode_multi_host): every step copies q, the block table and the
-          lengths from pinned host memory, attends, and copies the output and
-          the call's status back before the call returns.
+e2e     : the same metric through the host-buffer calls: every step copies
+          q, the block table and the lengths from pinned host memory, attends,
+          and writes the output and the step's status word back to pinned
+          host memory.  value: the asynchronous call (pa_decode_host_async /
+          pa_decode_multi_host_async) with two buffer sets on alternating
+          staging slots, steps issued back to back, one synchronisation at the
+          end; sync_*: the synchronous call, which waits for every step.
 roofline: the split kernel alone (CUDA events around phase 1 in the same timed
           loop) against the measured HBM copy bandwidth.
 cpu_baseline / --impl reference: the float64 oracle on the host cores, on a
@@ -378,6 +381,19 @@ class Stepper:
             self.cu = None
             self.ws = pg.alloc_workspace(pg.shape_of(q, k, t), self.opts, dev)
         self.stream = torch.cuda.current_stream(dev)
+        # the step's calls, bound once (per-call Python checks would make the
+        # small steps host-bound)
+        if self.multi:
+            self.bound = {ph: pg.bind_decode_multi(q, self.cu, w.max_q, w.causal, self.k, self.v,
+                                                   t, self.sl, w.scale, self.out, self.ws, o,
+                                                   self.stream)
+                          for ph, o in ((0, self.opts), (1, self.opts_split),
+                                        (2, self.opts_merge))}
+        else:
+            self.bound = {ph: pg.bind_decode(q, self.k, self.v, t, self.sl, w.scale, self.out,
+                                             self.ws, o, self.stream)
+                          for ph, o in ((0, self.opts), (1, self.opts_split),
+                                        (2, self.opts_merge))}
         self.kv_bytes = w.kv_bytes()
         self.flush = self.kv_bytes <= 2 * L2_BYTES
         self.scratch = (torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -399,9 +415,9 @@ class Stepper:
             self.kn = torch.randn((w.B, w.Hkv, w.d), generator=gen, device=dev).to(k.dtype)
             self.vn = torch.randn((w.B, w.Hkv, w.d), generator=gen, device=dev).to(k.dtype)
             self.kv_bytes += w.B * w.Hkv * w.d * 2 * 2  # the appended rows
-            self.decode_step = lambda: pg.pa_decode_append(
+            self.decode_step = pg.bind_decode_append(
                 self.q, self.kn, self.vn, self.k, self.v, self.t, self.sl, w.scale, self.out,
-                self.ws, self.opts)
+                self.ws, self.opts, self.stream)
         self.graph = None
         if graph:
             # one decode step captured once and replayed (host launch cost removed)
@@ -423,12 +439,7 @@ class Stepper:
 
     def attend(self, o):
         """One step of the path through the C ABI (o selects the phases)."""
-        w, pg = self.w, self.pg
-        if self.multi:
-            pg.pa_decode_multi(self.q, self.cu, w.max_q, w.causal, self.k, self.v, self.t,
-                               self.sl, w.scale, self.out, self.ws, o)
-        else:
-            pg.pa_decode(self.q, self.k, self.v, self.t, self.sl, w.scale, self.out, self.ws, o)
+        self.bound[o.phase]()
 
     def steps(self, K):
         """K decode steps; device ms per step.  With the L2 flushed between
@@ -477,64 +488,91 @@ class Stepper:
         return float(np.mean(split_ms)), float(np.mean(merge_ms))
 
     def e2e(self, K):
-        """End to end through the host-buffer call: every step is one call of
-        the library's host-buffer entry point (bound once to the step's
-        buffers, as a serving loop would).  It moves q, the block table and
-        the lengths (and the query offsets) from pinned host memory into the
-        workspace's staging, runs both phases with the output written to
-        pinned host memory, publishes the call's status there too, and waits
-        for the stream.  Returns (ms per step, h2d bytes, d2h bytes)."""
+        """End to end through the library's host-buffer entry points: every
+        step moves q, the block table and the lengths (and the query
+        offsets) from pinned host memory into the workspace's staging, runs
+        both phases with the output written to pinned host memory, and
+        publishes the step's status word there too.
+
+        async: the serving-loop form -- two buffer sets, one per staging
+        slot, and a bound call each (pa_decode_host_async); steps are issued
+        back to back and the host synchronises only after the last one, so
+        step i + 1's staging overlaps step i's kernels.  sync: one
+        pa_decode_host call per step, which waits for the stream before it
+        returns.  Returns (async ms per step, sync ms per step, h2d bytes,
+        d2h bytes)."""
         import torch
 
         pg, w = self.pg, self.w
         q, k, v, t, sl, out, dev, stream = (self.q, self.k, self.v, self.t, self.sl, self.out,
                                             self.dev, self.stream)
         Ke = max(3, min(K, 200))
-        q_h, t_h, sl_h = (x.cpu().contiguous().pin_memory() for x in (q, t, sl))
-        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        parts = [q_h, t_h, sl_h]
-        if self.multi:
-            cu_h = self.cu.cpu().contiguous().pin_memory()
-            parts.append(cu_h)
-            ws_h = pg.alloc_workspace_multi_host(pg.shape_multi(q, k, t), w.max_q, q.shape[0],
-                                                 self.opts, dev)
-            attend_host = pg.bind_decode_multi_host(q_h, cu_h, w.max_q, w.causal, k, v, t_h,
-                                                    sl_h, w.scale, out_h, ws_h, self.opts,
-                                                    stream)
-        else:
-            ws_h = pg.alloc_workspace_host(pg.shape_of(q, k, t), self.opts, dev)
-            attend_host = pg.bind_decode_host(q_h, k, v, t_h, sl_h, w.scale, out_h, ws_h,
-                                              self.opts, stream)
-        h2d = sum(x.numel() * x.element_size() for x in parts)
-        d2h = out_h.numel() * 4 + 4  # the output and the call's status word
+        shape = pg.shape_multi(q, k, t) if self.multi else pg.shape_of(q, k, t)
+        sets = []
         for _ in range(2):
-            attend_host()
-        torch.cuda.synchronize()
-        status = 0
-        if self.flush:
-            # L2 flushed before every step, outside its events
-            eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(Ke)]
-            for i in range(Ke):
-                self.flush_l2()
-                eve[i][0].record(stream)
-                status |= attend_host()
-                eve[i][1].record(stream)
-            torch.cuda.synchronize()
-            ms = float(sum(eve[i][0].elapsed_time(eve[i][1]) for i in range(Ke))) / Ke
+            parts = [x.cpu().contiguous().pin_memory() for x in (q, t, sl)]
+            if self.multi:
+                parts.append(self.cu.cpu().contiguous().pin_memory())
+            sets.append((parts, torch.empty(out.shape, dtype=out.dtype).pin_memory()))
+        h2d = sum(x.numel() * x.element_size() for x in sets[0][0])
+        d2h = sets[0][1].numel() * 4 + 4  # the output and the step's status word
+        if self.multi:
+            ws_a = pg.alloc_workspace_multi_host_async(shape, w.max_q, q.shape[0], self.opts, dev)
+            ws_s = pg.alloc_workspace_multi_host(shape, w.max_q, q.shape[0], self.opts, dev)
+            calls = [pg.bind_decode_multi_host_async(p[0], p[3], w.max_q, w.causal, k, v, p[1],
+                                                     p[2], w.scale, o, ws_a, s, self.opts,
+                                                     stream)
+                     for s, (p, o) in enumerate(sets)]
+            sync = pg.bind_decode_multi_host(sets[0][0][0], sets[0][0][3], w.max_q, w.causal, k,
+                                             v, sets[0][0][1], sets[0][0][2], w.scale,
+                                             sets[0][1], ws_s, self.opts, stream)
         else:
+            ws_a = pg.alloc_workspace_host_async(shape, self.opts, dev)
+            ws_s = pg.alloc_workspace_host(shape, self.opts, dev)
+            calls = [pg.bind_decode_host_async(p[0], k, v, p[1], p[2], w.scale, o, ws_a, s,
+                                               self.opts, stream)
+                     for s, (p, o) in enumerate(sets)]
+            sync = pg.bind_decode_host(sets[0][0][0], k, v, sets[0][0][1], sets[0][0][2],
+                                       w.scale, sets[0][1], ws_s, self.opts, stream)
+
+        def timed(run_step):
+            for i in range(2):
+                run_step(i)
+            torch.cuda.synchronize()
+            if self.flush:
+                # L2 flushed before every step, outside its events
+                ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                      for _ in range(Ke)]
+                for i in range(Ke):
+                    self.flush_l2()
+                    ev[i][0].record(stream)
+                    run_step(i)
+                    ev[i][1].record(stream)
+                torch.cuda.synchronize()
+                return float(sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(Ke))) / Ke
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for _ in range(Ke):
-                status |= attend_host()
+            for i in range(Ke):
+                run_step(i)
             e1.record(stream)
             torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / Ke
-        if status != 0:
-            raise RuntimeError(f"device status bits {status:#x} during the end-to-end steps")
-        if not torch.equal(out_h, out.cpu()):
-            raise RuntimeError("the end-to-end output differs from the device-buffer output")
-        return ms, h2d, d2h
+            return e0.elapsed_time(e1) / Ke
+
+        status = [0]
+
+        def step_sync(i):
+            status[0] |= sync()
+
+        ms_sync = timed(step_sync)
+        ms_async = timed(lambda i: calls[i % 2]())
+        status[0] |= calls[0].status() | calls[1].status()
+        if status[0] != 0:
+            raise RuntimeError(f"device status bits {status[0]:#x} during the end-to-end steps")
+        for _, o in sets:
+            if not torch.equal(o, out.cpu()):
+                raise RuntimeError("the end-to-end output differs from the device-buffer output")
+        return ms_async, ms_sync, h2d, d2h
 
     def parity(self, n, seed=0):
         """The last output against the oracle on n sampled (row, head) outputs
@@ -577,7 +615,7 @@ def per_config_entry(name, part, args, dev, peak):
     K = max(args.steps, 20)
     ms = st.steps(K)
     split_ms, merge_ms = st.phases(K)
-    e2e_ms, _, _ = st.e2e(K)
+    e2e_ms, e2e_sync_ms, _, _ = st.e2e(K)
     par = st.parity(256)
     traffic = recorded_traffic(w.name, opts_key(kw))
     kvb = st.kv_bytes
@@ -586,7 +624,7 @@ def per_config_entry(name, part, args, dev, peak):
              "split_us": round(split_ms * 1e3, 3), "merge_us": round(merge_ms * 1e3, 3),
              "frac": round(kvb / (split_ms * 1e-3) / 1e9 / peak, 4),
              "step_frac": round(kvb / (ms * 1e-3) / 1e9 / peak, 4),
-             "e2e_us": round(e2e_ms * 1e3, 3),
+             "e2e_us": round(e2e_ms * 1e3, 3), "e2e_sync_us": round(e2e_sync_ms * 1e3, 3),
              "kv_bytes_per_step": kvb,
              "traffic_ratio": round(traffic / kvb, 4) if traffic else None,
              "l2": ("inputs larger than L2" if not st.flush
@@ -639,12 +677,12 @@ def run_ours(args, rank, world, local_rank):
     # ---- e2e: host buffers, transfers inside the timed region
     if world > 1:
         torch.distributed.barrier()
-    e2e_ms, h2d, d2h = st.e2e(K)
+    e2e_ms, e2e_sync_ms, h2d, d2h = st.e2e(K)
 
     # ---- max over ranks
     total_ms = ms_value * K
-    total_ms, e2e_ms, split_avg_ms, merge_avg_ms = max_over_ranks(
-        [total_ms, e2e_ms, split_ms, merge_ms], dev)
+    total_ms, e2e_ms, e2e_sync_ms, split_avg_ms, merge_avg_ms = max_over_ranks(
+        [total_ms, e2e_ms, e2e_sync_ms, split_ms, merge_ms], dev)
     peak, peak_kind = peaks()
     cpu = None
     parity = None
@@ -701,7 +739,11 @@ def run_ours(args, rank, world, local_rank):
                      "avg_launch_us": round(split_avg_ms * 1e3, 3),
                      "merge_avg_launch_us": round(merge_avg_ms * 1e3, 3)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_ms * 1e3, 2)},
+                "d2h_bytes_per_step": d2h, "us_per_step": round(e2e_ms * 1e3, 2),
+                "mode": "pa_decode_host_async, two pinned buffer sets alternating staging slots, "
+                        "one host synchronisation after the last step",
+                "sync_us_per_step": round(e2e_sync_ms * 1e3, 2),
+                "sync_value": round(whole_job_gbs(kv_bytes, world, e2e_sync_ms), 2)},
         "repeats": {"n": len(rep_us), "steps_each": K,
                     "us_per_step_min": round(rep_us[0], 2),
                     "us_per_step_median": round(statistics.median(rep_us), 2),

@@ -47,7 +47,7 @@
  *     Hkv * (max_blocks_per_seq + 64) below 2^31 (else PA_ERR_SHAPE).
  *   - Work is enqueued on `stream` (NULL = legacy default stream).  No entry
  *     point allocates or picks a launch shape from device data, and none but
- *     pa_read_status and the host-buffer calls synchronises (the first
+ *     pa_read_status and the synchronous host-buffer calls synchronises (the first
  *     pa_decode_noalloc call on a device also enqueues one memset on its
  *     stream), so pa_decode and
  *     pa_cache_append can be captured in a CUDA graph
@@ -300,6 +300,52 @@ int pa_decode_multi_host(const pa_shape* shape, const pa_options* options, const
                          const int32_t* block_table_host, const int32_t* cache_seqlens_host,
                          float scale, float* out_host, uint32_t* status_host, void* workspace,
                          size_t workspace_bytes, pa_stream_t stream);
+
+/* pa_decode_host / pa_decode_multi_host without the wait: the call enqueues
+ * the same work on `stream` and returns.  A serving loop that issues step
+ * i + 1 before step i has finished keeps the GPU busy through the host's
+ * own time per call, and step i + 1's staging of its inputs runs while step
+ * i's last kernel finishes: the staging kernel is a programmatic dependent
+ * of the kernel before it on the stream, fills its staging area, and only
+ * then waits for that kernel.  (The decoding path of the Hugging Face
+ * "Paged attention" page reads the cache in place at every step; only the
+ * step's q, table and lengths move.)
+ *   slot: 0 or 1, which of the workspace's two staging areas this call uses
+ *         (else PA_ERR_OPTION).  Consecutive calls on a stream must
+ *         alternate slots: a call may still be reading its slot while the
+ *         next call fills the other one.
+ *   workspace: pa_workspace_size_host_async / pa_workspace_size_multi_host_async
+ *         bytes (room for both slots), zero-filled once; the partial states
+ *         are shared by both slots (the kernels of consecutive calls on one
+ *         stream never overlap where they use them).
+ *   Host buffers: page-locked (cudaHostAlloc / cudaHostRegister) or
+ *         device memory, as for pa_decode_host.  Pageable buffers work but
+ *         the driver's staged copies make the call wait for them.  The call's
+ *         inputs must stay unchanged, and out_host / status_host unread,
+ *         until the stream has passed the call (cudaStreamSynchronize, or an
+ *         event recorded after it); give each slot its own buffers when the
+ *         next step is issued before the previous one is read.
+ *   status_host: as for pa_decode_host, written when the call's kernels run.
+ * Everything else (arguments, results, status bits, errors before anything
+ * is enqueued) is as for the synchronous calls, and the result bits are the
+ * same. */
+int pa_workspace_size_host_async(const pa_shape* shape, const pa_options* options,
+                                 size_t* bytes);
+int pa_decode_host_async(const pa_shape* shape, const pa_options* options, const void* q_host,
+                         const void* k_cache, const void* v_cache,
+                         const int32_t* block_table_host, const int32_t* cache_seqlens_host,
+                         float scale, float* out_host, uint32_t* status_host, int32_t slot,
+                         void* workspace, size_t workspace_bytes, pa_stream_t stream);
+int pa_workspace_size_multi_host_async(const pa_shape* shape, const pa_options* options,
+                                       int32_t max_q, int32_t max_total_q, size_t* bytes);
+int pa_decode_multi_host_async(const pa_shape* shape, const pa_options* options,
+                               const void* q_host, const int32_t* cu_seqlens_q_host,
+                               int32_t total_q, int32_t max_q, int32_t causal,
+                               const void* k_cache, const void* v_cache,
+                               const int32_t* block_table_host,
+                               const int32_t* cache_seqlens_host, float scale, float* out_host,
+                               uint32_t* status_host, int32_t slot, void* workspace,
+                               size_t workspace_bytes, pa_stream_t stream);
 
 /* Append one new token per sequence to the paged cache, in place: for every
  * b and kv head j, k_new[b,j,:] and v_new[b,j,:] are copied bit for bit to

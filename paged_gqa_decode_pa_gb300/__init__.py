@@ -16,7 +16,10 @@ from ._binding import (  # noqa: F401
     pa_copy_blocks, pa_decode_multi, pa_workspace_size_multi, alloc_workspace_multi,
     shape_multi, pa_decode_host, pa_workspace_size_host, alloc_workspace_host,
     pa_decode_multi_host, pa_workspace_size_multi_host, alloc_workspace_multi_host,
-    bind_decode_host, bind_decode_multi_host,
+    bind_decode, bind_decode_multi, bind_decode_append, bind_decode_host, bind_decode_multi_host,
+    pa_workspace_size_host_async,
+    alloc_workspace_host_async, pa_workspace_size_multi_host_async,
+    alloc_workspace_multi_host_async, bind_decode_host_async, bind_decode_multi_host_async,
     PA_MAX_QUERY_TOKENS, PA_MAX_BATCH, PA_STATIC_SCRATCH_BYTES, PA_PHASE_BOTH, PA_PHASE_SPLIT, PA_PHASE_MERGE, PA_ERR_STATE, PA_ERR_NO_BLOCKS, PA_BM_FREE_BLOCKS, PA_BM_REF_COUNT,
     PA_BM_SEQ_BLOCKS,
     PA_OK, PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_ALIGN, PA_ERR_WORKSPACE, PA_ERR_CUDA,

@@ -58,7 +58,9 @@ EXPORTS = ("pa_workspace_size", "pa_decode", "pa_decode_split", "pa_decode_merge
            "pa_bm_share_prefix", "pa_bm_copy_on_write", "pa_bm_reserve_slot",
            "pa_bm_block_table", "pa_bm_query", "pa_copy_blocks", "pa_decode_multi",
            "pa_workspace_size_multi", "pa_decode_host", "pa_workspace_size_host",
-           "pa_decode_multi_host", "pa_workspace_size_multi_host")
+           "pa_decode_multi_host", "pa_workspace_size_multi_host", "pa_decode_host_async",
+           "pa_workspace_size_host_async", "pa_decode_multi_host_async",
+           "pa_workspace_size_multi_host_async")
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -173,6 +175,17 @@ def lib():
         L.pa_decode_multi_host.argtypes = [SP, OP, P, P, i32, i32, i32, P, P, P, P,
                                            ctypes.c_float, P, P, P, ctypes.c_size_t, P]
         L.pa_decode_multi_host.restype = ctypes.c_int
+        L.pa_workspace_size_host_async.argtypes = [SP, OP, ctypes.POINTER(ctypes.c_size_t)]
+        L.pa_workspace_size_host_async.restype = ctypes.c_int
+        L.pa_decode_host_async.argtypes = [SP, OP, P, P, P, P, P, ctypes.c_float, P, P, i32, P,
+                                           ctypes.c_size_t, P]
+        L.pa_decode_host_async.restype = ctypes.c_int
+        L.pa_workspace_size_multi_host_async.argtypes = [SP, OP, i32, i32,
+                                                         ctypes.POINTER(ctypes.c_size_t)]
+        L.pa_workspace_size_multi_host_async.restype = ctypes.c_int
+        L.pa_decode_multi_host_async.argtypes = [SP, OP, P, P, i32, i32, i32, P, P, P, P,
+                                                 ctypes.c_float, P, P, i32, P, ctypes.c_size_t, P]
+        L.pa_decode_multi_host_async.restype = ctypes.c_int
         L.pa_version.argtypes = []
         L.pa_version.restype = ctypes.c_int
         _lib = L
@@ -484,6 +497,122 @@ def bind_decode_multi_host(q, cu_seqlens_q, max_q, causal, k_cache, v_cache, blo
     return _BoundCall(lib().pa_decode_multi_host, "pa_decode_multi_host", args, keep, st)
 
 
+def pa_workspace_size_host_async(shape: pa_shape, opts: Optional[pa_options] = None) -> int:
+    n = ctypes.c_size_t(0)
+    rc = lib().pa_workspace_size_host_async(ctypes.byref(shape),
+                                            ctypes.byref(opts) if opts else None, ctypes.byref(n))
+    _check(rc, "pa_workspace_size_host_async")
+    return int(n.value)
+
+
+def alloc_workspace_host_async(shape: pa_shape, opts: Optional[pa_options] = None, device=None):
+    """Zero-filled device workspace for pa_decode_host_async (two staging slots)."""
+    import torch
+
+    return torch.zeros(pa_workspace_size_host_async(shape, opts), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def pa_workspace_size_multi_host_async(shape: pa_shape, max_q: int, max_total_q: int,
+                                       opts: Optional[pa_options] = None) -> int:
+    n = ctypes.c_size_t(0)
+    rc = lib().pa_workspace_size_multi_host_async(ctypes.byref(shape),
+                                                  ctypes.byref(opts) if opts else None,
+                                                  int(max_q), int(max_total_q), ctypes.byref(n))
+    _check(rc, "pa_workspace_size_multi_host_async")
+    return int(n.value)
+
+
+def alloc_workspace_multi_host_async(shape: pa_shape, max_q: int, max_total_q: int,
+                                     opts: Optional[pa_options] = None, device=None):
+    """Zero-filled device workspace for pa_decode_multi_host_async."""
+    import torch
+
+    return torch.zeros(pa_workspace_size_multi_host_async(shape, max_q, max_total_q, opts),
+                       dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+class _BoundAsyncCall:
+    """An asynchronous host-buffer entry point with its arguments marshalled
+    once: calling it enqueues one step and returns at once.  status() reads
+    the step's device status bits, valid once the stream has passed the call
+    (e.g. after torch.cuda.synchronize()).  Holds references to every tensor
+    it points at, its own page-locked status word included."""
+
+    def __init__(self, fn, name, args, keep, status):
+        self._fn, self._name, self._args, self._keep = fn, name, args, keep
+        self._status = status
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc != PA_OK:
+            raise PagedGQAError(rc, self._name)
+
+    def status(self) -> int:
+        return int(self._status[1][0])
+
+
+def _own_status_word():
+    import torch
+
+    t = torch.zeros(1, dtype=torch.int32).pin_memory()
+    return t, t.numpy().view("uint32")
+
+
+def bind_decode_host_async(q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
+                           workspace, slot: int, opts: Optional[pa_options] = None,
+                           stream=None) -> _BoundAsyncCall:
+    """pa_decode_host_async on these buffers and this staging slot (0 or 1),
+    checked and marshalled once.  A loop alternates two bound calls (slot 0
+    and slot 1, each with its own host buffers) and synchronises only when
+    it reads a result.  The stream is taken at bind time."""
+    _check_host(q, block_table, cache_seqlens, out, k_cache, v_cache)
+    if slot not in (0, 1):
+        raise ValueError("slot must be 0 or 1")
+    shape = shape_of(q, k_cache, block_table)
+    st = _own_status_word()
+    V = ctypes.c_void_p
+    opt = pa_options.from_buffer_copy(opts) if opts else None
+    args = (ctypes.byref(shape), ctypes.byref(opt) if opt else None, V(_ptr(q)), V(_ptr(k_cache)),
+            V(_ptr(v_cache)), V(_ptr(block_table)), V(_ptr(cache_seqlens)),
+            ctypes.c_float(scale), V(_ptr(out)), V(st[0].data_ptr()), ctypes.c_int32(slot),
+            V(_ptr(workspace)), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+            V(_stream(stream)))
+    keep = (shape, opt, q, k_cache, v_cache, block_table, cache_seqlens, out, workspace, st)
+    return _BoundAsyncCall(lib().pa_decode_host_async, "pa_decode_host_async", args, keep, st)
+
+
+def bind_decode_multi_host_async(q, cu_seqlens_q, max_q, causal, k_cache, v_cache, block_table,
+                                 cache_seqlens, scale, out, workspace, slot: int,
+                                 opts: Optional[pa_options] = None,
+                                 stream=None) -> _BoundAsyncCall:
+    """pa_decode_multi_host_async on these buffers and this staging slot (as
+    bind_decode_host_async; total_q is q's row count)."""
+    import torch
+
+    _check_host(q, block_table, cache_seqlens, out, k_cache, v_cache,
+                (("cu_seqlens_q", cu_seqlens_q),))
+    if cu_seqlens_q.dtype != torch.int32 or tuple(cu_seqlens_q.shape) != (block_table.shape[0] + 1,):
+        raise TypeError("cu_seqlens_q must be int32 [B + 1]")
+    if slot not in (0, 1):
+        raise ValueError("slot must be 0 or 1")
+    shape = shape_multi(q, k_cache, block_table)
+    st = _own_status_word()
+    V = ctypes.c_void_p
+    i32 = ctypes.c_int32
+    opt = pa_options.from_buffer_copy(opts) if opts else None
+    args = (ctypes.byref(shape), ctypes.byref(opt) if opt else None, V(_ptr(q)),
+            V(_ptr(cu_seqlens_q)), i32(q.shape[0]), i32(max_q), i32(int(bool(causal))),
+            V(_ptr(k_cache)), V(_ptr(v_cache)), V(_ptr(block_table)), V(_ptr(cache_seqlens)),
+            ctypes.c_float(scale), V(_ptr(out)), V(st[0].data_ptr()), i32(slot),
+            V(_ptr(workspace)), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+            V(_stream(stream)))
+    keep = (shape, opt, q, cu_seqlens_q, k_cache, v_cache, block_table, cache_seqlens, out,
+            workspace, st)
+    return _BoundAsyncCall(lib().pa_decode_multi_host_async, "pa_decode_multi_host_async", args,
+                           keep, st)
+
+
 def _decode_call(name, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                  workspace, opts, stream):
     _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out)
@@ -500,6 +629,92 @@ def pa_decode(q, k_cache, v_cache, block_table, cache_seqlens, scale, out, works
     """out[B,H,d] (fp32) = paged GQA decode attention; see include/pagedgqa.h."""
     _decode_call("pa_decode", q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                  workspace, opts, stream)
+
+
+class _BoundDeviceCall:
+    """A device-buffer entry point with its arguments marshalled once:
+    calling it enqueues the call again on the same buffers (whose contents
+    may have changed in place).  Holds references to every tensor it points
+    at.  The per-call Python checks cost tens of microseconds on the host,
+    more than a small decode step takes on the GPU."""
+
+    def __init__(self, fn, name, args, keep):
+        self._fn, self._name, self._args, self._keep = fn, name, args, keep
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc != PA_OK:
+            raise PagedGQAError(rc, self._name)
+
+
+def bind_decode(q, k_cache, v_cache, block_table, cache_seqlens, scale, out, workspace,
+                opts: Optional[pa_options] = None, stream=None,
+                name: str = "pa_decode") -> _BoundDeviceCall:
+    """pa_decode (or pa_decode_split / pa_decode_merge, by `name`) on these
+    device buffers, checked and marshalled once; each call of the result
+    enqueues one step.  The stream is taken at bind time."""
+    if name not in ("pa_decode", "pa_decode_split", "pa_decode_merge"):
+        raise ValueError(name)
+    _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out)
+    shape = shape_of(q, k_cache, block_table)
+    V = ctypes.c_void_p
+    opt = pa_options.from_buffer_copy(opts) if opts else None
+    args = (ctypes.byref(shape), ctypes.byref(opt) if opt else None, V(_ptr(q)), V(_ptr(k_cache)),
+            V(_ptr(v_cache)), V(_ptr(block_table)), V(_ptr(cache_seqlens)),
+            ctypes.c_float(scale), V(_ptr(out)), V(_ptr(workspace)),
+            ctypes.c_size_t(workspace.numel() * workspace.element_size()), V(_stream(stream)))
+    keep = (shape, opt, q, k_cache, v_cache, block_table, cache_seqlens, out, workspace)
+    return _BoundDeviceCall(getattr(lib(), name), name, args, keep)
+
+
+def bind_decode_multi(q, cu_seqlens_q, max_q, causal, k_cache, v_cache, block_table,
+                      cache_seqlens, scale, out, workspace, opts: Optional[pa_options] = None,
+                      stream=None) -> _BoundDeviceCall:
+    """pa_decode_multi on these device buffers, checked and marshalled once
+    (total_q is q's row count; the stream is taken at bind time)."""
+    import torch
+
+    _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out)
+    if not cu_seqlens_q.is_cuda or cu_seqlens_q.dtype != torch.int32:
+        raise TypeError("cu_seqlens_q must be an int32 CUDA tensor")
+    if tuple(cu_seqlens_q.shape) != (block_table.shape[0] + 1,):
+        raise ValueError("cu_seqlens_q must be [B + 1]")
+    shape = shape_multi(q, k_cache, block_table)
+    V = ctypes.c_void_p
+    i32 = ctypes.c_int32
+    opt = pa_options.from_buffer_copy(opts) if opts else None
+    args = (ctypes.byref(shape), ctypes.byref(opt) if opt else None, V(_ptr(q)),
+            V(_ptr(cu_seqlens_q)), i32(q.shape[0]), i32(max_q), i32(int(bool(causal))),
+            V(_ptr(k_cache)), V(_ptr(v_cache)), V(_ptr(block_table)), V(_ptr(cache_seqlens)),
+            ctypes.c_float(scale), V(_ptr(out)), V(_ptr(workspace)),
+            ctypes.c_size_t(workspace.numel() * workspace.element_size()), V(_stream(stream)))
+    keep = (shape, opt, q, cu_seqlens_q, k_cache, v_cache, block_table, cache_seqlens, out,
+            workspace)
+    return _BoundDeviceCall(lib().pa_decode_multi, "pa_decode_multi", args, keep)
+
+
+def bind_decode_append(q, k_new, v_new, k_cache, v_cache, block_table, cache_seqlens, scale,
+                       out, workspace, opts: Optional[pa_options] = None,
+                       stream=None) -> _BoundDeviceCall:
+    """pa_decode_append on these device buffers, checked and marshalled once
+    (the stream is taken at bind time)."""
+    _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out)
+    P_, bs, Hkv, d = k_cache.shape
+    for nm, t in (("k_new", k_new), ("v_new", v_new)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != k_cache.dtype:
+            raise ValueError(f"{nm} must be a contiguous CUDA tensor of the cache dtype")
+        if tuple(t.shape) != (q.shape[0], Hkv, d):
+            raise ValueError(f"{nm} must be [B, Hkv, d]")
+    shape = shape_of(q, k_cache, block_table)
+    V = ctypes.c_void_p
+    opt = pa_options.from_buffer_copy(opts) if opts else None
+    args = (ctypes.byref(shape), ctypes.byref(opt) if opt else None, V(_ptr(q)), V(_ptr(k_new)),
+            V(_ptr(v_new)), V(_ptr(k_cache)), V(_ptr(v_cache)), V(_ptr(block_table)),
+            V(_ptr(cache_seqlens)), ctypes.c_float(scale), V(_ptr(out)), V(_ptr(workspace)),
+            ctypes.c_size_t(workspace.numel() * workspace.element_size()), V(_stream(stream)))
+    keep = (shape, opt, q, k_new, v_new, k_cache, v_cache, block_table, cache_seqlens, out,
+            workspace)
+    return _BoundDeviceCall(lib().pa_decode_append, "pa_decode_append", args, keep)
 
 
 def pa_decode_split(q, k_cache, v_cache, block_table, cache_seqlens, scale, out, workspace,

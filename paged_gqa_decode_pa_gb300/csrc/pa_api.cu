@@ -189,7 +189,12 @@ __device__ __forceinline__ bool find_segment(const MergeArgs& a, int k, int& seg
 // Staging of a host-buffer call's inputs by the SMs (see StageArgs): each
 // thread moves 16-byte chunks, four in flight, then the parts' 4-byte tails.
 // Dependents (the split kernel) may be scheduled at once; they wait for this
-// grid before reading what it writes.
+// grid before reading what it writes.  Launched as a programmatic dependent
+// of the kernel before it (the asynchronous host-buffer calls), the grid
+// fills its staging slot -- which no kernel still running reads: the calls
+// alternate between two slots -- while that kernel finishes, and waits for
+// it only at the end, so its own dependents still see everything before it
+// complete.  Launched plainly, the wait returns at once.
 constexpr int kStageThreads = 256;
 __global__ void __launch_bounds__(kStageThreads) pa_stage_in_kernel(const StageArgs s) {
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -213,6 +218,7 @@ __global__ void __launch_bounds__(kStageThreads) pa_stage_in_kernel(const StageA
     for (; i < n16; i += nth) dst[i] = src[i];
     for (int64_t k = 4 * n16 + tid; k < s.words[p]; k += nth) s.dst[p][k] = s.src[p][k];
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int D>
@@ -843,7 +849,9 @@ struct HostLayout {
   size_t table_bytes, lens_bytes, cu_bytes, out_bytes, q_bytes;
 };
 
-HostLayout host_layout(const Plan& p, const pa_shape* s, int64_t rows, bool multi) {
+// slot: which of the asynchronous calls' two staging areas (0 for the
+// synchronous calls, which have one); `total` covers the slots 0..slot.
+HostLayout host_layout(const Plan& p, const pa_shape* s, int64_t rows, bool multi, int slot = 0) {
   HostLayout h;
   const size_t B = (size_t)s->batch, row = (size_t)s->num_heads * s->head_dim;
   h.table_bytes = sizeof(int32_t) * B * (size_t)s->max_blocks_per_seq;
@@ -851,7 +859,10 @@ HostLayout host_layout(const Plan& p, const pa_shape* s, int64_t rows, bool mult
   h.cu_bytes = multi ? sizeof(int32_t) * (B + 1) : 0;
   h.out_bytes = sizeof(float) * (size_t)rows * row;
   h.q_bytes = 2 * (size_t)rows * row;
-  size_t off = round256(p.total);
+  // one slot's bytes, laid out as below
+  size_t one = round256(h.table_bytes) + round256(h.lens_bytes) + round256(h.cu_bytes) +
+               round256(2 * sizeof(uint32_t)) + round256(h.out_bytes) + round256(h.q_bytes);
+  size_t off = round256(p.total) + (size_t)slot * one;
   h.table = off;
   off = round256(off + h.table_bytes);
   h.lens = off;
@@ -913,7 +924,7 @@ float* host_out_target(const HostLayout& h, uint8_t* ws, float* out_host) {
 // target host_out_target chose.
 int run_host_step(const pa_shape* s, const pa_options* o, const HostLayout& h, uint8_t* ws,
                   const HostBuffers& hb, const void* k_cache, const void* v_cache, Call* c,
-                  cudaStream_t st) {
+                  cudaStream_t st, bool async = false) {
   StageArgs sa = {};
   auto part = [&](const void* host, size_t off, size_t bytes) {
     if (bytes == 0) return PA_OK;
@@ -948,8 +959,23 @@ int run_host_step(const pa_shape* s, const pa_options* o, const HostLayout& h, u
   for (int i = 0; i < sa.n; ++i) vec += sa.words[i] / 4;
   const int64_t want = (vec + kStageThreads * 4 - 1) / (kStageThreads * 4);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, 2 * (int64_t)c->plan.grid));
-  pa_stage_in_kernel<<<grid, kStageThreads, 0, st>>>(sa);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (async) {
+    // a programmatic dependent of the previous step's merge: fills this
+    // call's slot while that kernel finishes (pa_stage_in_kernel)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kStageThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, pa_stage_in_kernel, sa) != cudaSuccess) return PA_ERR_CUDA;
+  } else {
+    pa_stage_in_kernel<<<grid, kStageThreads, 0, st>>>(sa);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  }
   rc = run_phases(s, o, k_cache, v_cache, c, st);
   if (rc) return rc;
   const cudaMemcpyKind back = cudaMemcpyDefault;
@@ -959,6 +985,7 @@ int run_host_step(const pa_shape* s, const pa_options* o, const HostLayout& h, u
   if (hb.status && !published &&
       cudaMemcpyAsync(hb.status, slot + 1, sizeof(uint32_t), back, st) != cudaSuccess)
     return PA_ERR_CUDA;
+  if (async) return PA_OK;
   return cudaStreamSynchronize(st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -1075,14 +1102,30 @@ int pa_workspace_size_host(const pa_shape* shape, const pa_options* options, siz
   return PA_OK;
 }
 
-int pa_decode_host(const pa_shape* shape, const pa_options* options, const void* q_host,
-                   const void* k_cache, const void* v_cache, const int32_t* block_table_host,
-                   const int32_t* cache_seqlens_host, float scale, float* out_host,
-                   uint32_t* status_host, void* workspace, size_t workspace_bytes,
-                   pa_stream_t stream) {
+int pa_workspace_size_host_async(const pa_shape* shape, const pa_options* options,
+                                 size_t* bytes) {
+  if (!shape || !bytes) return PA_ERR_NULL;
+  Plan p;
+  int rc = make_plan(shape, options, false, &p);
+  if (rc) return rc;
+  *bytes = host_layout(p, shape, shape->batch, false, 1).total;
+  return PA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// pa_decode_host and pa_decode_host_async: slot < 0 waits for the stream.
+int decode_host(const pa_shape* shape, const pa_options* options, const void* q_host,
+                const void* k_cache, const void* v_cache, const int32_t* block_table_host,
+                const int32_t* cache_seqlens_host, float scale, float* out_host,
+                uint32_t* status_host, int slot, void* workspace, size_t workspace_bytes,
+                pa_stream_t stream) {
   int rc = check_shape(shape);
   if (rc) return rc;
   if (options && options->phase != PA_PHASE_BOTH) return PA_ERR_OPTION;
+  if (slot > 1) return PA_ERR_OPTION;
   if (shape->batch == 0) {  // a no-op, as for pa_decode
     if (status_host) *status_host = 0;
     return PA_OK;
@@ -1092,7 +1135,7 @@ int pa_decode_host(const pa_shape* shape, const pa_options* options, const void*
   Plan p;
   rc = make_plan(shape, options, false, &p);
   if (rc) return rc;
-  const HostLayout h = host_layout(p, shape, shape->batch, false);
+  const HostLayout h = host_layout(p, shape, shape->batch, false, slot < 0 ? 0 : slot);
   if (workspace_bytes < h.total) return PA_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   Call c;
@@ -1104,30 +1147,20 @@ int pa_decode_host(const pa_shape* shape, const pa_options* options, const void*
   const HostBuffers hb{q_host, nullptr, block_table_host, cache_seqlens_host, out_host,
                        status_host};
   return run_host_step(shape, options, h, ws, hb, k_cache, v_cache, &c,
-                       reinterpret_cast<cudaStream_t>(stream));
+                       reinterpret_cast<cudaStream_t>(stream), slot >= 0);
 }
 
-int pa_workspace_size_multi_host(const pa_shape* shape, const pa_options* options, int32_t max_q,
-                                 int32_t max_total_q, size_t* bytes) {
-  if (!shape || !bytes) return PA_ERR_NULL;
-  if (max_q < 1 || max_total_q < 0) return PA_ERR_SHAPE;
-  Plan p;
-  int rc = make_plan(shape, options, false, &p, max_q);
-  if (rc) return rc;
-  *bytes = host_layout(p, shape, max_total_q, true).total;
-  return PA_OK;
-}
-
-int pa_decode_multi_host(const pa_shape* shape, const pa_options* options, const void* q_host,
-                         const int32_t* cu_seqlens_q_host, int32_t total_q, int32_t max_q,
-                         int32_t causal, const void* k_cache, const void* v_cache,
-                         const int32_t* block_table_host, const int32_t* cache_seqlens_host,
-                         float scale, float* out_host, uint32_t* status_host, void* workspace,
-                         size_t workspace_bytes, pa_stream_t stream) {
+int decode_multi_host(const pa_shape* shape, const pa_options* options, const void* q_host,
+                      const int32_t* cu_seqlens_q_host, int32_t total_q, int32_t max_q,
+                      int32_t causal, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table_host, const int32_t* cache_seqlens_host,
+                      float scale, float* out_host, uint32_t* status_host, int slot,
+                      void* workspace, size_t workspace_bytes, pa_stream_t stream) {
   if (max_q < 1 || total_q < 0) return PA_ERR_SHAPE;
   int rc = check_shape(shape);
   if (rc) return rc;
   if (options && options->phase != PA_PHASE_BOTH) return PA_ERR_OPTION;
+  if (slot > 1) return PA_ERR_OPTION;
   if (shape->batch == 0 || total_q == 0) {  // nothing to attend
     if (status_host) *status_host = 0;
     return PA_OK;
@@ -1138,7 +1171,7 @@ int pa_decode_multi_host(const pa_shape* shape, const pa_options* options, const
   Plan p;
   rc = make_plan(shape, options, false, &p, max_q);
   if (rc) return rc;
-  const HostLayout h = host_layout(p, shape, total_q, true);
+  const HostLayout h = host_layout(p, shape, total_q, true, slot < 0 ? 0 : slot);
   if (workspace_bytes < h.total) return PA_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   Call c;
@@ -1156,7 +1189,79 @@ int pa_decode_multi_host(const pa_shape* shape, const pa_options* options, const
   const HostBuffers hb{q_host, cu_seqlens_q_host, block_table_host, cache_seqlens_host, out_host,
                        status_host};
   return run_host_step(shape, options, h, ws, hb, k_cache, v_cache, &c,
-                       reinterpret_cast<cudaStream_t>(stream));
+                       reinterpret_cast<cudaStream_t>(stream), slot >= 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode_host(const pa_shape* shape, const pa_options* options, const void* q_host,
+                   const void* k_cache, const void* v_cache, const int32_t* block_table_host,
+                   const int32_t* cache_seqlens_host, float scale, float* out_host,
+                   uint32_t* status_host, void* workspace, size_t workspace_bytes,
+                   pa_stream_t stream) {
+  return decode_host(shape, options, q_host, k_cache, v_cache, block_table_host,
+                     cache_seqlens_host, scale, out_host, status_host, -1, workspace,
+                     workspace_bytes, stream);
+}
+
+int pa_decode_host_async(const pa_shape* shape, const pa_options* options, const void* q_host,
+                         const void* k_cache, const void* v_cache,
+                         const int32_t* block_table_host, const int32_t* cache_seqlens_host,
+                         float scale, float* out_host, uint32_t* status_host, int32_t slot,
+                         void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  if (slot < 0) return PA_ERR_OPTION;
+  return decode_host(shape, options, q_host, k_cache, v_cache, block_table_host,
+                     cache_seqlens_host, scale, out_host, status_host, slot, workspace,
+                     workspace_bytes, stream);
+}
+
+int pa_workspace_size_multi_host(const pa_shape* shape, const pa_options* options, int32_t max_q,
+                                 int32_t max_total_q, size_t* bytes) {
+  if (!shape || !bytes) return PA_ERR_NULL;
+  if (max_q < 1 || max_total_q < 0) return PA_ERR_SHAPE;
+  Plan p;
+  int rc = make_plan(shape, options, false, &p, max_q);
+  if (rc) return rc;
+  *bytes = host_layout(p, shape, max_total_q, true).total;
+  return PA_OK;
+}
+
+int pa_workspace_size_multi_host_async(const pa_shape* shape, const pa_options* options,
+                                       int32_t max_q, int32_t max_total_q, size_t* bytes) {
+  if (!shape || !bytes) return PA_ERR_NULL;
+  if (max_q < 1 || max_total_q < 0) return PA_ERR_SHAPE;
+  Plan p;
+  int rc = make_plan(shape, options, false, &p, max_q);
+  if (rc) return rc;
+  *bytes = host_layout(p, shape, max_total_q, true, 1).total;
+  return PA_OK;
+}
+
+int pa_decode_multi_host(const pa_shape* shape, const pa_options* options, const void* q_host,
+                         const int32_t* cu_seqlens_q_host, int32_t total_q, int32_t max_q,
+                         int32_t causal, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table_host, const int32_t* cache_seqlens_host,
+                         float scale, float* out_host, uint32_t* status_host, void* workspace,
+                         size_t workspace_bytes, pa_stream_t stream) {
+  return decode_multi_host(shape, options, q_host, cu_seqlens_q_host, total_q, max_q, causal,
+                           k_cache, v_cache, block_table_host, cache_seqlens_host, scale,
+                           out_host, status_host, -1, workspace, workspace_bytes, stream);
+}
+
+int pa_decode_multi_host_async(const pa_shape* shape, const pa_options* options,
+                               const void* q_host, const int32_t* cu_seqlens_q_host,
+                               int32_t total_q, int32_t max_q, int32_t causal,
+                               const void* k_cache, const void* v_cache,
+                               const int32_t* block_table_host,
+                               const int32_t* cache_seqlens_host, float scale, float* out_host,
+                               uint32_t* status_host, int32_t slot, void* workspace,
+                               size_t workspace_bytes, pa_stream_t stream) {
+  if (slot < 0) return PA_ERR_OPTION;
+  return decode_multi_host(shape, options, q_host, cu_seqlens_q_host, total_q, max_q, causal,
+                           k_cache, v_cache, block_table_host, cache_seqlens_host, scale,
+                           out_host, status_host, slot, workspace, workspace_bytes, stream);
 }
 
 int pa_cache_append(const pa_shape* shape, const void* k_new, const void* v_new, void* k_cache,

@@ -100,7 +100,9 @@ def test_bench_line_on_the_gpu(extra):
     assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"], abs=1e-4)  # rounded to 4 places
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
-    assert e["value"] < d["value"]  # the copies cost time
+    # the synchronous host-buffer step costs more than the device step; the
+    # pipelined one adds its staging kernel to every step
+    assert e["sync_value"] < d["value"] and e["value"] <= 1.05 * d["value"]
     assert d["gpu_launches"] >= 2 * d["steps"]
     assert d["clocks"]["sm_max_mhz"] > 0
     assert d["parity_vs_oracle"]["max_abs_err"] <= 2e-3

@@ -259,3 +259,159 @@ def test_decode_host_accepts_device_buffers():
                                      pg._binding._stream(None))
         assert rc == pg.PA_OK and stw.value == 0
         assert np.array_equal(out.cpu().numpy().astype(np.float64), ref), mix
+
+
+# ------------------------------------------------------- asynchronous calls
+
+
+def test_async_host_calls_reject_bad_slots_before_any_cuda_call():
+    L = pg.lib()
+    s = pg.pa_shape(3, 4, 2, 64, 32, 4, 8, pg.PA_F16)
+    o = pg.options(num_ctas=8)
+    F = 1 << 20
+    for slot in (-1, 2):
+        assert L.pa_decode_host_async(ctypes.byref(s), ctypes.byref(o), F, F, F, F, F, 0.1, F,
+                                      None, slot, F, 1 << 30, None) == pg.PA_ERR_OPTION
+        assert L.pa_decode_multi_host_async(ctypes.byref(s), ctypes.byref(o), F, F, 6, 2, 1, F,
+                                            F, F, F, 0.1, F, None, slot, F, 1 << 30,
+                                            None) == pg.PA_ERR_OPTION
+    # room for two staging slots
+    one = pg.pa_workspace_size_host(s, o)
+    two = pg.pa_workspace_size_host_async(s, o)
+    plain = pg.pa_workspace_size(s, o)
+    assert two - one >= one - plain > 0
+    assert L.pa_decode_host_async(ctypes.byref(s), ctypes.byref(o), F, F, F, F, F, 0.1, F, None,
+                                  1, F, one, None) == pg.PA_ERR_WORKSPACE
+    m1 = pg.pa_workspace_size_multi_host(s, 2, 6, o)
+    m2 = pg.pa_workspace_size_multi_host_async(s, 2, 6, o)
+    assert m2 - m1 >= m1 - pg.pa_workspace_size_multi(s, 2, o) > 0
+
+
+def _step_inputs(w, i, pinned=True):
+    """Step i's host inputs over one cache: new queries, the tables and
+    lengths rotated among the sequences, one sequence shortened."""
+    import torch
+
+    q, k, v, t, sl = w.torch_tensors("cpu")
+    perm = np.roll(np.arange(w.B), i)
+    q = torch.randn(q.shape, generator=torch.Generator().manual_seed(1000 + i)).to(q.dtype)
+    t, sl = t[perm].clone(), sl[perm].clone()
+    sl[i % w.B] = max(0, int(sl[i % w.B]) - 7 * i)
+    if pinned:
+        q, t, sl = q.pin_memory(), t.pin_memory(), sl.pin_memory()
+    return q, t, sl
+
+
+ASYNC = [
+    # lens, H, Hkv, d, bs, dtype, opts
+    ([1, 15, 16, 17, 100, 0, 255, 1024, 129, 3000], 16, 4, 128, 16, "bf16", dict()),
+    ([300, 2, 1500, 40], 24, 4, 256, 16, "bf16", dict(partition_tokens=256)),
+    ([5, 31, 32, 33, 700], 14, 2, 64, 16, "f16", dict(num_ctas=7)),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", range(len(ASYNC)))
+def test_async_steps_alternating_slots_match_the_device_call(case):
+    """Six steps issued back to back without waiting, slots 0, 1, 0, ...,
+    each with its own host buffers and inputs; after one synchronisation
+    every step's output equals pa_decode's on the same inputs, bit for bit."""
+    import torch
+
+    lens, H, Hkv, d, bs, dtype, kw = ASYNC[case]
+    w = wl.random_workload(lens, H=H, Hkv=Hkv, d=d, bs=bs, dtype=dtype, seed=300 + case,
+                           poison=True, outlier_frac=0.02)
+    o = pg.options(**kw)
+    _, k, v, _, _ = host_inputs(w, True)
+    steps = [_step_inputs(w, i) for i in range(6)]
+    shape = pg.shape_of(steps[0][0], k, steps[0][1])
+    ws = pg.alloc_workspace_host_async(shape, o)
+    outs = [empty_out((w.B, w.H, w.d), True) for _ in steps]
+    calls = [pg.bind_decode_host_async(q, k, v, t, sl, w.scale, out, ws, i % 2, o)
+             for i, ((q, t, sl), out) in enumerate(zip(steps, outs))]
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    wsd = pg.alloc_workspace(shape, o)
+    for i, ((q, t, sl), out, c) in enumerate(zip(steps, outs, calls)):
+        assert c.status() == 0, i
+        ref = torch.full((w.B, w.H, w.d), float("nan"), dtype=torch.float32, device="cuda")
+        pg.pa_decode(q.cuda(), k, v, t.cuda(), sl.cuda(), w.scale, ref, wsd, o)
+        assert pg.pa_read_status(wsd) == 0
+        assert torch.equal(out, ref.cpu()), f"step {i}"
+
+
+@pytest.mark.gpu
+def test_async_loop_reusing_two_buffer_sets():
+    """A serving loop's shape: two buffer sets, one per slot; each step
+    rewrites its set only after the step that last used it has finished
+    (one synchronisation per step, a step behind).  Status bits land in the
+    step's own word."""
+    import torch
+
+    w = wl.random_workload([40, 300, 60, 1000, 7], H=16, Hkv=4, d=128, bs=32, dtype="bf16",
+                           seed=320)
+    _, k, v, _, _ = host_inputs(w, True)
+    sets = [_step_inputs(w, 0), _step_inputs(w, 1)]
+    outs = [empty_out((w.B, w.H, w.d), True) for _ in range(2)]
+    shape = pg.shape_of(sets[0][0], k, sets[0][1])
+    ws = pg.alloc_workspace_host_async(shape)
+    calls = [pg.bind_decode_host_async(q, k, v, t, sl, w.scale, outs[s], ws, s)
+             for s, (q, t, sl) in enumerate(sets)]
+    wsd = pg.alloc_workspace(shape)
+    done = torch.cuda.Event()
+    for i in range(8):
+        s = i % 2
+        q, t, sl = sets[s]
+        nq, nt, nsl = _step_inputs(w, i)
+        if i == 5:
+            nt[2, 0] = -1  # a bad table entry in one step
+        q.copy_(nq), t.copy_(nt), sl.copy_(nsl)
+        calls[s]()
+        if i > 0:
+            done.synchronize()  # the previous step: check it while this one runs
+            check_step(i - 1, prev, calls[1 - s], outs[1 - s], k, v, w, wsd)
+        done.record()
+        prev = (nq.clone(), nt.clone(), nsl.clone())
+    done.synchronize()
+    check_step(7, prev, calls[1], outs[1], k, v, w, wsd)
+
+
+def check_step(i, inputs, call, out, k, v, w, wsd):
+    import torch
+
+    q, t, sl = inputs
+    st = call.status()
+    if i == 5:
+        assert st & pg.PA_STATUS_BAD_BLOCK and torch.isnan(out[2]).all()
+        return
+    assert st == 0, i
+    ref = torch.full((w.B, w.H, w.d), float("nan"), dtype=torch.float32, device="cuda")
+    pg.pa_decode(q.cuda(), k, v, t.cuda(), sl.cuda(), w.scale, ref, wsd)
+    assert pg.pa_read_status(wsd) == 0
+    assert torch.equal(out, ref.cpu()), f"step {i}"
+
+
+@pytest.mark.gpu
+def test_async_multi_steps_match_the_synchronous_call():
+    import torch
+
+    w = wl.random_workload([300, 17, 1, 64, 513], H=16, Hkv=4, d=128, bs=16, dtype="bf16",
+                           seed=330, poison=True)
+    w = wl.with_query_tokens(w, [4, 3, 1, 4, 2], seed=331)
+    q, k, v, t, sl = host_inputs(w, True)
+    cu = torch.from_numpy(w.cu_q).pin_memory()
+    shape = pg.shape_multi(q, k, t)
+    ref = empty_out((q.shape[0], w.H, w.d), True)
+    ws1 = pg.alloc_workspace_multi_host(shape, w.max_q, q.shape[0])
+    assert pg.pa_decode_multi_host(q, cu, w.max_q, w.causal, k, v, t, sl, w.scale, ref, ws1) == 0
+    ws = pg.alloc_workspace_multi_host_async(shape, w.max_q, q.shape[0])
+    outs = [empty_out((q.shape[0], w.H, w.d), True) for _ in range(4)]
+    calls = [pg.bind_decode_multi_host_async(q, cu, w.max_q, w.causal, k, v, t, sl, w.scale,
+                                             outs[i], ws, i % 2) for i in range(4)]
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    for c, out in zip(calls, outs):
+        assert c.status() == 0
+        assert torch.equal(out, ref)
