@@ -29,8 +29,8 @@ namespace {
 // (find_segment); with the fixed split, block (seg, g) takes column g of
 // segment seg.  The fold uses the combine op ("Paged Attention Kernel
 // Architecture for BI-V100", section 2, Level 1 binary op / Level 3): warp w
-// folds pieces w, w+4, ... in order, each lane holding D/32 of the dims; the
-// four warp states are then folded in a fixed order, so the result is
+// of NW folds pieces w, w+NW, ... in order, each lane holding D/32 of the
+// dims; the NW warp states are then folded in a fixed order, so the result is
 // deterministic.  The loads of up to kMergeBatch pieces are issued before
 // any of them is folded, so a segment of many pieces costs few round trips.
 constexpr int kMergeBatch = 16;
@@ -63,10 +63,9 @@ __device__ __forceinline__ Vec<V> load_vec(const float* p) {
   return r;
 }
 
-template <int D>
+template <int D, int NW>
 __device__ __forceinline__ void merge_column(const MergeArgs& a, const MergeSeg& ms, int g,
                                              int64_t out_row) {
-  constexpr int NW = kMergeThreads / 32;
   constexpr int V = D / 32;  // dims per lane
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   __shared__ float wm[NW], wl[NW];
@@ -113,7 +112,7 @@ __device__ __forceinline__ void merge_column(const MergeArgs& a, const MergeSeg&
 #pragma unroll
   for (int i = 0; i < V; ++i) wacc[w][lane * V + i] = acc[i];
   __syncthreads();
-  // warp 0 folds the four warp states in order and writes the column
+  // warp 0 folds the NW warp states in order and writes the column
   if (w == 0) {
     float M = -INFINITY;
 #pragma unroll
@@ -141,8 +140,9 @@ __device__ __forceinline__ void merge_column(const MergeArgs& a, const MergeSeg&
 // CTA takes the k-th of them in CTA order, k = blockIdx.x / C, so the CTAs
 // that have work are the first ones of the grid and start in its first wave.
 // Returns false when fewer than k + 1 segments have pieces to merge.
+template <int NW>
 __device__ __forceinline__ bool find_segment(const MergeArgs& a, int k, int& seg, int4& desc) {
-  constexpr int NW = kMergeThreads / 32;
+  constexpr int kThreads = NW * 32;
   constexpr int kPre = 4;  // descriptor chunks loaded before the scan
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   __shared__ int wcount[NW];
@@ -152,12 +152,12 @@ __device__ __forceinline__ bool find_segment(const MergeArgs& a, int k, int& seg
   int4 pre[kPre];
 #pragma unroll
   for (int i = 0; i < kPre; ++i) {
-    const int c = i * kMergeThreads + tid;
+    const int c = i * kThreads + tid;
     pre[i] = c < a.num_ctas ? a.ws_desc[c] : make_int4(-1, 0, 0, 0);
   }
   int base = 0;  // segments found in the chunks before
-  for (int i = 0; i * kMergeThreads < a.num_ctas; ++i) {
-    const int c = i * kMergeThreads + tid;
+  for (int i = 0; i * kThreads < a.num_ctas; ++i) {
+    const int c = i * kThreads + tid;
     int4 d = make_int4(-1, 0, 0, 0);
 #pragma unroll
     for (int u = 0; u < kPre; ++u)
@@ -221,8 +221,10 @@ __global__ void __launch_bounds__(kStageThreads) pa_stage_in_kernel(const StageA
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <int D>
-__global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs a) {
+// NW warps per CTA: 4, or 8 where a segment may have many pieces (one
+// round of loads covers kMergeBatch pieces per warp).
+template <int D, int NW>
+__global__ void __launch_bounds__(NW * 32) pa_merge_kernel(const MergeArgs a) {
   // The next kernel on the stream (the next step's split kernel) may be
   // scheduled now: it waits for this grid to finish before touching memory.
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs
   int4 desc = make_int4(-1, 0, 0, 0);
   if (a.part_blocks == 0) {
     g = blockIdx.x % a.C;
-    if (!find_segment(a, blockIdx.x / a.C, seg, desc)) return;
+    if (!find_segment<NW>(a, blockIdx.x / a.C, seg, desc)) return;
   } else {
     seg = blockIdx.x;  // segment (b, j) = (seg / Hkv, seg % Hkv)
     g = blockIdx.y;
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(kMergeThreads) pa_merge_kernel(const MergeArgs
     if (tok >= nq) return;  // the column holds no query (uniform over the block)
     out_row = (int64_t)(q0 + tok) * a.H + (int64_t)ms.j * a.G + g % a.G;
   }
-  merge_column<D>(a, ms, g, out_row);
+  merge_column<D, NW>(a, ms, g, out_row);
 }
 
 // --------------------------------------------------------------- append
@@ -810,9 +812,16 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   // segments continue past a split CTA, so there are fewer than the split
   // CTAs and at most one per row.  Fixed split: one per (row, column).
   const int rows = c->sa.B * c->sa.Hkv;
+  // the most pieces a segment can have: its partitions (fixed split), or
+  // about the split CTAs per (row, kv head) (balanced split)
+  const int64_t pieces =
+      p.part_blocks > 0
+          ? ((int64_t)c->sa.maxblk + p.part_blocks - 1) / p.part_blocks
+          : (int64_t)p.grid / std::max(1, rows) + 2;
+  const bool wide = pieces > 4 * kMergeBatch;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = p.part_blocks == 0 ? dim3(std::min(p.grid, rows) * p.C, 1, 1) : dim3(rows, p.C, 1);
-  cfg.blockDim = dim3(kMergeThreads);
+  cfg.blockDim = dim3(wide ? 2 * kMergeThreads : kMergeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -821,9 +830,13 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
   cudaError_t e = cudaErrorInvalidValue;
-  if (p.D == 64) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<64>, c->ma);
-  if (p.D == 128) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<128>, c->ma);
-  if (p.D == 256) e = cudaLaunchKernelEx(&cfg, pa_merge_kernel<256>, c->ma);
+  constexpr int NW = kMergeThreads / 32;
+  if (p.D == 64) e = wide ? cudaLaunchKernelEx(&cfg, pa_merge_kernel<64, 2 * NW>, c->ma)
+                          : cudaLaunchKernelEx(&cfg, pa_merge_kernel<64, NW>, c->ma);
+  if (p.D == 128) e = wide ? cudaLaunchKernelEx(&cfg, pa_merge_kernel<128, 2 * NW>, c->ma)
+                           : cudaLaunchKernelEx(&cfg, pa_merge_kernel<128, NW>, c->ma);
+  if (p.D == 256) e = wide ? cudaLaunchKernelEx(&cfg, pa_merge_kernel<256, 2 * NW>, c->ma)
+                           : cudaLaunchKernelEx(&cfg, pa_merge_kernel<256, NW>, c->ma);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

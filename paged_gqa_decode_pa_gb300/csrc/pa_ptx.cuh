@@ -241,6 +241,12 @@ __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
 // 16-byte asynchronous copy global -> shared (L2 only), completed by
 // cp_async_wait_all; src_bytes == 0 fills the 16 bytes with zeros and reads
 // nothing.
+// Bring the line holding p into this SM's L1 (a hint: no register result,
+// nothing waits for it).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");

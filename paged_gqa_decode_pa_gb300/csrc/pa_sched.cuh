@@ -175,6 +175,25 @@ struct PieceIterT {
     }
   }
 
+  // The row and first block of the piece next() would return, without
+  // advancing (false when there is none).  Only reads the iterator.
+  PA_HD bool peek_start(int32_t& b, int32_t& blk0) const {
+    if (s.part_blocks == 0) {
+      if (u >= u_end) return false;
+      b = find_seq(pre, s.B, s.Hkv, u);
+      const int32_t n = pre[b + 1] - pre[b];
+      const int32_t r = (int32_t)(u - (int64_t)s.Hkv * pre[b]);
+      const int32_t off = r - (r / n) * n;
+      blk0 = off < s.K ? 0 : off - s.K;
+      return true;
+    }
+    if (item >= items) return false;
+    b = find_seq(pre, s.B, s.Hkv, item);
+    const int64_t r = item - (int64_t)s.Hkv * pre[b];
+    blk0 = (int32_t)(r / s.Hkv) * s.part_blocks;
+    return true;
+  }
+
   // Next piece; false when the CTA has no more work.
   PA_HD bool next(Piece& p) {
     if (s.part_blocks == 0) {

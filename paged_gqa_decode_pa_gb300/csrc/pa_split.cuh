@@ -596,6 +596,16 @@ __device__ __forceinline__ void issue_next(IssuerT<LenOf>& is, const SplitArgs& 
     is.seq = pa.nqg > 1 ? is.pc.b / pa.nqg : is.pc.b;
     is.entry = table_entry(pa, is.pc, is.seq, is.cnt, lane, sl, s, S);
     is.entry_next = table_entry(pa, is.pc, is.seq, is.cnt, 32 + lane, sl, s, S);
+    // the piece after this one: its length and first window of table
+    // entries are brought into L1 now, so that the next move finds them
+    // there instead of waiting an L2 round trip behind the K/V stream
+    int32_t nb, nblk0;
+    if (is.it.peek_start(nb, nblk0)) {
+      const int32_t nseq = pa.nqg > 1 ? nb / pa.nqg : nb;
+      const int32_t blk = nblk0 + ((s + S * lane) >> sl);
+      if (blk < pa.maxblk) prefetch_l1(pa.table + (int64_t)nseq * pa.maxblk + blk);
+      if (lane == 0) prefetch_l1(pa.seqlens + nseq);
+    }
   }
   if (is.done) return;
   if (is.i >= is.win + 32) {
