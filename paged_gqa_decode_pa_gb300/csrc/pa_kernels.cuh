@@ -186,6 +186,7 @@ struct SmemLayout {
   uint32_t stage;                   // [streams][R] stages: K chunks | V chunks, 16 rows each
   uint32_t stage_bytes;
   uint32_t mo, mm, ml, mbad;        // per-warp partial states for the CTA combine
+  uint32_t cwt;                     // [kRowCols][kMaxWarps + 2] fp32 combine weights, max, sum
   uint32_t qs;                      // [C][D+4] fp32 q of the current piece (x scale*log2(e): CUDA cores)
   uint32_t qlim;                    // [kRowCols] int32 key limit per column (several tokens)
   uint32_t qraw;                    // [C][D] raw 16-bit q of the next piece (cp.async target)
@@ -226,6 +227,8 @@ PA_HD SmemLayout split_smem_layout(int D, int C, int B, int W, int R, int mode) 
   off += (uint32_t)W * kColMax * 4u;
   L.mbad = off;
   off += (uint32_t)W * 4u;
+  L.cwt = off;
+  off += (uint32_t)kRowCols * (kMaxWarps + 2) * 4u;
   L.abort_flag = off;  // followed by the current piece's stored length, q0, nq
   off += 16u;
   L.qlim = off;

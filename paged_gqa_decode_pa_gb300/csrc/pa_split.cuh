@@ -487,33 +487,44 @@ __device__ __forceinline__ int64_t column_out(const SplitArgs& a, int row, int j
 // kPair: warp pairs, warps [0, W/2) hold columns [0, cw) and warps
 // [W/2, W) columns [cw, C), each state with cw columns; otherwise every warp
 // holds all C columns.
+//
+// Two passes, one barrier between them: first one thread per column folds
+// the warps' maxima and sums into the column's weights (e_w = 2^(m_w - M),
+// divided by the column's sum when the piece's result is final); then every
+// thread takes 4 consecutive dims of one column at a time, weighs the warps'
+// accumulators with float4 shared loads and writes a float4.  The fold order
+// over the warps is fixed, so the result is deterministic.
 template <int D, int W, bool kQ, bool kPair>
 __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem, const SmemLayout& L,
                                               const Piece& pc, int q0, int nq, int cw) {
   const int C = a.C;
   const int stride = kPair ? cw : C;  // columns of one published warp state
+  constexpr int NW = kPair ? W / 2 : W;  // warps holding a column
+  constexpr int WS = kMaxWarps + 2;      // floats per column in the weight table
   const float* mm = reinterpret_cast<const float*>(smem + L.mm);
   const float* ml = reinterpret_cast<const float*>(smem + L.ml);
   const float* mo = reinterpret_cast<const float*>(smem + L.mo);
   const int* mbad = reinterpret_cast<const int*>(smem + L.mbad);
+  float* cwt = reinterpret_cast<float*>(smem + L.cwt);
   bool bad = false;
 #pragma unroll
   for (int w = 0; w < W; ++w) bad |= (mbad[w] != 0);
   const float qnan = __int_as_float(0x7fc00000);
-  // Each thread folds its element from the W warp states directly: the
-  // column's maxima and sums are read by every lane of the warp (the 32
-  // elements a warp takes share their column, D being a multiple of 32, so
-  // these are broadcast loads), with no shuffles on the way.
-  for (int idx = threadIdx.x; idx < C * D; idx += blockDim.x) {
-    const int c = idx / D, dim = idx % D;
-    // the warps holding column c, and its index in their states
-    constexpr int NW = kPair ? W / 2 : W;  // warps holding a column
-    int w0 = 0, lc = c;
+  const bool final_out = pc.slot < 0;
+  // the warps holding column c, and its index in their states
+  auto col_warps = [&](int c, int& w0, int& lc) {
+    w0 = 0;
+    lc = c;
     if constexpr (kPair) {
       const int cg = c >= cw ? 1 : 0;
       w0 = cg * NW;
       lc = c - cg * cw;
     }
+  };
+  if (threadIdx.x < C) {
+    const int c = threadIdx.x;
+    int w0, lc;
+    col_warps(c, w0, lc);
     float mw[NW];
     float M = -INFINITY;
 #pragma unroll
@@ -521,22 +532,43 @@ __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem,
       mw[w] = mm[(w0 + w) * kColMax + lc];
       M = fmaxf(M, mw[w]);
     }
-    float Lsum = 0.f, o = 0.f;
+    float e[NW];
+    float Lsum = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float e = (mw[w] == -INFINITY) ? 0.f : ex2(mw[w] - M);
-      Lsum = fmaf(e, ml[(w0 + w) * kColMax + lc], Lsum);
-      o = fmaf(e, mo[((w0 + w) * stride + lc) * (D + 4) + dim], o);
+      e[w] = (mw[w] == -INFINITY) ? 0.f : ex2(mw[w] - M);
+      Lsum = fmaf(e[w], ml[(w0 + w) * kColMax + lc], Lsum);
     }
-    if (pc.slot < 0) {
+    const float inv = final_out ? (Lsum == 0.f ? 0.f : 1.f / Lsum) : 1.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) cwt[c * WS + w] = e[w] * inv;
+    if (!final_out) {
+      a.ws_ml[((int64_t)pc.slot * C + c) * 2 + 0] = M;
+      a.ws_ml[((int64_t)pc.slot * C + c) * 2 + 1] = bad ? qnan : Lsum;
+    }
+  }
+  named_bar_sync(2, blockDim.x);
+  constexpr int DV = D / 4;  // float4s per column
+  for (int v = threadIdx.x; v < C * DV; v += blockDim.x) {
+    const int c = v / DV, d4 = (v - c * DV) * 4;
+    int w0, lc;
+    col_warps(c, w0, lc);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float ew = cwt[c * WS + w];
+      const float4 x = *reinterpret_cast<const float4*>(mo + ((w0 + w) * stride + lc) * (D + 4) + d4);
+      o.x = fmaf(ew, x.x, o.x);
+      o.y = fmaf(ew, x.y, o.y);
+      o.z = fmaf(ew, x.z, o.z);
+      o.w = fmaf(ew, x.w, o.w);
+    }
+    if (bad) o = make_float4(qnan, qnan, qnan, qnan);
+    if (final_out) {
       const int64_t r = column_out<kQ>(a, pc.b, pc.j, c, q0, nq);
-      if (r >= 0) a.out[r * D + dim] = bad ? qnan : (Lsum == 0.f ? 0.f : o / Lsum);
+      if (r >= 0) *reinterpret_cast<float4*>(a.out + r * D + d4) = o;
     } else {
-      a.ws_acc[((int64_t)pc.slot * C + c) * D + dim] = bad ? qnan : o;
-      if (dim == 0) {
-        a.ws_ml[((int64_t)pc.slot * C + c) * 2 + 0] = M;
-        a.ws_ml[((int64_t)pc.slot * C + c) * 2 + 1] = bad ? qnan : Lsum;
-      }
+      *reinterpret_cast<float4*>(a.ws_acc + ((int64_t)pc.slot * C + c) * D + d4) = o;
     }
   }
 }

@@ -101,8 +101,11 @@ def test_bench_line_on_the_gpu(extra):
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     # the synchronous host-buffer step costs more than the device step; the
-    # pipelined one adds its staging kernel to every step
-    assert e["sync_value"] < d["value"] and e["value"] <= 1.05 * d["value"]
+    # pipelined one adds its staging kernel to every step (with --fused-append
+    # the timed step also writes the new rows, which the host-buffer step
+    # does not, so there the two are not comparable)
+    if "--fused-append" not in extra:
+        assert e["sync_value"] < d["value"] and e["value"] <= 1.05 * d["value"]
     assert d["gpu_launches"] >= 2 * d["steps"]
     assert d["clocks"]["sm_max_mhz"] > 0
     assert d["parity_vs_oracle"]["max_abs_err"] <= 2e-3
