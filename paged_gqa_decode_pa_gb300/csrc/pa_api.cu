@@ -128,10 +128,22 @@ __device__ __forceinline__ void merge_column(const MergeArgs& a, const MergeSeg&
 #pragma unroll
       for (int i = 0; i < V; ++i) o[i] = fmaf(e, wacc[v][lane * V + i], o[i]);
     }
-    // a column that saw no key (causal limit 0) gets 0; NaN passes through
+    // a column that saw no key (causal limit 0) gets 0; NaN passes through.
+    // Each lane's V dims go out as 16- (or 8-) byte stores, so the warp
+    // writes whole lines: out may be page-locked host memory, where strided
+    // 4-byte stores become partial-line writes across the chip link.
     float* dst = a.out + out_row * D + lane * V;
+    float r[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) dst[i] = L == 0.f ? 0.f : o[i] / L;
+    for (int i = 0; i < V; ++i) r[i] = L == 0.f ? 0.f : o[i] / L;
+    if constexpr (V % 4 == 0) {
+#pragma unroll
+      for (int i = 0; i < V; i += 4)
+        *reinterpret_cast<float4*>(dst + i) = make_float4(r[i], r[i + 1], r[i + 2], r[i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < V; i += 2) *reinterpret_cast<float2*>(dst + i) = make_float2(r[i], r[i + 1]);
+    }
   }
 }
 
