@@ -660,7 +660,8 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.P = s->num_blocks;
   a.part_blocks = p.part_blocks;
   a.piece_k = p.part_blocks == 0
-                  ? piece_units(s->block_size, s->head_dim, p.multi ? kPieceKbMulti : kPieceKb)
+                  ? piece_units(s->block_size, s->head_dim,
+                                !p.multi ? kPieceKb : (p.mode == kMmaP ? kPieceKbPair : kPieceKbMulti))
                   : 0;
   a.warps = p.warps;
   a.ring = p.ring;

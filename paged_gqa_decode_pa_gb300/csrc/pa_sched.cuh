@@ -54,13 +54,17 @@ struct SchedShape {
 
 // Overhead units per segment of the balanced split: a piece's fixed cost in
 // units of one block of one kv head (4 bs D bytes of K and V).  Measured
-// best on GB300 at about 200 KB worth (sweeps of 0 to 320 KB on the serving
-// and prefix-sharing steps).  With several query tokens per sequence a
-// piece's fold and prefix cover up to 16 columns and cost more: measured best
-// at about 440 KB (sweeps of 200 to 1400 KB on steps of 2, 4 and 8 query
-// tokens per sequence; 400 to 480 within 1%).
+// best on GB300 at about 200 KB worth (sweeps of 60 to 320 KB on the serving
+// and prefix-sharing steps; long context does not move).  With several query
+// tokens per sequence a piece's fold and q cover up to 16 columns and cost
+// more: measured best at about 300 KB (sweeps of 120 to 600 KB on the 4-token
+// serving step and the 2-token prefix-sharing step).  Rows of warp pairs (up
+// to 32 columns) spend twice the compute on every block, so the same piece
+// cost is fewer blocks' worth: best at about 220 KB (sweep of 40 to 440 KB on
+// the 8-token serving step: 906 us against 990 at 440 KB).
 constexpr int32_t kPieceKb = 200;
-constexpr int32_t kPieceKbMulti = 440;
+constexpr int32_t kPieceKbMulti = 300;
+constexpr int32_t kPieceKbPair = 220;
 PA_HD int32_t piece_units(int32_t bs, int32_t D, int32_t kb = kPieceKb) {
   const int32_t unit = 4 * bs * D;
   const int32_t k = (kb * 1024 + unit / 2) / unit;
