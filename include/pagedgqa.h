@@ -178,9 +178,10 @@ int pa_workspace_size(const pa_shape* shape, const pa_options* options, size_t* 
 /* One decode step: out = paged GQA decode attention (formula at the top).
  * Launches the split kernel (phase 1: each persistent CTA streams its share
  * of (sequence, kv head, block) work through a multi-stage TMA pipeline and
- * computes all G query heads of the kv head at once) and, when some
- * sequence was split across CTAs, the merge kernel (phase 2: combine op over
- * that sequence's pieces).  Sequences with cache_seqlens[b] == 0 get out = 0.
+ * computes all G query heads of the kv head at once) and the merge kernel
+ * (phase 2: combine op over the pieces of every sequence that was split
+ * across CTAs) -- or, for a step with few segments, the one cluster kernel
+ * (see pa_launch_plan).  Sequences with cache_seqlens[b] == 0 get out = 0.
  * scale multiplies q . k (typically 1/sqrt(d)).  Table entries at or beyond
  * ceil(cache_seqlens[b] / bs) are never read.
  * Errors: PA_ERR_* before any launch; device-side data errors as status
@@ -190,15 +191,35 @@ int pa_decode(const pa_shape* shape, const pa_options* options, const void* q,
               const int32_t* cache_seqlens, float scale, float* out, void* workspace,
               size_t workspace_bytes, pa_stream_t stream);
 
+/* Which kernels a step with this shape and these options launches on the
+ * current device (max_q = 0: pa_decode; > 0: pa_decode_multi with at most
+ * max_q query tokens per sequence).  info[0] = kernels per step (1: the
+ * cluster kernel does the whole step -- a step with few (sequence, kv head)
+ * segments and at most 64 MB of K/V even with every table row full, one
+ * query token per sequence, the mma path with the balanced split and the
+ * library's grid: each segment gets one thread-block cluster whose CTAs
+ * fold their partial states through distributed shared memory, so no
+ * workspace round trip and no second kernel; 2: the persistent split
+ * kernel and the merge kernel), info[1] = CTAs of the step's first kernel,
+ * info[2] = CTAs per cluster (0 without clusters), info[3] = ring slots per
+ * warp.  Chosen from the shape and options only (a captured graph stays
+ * valid); pa_decode_split then runs the whole step and pa_decode_merge
+ * nothing.  The host-buffer calls make the same choice; pa_decode_append
+ * and pa_decode_multi always use the two kernels.  Returns PA_OK or PA_ERR_*. */
+int pa_launch_plan(const pa_shape* shape, const pa_options* options, int32_t max_q,
+                   int32_t* info);
+
 /* Phase 1 of pa_decode alone (same arguments).  Writes the outputs of every
- * sequence handled whole by one CTA and the partial states of the others. */
+ * sequence handled whole by one CTA and the partial states of the others
+ * (with the cluster kernel: the whole step). */
 int pa_decode_split(const pa_shape* shape, const pa_options* options, const void* q,
                     const void* k_cache, const void* v_cache, const int32_t* block_table,
                     const int32_t* cache_seqlens, float scale, float* out, void* workspace,
                     size_t workspace_bytes, pa_stream_t stream);
 
 /* Phase 2 of pa_decode alone (same arguments; q, k_cache and v_cache are not
- * read).  Must follow pa_decode_split of the same step on the same stream. */
+ * read).  Must follow pa_decode_split of the same step on the same stream.
+ * Launches nothing when the step runs on the cluster kernel. */
 int pa_decode_merge(const pa_shape* shape, const pa_options* options, const void* q,
                     const void* k_cache, const void* v_cache, const int32_t* block_table,
                     const int32_t* cache_seqlens, float scale, float* out, void* workspace,

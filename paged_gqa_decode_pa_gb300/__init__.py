@@ -9,7 +9,7 @@ from ._binding import (  # noqa: F401
     EXPORTS, LIB_PATH, LibraryNotBuilt, PagedGQAError, alloc_workspace, lib, options,
     pa_cache_append, pa_decode, pa_decode_append, pa_decode_merge, pa_decode_noalloc,
     pa_decode_split, pa_options,
-    pa_plan_merge, pa_plan_pieces, pa_read_status, pa_shape, pa_version, pa_workspace_size,
+    pa_plan_merge, pa_plan_pieces, pa_launch_plan, pa_read_status, pa_shape, pa_version, pa_workspace_size,
     shape_of, status_string,
     BlockManager, pa_bm_create, pa_bm_destroy, pa_bm_allocate, pa_bm_free_sequence,
     pa_bm_share_prefix, pa_bm_copy_on_write, pa_bm_reserve_slot, pa_bm_block_table, pa_bm_query,

@@ -60,7 +60,7 @@ EXPORTS = ("pa_workspace_size", "pa_decode", "pa_decode_split", "pa_decode_merge
            "pa_workspace_size_multi", "pa_decode_host", "pa_workspace_size_host",
            "pa_decode_multi_host", "pa_workspace_size_multi_host", "pa_decode_host_async",
            "pa_workspace_size_host_async", "pa_decode_multi_host_async",
-           "pa_workspace_size_multi_host_async")
+           "pa_workspace_size_multi_host_async", "pa_launch_plan")
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -186,6 +186,8 @@ def lib():
         L.pa_decode_multi_host_async.argtypes = [SP, OP, P, P, i32, i32, i32, P, P, P, P,
                                                  ctypes.c_float, P, P, i32, P, ctypes.c_size_t, P]
         L.pa_decode_multi_host_async.restype = ctypes.c_int
+        L.pa_launch_plan.argtypes = [SP, OP, i32, ctypes.POINTER(i32)]
+        L.pa_launch_plan.restype = ctypes.c_int
         L.pa_version.argtypes = []
         L.pa_version.restype = ctypes.c_int
         _lib = L
@@ -254,6 +256,18 @@ def _check_tensors(q, k_cache, v_cache, block_table, cache_seqlens, out):
         raise TypeError("block_table and cache_seqlens must be int32")
     if out is not None and (out.dtype != torch.float32 or tuple(out.shape) != tuple(q.shape)):
         raise TypeError("out must be float32 with q's shape")
+
+
+def pa_launch_plan(shape: pa_shape, opts: Optional[pa_options] = None, max_q: int = 0) -> dict:
+    """Which kernels a step launches on the current device (see
+    include/pagedgqa.h): kernels per step, CTAs of the first kernel, CTAs per
+    cluster (0 = none), ring slots per warp."""
+    info = (ctypes.c_int32 * 4)()
+    rc = lib().pa_launch_plan(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                              int(max_q), info)
+    _check(rc, "pa_launch_plan")
+    return {"kernels": int(info[0]), "ctas": int(info[1]), "cluster": int(info[2]),
+            "ring": int(info[3])}
 
 
 def pa_workspace_size(shape: pa_shape, opts: Optional[pa_options] = None) -> int:

@@ -304,6 +304,8 @@ __global__ void pa_append_kernel(const AppendArgs a) {
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kHeaderBytes = 256;
+// Workspace header: the status word at 0; the cluster kernel's CTA count.
+constexpr size_t kDoneOffset = 16;
 constexpr int kMaxDynamicSmem = 227 * 1024 - 64;  // minus the kernel's static shared memory
 
 struct DeviceInfo {
@@ -371,6 +373,11 @@ struct Plan {
   size_t smem;
   int64_t slots;
   size_t off_pre, off_desc, off_ml, off_acc, total;
+  // > 0: the step runs as one cluster kernel (pa_cluster.cuh) with clusters
+  // of `cluster` CTAs, rings of `cring` slots per warp and `csmem` bytes of
+  // shared memory; the merge phase is then empty
+  int cluster, cring;
+  size_t csmem;
 };
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
@@ -462,6 +469,97 @@ int device_sms(int* dev_out, int* sms_out) {
   return PA_OK;
 }
 
+// Clusters of the cluster kernel that can be resident at once, cached per
+// (device, dtype, head dimension, cluster size, shared memory).
+struct ClusterCap {
+  int dev, dtype, D, cs;
+  size_t smem;
+  int n;
+};
+constexpr int kClusterCapCache = 64;
+ClusterCap g_ccap[kClusterCapCache];
+int g_nccap = 0;
+
+int cluster_cap(int dev, int dtype, int D, int cs, size_t smem) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_nccap; ++i) {
+      const ClusterCap& e = g_ccap[i];
+      if (e.dev == dev && e.dtype == dtype && e.D == D && e.cs == cs && e.smem == smem) return e.n;
+    }
+  }
+  int n = 0;
+#define PA_CAP(T, DD) \
+  if (D == DD) n = cluster_capacity<T, DD>(cs, smem, kMaxDynamicSmem);
+  if (dtype == PA_BF16) {
+    PA_CAP(__nv_bfloat16, 64)
+    PA_CAP(__nv_bfloat16, 128)
+    PA_CAP(__nv_bfloat16, 256)
+  } else {
+    PA_CAP(__half, 64)
+    PA_CAP(__half, 128)
+    PA_CAP(__half, 256)
+  }
+#undef PA_CAP
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_nccap < kClusterCapCache) g_ccap[g_nccap++] = ClusterCap{dev, dtype, D, cs, smem, n};
+  return n;
+}
+
+// The cluster kernel's plan for a decode step, or cluster = 0 when the
+// persistent split kernel (with the merge kernel) is the better choice.
+// Chosen from the shape and options only, so a captured graph stays valid:
+// one query token per sequence on the mma.sync path with the balanced split
+// and the library's grid; a small step (at most 64 MB of K/V even with
+// every table row full: above that the persistent grid's even split of the
+// bytes wins); a table row that fits in shared memory.  The ring is as deep
+// as shared memory allows (up to 8 slots per warp).  The cluster is the
+// smallest (1 to 8 CTAs) whose CTAs each hold their share of the longest
+// possible segment in one ring load -- every tile then is in flight at once
+// and the fold across the cluster stays short -- else the largest that fits;
+// all B * Hkv clusters must be resident at once.
+void plan_cluster(const pa_shape* s, const pa_options* o, int dev, int sms, Plan* p) {
+  p->cluster = 0;
+  p->cring = 0;
+  p->csmem = 0;
+  if (p->multi || p->mode != kMma || p->part_blocks != 0) return;
+  if (o && (o->num_ctas > 0 || o->stall_test)) return;
+  const int64_t segs = (int64_t)s->batch * s->num_kv_heads;
+  const int64_t worst = (int64_t)s->batch * s->max_blocks_per_seq * s->block_size *
+                        s->num_kv_heads * s->head_dim * 4;
+  if (segs < 1 || segs > sms || worst > (64ll << 20) || s->max_blocks_per_seq > kClusterMaxTable)
+    return;
+  const int W = split_warps(p->D);
+  int ring = 0;
+  size_t smem = 0;
+  for (int r = (o && o->stages > 0) ? o->stages : kMaxSlots / W; r >= 1; --r) {
+    if (W * r > kMaxSlots) continue;
+    const size_t t = cluster_layout(p->D, p->C, W, r, s->max_blocks_per_seq).total;
+    if (t <= (size_t)kMaxDynamicSmem) {
+      ring = r;
+      smem = t;
+      break;
+    }
+    if (o && o->stages > 0) return;  // the asked-for depth does not fit
+  }
+  if (ring == 0) return;
+  const int64_t tiles = (int64_t)s->max_blocks_per_seq * (s->block_size / kTile);
+  const int64_t want64 = (tiles + (int64_t)W * ring - 1) / ((int64_t)W * ring);
+  const int want = (int)std::min<int64_t>(std::max<int64_t>(want64, 1), kMaxCluster);
+  auto fits = [&](int cs) {
+    return segs * cs <= sms && cluster_cap(dev, s->dtype, p->D, cs, smem) >= segs;
+  };
+  int cs = 0;
+  for (int c = want; c <= kMaxCluster && !cs; ++c)
+    if (fits(c)) cs = c;
+  for (int c = want - 1; c >= 1 && !cs; --c)
+    if (fits(c)) cs = c;
+  if (!cs) return;
+  p->cluster = cs;
+  p->cring = ring;
+  p->csmem = smem;
+}
+
 // Sizes and offsets of everything one call needs.  `need_device` = false
 // only when options->num_ctas fixes the grid (pure host computation).
 // max_q > 0: several query tokens per sequence, at most max_q each.
@@ -524,6 +622,11 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
     rc = occupancy(fn, dev, p->smem, 32 * p->warps, &occ);
     if (rc) return rc;
     if (!fixed_grid) p->grid = sms * occ;
+    plan_cluster(s, o, dev, sms, p);
+  } else {
+    p->cluster = 0;
+    p->cring = 0;
+    p->csmem = 0;
   }
   if (p->part_blocks == 0) {
     p->slots = 2 * (int64_t)p->grid;
@@ -678,6 +781,8 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.max_q = max_q;
   a.wait_us = o ? o->wait_limit_us : 0;
   a.stall_test = o ? o->stall_test : 0;
+  a.status_out = nullptr;
+  a.done = reinterpret_cast<uint32_t*>(ws + kDoneOffset);
   MergeArgs& m = c->ma;
   m.seqlens = cache_seqlens;
   m.out = out;
@@ -780,6 +885,38 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
   }
   int swap = 0;
+  if (p.cluster > 0) {
+    // the whole step in one kernel (pa_cluster.cuh)
+    if (pool_map(&tmk, k_cache, v_cache, s, &swap) == PA_OK) {
+      c->sa.kv_fused = 1;
+      c->sa.kv_swap = swap;
+      tmv = tmk;
+    } else {
+      c->sa.kv_fused = 0;
+      c->sa.kv_swap = 0;
+      rc = pool_map(&tmk, k_cache, nullptr, s, nullptr);
+      if (rc) return rc;
+      rc = pool_map(&tmv, v_cache, nullptr, s, nullptr);
+      if (rc) return rc;
+    }
+    SplitArgs a = c->sa;
+    a.ring = p.cring;
+    const int segs = s->batch * s->num_kv_heads;
+    cudaError_t e = cudaErrorInvalidValue;
+#define PA_LAUNCH_CL(T, DD) \
+  if (p.D == DD) e = launch_cluster<T, DD>(tmk, tmv, a, p.cluster, segs, p.csmem, stream);
+    if (s->dtype == PA_BF16) {
+      PA_LAUNCH_CL(__nv_bfloat16, 64)
+      PA_LAUNCH_CL(__nv_bfloat16, 128)
+      PA_LAUNCH_CL(__nv_bfloat16, 256)
+    } else {
+      PA_LAUNCH_CL(__half, 64)
+      PA_LAUNCH_CL(__half, 128)
+      PA_LAUNCH_CL(__half, 256)
+    }
+#undef PA_LAUNCH_CL
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
   if (pool_map(&tmk, k_cache, v_cache, s, &swap) == PA_OK) {
     // one copy per tile for K and V
     c->sa.kv_fused = 1;
@@ -821,6 +958,7 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
 // split kernel drains; griddepcontrol.wait orders the reads).
 int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   const Plan& p = c->plan;
+  if (p.cluster > 0) return PA_OK;  // the cluster kernel merged already
   // balanced split: one CTA per (segment with pieces to merge, column); such
   // segments continue past a split CTA, so there are fewer than the split
   // CTAs and at most one per row.  Fixed split: one per (row, column).
@@ -980,6 +1118,7 @@ int run_host_step(const pa_shape* s, const pa_options* o, const HostLayout& h, u
     c->ma.status = slot;
     published = static_cast<uint32_t*>(mapped_host(hb.status, 4));
     c->ma.status_out = published ? published : slot + 1;
+    c->sa.status_out = c->ma.status_out;  // the cluster kernel publishes it itself
   }
   int64_t vec = 0;
   for (int i = 0; i < sa.n; ++i) vec += sa.words[i] / 4;
@@ -1027,6 +1166,20 @@ int pa_workspace_size(const pa_shape* shape, const pa_options* options, size_t* 
   int rc = make_plan(shape, options, false, &p);
   if (rc) return rc;
   *bytes = p.total;
+  return PA_OK;
+}
+
+int pa_launch_plan(const pa_shape* shape, const pa_options* options, int32_t max_q,
+                   int32_t* info) {
+  if (!shape || !info) return PA_ERR_NULL;
+  if (max_q < 0) return PA_ERR_SHAPE;
+  Plan p;
+  const int rc = make_plan(shape, options, true, &p, max_q);
+  if (rc) return rc;
+  info[0] = p.cluster > 0 ? 1 : 2;
+  info[1] = p.cluster > 0 ? p.cluster * shape->batch * shape->num_kv_heads : p.grid;
+  info[2] = p.cluster;
+  info[3] = p.cluster > 0 ? p.cring : p.ring;
   return PA_OK;
 }
 
@@ -1078,6 +1231,7 @@ int pa_decode_append(const pa_shape* shape, const pa_options* options, const voi
   int rc = prepare(shape, options, q, k_cache, v_cache, block_table, cache_seqlens, scale, out,
                    workspace, workspace_bytes, true, &c);
   if (rc) return rc;
+  c.plan.cluster = 0;  // the appended row is written by the split kernel
   c.sa.len_add = 1;
   c.sa.k_new = static_cast<const uint16_t*>(k_new);
   c.sa.v_new = static_cast<const uint16_t*>(v_new);

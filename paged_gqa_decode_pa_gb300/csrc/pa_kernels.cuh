@@ -80,6 +80,11 @@ struct SplitArgs {
   // kWaitLimitNs), and the timeout-path test: 1 = warp 0 of every CTA waits
   // for its first tile on a barrier that nothing completes
   int32_t wait_us, stall_test;
+  // the cluster kernel (pa_cluster.cuh), host-buffer calls: once every CTA
+  // has counted itself in `done` (a workspace word, zero between calls), the
+  // last one copies *status to *status_out and clears both words
+  uint32_t* status_out;
+  uint32_t* done;
 };
 
 // Query rows [q0, q0 + nq) of sequence s, or false when cu_q is not a valid
@@ -338,7 +343,41 @@ PA_HD int tc_stages(int rows, int max_smem) {
   return 0;
 }
 
-// Launchers (explicitly instantiated in pa_split_*.cu).
+// ---- the cluster kernel (pa_cluster.cuh): small steps, one thread-block
+// cluster of up to kMaxCluster CTAs per (sequence, kv head) segment.
+
+constexpr int kMaxCluster = 8;
+constexpr int kClusterMaxTable = 4096;  // block-table entries staged in shared memory
+
+// Shared memory: the split kernel's carve-up for one row (rings, warp states,
+// q), then the segment's block-table row, the CTA's folded state and the
+// weights of the cluster's states.
+struct ClusterLayout {
+  SmemLayout s;
+  uint32_t table;   // [maxblk] int32
+  uint32_t st_acc;  // [C][D] fp32: the CTA's accumulator, relative to st_ml's max
+  uint32_t st_ml;   // [C][2] fp32: max (log2 units), exp-sum
+  uint32_t wts;     // [C][kMaxCluster] fp32
+  uint32_t total;
+};
+
+PA_HD ClusterLayout cluster_layout(int D, int C, int W, int R, int maxblk) {
+  ClusterLayout L;
+  L.s = split_smem_layout(D, C, 0, W, R, kMma);
+  uint32_t off = align_up(L.s.total - 1024, 16);
+  L.table = off;
+  off = align_up(off + (uint32_t)maxblk * 4u, 16);
+  L.st_acc = off;
+  off += (uint32_t)(C * D) * 4u;
+  L.st_ml = off;
+  off += (uint32_t)C * 8u;
+  L.wts = off;
+  off += (uint32_t)(C * kMaxCluster) * 4u;
+  L.total = align_up(off, 16) + 1024;  // slack to align the base to 1024 bytes
+  return L;
+}
+
+// Launchers (explicitly instantiated in pa_split_*.cu, pa_cluster_*.cu).
 template <typename T, int D, int MODE>
 cudaError_t launch_split(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a,
                          int grid, int threads, size_t smem, cudaStream_t stream);
@@ -354,5 +393,14 @@ cudaError_t launch_split_tc(const CUtensorMap& tmk, const CUtensorMap& tmv, cons
 
 template <typename T, bool kQ>
 const void* split_tc_kernel_ptr(int C);  // the variant for C query columns
+
+// The cluster kernel: grid (cs, segs), clusters of cs CTAs along x.
+template <typename T, int D>
+cudaError_t launch_cluster(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a, int cs,
+                           int segs, size_t smem, cudaStream_t stream);
+
+// Clusters of cs CTAs with `smem` bytes each that can be resident at once.
+template <typename T, int D>
+int cluster_capacity(int cs, size_t smem, int max_smem);
 
 }  // namespace pa
