@@ -67,15 +67,17 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-SPLIT_SOURCES = ("pa_split.cuh", "pa_ptx.cuh", "pa_kernels.cuh", "pa_sched.cuh")
+SPLIT_SOURCES = ("pa_split.cuh", "pa_ptx.cuh", "pa_kernels.cuh", "pa_sched.cuh", "pa_cluster.cuh")
 
 
 def source_hash() -> str:
-    """Hash of the split kernel's sources: recorded ncu traffic is tied to it."""
+    """Hash of the sources of a step's first kernel (the split kernel or the
+    cluster kernel): recorded ncu traffic is tied to it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_gqa_decode_pa_gb300", "csrc")
     names = sorted(f for f in os.listdir(csrc)
-                   if f in SPLIT_SOURCES or (f.startswith("pa_split_") and f.endswith(".cu")))
+                   if f in SPLIT_SOURCES or (f.startswith(("pa_split_", "pa_cluster_"))
+                                             and f.endswith(".cu")))
     for f in names:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
