@@ -883,8 +883,6 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
                          a.part_blocks, (int32_t)gridDim.x, a.len_add, a.piece_k};
   const int cta = blockIdx.x;
 
-  rows_without_keys_and_descriptors<D, kQ>(a, len_of, pre, sched, cta);
-
   const int w = warp;
   // the warp's tile stream and column group: with warp pairs, warps w and
   // w + W/2 take the same tiles, the lower one issuing their copies
@@ -921,6 +919,10 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   is.done = false;
   if (issuer)
     for (int r = 0; r < R; ++r) issue_next<D>(is, a, *sa, &tmk, &tmv, base, L, sw, S, (uint32_t)r, sl);
+
+  // outputs of rows without keys, and the merge kernel's descriptors: after
+  // the first copies are on their way (nothing above depends on them)
+  rows_without_keys_and_descriptors<D, kQ>(a, len_of, pre, sched, cta);
 
   // ---- the computing side
   if (have) cp_async_wait_all();
