@@ -652,6 +652,13 @@ def run_ours(args, rank, world, local_rank):
     q = st.q
     kv_bytes = st.kv_bytes
     K = args.steps
+    # the library's own kernels per step (split + merge, or one cluster kernel)
+    import paged_gqa_decode_pa_gb300 as pg
+
+    plan = pg.pa_launch_plan(pg.shape_multi(st.q, st.k, st.t) if st.multi
+                             else pg.shape_of(st.q, st.k, st.t), st.opts,
+                             w.max_q if st.multi else 0)
+    kernels_per_step = 2 if args.fused_append else plan["kernels"]
     props = torch.cuda.get_device_properties(dev)
     uuid = getattr(props, "uuid", None)
     sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local_rank))
@@ -732,7 +739,7 @@ def run_ours(args, rank, world, local_rank):
         "tokens_per_s": round(world * int(q.shape[0]) / (ms_per_step * 1e-3), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic", "config": workload_config(w, args),
-        "gpu_launches": 2 * K,
+        "gpu_launches": kernels_per_step * K,
         "roofline": {"bound": "hbm", "kernel": "pa_split_kernel",
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),

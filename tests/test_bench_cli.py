@@ -106,7 +106,7 @@ def test_bench_line_on_the_gpu(extra):
     # does not, so there the two are not comparable)
     if "--fused-append" not in extra:
         assert e["sync_value"] < d["value"] and e["value"] <= 1.05 * d["value"]
-    assert d["gpu_launches"] >= 2 * d["steps"]
+    assert d["gpu_launches"] >= d["steps"]  # one cluster kernel, or split + merge, per step
     assert d["clocks"]["sm_max_mhz"] > 0
     assert d["parity_vs_oracle"]["max_abs_err"] <= 2e-3
     assert d["cpu_baseline"]["kind"] == "oracle"
