@@ -422,15 +422,26 @@ class Stepper:
                 self.ws, self.opts, self.stream)
         self.graph = None
         if graph:
-            # one decode step captured once and replayed (host launch cost removed)
+            # one decode step captured once and replayed (host launch cost
+            # removed); the captured call is bound to the capture stream
             self.graph = torch.cuda.CUDAGraph()
             cap = torch.cuda.Stream(dev)
             cap.wait_stream(self.stream)
+            if fused_append:
+                cap_step = pg.bind_decode_append(self.q, self.kn, self.vn, self.k, self.v, self.t,
+                                                 self.sl, w.scale, self.out, self.ws, self.opts,
+                                                 cap)
+            elif self.multi:
+                cap_step = pg.bind_decode_multi(q, self.cu, w.max_q, w.causal, self.k, self.v, t,
+                                                self.sl, w.scale, self.out, self.ws, self.opts, cap)
+            else:
+                cap_step = pg.bind_decode(q, self.k, self.v, t, self.sl, w.scale, self.out,
+                                          self.ws, self.opts, cap)
             with torch.cuda.stream(cap):
-                self.decode_step()
+                cap_step()
             cap.synchronize()
             with torch.cuda.graph(self.graph, stream=cap):
-                self.decode_step()
+                cap_step()
             for _ in range(warmup):
                 self.graph.replay()
             torch.cuda.synchronize()
@@ -712,9 +723,10 @@ def run_ours(args, rank, world, local_rank):
                                 "sample": f"{len(pairs1)} outputs, {toks1} cached tokens, "
                                           f"{passes1} pass(es), {dt1:.1f} s"}}
         parity = st.parity(256)
-        if args.per_config == "all" or (args.per_config == "auto" and args.config ==
-                                         DEFAULT_WORKLOAD and not (args.query_tokens or
-                                         args.group or args.fused_append or args.graph)):
+        default_run = (args.config == DEFAULT_WORKLOAD and args.compute in ("mma", "auto")
+                       and not (args.query_tokens or args.group or args.fused_append
+                                or args.graph or args.partition_tokens or args.stages))
+        if args.per_config == "all" or (args.per_config == "auto" and default_run):
             del st
             torch.cuda.synchronize()
             torch.cuda.empty_cache()
@@ -728,6 +740,10 @@ def run_ours(args, rank, world, local_rank):
         return
     ms_per_step = total_ms / K
     value = whole_job_gbs(kv_bytes, world, ms_per_step)
+    peak_gbs = peaks()[0]
+    if value > 2 * world * peak_gbs or kv_bytes / (split_avg_ms * 1e-3) / 1e9 > 2 * peak_gbs:
+        # far above the copy bandwidth: the timed region did not do the work
+        raise RuntimeError(f"implausible timing: {value:.0f} GB/s against a {peak_gbs:.0f} GB/s peak")
     e2e_value = whole_job_gbs(kv_bytes, world, e2e_ms)
     achieved = kv_bytes / (split_avg_ms * 1e-3) / 1e9
     traffic = recorded_traffic(w.name, opts_key(opt_kw))
@@ -788,7 +804,7 @@ def main():
                          "cores (0 = skip); the one-core sample takes half as long")
     ap.add_argument("--per-config", default="auto", choices=["auto", "all", "none"],
                     help="also measure the other configurations (auto: when the headline "
-                         "workload runs with default workload options)")
+                         "workload runs with the default options)")
     ap.add_argument("--repeat-s", type=float, default=0.3,
                     help="seconds of repeated K-step regions after the timed one (spread)")
     args = ap.parse_args()

@@ -98,6 +98,8 @@ def test_bench_line_on_the_gpu(extra):
     rf = d["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"], abs=1e-4)  # rounded to 4 places
+    # the timed steps do the work: no faster than the device's memory allows
+    assert d["value"] < 1.5 * rf["peak"] and rf["frac"] < 1.5
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     # the synchronous host-buffer step costs more than the device step; the
