@@ -969,7 +969,10 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
       p.part_blocks > 0
           ? ((int64_t)c->sa.maxblk + p.part_blocks - 1) / p.part_blocks
           : (int64_t)p.grid / std::max(1, rows) + 2;
-  const bool wide = pieces > 4 * kMergeBatch;
+  // 8 warps (two rounds of loads fewer): long context, 38 pieces per
+  // column, 68.8 -> 68.0 us per step; nothing changes where segments have
+  // two or three pieces
+  const bool wide = pieces > 2 * kMergeBatch;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = p.part_blocks == 0 ? dim3(std::min(p.grid, rows) * p.C, 1, 1) : dim3(rows, p.C, 1);
   cfg.blockDim = dim3(wide ? 2 * kMergeThreads : kMergeThreads);
