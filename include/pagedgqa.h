@@ -168,8 +168,10 @@ typedef struct pa_options {
  * pa_cache_append need for this shape and these options (NULL = defaults).
  * The workspace holds the status word, the per-step length prefix sums and
  * the split-KV partial states (m, l, weighted_v[d]) in float32.  The caller
- * allocates it once, zero-fills it once (the status word must start at 0),
- * and may reuse it for every later call with the same shape and options.
+ * allocates it once, zero-fills it once (the status word and the cluster
+ * kernel's CTA count in the first 256 bytes must start at 0; every call
+ * leaves them 0 again, status bits aside), and may reuse it for every later
+ * call with the same shape and options.
  * Two calls in flight at the same time must not share a workspace.
  * Returns PA_OK and writes *bytes, or a negative code.  With
  * options->num_ctas == 0 the size depends on the current device's SM count. */
