@@ -1092,6 +1092,39 @@ float* host_out_target(const HostLayout& h, uint8_t* ws, float* out_host) {
 int run_host_step(const pa_shape* s, const pa_options* o, const HostLayout& h, uint8_t* ws,
                   const HostBuffers& hb, const void* k_cache, const void* v_cache, Call* c,
                   cudaStream_t st, bool async = false) {
+  // The cluster kernel reads the length, the table row and q once, in its
+  // first round trip: when all three sit in page-locked memory the device
+  // maps, it reads them there directly and the staging kernel is skipped.
+  if (c->plan.cluster > 0 && !hb.cu) {
+    const void* dq = mapped_host(hb.q, 16);
+    const void* dt = mapped_host(hb.table, 16);
+    const void* dl = mapped_host(hb.lens, 16);
+    if (dq && dt && dl) {
+      uint32_t* slot = reinterpret_cast<uint32_t*>(ws + h.status);
+      c->sa.q = static_cast<const uint16_t*>(dq);
+      c->sa.table = static_cast<const int32_t*>(dt);
+      c->sa.seqlens = static_cast<const int32_t*>(dl);
+      uint32_t* published = nullptr;
+      if (hb.status) {
+        // this call's bits: the slot's word (left at zero by the kernel that
+        // published the previous call's), published by the last CTA
+        c->sa.status = slot;
+        published = static_cast<uint32_t*>(mapped_host(hb.status, 4));
+        c->sa.status_out = published ? published : slot + 1;
+      }
+      int rc = launch_split_phase(s, k_cache, v_cache, c, st);
+      if (rc) return rc;
+      if (c->sa.out == reinterpret_cast<float*>(ws + h.out) &&
+          cudaMemcpyAsync(hb.out, ws + h.out, h.out_bytes, cudaMemcpyDefault, st) != cudaSuccess)
+        return PA_ERR_CUDA;
+      if (hb.status && !published &&
+          cudaMemcpyAsync(hb.status, slot + 1, sizeof(uint32_t), cudaMemcpyDefault, st) !=
+              cudaSuccess)
+        return PA_ERR_CUDA;
+      if (async) return PA_OK;
+      return cudaStreamSynchronize(st) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
+  }
   StageArgs sa = {};
   auto part = [&](const void* host, size_t off, size_t bytes) {
     if (bytes == 0) return PA_OK;

@@ -75,13 +75,14 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ---- one round trip: the length, the whole table row, q
-  const int32_t stored = __ldg(a.seqlens + b);
-  for (int i = tid; i < a.maxblk; i += blockDim.x) tab[i] = __ldg(a.table + (int64_t)b * a.maxblk + i);
+  // ---- one round trip: the length, the whole table row, q.  Plain loads:
+  // with the host-buffer calls these three may be page-locked host memory
+  // the device maps, read here directly.
+  const int32_t stored = a.seqlens[b];
+  for (int i = tid; i < a.maxblk; i += blockDim.x) tab[i] = a.table[(int64_t)b * a.maxblk + i];
   {
-    const char* src = reinterpret_cast<const char*>(a.q + ((int64_t)b * a.H + (int64_t)j * a.G) * D);
-    for (int i = tid; i < C * D / 8; i += blockDim.x) cp_async16(qraw + 16u * i, src + 16 * (int64_t)i, 16u);
-    cp_async_commit();
+    const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * a.H + (int64_t)j * a.G) * D);
+    for (int i = tid; i < C * D / 8; i += blockDim.x) sts128(qraw + 16u * i, src[i]);
   }
   const int32_t len = eff_len(stored, 0, a.bs, a.maxblk);  // -1: not a valid length
   const int nblk = len >= 0 ? seq_blocks(len, a.bs, a.maxblk) : 0;
@@ -90,7 +91,6 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   const int nt = (blk1 - blk0) << sl;
   const int cnt = nt > w ? (nt - w + W - 1) / W : 0;  // this warp's tiles: w, w + W, ...
   if (len < 0 && rank == 0 && tid == 0) atomicOr(a.status, kStatusBadSeqlen);
-  cp_async_wait_all();
   __syncthreads();  // the table row, q and the argument copy are in place
   for (int i = tid; i < C * D / 2; i += blockDim.x) {
     const int c = (2 * i) / D, d = (2 * i) % D;
