@@ -29,7 +29,11 @@ per_config: with the default workload, the other configurations the metric
           with the default split and with 512-token partitions, prefix
           sharing), each with device and end-to-end time per step, the split
           kernel's fraction of the HBM peak, the recorded ncu traffic ratio
-          and an oracle parity sample.
+          and an oracle parity sample.  A workload that fits in L2 is timed
+          two ways: one step at a time with L2 flushed before each (events
+          around every step), and as the decode of consecutive layers of a
+          model (layer_steps: enough copies of the inputs to exceed L2,
+          attended in turn back to back).
 N > 1   : independent replicas (the path has no exchange step), one per GPU,
           scaling "weak".
 """
@@ -616,6 +620,69 @@ PER_CONFIG = [
 ]
 
 
+def per_config_entries(spec: str, default_run: bool):
+    """The PER_CONFIG entries --per-config selects."""
+    if spec == "none" or (spec == "auto" and not default_run):
+        return []
+    if spec in ("auto", "all"):
+        return list(PER_CONFIG)
+    names = [x for x in spec.split(",") if x]
+    known = {e[0]: e for e in PER_CONFIG}
+    bad = [x for x in names if x not in known]
+    if bad:
+        raise SystemExit(f"--per-config: unknown entries {bad}; choose from {sorted(known)}")
+    return [known[x] for x in names]
+
+
+MAX_LAYERS = 128
+
+
+def layer_steps(w, kw, dev, steps, warmup):
+    """A step of a small workload as it runs inside a model: the decode of
+    consecutive layers, each over its own cache.  L copies of the inputs
+    (at least 24, and together more than 2.5x L2, so a copy's K/V rows are
+    gone from L2 before its next turn and no flush is needed) are attended in
+    turn, back to back on one stream, with events around the whole run.
+    Returns (L, device ms per step, MB of K/V over the copies), or None when
+    that would need more than MAX_LAYERS copies."""
+    import torch
+
+    import paged_gqa_decode_pa_gb300 as pg
+
+    L = max(24, math.ceil(2.5 * L2_BYTES / w.kv_bytes()))
+    if L > MAX_LAYERS:
+        return None
+    opts = pg.options(**kw)
+    stream = torch.cuda.current_stream(dev)
+    calls, outs, wss = [], [], []
+    for _ in range(L):
+        q, k, v, t, sl = w.torch_tensors(dev)
+        out = torch.empty((w.B, w.H, w.d), dtype=torch.float32, device=dev)
+        ws = pg.alloc_workspace(pg.shape_of(q, k, t), opts, dev)
+        calls.append(pg.bind_decode(q, k, v, t, sl, w.scale, out, ws, opts, stream))
+        outs.append(out)
+        wss.append(ws)
+    for _ in range(max(warmup, 3)):
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    reps = max(2, math.ceil(steps / L))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        for c in calls:
+            c()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * L)
+    if any(pg.pa_read_status(x) != 0 for x in wss):
+        raise RuntimeError("device status bits set during the layer steps")
+    if not all(torch.equal(outs[0], o) for o in outs[1:]):
+        raise RuntimeError("the layers' outputs differ on identical inputs")
+    return L, ms, L * w.kv_bytes() / 1e6
+
+
 def per_config_entry(name, part, args, dev, peak):
     """One configuration at a glance: device and end-to-end time per step,
     the split kernel's fraction of the HBM peak, the recorded ncu traffic
@@ -632,6 +699,22 @@ def per_config_entry(name, part, args, dev, peak):
     par = st.parity(256)
     traffic = recorded_traffic(w.name, opts_key(kw))
     kvb = st.kv_bytes
+    flushed = st.flush
+    layers = None
+    if flushed:
+        del st
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        lr = layer_steps(w, kw, dev, K, args.warmup)
+        if lr is not None:
+            n, lms, mb = lr
+            if kvb / (lms * 1e-3) / 1e9 > 2 * peak:
+                raise RuntimeError("implausible layer-step timing")
+            layers = {"layers": n, "us_per_step": round(lms * 1e3, 3),
+                      "gbs": round(kvb / (lms * 1e-3) / 1e9, 2),
+                      "step_frac": round(kvb / (lms * 1e-3) / 1e9 / peak, 4),
+                      "l2": f"{n} copies of the inputs ({mb:.0f} MB of K/V) attended in turn, "
+                            f"back to back; no flush"}
     entry = {"workload": w.name, "partition_tokens": part, "steps": K,
              "us_per_step": round(ms * 1e3, 3), "gbs": round(kvb / (ms * 1e-3) / 1e9, 2),
              "split_us": round(split_ms * 1e3, 3), "merge_us": round(merge_ms * 1e3, 3),
@@ -640,11 +723,12 @@ def per_config_entry(name, part, args, dev, peak):
              "e2e_us": round(e2e_ms * 1e3, 3), "e2e_sync_us": round(e2e_sync_ms * 1e3, 3),
              "kv_bytes_per_step": kvb,
              "traffic_ratio": round(traffic / kvb, 4) if traffic else None,
-             "l2": ("inputs larger than L2" if not st.flush
+             "l2": ("inputs larger than L2" if not flushed
                     else "L2 flushed between timed steps"),
              "max_abs_err": par["max_abs_err"], "mean_abs_err": par["mean_abs_err"],
-             "parity_outputs": par["pairs"]}
-    del st
+             "parity_outputs": par["pairs"], "layer_steps": layers}
+    if not flushed:
+        del st
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return entry
@@ -726,12 +810,13 @@ def run_ours(args, rank, world, local_rank):
         default_run = (args.config == DEFAULT_WORKLOAD and args.compute in ("mma", "auto")
                        and not (args.query_tokens or args.group or args.fused_append
                                 or args.graph or args.partition_tokens or args.stages))
-        if args.per_config == "all" or (args.per_config == "auto" and default_run):
+        chosen = per_config_entries(args.per_config, default_run)
+        if chosen:
             del st
             torch.cuda.synchronize()
             torch.cuda.empty_cache()
             per_config = {}
-            for entry, name, part in PER_CONFIG:
+            for entry, name, part in chosen:
                 t0 = time.time()
                 per_config[entry] = per_config_entry(name, part, args, dev, peak)
                 per_config[entry]["clocks"] = sampler.window(t0, time.time())
@@ -802,9 +887,10 @@ def main():
     ap.add_argument("--cpu-baseline-s", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample on all host "
                          "cores (0 = skip); the one-core sample takes half as long")
-    ap.add_argument("--per-config", default="auto", choices=["auto", "all", "none"],
-                    help="also measure the other configurations (auto: when the headline "
-                         "workload runs with the default options)")
+    ap.add_argument("--per-config", default="auto",
+                    help="also measure the other configurations: auto (when the headline "
+                         "workload runs with the default options), all, none, or a "
+                         "comma-separated list of entry names")
     ap.add_argument("--repeat-s", type=float, default=0.3,
                     help="seconds of repeated K-step regions after the timed one (spread)")
     args = ap.parse_args()

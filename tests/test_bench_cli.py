@@ -112,3 +112,19 @@ def test_bench_line_on_the_gpu(extra):
     assert d["clocks"]["sm_max_mhz"] > 0
     assert d["parity_vs_oracle"]["max_abs_err"] <= 2e-3
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_per_config_selection():
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    import bench
+
+    every = [e[0] for e in bench.PER_CONFIG]
+    assert bench.per_config_entries("none", True) == []
+    assert bench.per_config_entries("auto", False) == []
+    assert [e[0] for e in bench.per_config_entries("auto", True)] == every
+    assert [e[0] for e in bench.per_config_entries("all", False)] == every
+    picked = bench.per_config_entries("qwen2_b8_g7_d64,p5_example", False)
+    assert [e[0] for e in picked] == ["qwen2_b8_g7_d64", "p5_example"]
+    with pytest.raises(SystemExit):
+        bench.per_config_entries("no_such_entry", True)
