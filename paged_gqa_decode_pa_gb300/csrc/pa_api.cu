@@ -401,6 +401,20 @@ int choose_ring(const pa_shape* s, const pa_options* o, int mode, int W, int C, 
   return fit < want ? fit : want;
 }
 
+// The wide-row kernel exists for head_dim <= 128 only.
+template <typename T, int DD>
+const void* wide_kernel_ptr() {
+  if constexpr (DD <= 128) return split_kernel_ptr<T, DD, kMmaW>();
+  return nullptr;
+}
+
+template <typename T, int DD>
+cudaError_t launch_wide(const CUtensorMap& tmk, const CUtensorMap& tmv, const SplitArgs& a, int grid,
+                        int threads, size_t smem, cudaStream_t stream) {
+  if constexpr (DD <= 128) return launch_split<T, DD, kMmaW>(tmk, tmv, a, grid, threads, smem, stream);
+  return cudaErrorInvalidValue;
+}
+
 const void* kernel_for(int dtype, int D, int mode, int multi, int C) {
   if (mode == kTc) {
     if (D != kTcD) return nullptr;
@@ -413,6 +427,7 @@ const void* kernel_for(int dtype, int D, int mode, int multi, int C) {
   if (D == DD) return mode == kSimt ? split_kernel_ptr<T, DD, kSimt>()                \
                       : mode == kMmaQ ? split_kernel_ptr<T, DD, kMmaQ>()              \
                       : mode == kMmaP ? split_kernel_ptr<T, DD, kMmaP>()              \
+                      : mode == kMmaW ? wide_kernel_ptr<T, DD>()                      \
                                       : split_kernel_ptr<T, DD, kMma>();
   if (dtype == PA_BF16) {
     PA_PICK(__nv_bfloat16, 64)
@@ -583,11 +598,13 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
     if (max_q > PA_MAX_QUERY_TOKENS) return PA_ERR_SHAPE;
     if (p->mode == kSimt) return PA_ERR_OPTION;  // tensor-core path only
     // groups of (token, head) columns: a warp keeps cw = 8 x mma_blocks of
-    // them; rows wider than that go to warp pairs (2 cw columns, one read of
-    // the K/V).  The tcgen05 kernel keeps groups of N = 16.
+    // them; rows wider than that (2 cw columns, one read of the K/V) go to
+    // wide rows (one warp, columns as the mma's M; head_dim <= 128) or warp
+    // pairs.  The tcgen05 kernel keeps groups of N = 16.
     const int cw = 8 * mma_blocks(p->D, kMmaQ);
-    if (p->mode != kTc) p->mode = (int64_t)max_q * p->G > cw ? kMmaP : kMmaQ;
-    p->tq = (p->mode == kTc ? kTcN : (p->mode == kMmaP ? 2 * cw : cw)) / p->G;
+    if (p->mode != kTc)
+      p->mode = (int64_t)max_q * p->G > cw ? (p->D <= 128 ? kMmaW : kMmaP) : kMmaQ;
+    p->tq = (p->mode == kTc ? kTcN : (p->mode == kMmaP || p->mode == kMmaW ? 2 * cw : cw)) / p->G;
     p->nqg = (max_q + p->tq - 1) / p->tq;
     p->C = p->tq * p->G;
     if ((int64_t)s->batch * p->nqg > PA_MAX_BATCH) return PA_ERR_SHAPE;
@@ -605,6 +622,12 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
     p->smem = tc_smem_layout(p->rows, p->ring).total;
   } else {
     p->ring = choose_ring(s, o, p->mode, p->warps, p->C, p->rows);
+    if (p->mode == kMmaW && p->ring < 2 && !(o && o->stages > 0)) {
+      // too many rows for two slots per warp next to the wide states: the
+      // same rows on warp pairs
+      p->mode = kMmaP;
+      p->ring = choose_ring(s, o, p->mode, p->warps, p->C, p->rows);
+    }
     if (p->ring < 1) return (o && o->stages > 0) ? PA_ERR_OPTION : PA_ERR_SHAPE;
     const SmemLayout L = split_smem_layout(p->D, p->C, p->rows, p->warps, p->ring, p->mode);
     p->smem = L.total;
@@ -764,7 +787,9 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.part_blocks = p.part_blocks;
   a.piece_k = p.part_blocks == 0
                   ? piece_units(s->block_size, s->head_dim,
-                                !p.multi ? kPieceKb : (p.mode == kMmaP ? kPieceKbPair : kPieceKbMulti))
+                                !p.multi ? kPieceKb
+                                         : (p.mode == kMmaP || p.mode == kMmaW ? kPieceKbPair
+                                                                              : kPieceKbMulti))
                   : 0;
   a.warps = p.warps;
   a.ring = p.ring;
@@ -939,6 +964,8 @@ int launch_split_phase(const pa_shape* s, const void* k_cache, const void* v_cac
             ? launch_split<T, DD, kMmaQ>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream)     \
         : p.mode == kMmaP                                                                       \
             ? launch_split<T, DD, kMmaP>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream)     \
+        : p.mode == kMmaW                                                                       \
+            ? launch_wide<T, DD>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream)             \
             : launch_split<T, DD, kMma>(tmk, tmv, c->sa, p.grid, 32 * p.warps, p.smem, stream);
   if (s->dtype == PA_BF16) {
     PA_LAUNCH(__nv_bfloat16, 64)

@@ -32,10 +32,15 @@ constexpr float kLazyMax = 8.f;
 // w % (W/2)), each for its own half of the row's columns ([0, 8 NB) and
 // [8 NB, C)), so a row of up to 16 NB columns reads its K/V once; the lower
 // warp loads the tiles, the upper one releases each ring slot through the
-// slot's "empty" mbarrier.
-enum Mode { kSimt = 1, kMma = 2, kMmaQ = 3, kTc = 4, kMmaP = 5 };  // kTc: pa_split_tc.cuh
+// slot's "empty" mbarrier.  kMmaW: rows of up to kRowCols columns held by
+// one warp, with the columns as the mma's M dimension (two m-tiles of 16):
+// the scores come out in the layout the P.V product takes them in, and each
+// tile's K/V fragments feed all the row's columns (head_dim <= 128).
+enum Mode { kSimt = 1, kMma = 2, kMmaQ = 3, kTc = 4, kMmaP = 5, kMmaW = 6 };  // kTc: pa_split_tc.cuh
 
-PA_HD constexpr bool several_tokens(int mode) { return mode == kMmaQ || mode == kMmaP; }
+PA_HD constexpr bool several_tokens(int mode) {
+  return mode == kMmaQ || mode == kMmaP || mode == kMmaW;
+}
 
 // mma n-blocks of 8 query columns a warp keeps (registers allow two below
 // d = 256).
@@ -192,7 +197,7 @@ struct SmemLayout {
   uint32_t stage_bytes;
   uint32_t mo, mm, ml, mbad;        // per-warp partial states for the CTA combine
   uint32_t cwt;                     // [kRowCols][kMaxWarps + 2] fp32 combine weights, max, sum
-  uint32_t qs;                      // [C][D+4] fp32 q of the current piece (x scale*log2(e): CUDA cores)
+  uint32_t qs;                      // [C][D+4] fp32 q of the current piece (x scale*log2(e): CUDA cores; kMmaW: 16-bit)
   uint32_t qlim;                    // [kRowCols] int32 key limit per column (several tokens)
   uint32_t qraw;                    // [C][D] raw 16-bit q of the next piece (cp.async target)
   uint32_t args;                    // a copy of the SplitArgs, read by the once-per-piece code
@@ -208,10 +213,16 @@ PA_HD uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 // Tile streams of a CTA: one per warp, or one per warp pair (kMmaP).
 PA_HD constexpr int split_streams(int W, int mode) { return mode == kMmaP ? W / 2 : W; }
 
-// Columns of the row a warp keeps (the stride of its published state).
+// Columns of the row a warp publishes at once (the stride of its published
+// state): its half of a pair's row, a wide row's 16-column m-tile, or the
+// whole row.
 PA_HD constexpr int warp_columns(int D, int C, int mode) {
-  return mode == kMmaP ? 8 * mma_blocks(D, mode) : C;
+  return mode == kMmaP ? 8 * mma_blocks(D, mode) : (mode == kMmaW ? kColMax : C);
 }
+
+// Row stride (bytes) of a wide row's 16-bit q copy: 16-byte rows for
+// ldmatrix, 8 rows landing in distinct bank groups.
+PA_HD constexpr uint32_t wide_q_stride(int D) { return (uint32_t)(D + 8) * 2u; }
 
 // C = query columns per row (G in decode), B = rows, R = ring slots per
 // tile stream.
@@ -239,14 +250,14 @@ PA_HD SmemLayout split_smem_layout(int D, int C, int B, int W, int R, int mode) 
   L.qlim = off;
   off += (uint32_t)kRowCols * 4u;
   off = align_up(off, 16);
-  L.qs = off;
-  off += (uint32_t)(C * (D + 4)) * 4u;
+  L.qs = off;  // kMmaW: the row's q as 16-bit [kRowCols][D + 8] (columns >= C zero)
+  off += mode == kMmaW ? (uint32_t)kRowCols * wide_q_stride(D) : (uint32_t)(C * (D + 4)) * 4u;
   L.qraw = off;
   off += (uint32_t)(C * D) * 2u;
   L.zrow = off;
   off += (uint32_t)D * 2u;
-  L.nrow = off;
-  off += (uint32_t)(W * 2 * D) * 2u;
+  L.nrow = off;  // the fused append only (one query token per sequence)
+  off += several_tokens(mode) ? 0u : (uint32_t)(W * 2 * D) * 2u;
   if (mode == kSimt) {
     L.ps = off;
     off += (uint32_t)(W * kTile * kGMax) * 4u;

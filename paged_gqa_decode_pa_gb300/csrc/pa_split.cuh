@@ -314,6 +314,189 @@ struct MmaState {
   }
 };
 
+// Rows of up to kRowCols (token, head) columns held by one warp, the columns
+// as the mma's M dimension (m-tile mt holds columns 16 mt .. 16 mt + 15):
+//   S[16 columns x 16 tokens] = q . K^T   (per m-tile; K is the B operand)
+//   O[16 columns x D]        += P . V     (P the A operand, V the B operand)
+// The C fragment of S -- row g / g + 8, tokens 2t, 2t+1 of each 8-token
+// n-block -- is already P's A fragment once packed to 16 bits, so no
+// transposes; each K and V fragment feeds both m-tiles.  q's A fragments are
+// read from the 16-bit copy in shared memory at every k-step (registers hold
+// the 2 x D/8 x 4 accumulators instead).  Each lane's exp-sums cover its own
+// tokens; the quad's are added when the state is published.
+template <typename T, int D>
+struct MmaWState {
+  static constexpr int MT = 2;      // m-tiles of 16 columns
+  static constexpr int NT = D / 8;  // n-blocks of 8 dims of O
+  float o[MT][NT][4];     // rows g, g+8 of each m-tile: [0,1] row g dims 2t, 2t+1; [2,3] row g+8
+  float m[MT][2], l[MT][2];
+  int32_t lim[MT][2];     // key limit of rows g, g+8 (tokens t < lim are visible)
+  float qsc;              // scale * log2(e), applied to the fp32 scores
+  bool bad;
+
+  __device__ __forceinline__ void load_lim(const int32_t* qlim, float qscale) {
+    const int g = (threadIdx.x & 31) >> 2;
+    qsc = qscale;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      lim[mt][0] = qlim[mt * 16 + g];
+      lim[mt][1] = qlim[mt * 16 + g + 8];
+    }
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[mt][n][c] = 0.f;
+      m[mt][0] = m[mt][1] = -INFINITY;
+      l[mt][0] = l[mt][1] = 0.f;
+    }
+    bad = false;
+  }
+
+  // One 16-token tile (see MmaState::tile for kb, vb, valid, tok0, zrow);
+  // qa: the row's 16-bit q, [kRowCols][D + 8].
+  __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int valid, int tok0, uint32_t zrow,
+                                       uint32_t qa) {
+    const int lane = threadIdx.x & 31;
+    const int t = lane & 3;
+    constexpr uint32_t chunk = kTile * 128u;
+    constexpr uint32_t qstride = wide_q_stride(D);
+    // ---- S = q . K^T: four independent accumulator chains (m-tile x n-block)
+    float acc[MT][2][4] = {};
+    {
+      // K, non-transposed: matrices (tokens 0-7 | 8-15) x (dims lo | hi of
+      // the k-step) give b0, b1 of n-block 0 and b0, b1 of n-block 1
+      const uint32_t ktok = (lane & 7) + (lane >> 4) * 8;
+      const uint32_t kuh = (uint32_t)((lane >> 3) & 1);
+      // q: matrices (columns 0-7 | 8-15) x (dims lo | hi) give a0 .. a3
+      const uint32_t qrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const uint32_t qoff = qa + qrow * qstride + (uint32_t)(lane >> 4) * 16u;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(kb + (uint32_t)(ks >> 2) * chunk + swz(ktok, 2u * (ks & 3) + kuh), b0, b1, b2, b3);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4(qoff + (uint32_t)mt * 16u * qstride + (uint32_t)ks * 32u, a0, a1, a2, a3);
+          mma_16816<T>(acc[mt][0], a0, a1, a2, a3, b0, b1);
+          mma_16816<T>(acc[mt][1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+    }
+    // ---- online softmax per row; P's A fragments (high and low parts)
+    uint32_t ph[MT][4], pl[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      float x[2][4];  // [row g, g+8][tokens 2t, 2t+1, 8+2t, 9+2t]
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          x[0][2 * nb + e] = acc[mt][nb][e] * qsc;
+          x[1][2 * nb + e] = acc[mt][nb][2 + e] * qsc;
+        }
+      }
+      float al[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tk = (i >> 1) * 8 + 2 * t + (i & 1);
+          if (tk >= valid || tok0 + tk >= lim[mt][r]) x[r][i] = -INFINITY;
+        }
+        float mx = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // lazy running max, as in MmaState::tile
+        const float nm = (mx > m[mt][r] + kLazyMax) ? mx : m[mt][r];
+        const float u = (nm == -INFINITY) ? 0.f : nm;
+        al[r] = ex2(m[mt][r] - u);
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          x[r][i] = ex2(x[r][i] - u);
+          sum += x[r][i];
+        }
+        l[mt][r] = l[mt][r] * al[r] + sum;
+        m[mt][r] = nm;
+      }
+      if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          o[mt][n][0] *= al[0];
+          o[mt][n][1] *= al[0];
+          o[mt][n][2] *= al[1];
+          o[mt][n][3] *= al[1];
+        }
+      }
+      // a0: row g tokens 2t, 2t+1; a1: row g+8; a2, a3: tokens 8 + 2t, 9 + 2t
+      auto split = [](float p0, float p1, uint32_t& hi, uint32_t& lo) {
+        hi = Cvt<T>::pack(p0, p1);
+        lo = Cvt<T>::pack(p0 - Cvt<T>::low(hi), p1 - Cvt<T>::high(hi));
+      };
+      split(x[0][0], x[0][1], ph[mt][0], pl[mt][0]);
+      split(x[1][0], x[1][1], ph[mt][1], pl[mt][1]);
+      split(x[0][2], x[0][3], ph[mt][2], pl[mt][2]);
+      split(x[1][2], x[1][3], ph[mt][3], pl[mt][3]);
+    }
+    // ---- O += P . V  (V transposed by ldmatrix; rows past the end read
+    // the zero row, so p = 0 adds 0 even where the pool holds NaN)
+    {
+      // matrices (tokens 0-7 | 8-15) x (dims of n-block 2p | 2p + 1)
+      const uint32_t vtok = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const uint32_t vuh = (uint32_t)(lane >> 4);
+      const bool vzero = (int)vtok >= valid;
+#pragma unroll
+      for (int p = 0; p < D / 16; ++p) {
+        uint32_t b0, b1, b2, b3;
+        const uint32_t unit = 2u * (p & 3) + vuh;
+        const uint32_t addr = vzero ? zrow + (uint32_t)(p >> 2) * 128u + unit * 16u
+                                    : vb + (uint32_t)(p >> 2) * chunk + swz(vtok, unit);
+        ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          mma_16816<T>(o[mt][2 * p], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], b0, b1);
+          mma_16816<T>(o[mt][2 * p + 1], ph[mt][0], ph[mt][1], ph[mt][2], ph[mt][3], b2, b3);
+          mma_16816<T>(o[mt][2 * p], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], b0, b1);
+          mma_16816<T>(o[mt][2 * p + 1], pl[mt][0], pl[mt][1], pl[mt][2], pl[mt][3], b2, b3);
+        }
+      }
+    }
+  }
+
+  // Publish m-tile MTI (columns 16 MTI .. 16 MTI + 15) of this warp's state
+  // for the CTA-level combine, as a 16-column state.
+  template <int MTI>
+  __device__ __forceinline__ void publish(uint8_t* smem, const SmemLayout& L, int w) {
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    float* mm = reinterpret_cast<float*>(smem + L.mm) + w * kColMax;
+    float* ml = reinterpret_cast<float*>(smem + L.ml) + w * kColMax;
+    float* mo = reinterpret_cast<float*>(smem + L.mo) + (size_t)w * kColMax * (D + 4);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float lr = l[MTI][r];
+      lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+      lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+      const int lc = g + 8 * r;
+      if (t == 0) {
+        mm[lc] = m[MTI][r];
+        ml[lc] = lr;
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+        *reinterpret_cast<float2*>(mo + lc * (D + 4) + n * 8 + 2 * t) =
+            make_float2(o[MTI][n][2 * r], o[MTI][n][2 * r + 1]);
+    }
+    if (lane == 0) reinterpret_cast<int*>(smem + L.mbad)[w] = bad ? 1 : 0;
+  }
+};
+
 template <typename T, int D>
 struct SimtState {
   float acc[kGMax][D / 32];  // dims c*64 + 2*lane + e, e in {0,1}, chunk c
@@ -494,11 +677,17 @@ __device__ __forceinline__ int64_t column_out(const SplitArgs& a, int row, int j
 // thread takes 4 consecutive dims of one column at a time, weighs the warps'
 // accumulators with float4 shared loads and writes a float4.  The fold order
 // over the warps is fixed, so the result is deterministic.
+// c0, nc, ns (not kPair): fold columns [c0, c0 + nc) of the row, published
+// by every warp as states of ns columns (a wide row's m-tiles, one at a
+// time: ns = 16); by default the whole row, ns = nc = C.
 template <int D, int W, bool kQ, bool kPair>
 __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem, const SmemLayout& L,
-                                              const Piece& pc, int q0, int nq, int cw) {
+                                              const Piece& pc, int q0, int nq, int cw, int c0 = 0,
+                                              int nc = -1, int ns = -1) {
   const int C = a.C;
-  const int stride = kPair ? cw : C;  // columns of one published warp state
+  if (nc < 0) nc = C;
+  if (ns < 0) ns = nc;
+  const int stride = kPair ? cw : ns;  // columns of one published warp state
   constexpr int NW = kPair ? W / 2 : W;  // warps holding a column
   constexpr int WS = kMaxWarps + 2;      // floats per column in the weight table
   const float* mm = reinterpret_cast<const float*>(smem + L.mm);
@@ -514,15 +703,15 @@ __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem,
   // the warps holding column c, and its index in their states
   auto col_warps = [&](int c, int& w0, int& lc) {
     w0 = 0;
-    lc = c;
+    lc = c - c0;
     if constexpr (kPair) {
       const int cg = c >= cw ? 1 : 0;
       w0 = cg * NW;
       lc = c - cg * cw;
     }
   };
-  if (threadIdx.x < C) {
-    const int c = threadIdx.x;
+  if (threadIdx.x < nc) {
+    const int c = c0 + threadIdx.x;
     int w0, lc;
     col_warps(c, w0, lc);
     float mw[NW];
@@ -549,8 +738,8 @@ __device__ __forceinline__ void combine_piece(const SplitArgs& a, uint8_t* smem,
   }
   named_bar_sync(2, blockDim.x);
   constexpr int DV = D / 4;  // float4s per column
-  for (int v = threadIdx.x; v < C * DV; v += blockDim.x) {
-    const int c = v / DV, d4 = (v - c * DV) * 4;
+  for (int v = threadIdx.x; v < nc * DV; v += blockDim.x) {
+    const int c = c0 + v / DV, d4 = (v % DV) * 4;
     int w0, lc;
     col_warps(c, w0, lc);
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -726,8 +915,10 @@ struct QStage {
     cp_async_commit();
   }
 
-  // After every thread's copies are complete and a barrier.
-  template <typename T, bool kScaled>
+  // After every thread's copies are complete and a barrier.  kWide: qs
+  // takes the raw 16-bit values, [kRowCols][D + 8] (columns >= C zero),
+  // instead of fp32.
+  template <typename T, bool kScaled, bool kWide = false>
   __device__ __forceinline__ void finish(const SplitArgs& a, uint32_t qraw, float* qs, int32_t* info,
                                          int32_t* qlim) {
     if (threadIdx.x == 0) {
@@ -747,6 +938,16 @@ struct QStage {
         if (c < a.C && tok < nq && a.causal) lim = max(0, min(len, len - nq + tok + 1));
         qlim[c] = lim;
       }
+    }
+    if constexpr (kWide) {
+      constexpr int per_col = D / 8;  // 16-byte units of a column
+      const uint32_t qa = smem_u32(qs);
+      for (int i = threadIdx.x; i < kRowCols * per_col; i += blockDim.x) {
+        const int c = i / per_col, k = i - c * per_col;
+        const uint4 v = c < a.C ? lds128(qraw + 16u * i) : make_uint4(0u, 0u, 0u, 0u);
+        sts128(qa + (uint32_t)c * wide_q_stride(D) + 16u * k, v);
+      }
+      return;
     }
     const int nw = a.C * D / 2;
     for (int i = threadIdx.x; i < nw; i += blockDim.x) {
@@ -927,7 +1128,7 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   // ---- the computing side
   if (have) cp_async_wait_all();
   __syncthreads();
-  if (have) qn.template finish<T, MODE == kSimt>(*sa, qraw, qs, piece_info, qlim);
+  if (have) qn.template finish<T, MODE == kSimt, MODE == kMmaW>(*sa, qraw, qs, piece_info, qlim);
   __syncthreads();
   uint32_t slot = 0, phase = 0;  // ring slot to consume next; per-slot parity bits
   uint32_t ephase = 0;           // warp pairs, issuer: per-slot parity of the "empty" barriers
@@ -936,11 +1137,14 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   // it issued may still be in flight when the loop ends (see the drain)
   int64_t first_fail = -1;
   bool stall = a.stall_test && w == 0;
-  MmaState<T, D, NB, kQ> mst;
+  typename std::conditional<MODE == kMmaW, MmaWState<T, D>, MmaState<T, D, NB, kQ>>::type mst;
   SimtState<T, D> sst;
   float* ps = reinterpret_cast<float*>(smem + L.ps) + w * kTile * kGMax;
   while (have) {
-    if constexpr (MODE != kSimt) {
+    if constexpr (MODE == kMmaW) {
+      mst.load_lim(qlim, A.qscale);
+      mst.reset();
+    } else if constexpr (MODE != kSimt) {
       if constexpr (kPair)
         mst.load_q(qs + cg * cw * (D + 4), cl, qlim + cg * cw, A.qscale);
       else
@@ -1021,7 +1225,9 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
             new_r = r;
           }
         }
-        if constexpr (MODE != kSimt) {
+        if constexpr (MODE == kMmaW) {
+          mst.tile(kb, vb, valid, tok0, base + L.zrow, base + L.qs);
+        } else if constexpr (MODE != kSimt) {
           mst.tile(kb, vb, valid, tok0, new_r, nkr, nvr, base + L.zrow);
         } else {
           sst.tile(kb, vb, valid, qs, ps, a.G, new_r, nkr, nvr);
@@ -1051,7 +1257,10 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     if constexpr (kQ) {
       if (more) qn.issue_copies(*sa, next, qraw);
     }
-    if constexpr (MODE != kSimt) {
+    if constexpr (MODE == kMmaW) {
+      mst.bad |= bad;
+      mst.template publish<0>(smem, L, w);
+    } else if constexpr (MODE != kSimt) {
       mst.bad |= bad;
       if constexpr (kPair)
         mst.publish(smem, L, w, cl, cw);
@@ -1066,8 +1275,21 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     const int q0 = kQ ? piece_info[2] : 0, nq = kQ ? piece_info[3] : 0;
     cp_async_wait_all();  // this thread's copies of the next q have landed
     named_bar_sync(1, blockDim.x);
-    combine_piece<D, W, kQ, kPair>(*sa, smem, L, pc, q0, nq, kPair ? cw : 0);
-    if (more) qn.template finish<T, MODE == kSimt>(*sa, qraw, qs, piece_info, qlim);
+    if constexpr (MODE == kMmaW) {
+      // a wide row's two m-tiles, folded one after the other through the
+      // same 16-column state buffers
+      combine_piece<D, W, kQ, false>(*sa, smem, L, pc, q0, nq, 0, 0, min(kColMax, A.C), kColMax);
+      if (A.C > kColMax) {
+        named_bar_sync(1, blockDim.x);  // m-tile 0's states are read
+        mst.template publish<1>(smem, L, w);
+        named_bar_sync(1, blockDim.x);
+        combine_piece<D, W, kQ, false>(*sa, smem, L, pc, q0, nq, 0, kColMax, A.C - kColMax,
+                                       kColMax);
+      }
+    } else {
+      combine_piece<D, W, kQ, kPair>(*sa, smem, L, pc, q0, nq, kPair ? cw : 0);
+    }
+    if (more) qn.template finish<T, MODE == kSimt, MODE == kMmaW>(*sa, qraw, qs, piece_info, qlim);
     named_bar_sync(1, blockDim.x);
     have = it.next(pc);
   }

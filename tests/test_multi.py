@@ -232,3 +232,22 @@ def test_full_size_settings_on_sampled_outputs(name):
     pairs = np.unique(np.stack([rows, heads], 1).astype(np.int32), axis=0)
     ref = oracle_multi(w, pairs=pairs)
     assert_close(got[pairs[:, 0], pairs[:, 1]], ref, name)
+
+
+@pytest.mark.gpu
+def test_eight_query_tokens_full_size_sampled():
+    """The serving mix with 8 query tokens per sequence (rows of 32 columns,
+    one warp per row: the columns are the mma's M dimension), causal."""
+    from _helpers import assert_close
+
+    base = wl.make("serving_mix_b256_g4_d128")
+    w = wl.with_query_tokens(base, np.full(base.B, 8, np.int32), seed=base.seed + 2000,
+                             causal=True)
+    got, status = run_multi(w)
+    assert status == 0
+    rng = np.random.default_rng(5)
+    rows = np.concatenate([[0, w.q.shape[0] - 1], rng.integers(0, w.q.shape[0], 126)])
+    heads = rng.integers(0, w.H, rows.shape[0])
+    pairs = np.unique(np.stack([rows, heads], 1).astype(np.int32), axis=0)
+    ref = oracle_multi(w, pairs=pairs)
+    assert_close(got[pairs[:, 0], pairs[:, 1]], ref, "8 query tokens")
