@@ -788,8 +788,9 @@ int prepare(const pa_shape* s, const pa_options* o, const void* q, const void* k
   a.piece_k = p.part_blocks == 0
                   ? piece_units(s->block_size, s->head_dim,
                                 !p.multi ? kPieceKb
-                                         : (p.mode == kMmaP || p.mode == kMmaW ? kPieceKbPair
-                                                                              : kPieceKbMulti))
+                                         : (p.mode == kMmaW   ? kPieceKbWide
+                                            : p.mode == kMmaP ? kPieceKbPair
+                                                              : kPieceKbMulti))
                   : 0;
   a.warps = p.warps;
   a.ring = p.ring;

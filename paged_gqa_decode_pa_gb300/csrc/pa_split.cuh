@@ -388,61 +388,69 @@ struct MmaWState {
         }
       }
     }
-    // ---- online softmax per row; P's A fragments (high and low parts)
-    uint32_t ph[MT][4], pl[MT][4];
+    // ---- online softmax per row, both m-tiles before any branch (so that
+    // their chains interleave); one vote for the rescale; then P's A
+    // fragments (high and low parts)
+    float x[MT][2][4];  // [m-tile][row g, g+8][tokens 2t, 2t+1, 8+2t, 9+2t]
+    float al[MT][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      float x[2][4];  // [row g, g+8][tokens 2t, 2t+1, 8+2t, 9+2t]
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          x[0][2 * nb + e] = acc[mt][nb][e] * qsc;
-          x[1][2 * nb + e] = acc[mt][nb][2 + e] * qsc;
+          x[mt][0][2 * nb + e] = acc[mt][nb][e] * qsc;
+          x[mt][1][2 * nb + e] = acc[mt][nb][2 + e] * qsc;
         }
       }
-      float al[2];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int tk = (i >> 1) * 8 + 2 * t + (i & 1);
-          if (tk >= valid || tok0 + tk >= lim[mt][r]) x[r][i] = -INFINITY;
+          if (tk >= valid || tok0 + tk >= lim[mt][r]) x[mt][r][i] = -INFINITY;
         }
-        float mx = fmaxf(fmaxf(x[r][0], x[r][1]), fmaxf(x[r][2], x[r][3]));
+        float mx = fmaxf(fmaxf(x[mt][r][0], x[mt][r][1]), fmaxf(x[mt][r][2], x[mt][r][3]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         // lazy running max, as in MmaState::tile
         const float nm = (mx > m[mt][r] + kLazyMax) ? mx : m[mt][r];
         const float u = (nm == -INFINITY) ? 0.f : nm;
-        al[r] = ex2(m[mt][r] - u);
+        al[mt][r] = ex2(m[mt][r] - u);
         float sum = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          x[r][i] = ex2(x[r][i] - u);
-          sum += x[r][i];
+          x[mt][r][i] = ex2(x[mt][r][i] - u);
+          sum += x[mt][r][i];
         }
-        l[mt][r] = l[mt][r] * al[r] + sum;
+        l[mt][r] = l[mt][r] * al[mt][r] + sum;
         m[mt][r] = nm;
       }
-      if (__any_sync(0xffffffffu, al[0] != 1.f || al[1] != 1.f)) {
+    }
+    if (__any_sync(0xffffffffu, al[0][0] != 1.f || al[0][1] != 1.f || al[1][0] != 1.f ||
+                                    al[1][1] != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          o[mt][n][0] *= al[0];
-          o[mt][n][1] *= al[0];
-          o[mt][n][2] *= al[1];
-          o[mt][n][3] *= al[1];
+          o[mt][n][0] *= al[mt][0];
+          o[mt][n][1] *= al[mt][0];
+          o[mt][n][2] *= al[mt][1];
+          o[mt][n][3] *= al[mt][1];
         }
-      }
+    }
+    uint32_t ph[MT][4], pl[MT][4];
+    auto split = [](float p0, float p1, uint32_t& hi, uint32_t& lo) {
+      hi = Cvt<T>::pack(p0, p1);
+      lo = Cvt<T>::pack(p0 - Cvt<T>::low(hi), p1 - Cvt<T>::high(hi));
+    };
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
       // a0: row g tokens 2t, 2t+1; a1: row g+8; a2, a3: tokens 8 + 2t, 9 + 2t
-      auto split = [](float p0, float p1, uint32_t& hi, uint32_t& lo) {
-        hi = Cvt<T>::pack(p0, p1);
-        lo = Cvt<T>::pack(p0 - Cvt<T>::low(hi), p1 - Cvt<T>::high(hi));
-      };
-      split(x[0][0], x[0][1], ph[mt][0], pl[mt][0]);
-      split(x[1][0], x[1][1], ph[mt][1], pl[mt][1]);
-      split(x[0][2], x[0][3], ph[mt][2], pl[mt][2]);
-      split(x[1][2], x[1][3], ph[mt][3], pl[mt][3]);
+      split(x[mt][0][0], x[mt][0][1], ph[mt][0], pl[mt][0]);
+      split(x[mt][1][0], x[mt][1][1], ph[mt][1], pl[mt][1]);
+      split(x[mt][0][2], x[mt][0][3], ph[mt][2], pl[mt][2]);
+      split(x[mt][1][2], x[mt][1][3], ph[mt][3], pl[mt][3]);
     }
     // ---- O += P . V  (V transposed by ldmatrix; rows past the end read
     // the zero row, so p = 0 adds 0 even where the pool holds NaN)
