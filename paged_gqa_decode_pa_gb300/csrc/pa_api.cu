@@ -397,7 +397,7 @@ int choose_ring(const pa_shape* s, const pa_options* o, int mode, int W, int C, 
   int fit = (kMaxDynamicSmem - (int)L0.total) / (streams * (int)L0.stage_bytes);
   if (fit > kMaxSlots / streams) fit = kMaxSlots / streams;
   if (o && o->stages > 0) return o->stages <= fit ? o->stages : -1;
-  const int want = mode == kMmaP ? 4 : 2;
+  const int want = mode == kMmaP ? 4 : (mode == kMmaW ? kWideRing : 2);
   return fit < want ? fit : want;
 }
 
@@ -621,11 +621,13 @@ int make_plan(const pa_shape* s, const pa_options* o, bool setup_kernel, Plan* p
     }
     p->smem = tc_smem_layout(p->rows, p->ring).total;
   } else {
+    p->warps = split_warps(p->D, p->mode);
     p->ring = choose_ring(s, o, p->mode, p->warps, p->C, p->rows);
     if (p->mode == kMmaW && p->ring < 2 && !(o && o->stages > 0)) {
       // too many rows for two slots per warp next to the wide states: the
       // same rows on warp pairs
       p->mode = kMmaP;
+      p->warps = split_warps(p->D, p->mode);
       p->ring = choose_ring(s, o, p->mode, p->warps, p->C, p->rows);
     }
     if (p->ring < 1) return (o && o->stages > 0) ? PA_ERR_OPTION : PA_ERR_SHAPE;

@@ -13,9 +13,6 @@ namespace pa {
 
 constexpr int kMaxWarps = 8;   // warps per split CTA (each runs its own TMA ring)
 
-// Warps per split CTA for a head dimension: 8, or 4 for d = 256 so that each
-// warp can keep three 16 KB stages in flight within the shared memory.
-PA_HD constexpr int split_warps(int D) { return D == 256 ? 4 : kMaxWarps; }
 constexpr int kMaxSlots = 64;  // warps x ring slots
 constexpr int kGMax = 8;       // query heads per kv head handled by one CTA
 constexpr int kColMax = 16;    // query columns (token, head) of a warp state: two mma n-blocks
@@ -37,6 +34,15 @@ constexpr float kLazyMax = 8.f;
 // the scores come out in the layout the P.V product takes them in, and each
 // tile's K/V fragments feed all the row's columns (head_dim <= 128).
 enum Mode { kSimt = 1, kMma = 2, kMmaQ = 3, kTc = 4, kMmaP = 5, kMmaW = 6 };  // kTc: pa_split_tc.cuh
+
+// Warps per split CTA for a head dimension (and kernel mode): 8, or 4 for
+// d = 256 so that each warp can keep three 16 KB stages in flight within the
+// shared memory; kWideWarps for wide rows, with kWideRing slots each.
+constexpr int kWideWarps = 8;
+constexpr int kWideRing = 2;
+PA_HD constexpr int split_warps(int D, int mode = kMma) {
+  return D == 256 ? 4 : (mode == kMmaW ? kWideWarps : kMaxWarps);
+}
 
 PA_HD constexpr bool several_tokens(int mode) {
   return mode == kMmaQ || mode == kMmaP || mode == kMmaW;

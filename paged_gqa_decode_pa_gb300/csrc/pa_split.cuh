@@ -405,10 +405,12 @@ struct MmaWState {
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
+        // tokens [0, vis) of the tile are real and below the row's key limit
+        const int vis = min(valid, lim[mt][r] - tok0);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int tk = (i >> 1) * 8 + 2 * t + (i & 1);
-          if (tk >= valid || tok0 + tk >= lim[mt][r]) x[mt][r][i] = -INFINITY;
+          if (tk >= vis) x[mt][r][i] = -INFINITY;
         }
         float mx = fmaxf(fmaxf(x[mt][r][0], x[mt][r][1]), fmaxf(x[mt][r][2], x[mt][r][3]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -1020,10 +1022,10 @@ __device__ __forceinline__ void rows_without_keys_and_descriptors(const SplitArg
 }
 
 template <typename T, int D, int MODE>
-__global__ void __launch_bounds__(32 * split_warps(D), 1)
+__global__ void __launch_bounds__(32 * split_warps(D, MODE), 1)
     pa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                     const __grid_constant__ SplitArgs a) {
-  constexpr int W = split_warps(D);
+  constexpr int W = split_warps(D, MODE);
   constexpr bool kQ = several_tokens(MODE);
   constexpr bool kPair = MODE == kMmaP;
   constexpr int NB = mma_blocks(D, MODE);
