@@ -251,3 +251,18 @@ def test_eight_query_tokens_full_size_sampled():
     pairs = np.unique(np.stack([rows, heads], 1).astype(np.int32), axis=0)
     ref = oracle_multi(w, pairs=pairs)
     assert_close(got[pairs[:, 0], pairs[:, 1]], ref, "8 query tokens")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("scale", [-0.2, 0.0, 0.7])
+def test_wide_rows_take_any_scale(scale):
+    """Rows of more than 16 columns apply |scale| with q negated for a
+    negative scale, and a zero scale gives every visible key the same weight."""
+    from _helpers import assert_close
+
+    w = wl.random_workload([300, 40, 1000], 16, 4, 128, 16, dtype="bf16", seed=61)
+    w = wl.with_query_tokens(w, [8, 5, 7], seed=62, causal=True)
+    w.scale = scale
+    got, status = run_multi(w)
+    assert status == 0
+    assert_close(got, oracle_multi(w), f"scale {scale}")

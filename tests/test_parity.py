@@ -255,3 +255,16 @@ def test_full_size_settings_sampled(name):
         assert np.isfinite(got).all()
         sub = got[pairs[:, 0], pairs[:, 1]]
         assert_close(sub, ref, name)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("scale", [-0.2, 0.0])
+def test_negative_and_zero_scale(mode, scale):
+    """A negative scale turns the softmax towards the smallest q.k; a zero
+    scale weighs every visible key the same (the mean of V)."""
+    w = wl.random_workload([300, 17, 1000, 64], H=16, Hkv=4, d=128, bs=16, dtype="bf16", seed=71)
+    w.scale = scale
+    for opts in (pg.options(compute=mode), pg.options(compute=mode, num_ctas=7)):
+        got, st = run_gpu(w, opts)
+        assert st == 0
+        assert_close(got, run_oracle(w), f"scale {scale} {mode}")
