@@ -27,8 +27,9 @@ repeats : the K-step region repeated for about --repeat-s seconds (spread);
 per_config: with the default workload, the other configurations the metric
           is quoted on (the tiny page example, Qwen2-style GQA, long context
           with the default split and with 512-token partitions, prefix
-          sharing), each with device and end-to-end time per step, the split
-          kernel's fraction of the HBM peak, the recorded ncu traffic ratio
+          sharing, the serving mix with 8 query tokens per sequence), each
+          with device and end-to-end time per step, the split kernel's
+          fraction of the HBM peak, the recorded ncu traffic ratio
           and an oracle parity sample.  A workload that fits in L2 is timed
           two ways: one step at a time with L2 flushed before each (events
           around every step), and as the decode of consecutive layers of a
@@ -610,13 +611,15 @@ def opts_key(kw) -> str:
 
 
 # The other configurations the metric is quoted on, measured in the same run
-# as the headline (one GPU): (entry name, workload, partition_tokens).
+# as the headline (one GPU): (entry name, workload, partition_tokens, query
+# tokens per sequence).
 PER_CONFIG = [
-    ("p5_example", "p5_example", 0),
-    ("qwen2_b8_g7_d64", "qwen2_b8_g7_d64", 0),
-    ("long_ctx_100k_g6_d256", "long_ctx_100k_g6_d256", 0),
-    ("long_ctx_100k_g6_d256_part512", "long_ctx_100k_g6_d256", 512),
-    ("prefix_share_b64_g8_d128", "prefix_share_b64_g8_d128", 0),
+    ("p5_example", "p5_example", 0, 0),
+    ("qwen2_b8_g7_d64", "qwen2_b8_g7_d64", 0, 0),
+    ("long_ctx_100k_g6_d256", "long_ctx_100k_g6_d256", 0, 0),
+    ("long_ctx_100k_g6_d256_part512", "long_ctx_100k_g6_d256", 512, 0),
+    ("prefix_share_b64_g8_d128", "prefix_share_b64_g8_d128", 0, 0),
+    ("serving_mix_b256_q8_g4_d128", "serving_mix_b256_g4_d128", 0, 8),
 ]
 
 
@@ -683,13 +686,13 @@ def layer_steps(w, kw, dev, steps, warmup):
     return L, ms, L * w.kv_bytes() / 1e6
 
 
-def per_config_entry(name, part, args, dev, peak):
+def per_config_entry(name, part, args, dev, peak, query_tokens=0):
     """One configuration at a glance: device and end-to-end time per step,
     the split kernel's fraction of the HBM peak, the recorded ncu traffic
     ratio (when taken on the current kernel sources) and the parity sample."""
     import torch
 
-    w = make_workload(name)
+    w = make_workload(name, query_tokens)
     kw = dict(partition_tokens=part, compute=args.compute, stages=args.stages)
     st = Stepper(w, kw, dev, warmup=args.warmup)
     K = max(args.steps, 20)
@@ -715,7 +718,8 @@ def per_config_entry(name, part, args, dev, peak):
                       "step_frac": round(kvb / (lms * 1e-3) / 1e9 / peak, 4),
                       "l2": f"{n} copies of the inputs ({mb:.0f} MB of K/V) attended in turn, "
                             f"back to back; no flush"}
-    entry = {"workload": w.name, "partition_tokens": part, "steps": K,
+    entry = {"workload": w.name, "partition_tokens": part, "query_tokens": query_tokens,
+             "steps": K,
              "us_per_step": round(ms * 1e3, 3), "gbs": round(kvb / (ms * 1e-3) / 1e9, 2),
              "split_us": round(split_ms * 1e3, 3), "merge_us": round(merge_ms * 1e3, 3),
              "frac": round(kvb / (split_ms * 1e-3) / 1e9 / peak, 4),
@@ -816,9 +820,9 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize()
             torch.cuda.empty_cache()
             per_config = {}
-            for entry, name, part in chosen:
+            for entry, name, part, nq in chosen:
                 t0 = time.time()
-                per_config[entry] = per_config_entry(name, part, args, dev, peak)
+                per_config[entry] = per_config_entry(name, part, args, dev, peak, nq)
                 per_config[entry]["clocks"] = sampler.window(t0, time.time())
     sampler.stop()
     if rank != 0:
