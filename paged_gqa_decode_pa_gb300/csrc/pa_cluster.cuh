@@ -92,13 +92,6 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   const int cnt = nt > w ? (nt - w + W - 1) / W : 0;  // this warp's tiles: w, w + W, ...
   if (len < 0 && rank == 0 && tid == 0) atomicOr(a.status, kStatusBadSeqlen);
   __syncthreads();  // the table row, q and the argument copy are in place
-  for (int i = tid; i < C * D / 2; i += blockDim.x) {
-    const int c = (2 * i) / D, d = (2 * i) % D;
-    const uint32_t v = lds32(qraw + 4u * i);
-    *reinterpret_cast<float2*>(qs + c * (D + 4) + d) = make_float2(Cvt<T>::low(v), Cvt<T>::high(v));
-  }
-  __syncthreads();
-
   // ---- the CTA's tiles through the warps' rings
   auto issue = [&](int n, uint32_t slot) {
     if (lane == 0) {
@@ -127,11 +120,20 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
       }
     }
   };
+  // the ring's first copies go out before q is widened: they need only
+  // the table row and the length
+  int issued = 0;
+  for (int r = 0; r < R && r < cnt; ++r, ++issued) issue(r, (uint32_t)r);
+  for (int i = tid; i < C * D / 2; i += blockDim.x) {
+    const int c = (2 * i) / D, d = (2 * i) % D;
+    const uint32_t v = lds32(qraw + 4u * i);
+    *reinterpret_cast<float2*>(qs + c * (D + 4) + d) = make_float2(Cvt<T>::low(v), Cvt<T>::high(v));
+  }
+  __syncthreads();
+
   MmaState<T, D, 1, false> mst;
   mst.load_q(qs, C, nullptr, a.qscale);
   mst.reset();
-  int issued = 0;
-  for (int r = 0; r < R && r < cnt; ++r, ++issued) issue(r, (uint32_t)r);
   bool bad = len < 0, stop = false;
   int first_fail = -1;
   uint32_t slot = 0, phase = 0;
