@@ -136,8 +136,10 @@ typedef struct pa_options {
                         CTAs on the current device.  Setting it makes
                         pa_workspace_size independent of the device. */
   int32_t stages;    /* TMA ring slots per warp (16-token K/V stages,
-                        1..8); with PA_COMPUTE_TC the CTA's 128-token V
-                        slots (2..4); 0 = library choice */
+                        1..8; more than fit in shared memory next to the
+                        kernel's other buffers is PA_ERR_OPTION); with
+                        PA_COMPUTE_TC the CTA's 128-token V slots (2..4);
+                        0 = library choice */
   int32_t phase;     /* pa_decode / pa_decode_append / pa_decode_multi:
                         PA_PHASE_BOTH (0) runs both kernels; PA_PHASE_SPLIT
                         only phase 1, PA_PHASE_MERGE only phase 2 (which must
