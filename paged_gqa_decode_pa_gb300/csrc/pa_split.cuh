@@ -365,8 +365,9 @@ struct MmaWState {
     const int t = lane & 3;
     constexpr uint32_t chunk = kTile * 128u;
     constexpr uint32_t qstride = wide_q_stride(D);
-    // ---- S = q . K^T: four independent accumulator chains (m-tile x n-block)
-    float acc[MT][2][4] = {};
+    // ---- S = q . K^T: eight independent accumulator chains (m-tile x
+    // n-block x k-step parity)
+    float acc2[MT][2][2][4] = {};
     {
       // K, non-transposed: matrices (tokens 0-7 | 8-15) x (dims lo | hi of
       // the k-step) give b0, b1 of n-block 0 and b0, b1 of n-block 1
@@ -383,8 +384,8 @@ struct MmaWState {
         for (int mt = 0; mt < MT; ++mt) {
           uint32_t a0, a1, a2, a3;
           ldmatrix_x4(qoff + (uint32_t)mt * 16u * qstride + (uint32_t)ks * 32u, a0, a1, a2, a3);
-          mma_16816<T>(acc[mt][0], a0, a1, a2, a3, b0, b1);
-          mma_16816<T>(acc[mt][1], a0, a1, a2, a3, b2, b3);
+          mma_16816<T>(acc2[mt][0][ks & 1], a0, a1, a2, a3, b0, b1);
+          mma_16816<T>(acc2[mt][1][ks & 1], a0, a1, a2, a3, b2, b3);
         }
       }
     }
@@ -399,8 +400,8 @@ struct MmaWState {
       for (int nb = 0; nb < 2; ++nb) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          x[mt][0][2 * nb + e] = acc[mt][nb][e] * qsc;
-          x[mt][1][2 * nb + e] = acc[mt][nb][2 + e] * qsc;
+          x[mt][0][2 * nb + e] = (acc2[mt][nb][0][e] + acc2[mt][nb][1][e]) * qsc;
+          x[mt][1][2 * nb + e] = (acc2[mt][nb][0][2 + e] + acc2[mt][nb][1][2 + e]) * qsc;
         }
       }
 #pragma unroll
