@@ -266,3 +266,37 @@ def test_wide_rows_take_any_scale(scale):
     got, status = run_multi(w)
     assert status == 0
     assert_close(got, oracle_multi(w), f"scale {scale}")
+
+
+@pytest.mark.gpu
+def test_wide_rows_bad_entries_poison_and_determinism():
+    """Rows of 32 columns (8 tokens at G = 4): a bad table entry inside one
+    sequence's length makes that sequence's rows NaN and sets the status bit,
+    the other sequences match the oracle, NaN-poisoned unread rows change no
+    bit, and two runs give the same bits."""
+    from _helpers import assert_close
+
+    lens_k, lens_q = [700, 90, 1500, 33], [8, 6, 8, 3]
+
+    def make(poison):
+        w = wl.random_workload(lens_k, 16, 4, 128, 16, dtype="bf16", seed=71, poison=poison,
+                               outlier_frac=0.02)
+        return wl.with_query_tokens(w, lens_q, seed=72, causal=True)
+
+    clean, st = run_multi(make(False))
+    assert st == 0
+    poisoned, st = run_multi(make(True))
+    assert st == 0
+    assert np.array_equal(clean, poisoned)
+    again, _ = run_multi(make(True))
+    assert np.array_equal(poisoned, again)
+    ref = oracle_multi(make(False))
+    assert_close(clean, ref, "wide rows")
+    w = make(False)
+    w.block_table[2, 40] = -1  # inside sequence 2's 1500 tokens
+    got, st = run_multi(w)
+    assert st == pg.PA_STATUS_BAD_BLOCK
+    rows2 = np.arange(int(w.cu_q[2]), int(w.cu_q[3]))
+    assert np.isnan(got[rows2]).all()
+    ok = np.setdiff1d(np.arange(int(w.cu_q[-1])), rows2)
+    assert_close(got[ok], ref[ok], "good rows beside a bad one")
