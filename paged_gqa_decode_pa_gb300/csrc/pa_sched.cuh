@@ -63,12 +63,13 @@ struct SchedShape {
 // cost is fewer blocks' worth: best at about 220 KB (sweep of 40 to 440 KB on
 // the 8-token serving step: 906 us against 990 at 440 KB).  Wide rows (one
 // warp per row of up to 32 columns, folded in two halves) are best at about
-// 320 KB (8-token serving split 701.5 us against 727.6 at 220, 726.8 at 440
-// and 799.1 at 120; 4-token prefix sharing 258.2 against 265.2 at 220).
+// 380 KB (8-token serving split on one box: 653.8 us, against 656.0 at 350,
+// 659.5 at 410, 665.6 at 320, 666.7 at 440, 682.5 at 520 and 694.0 at 260;
+// the 6-token step and 4-token prefix sharing agree).
 constexpr int32_t kPieceKb = 200;
 constexpr int32_t kPieceKbMulti = 300;
 constexpr int32_t kPieceKbPair = 220;
-constexpr int32_t kPieceKbWide = 320;
+constexpr int32_t kPieceKbWide = 380;
 PA_HD int32_t piece_units(int32_t bs, int32_t D, int32_t kb = kPieceKb) {
   const int32_t unit = 4 * bs * D;
   const int32_t k = (kb * 1024 + unit / 2) / unit;
