@@ -57,8 +57,11 @@ struct SchedShape {
 // best on GB300 at about 200 KB worth (sweeps of 60 to 320 KB on the serving
 // and prefix-sharing steps; long context does not move).  With several query
 // tokens per sequence a piece's fold and q cover up to 16 columns and cost
-// more: measured best at about 300 KB (sweeps of 120 to 600 KB on the 4-token
-// serving step and the 2-token prefix-sharing step).  Rows of warp pairs (up
+// more: measured best at about 360 KB (sweeps of 120 to 600 KB on the 4-token
+// serving step and the 2-token prefix-sharing step; on one box the 4-token
+// serving split took 510.7 us at 360 against 519.6 at 300, 513.8 at 340,
+// 512.2 at 380, 523.2 at 460 and 537.1 at 220, and 2-token prefix sharing
+// 186.6 against 185.9 at 300).  Rows of warp pairs (up
 // to 32 columns) spend twice the compute on every block, so the same piece
 // cost is fewer blocks' worth: best at about 220 KB (sweep of 40 to 440 KB on
 // the 8-token serving step: 906 us against 990 at 440 KB).  Wide rows (one
@@ -67,7 +70,7 @@ struct SchedShape {
 // 659.5 at 410, 665.6 at 320, 666.7 at 440, 682.5 at 520 and 694.0 at 260;
 // the 6-token step and 4-token prefix sharing agree).
 constexpr int32_t kPieceKb = 200;
-constexpr int32_t kPieceKbMulti = 300;
+constexpr int32_t kPieceKbMulti = 360;
 constexpr int32_t kPieceKbPair = 220;
 constexpr int32_t kPieceKbWide = 380;
 PA_HD int32_t piece_units(int32_t bs, int32_t D, int32_t kb = kPieceKb) {
