@@ -198,6 +198,92 @@ __device__ __forceinline__ bool find_segment(const MergeArgs& a, int k, int& seg
   return seg >= 0;
 }
 
+// Balanced split whose segments have few pieces (typically at most
+// kMergeBatch: many more rows than split CTAs): CTA i takes column group i mod ng (kColGroup
+// columns, one per warp) of the (i / ng)-th segment with pieces to merge.
+// Each warp folds its column's pieces in piece order with one round of loads
+// and writes the column; no warp waits for another after the segment scan,
+// and the scan runs once per column group instead of once per column.
+constexpr int kColGroup = 4;
+template <int D>
+__global__ void __launch_bounds__(kColGroup * 32) pa_merge_cols_kernel(const MergeArgs a) {
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (a.status_out && blockIdx.x == 0 && threadIdx.x == 0) {
+    volatile uint32_t* st = a.status;
+    *a.status_out = *st;
+    *st = 0u;
+  }
+  const int ng = (a.C + kColGroup - 1) / kColGroup;
+  const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas, 0, 0};
+  int seg;
+  int4 desc = make_int4(-1, 0, 0, 0);
+  if (!find_segment<kColGroup>(a, blockIdx.x / ng, seg, desc)) return;
+  const MergeSeg ms = merge_segment(sched, seg, desc.x, desc.y, desc.z, desc.w, a.ws_pre);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int g = (blockIdx.x % ng) * kColGroup + w;
+  if (ms.np == 0 || g >= a.C) return;
+  int64_t out_row = (int64_t)ms.b * a.H + (int64_t)ms.j * a.G + g;
+  if (a.cu_q) {
+    const int sq = ms.b / a.nqg, grp = ms.b - sq * a.nqg;
+    int32_t q0, nq;
+    query_span(a.cu_q, sq, a.total_q, a.max_q, q0, nq);
+    const int tok = grp * a.tq + g / a.G;
+    if (tok >= nq) return;  // the column holds no query
+    out_row = (int64_t)(q0 + tok) * a.H + (int64_t)ms.j * a.G + g % a.G;
+  }
+  constexpr int V = D / 32;  // dims per lane
+  float m = -INFINITY, l = 0.f;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  // batches of kMergeBatch pieces (a long segment among short ones can span
+  // more split CTAs than the average suggests)
+  for (int p0 = 0; p0 < ms.np; p0 += kMergeBatch) {
+    float mp[kMergeBatch], lp[kMergeBatch];
+    Vec<V> x[kMergeBatch];
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      mp[u] = -INFINITY;
+      lp[u] = 0.f;
+      if (p0 + u < ms.np) {
+        const int64_t sl = ms.slot(p0 + u);
+        mp[u] = a.ws_ml[(sl * a.C + g) * 2];
+        lp[u] = a.ws_ml[(sl * a.C + g) * 2 + 1];
+        x[u] = load_vec<V>(a.ws_acc + (sl * a.C + g) * D + lane * V);
+      } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) x[u].v[i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      // an empty state (m = -inf) gets weight 0; a NaN it carries (a bad
+      // piece) still reaches the result
+      const float nm = fmaxf(m, mp[u]);
+      const float sa = (m == -INFINITY) ? 0.f : ex2(m - nm);
+      const float sb = (mp[u] == -INFINITY) ? 0.f : ex2(mp[u] - nm);
+      l = l * sa + lp[u] * sb;
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = acc[i] * sa + x[u].v[i] * sb;
+      m = nm;
+    }
+  }
+  // a column that saw no key gets 0; NaN passes through; whole-line stores
+  float* dst = a.out + out_row * D + lane * V;
+  float r[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) r[i] = l == 0.f ? 0.f : acc[i] / l;
+  if constexpr (V % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < V; i += 4)
+      *reinterpret_cast<float4*>(dst + i) = make_float4(r[i], r[i + 1], r[i + 2], r[i + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; i += 2) *reinterpret_cast<float2*>(dst + i) = make_float2(r[i], r[i + 1]);
+  }
+}
+
 // Staging of a host-buffer call's inputs by the SMs (see StageArgs): each
 // thread moves 16-byte chunks, four in flight, then the parts' 4-byte tails.
 // Dependents (the split kernel) may be scheduled at once; they wait for this
@@ -1003,9 +1089,18 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   // column, 68.8 -> 68.0 us per step; nothing changes where segments have
   // two or three pieces
   const bool wide = pieces > 2 * kMergeBatch;
+  // few pieces per segment (balanced split) and more than one column group:
+  // column groups, a warp per column.  Same box, step times: 8-token serving
+  // 668.2 -> 657.8 us, 4-token prefix sharing 250.9 -> 241.1, 4-token serving
+  // 515.2 -> 510.5, prefix sharing (G = 8) 180.8 -> 178.8; the serving mix
+  // (4 columns, one group) 493.4 against 494.3, so it keeps the per-column grid
+  const bool cols = p.part_blocks == 0 && pieces <= kMergeBatch && p.C > kColGroup;
+  const int ng = (p.C + kColGroup - 1) / kColGroup;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = p.part_blocks == 0 ? dim3(std::min(p.grid, rows) * p.C, 1, 1) : dim3(rows, p.C, 1);
-  cfg.blockDim = dim3(wide ? 2 * kMergeThreads : kMergeThreads);
+  cfg.gridDim = cols ? dim3(std::min(p.grid, rows) * ng, 1, 1)
+                : p.part_blocks == 0 ? dim3(std::min(p.grid, rows) * p.C, 1, 1)
+                                     : dim3(rows, p.C, 1);
+  cfg.blockDim = dim3(cols ? 32 * kColGroup : (wide ? 2 * kMergeThreads : kMergeThreads));
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1014,6 +1109,12 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
   cudaError_t e = cudaErrorInvalidValue;
+  if (cols) {
+    if (p.D == 64) e = cudaLaunchKernelEx(&cfg, pa_merge_cols_kernel<64>, c->ma);
+    if (p.D == 128) e = cudaLaunchKernelEx(&cfg, pa_merge_cols_kernel<128>, c->ma);
+    if (p.D == 256) e = cudaLaunchKernelEx(&cfg, pa_merge_cols_kernel<256>, c->ma);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
   constexpr int NW = kMergeThreads / 32;
   if (p.D == 64) e = wide ? cudaLaunchKernelEx(&cfg, pa_merge_kernel<64, 2 * NW>, c->ma)
                           : cudaLaunchKernelEx(&cfg, pa_merge_kernel<64, NW>, c->ma);

@@ -268,3 +268,18 @@ def test_negative_and_zero_scale(mode, scale):
         got, st = run_gpu(w, opts)
         assert st == 0
         assert_close(got, run_oracle(w), f"scale {scale} {mode}")
+
+
+@pytest.mark.parametrize("G", [1, 8])
+def test_one_long_sequence_among_many_short_ones(G):
+    """Many more rows than split CTAs, but one segment holding most of the
+    keys: it spans most of the persistent grid, so its merge folds well over
+    a hundred pieces (more than one batch of loads)."""
+    lens = [1] * 300 + [40000] + [3] * 100
+    w = wl.random_workload(lens, H=G, Hkv=1, d=128, bs=16, dtype="bf16", seed=81 + G,
+                           poison=True)
+    got, st = run_gpu(w)
+    assert st == 0
+    assert_close(got, run_oracle(w), f"one long sequence, G={G}")
+    again, _ = run_gpu(w)
+    assert np.array_equal(got, again)
