@@ -199,12 +199,13 @@ __device__ __forceinline__ bool find_segment(const MergeArgs& a, int k, int& seg
 }
 
 // Balanced split whose segments have few pieces (typically at most
-// kMergeBatch: many more rows than split CTAs): CTA i takes column group i mod ng (kColGroup
-// columns, one per warp) of the (i / ng)-th segment with pieces to merge.
-// Each warp folds its column's pieces in piece order with one round of loads
-// and writes the column; no warp waits for another after the segment scan,
-// and the scan runs once per column group instead of once per column.
+// kMergeBatch: many more rows than split CTAs): CTA i takes column group
+// i mod ng (kColGroup columns, one per warp) of the segment that split CTA
+// i / ng begins and cuts, if any.  Each warp folds its column's pieces in
+// piece order, a batch of loads at a time, and writes the column; no warp
+// waits for another.
 constexpr int kColGroup = 4;
+constexpr int kColBatch = 4;
 template <int D>
 __global__ void __launch_bounds__(kColGroup * 32) pa_merge_cols_kernel(const MergeArgs a) {
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -216,9 +217,12 @@ __global__ void __launch_bounds__(kColGroup * 32) pa_merge_cols_kernel(const Mer
   }
   const int ng = (a.C + kColGroup - 1) / kColGroup;
   const SchedShape sched{a.B, a.Hkv, a.bs, a.maxblk, a.part_blocks, a.num_ctas, 0, 0};
-  int seg;
-  int4 desc = make_int4(-1, 0, 0, 0);
-  if (!find_segment<kColGroup>(a, blockIdx.x / ng, seg, desc)) return;
+  // the descriptor of split CTA seg: the segment that begins in it and
+  // continues past it, if any (the grid fits in one wave, so CTAs without
+  // work cost no dispatch round)
+  const int seg = blockIdx.x / ng;
+  const int4 desc = a.ws_desc[seg];
+  if (desc.x < 0) return;
   const MergeSeg ms = merge_segment(sched, seg, desc.x, desc.y, desc.z, desc.w, a.ws_pre);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int g = (blockIdx.x % ng) * kColGroup + w;
@@ -237,13 +241,14 @@ __global__ void __launch_bounds__(kColGroup * 32) pa_merge_cols_kernel(const Mer
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
-  // batches of kMergeBatch pieces (a long segment among short ones can span
-  // more split CTAs than the average suggests)
-  for (int p0 = 0; p0 < ms.np; p0 += kMergeBatch) {
-    float mp[kMergeBatch], lp[kMergeBatch];
-    Vec<V> x[kMergeBatch];
+  // batches of kColBatch pieces: segments here have two or three pieces as
+  // a rule, and few registers keep the whole grid in one wave; a long
+  // segment among short ones can span many more split CTAs
+  for (int p0 = 0; p0 < ms.np; p0 += kColBatch) {
+    float mp[kColBatch], lp[kColBatch];
+    Vec<V> x[kColBatch];
 #pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
+    for (int u = 0; u < kColBatch; ++u) {
       mp[u] = -INFINITY;
       lp[u] = 0.f;
       if (p0 + u < ms.np) {
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(kColGroup * 32) pa_merge_cols_kernel(const Mer
       }
     }
 #pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
+    for (int u = 0; u < kColBatch; ++u) {
       // an empty state (m = -inf) gets weight 0; a NaN it carries (a bad
       // piece) still reaches the result
       const float nm = fmaxf(m, mp[u]);
@@ -1097,7 +1102,7 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   const bool cols = p.part_blocks == 0 && pieces <= kMergeBatch && p.C > kColGroup;
   const int ng = (p.C + kColGroup - 1) / kColGroup;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = cols ? dim3(std::min(p.grid, rows) * ng, 1, 1)
+  cfg.gridDim = cols ? dim3(p.grid * ng, 1, 1)
                 : p.part_blocks == 0 ? dim3(std::min(p.grid, rows) * p.C, 1, 1)
                                      : dim3(rows, p.C, 1);
   cfg.blockDim = dim3(cols ? 32 * kColGroup : (wide ? 2 * kMergeThreads : kMergeThreads));
