@@ -1094,12 +1094,12 @@ int launch_merge_phase(Call* c, cudaStream_t stream, bool overlap) {
   // column, 68.8 -> 68.0 us per step; nothing changes where segments have
   // two or three pieces
   const bool wide = pieces > 2 * kMergeBatch;
-  // few pieces per segment (balanced split) and more than one column group:
-  // column groups, a warp per column.  Same box, step times: 8-token serving
-  // 668.2 -> 657.8 us, 4-token prefix sharing 250.9 -> 241.1, 4-token serving
-  // 515.2 -> 510.5, prefix sharing (G = 8) 180.8 -> 178.8; the serving mix
-  // (4 columns, one group) 493.4 against 494.3, so it keeps the per-column grid
-  const bool cols = p.part_blocks == 0 && pieces <= kMergeBatch && p.C > kColGroup;
+  // few pieces per segment (balanced split): column groups, a warp per
+  // column.  Same box, step times against the per-column grid: 8-token
+  // serving 668.2 -> 654.9 us, 4-token prefix sharing 250.9 -> 238.4,
+  // 4-token serving 515.2 -> 510.5, prefix sharing (G = 8) 180.8 -> 178.8,
+  // the serving mix 479.4 -> 477.8
+  const bool cols = p.part_blocks == 0 && pieces <= kMergeBatch;
   const int ng = (p.C + kColGroup - 1) / kColGroup;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = cols ? dim3(p.grid * ng, 1, 1)
