@@ -183,9 +183,9 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
   __syncthreads();
   const Piece pc{b, j, blk0, blk1, 0};
   combine_piece<D, W, false, false>(*sa, smem, L, pc, 0, 0, 0);
-  __syncthreads();
 
-  // ---- the cluster's states, folded in rank order
+  // ---- the cluster's states, folded in rank order (the cluster barrier
+  // also orders this CTA's own threads: no separate CTA barrier)
   cluster_sync();
   float* wts = reinterpret_cast<float*>(smem + CL.wts);
   const uint32_t ml_addr = base + CL.st_ml, acc_addr = base + CL.st_acc;
@@ -234,20 +234,25 @@ __global__ void __launch_bounds__(32 * split_warps(D), 1)
     }
     *reinterpret_cast<float4*>(a.out + ((int64_t)b * a.H + (int64_t)j * a.G + c) * D + d4) = o;
   }
-  // this thread's status bits and outputs, before the count below
-  __threadfence();
-  // no CTA leaves while another still reads its shared memory
-  cluster_sync();
-  if (a.status_out && tid == 0) {
-    // host-buffer calls: the last CTA to finish publishes the call's status
-    if (atomicAdd(a.done, 1u) == gridDim.x * gridDim.y - 1) {
-      __threadfence();
-      volatile uint32_t* st = a.status;
-      *a.status_out = *st;
-      *st = 0u;
-      *reinterpret_cast<volatile uint32_t*>(a.done) = 0u;
+  // this thread is done reading the others' shared memory
+  cluster_arrive();
+  if (a.status_out) {
+    // this thread's status bits and outputs, before the count below
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      // host-buffer calls: the last CTA to finish publishes the call's status
+      if (atomicAdd(a.done, 1u) == gridDim.x * gridDim.y - 1) {
+        __threadfence();
+        volatile uint32_t* st = a.status;
+        *a.status_out = *st;
+        *st = 0u;
+        *reinterpret_cast<volatile uint32_t*>(a.done) = 0u;
+      }
     }
   }
+  // no CTA leaves while another still reads its shared memory
+  cluster_wait();
 }
 
 template <typename T, int D>

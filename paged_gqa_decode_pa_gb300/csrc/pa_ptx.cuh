@@ -278,6 +278,16 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// The two halves of cluster_sync, for a CTA that has work to do between
+// finishing its reads of the others' shared memory (arrive) and needing
+// every other CTA to have finished reading its own (wait).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // The address of `addr` (this CTA's shared memory) in CTA `rank`'s shared
 // memory, in the cluster's shared window.
 __device__ __forceinline__ uint32_t dsmem_addr(uint32_t addr, uint32_t rank) {
