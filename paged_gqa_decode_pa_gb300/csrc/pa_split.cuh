@@ -198,16 +198,17 @@ struct MmaState {
       float s1 = ((acc4[nb][0][1] + acc4[nb][1][1]) + (acc4[nb][2][1] + acc4[nb][3][1])) * qsc;
       float s2 = ((acc4[nb][0][2] + acc4[nb][1][2]) + (acc4[nb][2][2] + acc4[nb][3][2])) * qsc;
       float s3 = ((acc4[nb][0][3] + acc4[nb][1][3]) + (acc4[nb][2][3] + acc4[nb][3][3])) * qsc;
-      if (tr >= valid) s0 = s1 = -INFINITY;
-      if (tr + 8 >= valid) s2 = s3 = -INFINITY;
       if constexpr (kQ) {
         // per-column visibility: token tok0 + row is seen by a column only
-        // below its limit
-        const int r0 = tok0 + tr, r1 = r0 + 8;
-        if (r0 >= lim[nb][0]) s0 = -INFINITY;
-        if (r0 >= lim[nb][1]) s1 = -INFINITY;
-        if (r1 >= lim[nb][0]) s2 = -INFINITY;
-        if (r1 >= lim[nb][1]) s3 = -INFINITY;
+        // below its limit; with the tile's real rows, rows [0, vis) count
+        const int vis0 = min(valid, lim[nb][0] - tok0), vis1 = min(valid, lim[nb][1] - tok0);
+        if (tr >= vis0) s0 = -INFINITY;
+        if (tr >= vis1) s1 = -INFINITY;
+        if (tr + 8 >= vis0) s2 = -INFINITY;
+        if (tr + 8 >= vis1) s3 = -INFINITY;
+      } else {
+        if (tr >= valid) s0 = s1 = -INFINITY;
+        if (tr + 8 >= valid) s2 = s3 = -INFINITY;
       }
       // ---- online softmax update for the lane's two columns
       float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
